@@ -1,0 +1,14 @@
+"""CPU oracle for the strict token-logprob operator (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package; the product path never does.
+"""
+from .logp_oracle import (VPAD, VREAL, NSHARD, SHARD_W, InvalidArgument, RowResult,
+                          bf16_bits_to_f32, validate, scaled_logits, logp_row,
+                          row_logprobs_all, restr_for_support_size, logp_batch,
+                          shard_summaries, merge_summaries, top_k_mask, top_p_mask)
+
+__all__ = ["VPAD", "VREAL", "NSHARD", "SHARD_W", "InvalidArgument", "RowResult",
+           "bf16_bits_to_f32", "validate", "scaled_logits", "logp_row", "row_logprobs_all",
+           "restr_for_support_size", "logp_batch", "shard_summaries", "merge_summaries",
+           "top_k_mask", "top_p_mask"]

@@ -1,0 +1,288 @@
+"""Plain fp64 CPU oracle for the strict token-logprob operator.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import this
+module: only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg
+of ``bench.py`` use it.  It shares no code with the CUDA path.
+
+What it computes, per row of BF16 logits (sources named by page title and
+section):
+
+* "Configurable H100 consistency runs", sampling-flags paragraph: logits are
+  the BF16 model logits, scaled by the temperature in float32; temperature 0
+  selects greedy sampling; top-p lies in (0, 1]; top-k is -1 (off) or
+  1..real vocabulary size and is independent of top-p and temperature; the
+  top-p/top-k support is computed over the real vocabulary.
+* same page, KL-reference paragraph: the KL reference logprob is
+  temperature-scaled over the *full* vocabulary (not truncated), while the
+  policy logprob keeps its actual top-p/top-k sampling support.
+* same page, topology paragraph: a padded vocabulary of 152576 columns is
+  used; the real vocabulary (151936 columns) is the part the support is
+  computed over.  Columns at or beyond the real size are ignored whatever
+  they hold.
+
+Readings where the pages are silent (each is listed in the design notes):
+
+* top-k is applied first, then top-p on the top-k-renormalised distribution;
+* top-k keeps every token whose scaled logit is >= the k-th largest one
+  (ties at the boundary are kept, so the set may exceed k);
+* top-p keeps token j iff the renormalised mass of tokens with a strictly
+  larger scaled logit is < p (equal tokens share one decision);
+* p == 1 disables top-p and k == -1 or k >= real vocab disables top-k, so with
+  both disabled the restricted logprob equals the full one;
+* temperature 0 gives 0 at the argmax (lowest index on ties) and -inf
+  elsewhere, for both outputs;
+* a NaN or +inf among the real logits, an all -inf row, or a scaled maximum
+  that overflows float32, gives NaN for both outputs.
+
+Everything is exact or fp64: the scaling is the stated float32 division,
+then all arithmetic is double precision with exactly rounded sums
+(``math.fsum``).  No blocking, fusion or reordering beyond the definition.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+
+VPAD = 152576   # padded vocabulary ("Configurable H100 consistency runs", topology paragraph)
+VREAL = 151936  # real vocabulary of the model the pages run (Qwen3-8B)
+NSHARD = 8      # fixed virtual TP8 partition (same paragraph)
+SHARD_W = VPAD // NSHARD
+
+
+class InvalidArgument(ValueError):
+    """A sampling parameter or target outside the documented domain."""
+
+
+@dataclass
+class RowResult:
+    full: float              # full-vocabulary logprob of the target (KL-reference side)
+    restr: float             # restricted, renormalised logprob of the target (policy side)
+    support: int             # number of real tokens in the restricted support (-1 if NaN row)
+    # distinct scaled values of the top-k set in descending order, with the
+    # renormalised mass strictly above each one (G); empty unless top-p ran.
+    values_desc: np.ndarray | None = None
+    counts_desc: np.ndarray | None = None
+    g_desc: np.ndarray | None = None
+    top_p: float = 1.0
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of BF16 bit patterns to float32 (BF16 is the top half of an f32)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32)
+
+
+def validate(tau: float, top_p: float, top_k: int, target: int, vreal: int = VREAL) -> None:
+    """Domain of the sampling flags ("Configurable H100 consistency runs", sampling flags)."""
+    if not (math.isfinite(tau) and tau >= 0.0):
+        raise InvalidArgument(f"temperature must be finite and >= 0, got {tau}")
+    if not (top_p > 0.0 and top_p <= 1.0):
+        raise InvalidArgument(f"top_p must be in (0, 1], got {top_p}")
+    if not (top_k == -1 or 1 <= top_k <= vreal):
+        raise InvalidArgument(f"top_k must be -1 or 1..{vreal}, got {top_k}")
+    if not (0 <= target < vreal):
+        raise InvalidArgument(f"target must be in [0, {vreal}), got {target}")
+
+
+def scaled_logits(bits_row: np.ndarray, tau: float, vreal: int = VREAL) -> np.ndarray:
+    """s_j = float32(x_j) / float32(tau), IEEE float32 division, widened to fp64.
+
+    "Both sides use float32 temperature scaling after the same BF16 model
+    logits" (Configurable H100 consistency runs, sampling flags).
+    """
+    x = bf16_bits_to_f32(bits_row[:vreal])
+    with np.errstate(over="ignore", invalid="ignore", divide="ignore"):
+        s = x / np.float32(tau)
+    assert s.dtype == np.float32
+    return s.astype(np.float64)
+
+
+def _nan_result() -> RowResult:
+    return RowResult(full=math.nan, restr=math.nan, support=-1)
+
+
+def top_k_mask(s: np.ndarray, top_k: int) -> np.ndarray:
+    """S_k = {j : s_j >= v_k}, v_k the k-th largest real scaled logit (ties kept)."""
+    n = s.shape[0]
+    if top_k == -1 or top_k >= n:
+        return np.ones(n, dtype=bool)
+    desc = np.sort(s)[::-1]
+    v_k = desc[top_k - 1]
+    return s >= v_k
+
+
+def top_p_mask(s: np.ndarray, sk: np.ndarray, top_p: float):
+    """Nucleus within S_k: keep j iff (mass of S_k strictly above s_j) / Z_k < p.
+
+    Returns (mask, distinct values desc, counts, G per distinct value).
+    Masses are w_j = exp(s_j - M) with M the row maximum; the common factor
+    cancels in the ratio.
+    """
+    m = np.max(s)
+    vals = s[sk]
+    uniq_asc, inv, counts_asc = np.unique(vals, return_inverse=True, return_counts=True)
+    uniq = uniq_asc[::-1]
+    counts = counts_asc[::-1]
+    with np.errstate(under="ignore"):
+        per_value_mass = counts.astype(np.float64) * np.exp(uniq - m)
+        z_k = math.fsum(np.exp(vals - m))
+    # mass strictly above each distinct value, in descending order of value
+    above = np.concatenate(([0.0], np.cumsum(per_value_mass)[:-1]))
+    g = above / z_k
+    g_asc = g[::-1]
+    mask = np.zeros_like(sk)
+    mask[np.nonzero(sk)[0]] = g_asc[inv] < top_p
+    return mask, uniq, counts, g
+
+
+def logp_row(bits_row: np.ndarray, tau: float, top_p: float, top_k: int, target: int,
+             vreal: int = VREAL, want_margins: bool = False) -> RowResult:
+    """Full and restricted logprob of ``target`` for one row of BF16 logit bits.
+
+    full  = s_t - logsumexp_{j < vreal}(s_j)             (KL-reference side)
+    restr = s_t - logsumexp_{j in S}(s_j) if t in S else -inf   (policy side)
+    with S the top-k-then-top-p support over the real vocabulary.
+    """
+    validate(tau, top_p, top_k, target, vreal)
+    bits_row = np.asarray(bits_row, dtype=np.uint16)
+    x = bf16_bits_to_f32(bits_row[:vreal])
+    if np.any(np.isnan(x)) or np.any(np.isposinf(x)) or np.all(np.isneginf(x)):
+        return _nan_result()
+
+    if tau == 0.0:
+        # greedy: argmax over the real vocabulary, lowest index on ties
+        a = int(np.argmax(x))
+        v = 0.0 if target == a else -math.inf
+        return RowResult(full=v, restr=v, support=1, top_p=top_p)
+
+    s = scaled_logits(bits_row, tau, vreal)
+    m = float(np.max(s))
+    if not math.isfinite(m):
+        return _nan_result()
+    with np.errstate(under="ignore"):
+        w = np.exp(s - m)
+    z = math.fsum(w)
+    s_t = float(s[target])
+    full = (s_t - m) - math.log(z)
+
+    k_on = not (top_k == -1 or top_k >= vreal)
+    p_on = top_p < 1.0
+    if not k_on and not p_on:
+        return RowResult(full=full, restr=full, support=vreal, top_p=top_p)
+
+    sk = top_k_mask(s, top_k)
+    values = counts = g = None
+    if p_on:
+        S, values, counts, g = top_p_mask(s, sk, top_p)
+    else:
+        S = sk
+    z_s = math.fsum(w[S])
+    restr = (s_t - m) - math.log(z_s) if S[target] else -math.inf
+    res = RowResult(full=full, restr=restr, support=int(np.count_nonzero(S)), top_p=top_p)
+    if want_margins and p_on:
+        res.values_desc, res.counts_desc, res.g_desc = values, counts, g
+    return res
+
+
+def row_logprobs_all(bits_row: np.ndarray, tau: float, top_p: float, top_k: int,
+                     vreal: int = VREAL):
+    """Full and restricted logprobs of every real token of one row (tau > 0).
+
+    Used by the invariant tests (both distributions sum to one).
+    """
+    validate(tau, top_p, top_k, 0, vreal)
+    s = scaled_logits(np.asarray(bits_row, dtype=np.uint16), tau, vreal)
+    m = float(np.max(s))
+    with np.errstate(under="ignore"):
+        w = np.exp(s - m)
+    full = (s - m) - math.log(math.fsum(w))
+    sk = top_k_mask(s, top_k)
+    if top_p < 1.0:
+        S = top_p_mask(s, sk, top_p)[0]
+    else:
+        S = sk
+    restr = np.full_like(s, -np.inf)
+    restr[S] = (s[S] - m) - math.log(math.fsum(w[S]))
+    return full, restr, S
+
+
+def restr_for_support_size(bits_row: np.ndarray, tau: float, target: int, n_support: int,
+                           vreal: int = VREAL) -> float:
+    """Restricted logprob when the support is the top ``n_support`` tokens by value.
+
+    Used only to score a row whose support differs from the oracle's at a
+    near-threshold tie class: the comparison is then made on the support the
+    other implementation chose.  ``n_support`` must end on a tie-class boundary.
+    """
+    s = scaled_logits(np.asarray(bits_row, dtype=np.uint16), tau, vreal)
+    m = float(np.max(s))
+    order = np.argsort(-s, kind="stable")
+    if n_support < vreal:
+        assert s[order[n_support - 1]] != s[order[n_support]], "not a tie-class boundary"
+    S = np.zeros(vreal, dtype=bool)
+    S[order[:n_support]] = True
+    if not S[target]:
+        return -math.inf
+    with np.errstate(under="ignore"):
+        z_s = math.fsum(np.exp(s[S] - m))
+    return (float(s[target]) - m) - math.log(z_s)
+
+
+def logp_batch(bits: np.ndarray, tau, top_p, top_k, target, rows=None):
+    """Row loop over ``bits[T, >=vreal]`` with scalar or per-row parameters.
+
+    Returns (full[T'], restr[T'], support[T']) for the selected ``rows``.
+    Invalid parameters give NaN / NaN / -1 for that row (the device contract).
+    """
+    T = bits.shape[0]
+    rows = np.arange(T) if rows is None else np.asarray(rows)
+
+    def at(v, i, cast):
+        return cast(v[i]) if np.ndim(v) else cast(v)
+
+    full = np.empty(len(rows))
+    restr = np.empty(len(rows))
+    sup = np.empty(len(rows), dtype=np.int64)
+    for n, i in enumerate(rows):
+        try:
+            r = logp_row(bits[i], at(tau, i, float), at(top_p, i, float),
+                         at(top_k, i, int), at(target, i, int))
+            full[n], restr[n], sup[n] = r.full, r.restr, r.support
+        except InvalidArgument:
+            full[n], restr[n], sup[n] = math.nan, math.nan, -1
+    return full, restr, sup
+
+
+def shard_summaries(bits_row: np.ndarray, tau: float):
+    """Per-virtual-shard (max, sum-exp) of the scaled logits, fp64.
+
+    "logp emits ... vocabulary summaries and merges them in fixed global-vocab
+    order" (Reproduce and profile the Qwen3-8B TP4/CP2 experiment, section
+    "How non-default CUDA topology reuses TP4/CP2"), with the fixed virtual
+    TP8 partition of the padded vocabulary.  Padded columns are excluded.
+    Returns arrays m[8], l[8] (l_r = sum over shard r of exp(s_j - m_r)).
+    """
+    s_real = scaled_logits(np.asarray(bits_row, dtype=np.uint16), tau)
+    s = np.full(VPAD, -np.inf)
+    s[:VREAL] = s_real
+    m = np.empty(NSHARD)
+    l = np.empty(NSHARD)
+    for r in range(NSHARD):
+        seg = s[r * SHARD_W:(r + 1) * SHARD_W]
+        m[r] = np.max(seg)
+        with np.errstate(under="ignore", invalid="ignore"):
+            l[r] = math.fsum(np.exp(seg - m[r])) if math.isfinite(m[r]) else 0.0
+    return m, l
+
+
+def merge_summaries(m: np.ndarray, l: np.ndarray) -> float:
+    """Log-sum-exp from shard summaries, left fold over shard index 0..7."""
+    M = float(np.max(m))
+    z = 0.0
+    for r in range(len(m)):
+        if l[r] > 0.0:
+            z += l[r] * math.exp(m[r] - M)
+    return M + math.log(z)
