@@ -1,0 +1,358 @@
+"""Throughput of the strict token-logprob step on GB300.
+
+One step = the whole hot path over one batch: the policy pass (full-vocabulary
+and top-k-then-top-p restricted logprobs from 8 virtual-shard summaries) and
+the reference pass with the per-row KL term, on the T = 8192 workload
+(4N(0,1) logits + hot sets of 1..256 columns, tau 1.3, top-p 0.99,
+top-k 128, reference = policy + N(0, 0.05^2)).  Inputs are synthetic and
+resident in HBM (5.0 GB per step, far above the 129 MB L2, so no flush).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0.  Under torchrun every rank processes its own
+8192 rows (weak scaling, no data-path collective).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "logprob tokens/sec at V=152576 (full+top-k/top-p) and % of GB300 HBM roofline"
+UNIT = "tokens/s"
+VPAD, VREAL = 152576, 151936
+T_ROWS, TAU, TOP_P, TOP_K = 8192, 1.3, 0.99, 128
+WORKLOAD = "c2_hot1-256_T8192_policy+ref_kl"
+KERNEL_SRC = os.path.join(ROOT, "rollout_consistent_vocab_gb300", "csrc", "rlk_logp.cu")
+NCU_SUMMARY = os.path.join(ROOT, "profiles", "logp_pair_kernel_c2.md")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_sha() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic():
+    """DRAM bytes per launch of the pair kernel from the committed ncu summary,
+    or None when the summary is missing or the kernel source changed since."""
+    try:
+        text = open(NCU_SUMMARY).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_b or m_sha.group(1) != kernel_sha():
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def cpu_oracle_rate(bits, ref_bits, targets, seconds: float):
+    """Rows per second of the oracle over a bounded sample (policy pair + ref full + KL)."""
+    import oracle
+    t0 = time.perf_counter()
+    n = 0
+    while n < bits.shape[0]:
+        t = int(targets[n])
+        oracle.logp_row(bits[n], TAU, TOP_P, TOP_K, t)
+        oracle.logp_row(ref_bits[n], TAU, 1.0, -1, t)
+        n += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    dt = time.perf_counter() - t0
+    return n / dt, n, dt
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is a bounded sample of the workload."""
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+    from rollout_consistent_vocab_gb300 import workloads as W
+    rows = max(1, min(8, 200 // max(1, args.steps)))
+    wl = W.workload_c2(device="cpu", T=64)
+    bits = wl.logits.view(torch.int16).numpy().view(np.uint16)
+    rbits = wl.ref_logits.view(torch.int16).numpy().view(np.uint16)
+    tg = W.structural_targets(64, wl.hot, wl.hot_n, seed=2).numpy()
+    import oracle
+    def step(i):
+        for j in range(rows):
+            r = (i * rows + j) % 64
+            oracle.logp_row(bits[r], TAU, TOP_P, TOP_K, int(tg[r]))
+            oracle.logp_row(rbits[r], TAU, 1.0, -1, int(tg[r]))
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = rows * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{rows} rows of the T=8192 workload per step (policy pair + ref full)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config():
+    return {"workload": WORKLOAD, "rows_per_gpu": T_ROWS, "vocab_padded": VPAD,
+            "vocab_real": VREAL, "temperature": TAU, "top_p": TOP_P, "top_k": TOP_K,
+            "l2": "inputs larger than L2 (5.0 GB of logits read per step), no flush",
+            "parallelism": "row-sharded replicas, no collective"}
+
+
+# ------------------------------------------------------------------ ours
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import rollout_consistent_vocab_gb300 as pkg
+    from rollout_consistent_vocab_gb300 import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkg.load_library()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    # each rank owns its own 8192 rows (weak scaling)
+    x, hot, n = W.hot_logits(T_ROWS, 1, 256, seed=2 + 1000 * rank, device=dev)
+    ref = W.perturbed_copy(x, 0.05, seed=102 + 1000 * rank)
+    tg = W.structural_targets(T_ROWS, hot, n, seed=2 + 1000 * rank, device=dev)
+    del hot, n
+    f32 = dict(dtype=torch.float32, device=dev)
+    full, restr, kl, full_ref = (torch.empty(T_ROWS, **f32) for _ in range(4))
+    sup = torch.empty(T_ROWS, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        pkg.logp_pair(x, tg, TAU, TOP_P, TOP_K, out_full=full, out_restr=restr, out_support=sup,
+                      stream=stream)
+        pkg.logp_kl_ref(ref, tg, full, TAU, out_full_ref=full_ref, out_kl=kl, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    smi_index = vis.split(",")[local] if vis else str(local)
+    with ClockSampler(smi_index) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(K):
+            ev[i][0].record(stream)
+            pkg.logp_pair(x, tg, TAU, TOP_P, TOP_K, out_full=full, out_restr=restr,
+                          out_support=sup, stream=stream)
+            ev[i][1].record(stream)
+            pkg.logp_kl_ref(ref, tg, full, TAU, out_full_ref=full_ref, out_kl=kl, stream=stream)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    pair_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    ref_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    value = world * T_ROWS * K / (total_ms / 1e3)
+
+    # ---- end to end through the public API from pinned host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+        hr = torch.empty(ref.shape, dtype=ref.dtype, pin_memory=True)
+        ht = torch.empty(tg.shape, dtype=tg.dtype, pin_memory=True)
+        hx.copy_(x)
+        hr.copy_(ref)
+        ht.copy_(tg)
+        outs_h = [torch.empty(T_ROWS, dtype=torch.float32, pin_memory=True) for _ in range(3)]
+        sup_h = torch.empty(T_ROWS, dtype=torch.int32, pin_memory=True)
+
+        def e2e_step():
+            x.copy_(hx, non_blocking=True)
+            ref.copy_(hr, non_blocking=True)
+            tg.copy_(ht, non_blocking=True)
+            pkg.logp_kl(x, ref, tg, TAU, TOP_P, TOP_K, out_full=full, out_restr=restr,
+                        out_support=sup, out_full_ref=full_ref, out_kl=kl, stream=stream)
+            outs_h[0].copy_(full, non_blocking=True)
+            outs_h[1].copy_(restr, non_blocking=True)
+            outs_h[2].copy_(kl, non_blocking=True)
+            sup_h.copy_(sup, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        et = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(et, op=dist.ReduceOp.MAX)
+        h2d = hx.numel() * 2 + hr.numel() * 2 + ht.numel() * 4
+        d2h = 3 * 4 * T_ROWS + 4 * T_ROWS
+        e2e = {"value": world * T_ROWS * args.e2e_steps / (float(et.item()) / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample_rows = np.arange(0, T_ROWS, 37)
+        ridx = torch.as_tensor(sample_rows, device=dev)
+        bits = x[ridx].view(torch.int16).cpu().numpy().view(np.uint16)
+        rbits = ref[ridx].view(torch.int16).cpu().numpy().view(np.uint16)
+        rate, nrows, secs = cpu_oracle_rate(bits, rbits, tg[ridx].cpu().numpy(), args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{nrows} rows of this workload (every 37th row), policy pair + reference "
+                         f"full per row, {secs:.1f} s on one host core"}
+
+    if rank == 0:
+        peak, peak_kind = measured_peak()
+        pair_avg = statistics.mean(pair_ms)
+        algo_bytes = T_ROWS * VPAD * 2
+        achieved = algo_bytes / (pair_avg / 1e3) / 1e9
+        traffic = ncu_traffic()
+        ref_avg = statistics.mean(ref_ms)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": max(args.warmup, 3), "ms_per_step": total_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": workload_config(),
+            "roofline": {"bound": "hbm", "kernel": "logp_kernel<true> (policy pair pass)",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind,
+                         "traffic": traffic, "algorithmic_bytes_per_launch": algo_bytes,
+                         "avg_launch_ms": pair_avg},
+            "ref_pass": {"avg_launch_ms": ref_avg,
+                         "achieved_gbs": algo_bytes / (ref_avg / 1e3) / 1e9},
+            "step_hbm_gbs": 2 * algo_bytes * K / (total_ms / 1e3) / 1e9,
+            "gpu_launches": 2 * K,
+            "clocks": clk.summary(),
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,153 @@
+/*
+ * rlk_logp.h -- C ABI of the strict, batch-invariant token-logprob operator
+ * for GB300 (sm_103a).
+ *
+ * The operator (sources named by page title and section):
+ *
+ *   "Configurable H100 consistency runs", topology paragraph: the CUDA path
+ *   uses a fixed virtual TP8 partition and a padded vocabulary of 152576
+ *   columns whatever the physical layout.  Here the real vocabulary is the
+ *   first 151936 columns; the 640 padded columns are never read.
+ *
+ *   "Reproduce and profile the Qwen3-8B TP4/CP2 experiment", section "How
+ *   non-default CUDA topology reuses TP4/CP2": logp emits per-shard vocabulary
+ *   summaries and merges them in fixed global-vocabulary order.  Here each of
+ *   the 8 shards of 19072 columns emits a (max, sum-exp) pair built in a fixed
+ *   reduction tree and the pairs merge as a left fold over shard index 0..7.
+ *
+ *   "Configurable H100 consistency runs", sampling-flags paragraph: float32
+ *   temperature scaling after the BF16 logits; temperature 0 is greedy;
+ *   top-p in (0, 1]; top-k is -1 (off) or 1..151936; the top-p/top-k support
+ *   is computed from the whole real vocabulary.  KL-reference paragraph: the
+ *   reference logprob is scaled over the full vocabulary (not truncated)
+ *   while the policy logprob keeps its actual top-p/top-k support.
+ *
+ * Per row i with target t = target[i]:
+ *   full[i]    = s_t - log sum_{j < 151936} exp(s_j),  s_j = x_j / tau_i
+ *   restr[i]   = s_t - log sum_{j in S} exp(s_j) if t in S, else -inf
+ *   support[i] = |S|
+ * S is top-k first (every token >= the k-th largest value, ties kept), then
+ * top-p on the renormalised top-k distribution (token j kept iff the mass of
+ * strictly larger tokens is < p of the top-k mass).  p == 1 together with
+ * k == -1 (or k == 151936) disables both filters and restr == full bit for
+ * bit, support == 151936.  tau == 0 (greedy): both outputs are 0 at the
+ * argmax (lowest column on ties) and -inf elsewhere, support == 1.
+ * A NaN or +inf among the real logits, a row that is all -inf, or a scaled
+ * maximum that overflows float32 gives NaN outputs and support -1.
+ *
+ * Results are bit-identical for a row whatever T, the row's position in the
+ * batch, or the buffer it sits in: every reduction has a fixed shape that
+ * depends only on the column index.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library allocates nothing, frees nothing and never synchronises: work
+ *     is enqueued on `stream` (a cudaStream_t passed as void*; NULL is the
+ *     legacy default stream) and outputs are ready when the stream reaches
+ *     that point.
+ *   - Host-checkable faults return a status before anything is enqueued:
+ *     RLK_EINVAL for a null required pointer, T < 0, row_stride <
+ *     vocab_padded, vocab sizes other than 151936/152576, a scalar parameter
+ *     out of its domain (used when the per-row array is NULL), or T too large
+ *     for one launch (T > 2^28); RLK_EALIGN for a logits base that is not
+ *     16-byte aligned, a row_stride that is not a multiple of 8 elements, or
+ *     an int/float array that is not 4-byte aligned.  T == 0 returns RLK_OK
+ *     with nothing enqueued.  RLK_ECUDA reports a launch failure.
+ *   - Per-row parameter arrays cannot be checked on the host without a
+ *     synchronisation: a row whose tau, top_p, top_k or target is out of
+ *     domain gets NaN outputs, support -1, and increments *err_count (an
+ *     optional device int32).  A shard load that does not complete within
+ *     about two seconds is treated the same way.
+ *   - rlk_last_error() returns a message for the last non-OK status of the
+ *     calling host thread.
+ */
+#ifndef RLK_LOGP_H
+#define RLK_LOGP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RLK_VOCAB_PADDED 152576
+#define RLK_VOCAB_REAL 151936
+#define RLK_NUM_SHARDS 8
+#define RLK_SHARD_WIDTH 19072
+#define RLK_ABI_VERSION 1
+
+typedef enum {
+  RLK_OK = 0,
+  RLK_EINVAL = 1,
+  RLK_EALIGN = 2,
+  RLK_ECUDA = 3
+} rlk_status;
+
+typedef struct rlk_logp_args {
+  /* bf16 logits, row-major: row i starts at logits + i * row_stride
+   * (elements).  Only columns 0..151935 are read. */
+  const void* logits;
+  int64_t T;                 /* rows */
+  int64_t row_stride;        /* elements between rows; >= vocab_padded, % 8 == 0 */
+  int32_t vocab_real;        /* must be RLK_VOCAB_REAL */
+  int32_t vocab_padded;      /* must be RLK_VOCAB_PADDED */
+  const int32_t* target;     /* [T] target column per row, 0 <= t < vocab_real */
+  /* Sampling parameters: a per-row device array [T], or NULL to use the
+   * scalar for every row.  top_p/top_k are ignored by rlk_logp_full. */
+  const float* temperature;  float temperature_scalar;  /* finite, >= 0 */
+  const float* top_p;        float top_p_scalar;        /* (0, 1]      */
+  const int32_t* top_k;      int32_t top_k_scalar;      /* -1 or 1..vocab_real */
+  int32_t* err_count;        /* optional device counter of rejected rows */
+} rlk_logp_args;
+
+/* Full-vocabulary logprob of the target (the KL-reference side).
+ * out_full: device float[T], required. */
+rlk_status rlk_logp_full(const rlk_logp_args* args, float* out_full, void* stream);
+
+/* Top-k-then-top-p restricted, renormalised logprob (the policy side).
+ * out_restr: device float[T], required.  out_support: device int32[T] or NULL. */
+rlk_status rlk_logp_restricted(const rlk_logp_args* args, float* out_restr,
+                               int32_t* out_support, void* stream);
+
+/* Both sides in one pass over the logits.  Each output pointer may be NULL
+ * except that at least one of out_full/out_restr must be given. */
+rlk_status rlk_logp_pair(const rlk_logp_args* args, float* out_full, float* out_restr,
+                         int32_t* out_support, void* stream);
+
+/* Policy pair plus the per-row KL term of the sampled token,
+ *   out_kl[i] = full_policy[i] - full_ref[i],
+ * where full_ref is the full-vocabulary logprob of the same target under the
+ * reference logits (same temperature; "Configurable H100 consistency runs",
+ * KL-reference paragraph).  ref_logits follows the same layout rules as
+ * args->logits with its own ref_row_stride.  out_full, out_full_ref and
+ * out_kl are required; out_restr and out_support may be NULL.  Two launches
+ * on `stream`: the policy pass, then the reference pass, whose epilogue
+ * forms the difference. */
+rlk_status rlk_logp_kl(const rlk_logp_args* policy, const void* ref_logits,
+                       int64_t ref_row_stride, float* out_full, float* out_restr,
+                       int32_t* out_support, float* out_full_ref, float* out_kl,
+                       void* stream);
+
+/* The reference half of rlk_logp_kl on its own: the full-vocabulary logprob
+ * of each row's target under ref->logits, and out_kl[i] = full_policy[i] -
+ * out_full_ref[i] with full_policy an earlier result of rlk_logp_full/pair
+ * on the same stream.  ref carries the reference logits, targets and
+ * temperatures (top_p/top_k are ignored).  full_policy, out_full_ref and
+ * out_kl are required device float[T]. */
+rlk_status rlk_logp_kl_ref(const rlk_logp_args* ref, const float* full_policy,
+                           float* out_full_ref, float* out_kl, void* stream);
+
+/* Static message for a status code. */
+const char* rlk_status_string(rlk_status status);
+
+/* Message for the last non-OK status returned on the calling host thread. */
+const char* rlk_last_error(void);
+
+/* RLK_ABI_VERSION of the built library. */
+int rlk_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RLK_LOGP_H */

@@ -1,0 +1,12 @@
+"""Strict, batch-invariant token logprob on GB300 (sm_103a).
+
+The compute lives in ``lib/librlk_logp.so`` (CUDA kernels behind a C ABI,
+declared in ``include/rlk_logp.h``); this package is its thin Python binding.
+"""
+
+from ._binding import (VOCAB_PADDED, VOCAB_REAL, NUM_SHARDS, SHARD_WIDTH, RlkError, LogpArgs,
+                       EXPORTS, load_library, logp_full, logp_pair, logp_restricted, logp_kl,
+                       logp_kl_ref)
+
+__all__ = ["VOCAB_PADDED", "VOCAB_REAL", "NUM_SHARDS", "SHARD_WIDTH", "RlkError", "LogpArgs",
+           "EXPORTS", "load_library", "logp_full", "logp_pair", "logp_restricted", "logp_kl", "logp_kl_ref"]

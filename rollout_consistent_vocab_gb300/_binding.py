@@ -1,0 +1,214 @@
+"""ctypes binding of ``librlk_logp.so``: argument marshalling only.
+
+Every step of the operator runs in the library's CUDA kernels; this module
+turns torch tensors into device pointers, picks the current CUDA stream and
+allocates outputs when the caller does not pass them.  There is no fallback:
+if the library is missing or a call fails, an exception is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB
+
+VOCAB_PADDED = 152576
+VOCAB_REAL = 151936
+NUM_SHARDS = 8
+SHARD_WIDTH = 19072
+
+RLK_OK, RLK_EINVAL, RLK_EALIGN, RLK_ECUDA = 0, 1, 2, 3
+
+
+class RlkError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"rlk status {status}: {message}")
+        self.status = status
+
+
+class LogpArgs(ctypes.Structure):
+    _fields_ = [
+        ("logits", ctypes.c_void_p),
+        ("T", ctypes.c_int64),
+        ("row_stride", ctypes.c_int64),
+        ("vocab_real", ctypes.c_int32),
+        ("vocab_padded", ctypes.c_int32),
+        ("target", ctypes.c_void_p),
+        ("temperature", ctypes.c_void_p),
+        ("temperature_scalar", ctypes.c_float),
+        ("top_p", ctypes.c_void_p),
+        ("top_p_scalar", ctypes.c_float),
+        ("top_k", ctypes.c_void_p),
+        ("top_k_scalar", ctypes.c_int32),
+        ("err_count", ctypes.c_void_p),
+    ]
+
+
+EXPORTS = ("rlk_logp_full", "rlk_logp_restricted", "rlk_logp_pair", "rlk_logp_kl", "rlk_logp_kl_ref",
+           "rlk_status_string", "rlk_last_error", "rlk_abi_version")
+
+_lib = None
+
+
+def load_library(path: str = LIB) -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"CUDA library {path} is missing: run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'` first")
+    lib = ctypes.CDLL(path)
+    P, VP = ctypes.POINTER, ctypes.c_void_p
+    A = P(LogpArgs)
+    lib.rlk_logp_full.argtypes = [A, VP, VP]
+    lib.rlk_logp_restricted.argtypes = [A, VP, VP, VP]
+    lib.rlk_logp_pair.argtypes = [A, VP, VP, VP, VP]
+    lib.rlk_logp_kl.argtypes = [A, VP, ctypes.c_int64, VP, VP, VP, VP, VP, VP]
+    lib.rlk_logp_kl_ref.argtypes = [A, VP, VP, VP, VP]
+    for f in ("rlk_logp_full", "rlk_logp_restricted", "rlk_logp_pair", "rlk_logp_kl",
+              "rlk_logp_kl_ref"):
+        getattr(lib, f).restype = ctypes.c_int
+    lib.rlk_status_string.argtypes = [ctypes.c_int]
+    lib.rlk_status_string.restype = ctypes.c_char_p
+    lib.rlk_last_error.argtypes = []
+    lib.rlk_last_error.restype = ctypes.c_char_p
+    lib.rlk_abi_version.argtypes = []
+    lib.rlk_abi_version.restype = ctypes.c_int
+    if lib.rlk_abi_version() != 1:
+        raise ImportError("librlk_logp.so ABI version mismatch")
+    _lib = lib
+    return lib
+
+
+def check(status: int) -> None:
+    if status != RLK_OK:
+        msg = load_library().rlk_last_error().decode()
+        raise RlkError(status, msg)
+
+
+# ------------------------------------------------------------ torch marshalling
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _param(v, T, dtype, name):
+    """(device pointer or None, scalar) for a per-row tensor or a Python scalar."""
+    torch = _torch()
+    if isinstance(v, torch.Tensor):
+        if v.dtype != dtype or v.dim() != 1 or v.shape[0] != T or not v.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape [{T}]")
+        if not v.is_cuda:
+            raise ValueError(f"{name} must live on the GPU")
+        return v.data_ptr(), 0
+    return None, v
+
+
+def make_args(logits, target, temperature=1.0, top_p=1.0, top_k=-1, err_count=None) -> LogpArgs:
+    torch = _torch()
+    if logits.dtype != torch.bfloat16 or logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be a bf16 [T, >=152576] tensor with unit column stride")
+    if logits.shape[1] < VOCAB_PADDED:
+        raise ValueError(f"logits must have at least {VOCAB_PADDED} columns")
+    T = logits.shape[0]
+    if target.dtype != torch.int32 or target.shape != (T,) or not target.is_contiguous():
+        raise ValueError("target must be a contiguous int32 tensor of shape [T]")
+    a = LogpArgs()
+    a.logits = logits.data_ptr() if T else None
+    a.T = T
+    a.row_stride = logits.stride(0) if T else VOCAB_PADDED
+    a.vocab_real = VOCAB_REAL
+    a.vocab_padded = VOCAB_PADDED
+    a.target = _ptr(target) if T else None
+    a.temperature, a.temperature_scalar = _param(temperature, T, torch.float32, "temperature")
+    a.top_p, a.top_p_scalar = _param(top_p, T, torch.float32, "top_p")
+    a.top_k, a.top_k_scalar = _param(top_k, T, torch.int32, "top_k")
+    a.err_count = _ptr(err_count)
+    return a
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _empty(T, dtype, like):
+    return _torch().empty((T,), dtype=dtype, device=like.device)
+
+
+def logp_full(logits, target, temperature=1.0, *, out=None, err_count=None, stream=None):
+    """Full-vocabulary logprob of each row's target (float32 [T])."""
+    lib = load_library()
+    torch = _torch()
+    a = make_args(logits, target, temperature, 1.0, -1, err_count)
+    out = _empty(a.T, torch.float32, logits) if out is None else out
+    check(lib.rlk_logp_full(ctypes.byref(a), _ptr(out), _stream(stream)))
+    return out
+
+
+def logp_pair(logits, target, temperature=1.0, top_p=1.0, top_k=-1, *, out_full=None,
+              out_restr=None, out_support=None, err_count=None, stream=None):
+    """(full, restricted, support) of each row's target in one pass."""
+    lib = load_library()
+    torch = _torch()
+    a = make_args(logits, target, temperature, top_p, top_k, err_count)
+    out_full = _empty(a.T, torch.float32, logits) if out_full is None else out_full
+    out_restr = _empty(a.T, torch.float32, logits) if out_restr is None else out_restr
+    out_support = _empty(a.T, torch.int32, logits) if out_support is None else out_support
+    check(lib.rlk_logp_pair(ctypes.byref(a), _ptr(out_full), _ptr(out_restr), _ptr(out_support),
+                            _stream(stream)))
+    return out_full, out_restr, out_support
+
+
+def logp_restricted(logits, target, temperature=1.0, top_p=1.0, top_k=-1, *, out=None,
+                    out_support=None, err_count=None, stream=None):
+    """(restricted, support) of each row's target."""
+    lib = load_library()
+    torch = _torch()
+    a = make_args(logits, target, temperature, top_p, top_k, err_count)
+    out = _empty(a.T, torch.float32, logits) if out is None else out
+    out_support = _empty(a.T, torch.int32, logits) if out_support is None else out_support
+    check(lib.rlk_logp_restricted(ctypes.byref(a), _ptr(out), _ptr(out_support), _stream(stream)))
+    return out, out_support
+
+
+def logp_kl(logits, ref_logits, target, temperature=1.0, top_p=1.0, top_k=-1, *, out_full=None,
+            out_restr=None, out_support=None, out_full_ref=None, out_kl=None, err_count=None,
+            stream=None):
+    """Policy (full, restricted, support), reference full logprob, and the KL term
+    full_policy - full_ref of each row's target."""
+    lib = load_library()
+    torch = _torch()
+    a = make_args(logits, target, temperature, top_p, top_k, err_count)
+    if ref_logits.dtype != torch.bfloat16 or ref_logits.shape[0] != a.T or ref_logits.stride(1) != 1:
+        raise ValueError("ref_logits must be a bf16 [T, >=152576] tensor like logits")
+    outs = [o if o is not None else _empty(a.T, dt, logits) for o, dt in
+            ((out_full, torch.float32), (out_restr, torch.float32), (out_support, torch.int32),
+             (out_full_ref, torch.float32), (out_kl, torch.float32))]
+    check(lib.rlk_logp_kl(ctypes.byref(a), ref_logits.data_ptr() if a.T else None,
+                          ref_logits.stride(0) if a.T else VOCAB_PADDED,
+                          *[_ptr(o) for o in outs], _stream(stream)))
+    return tuple(outs)
+
+
+def logp_kl_ref(ref_logits, target, full_policy, temperature=1.0, *, out_full_ref=None,
+                out_kl=None, stream=None):
+    """Reference pass alone: (full_ref, kl = full_policy - full_ref) of each row's target."""
+    lib = load_library()
+    torch = _torch()
+    a = make_args(ref_logits, target, temperature, 1.0, -1, None)
+    if full_policy.dtype != torch.float32 or full_policy.shape != (a.T,):
+        raise ValueError("full_policy must be a float32 tensor of shape [T]")
+    out_full_ref = _empty(a.T, torch.float32, ref_logits) if out_full_ref is None else out_full_ref
+    out_kl = _empty(a.T, torch.float32, ref_logits) if out_kl is None else out_kl
+    check(lib.rlk_logp_kl_ref(ctypes.byref(a), _ptr(full_policy), _ptr(out_full_ref), _ptr(out_kl),
+                              _stream(stream)))
+    return out_full_ref, out_kl

@@ -1,0 +1,127 @@
+"""The C-ABI library loads, exports every declared entry point, and rejects
+bad arguments on the host before touching the GPU (runs without a GPU)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import rollout_consistent_vocab_gb300 as pkg
+from rollout_consistent_vocab_gb300 import _binding as b
+from rollout_consistent_vocab_gb300.build import build_library
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_library()
+    return pkg.load_library()
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(rlk_\w+)\s*\(", text, re.M))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert {"rlk_logp_full", "rlk_logp_restricted", "rlk_logp_pair", "rlk_logp_kl"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(b.EXPORTS) == names
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.rlk_abi_version() == 1
+    assert lib.rlk_status_string(0) == b"ok"
+    assert lib.rlk_status_string(2) == b"misaligned pointer or stride"
+
+
+def _args(**kw):
+    a = b.LogpArgs()
+    a.logits = 0x10000
+    a.T = 4
+    a.row_stride = b.VOCAB_PADDED
+    a.vocab_real = b.VOCAB_REAL
+    a.vocab_padded = b.VOCAB_PADDED
+    a.target = 0x20000
+    a.temperature = None
+    a.temperature_scalar = 0.7
+    a.top_p = None
+    a.top_p_scalar = 0.95
+    a.top_k = None
+    a.top_k_scalar = -1
+    a.err_count = None
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+OUT = 0x30000
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=-1), b.RLK_EINVAL),
+    (dict(T=1 << 28), b.RLK_EINVAL),
+    (dict(vocab_real=151935), b.RLK_EINVAL),
+    (dict(vocab_padded=152577), b.RLK_EINVAL),
+    (dict(logits=None), b.RLK_EINVAL),
+    (dict(target=None), b.RLK_EINVAL),
+    (dict(row_stride=152575), b.RLK_EINVAL),
+    (dict(logits=0x10008), b.RLK_EALIGN),
+    (dict(row_stride=152580), b.RLK_EALIGN),
+    (dict(target=0x20002), b.RLK_EALIGN),
+    (dict(temperature_scalar=-0.5), b.RLK_EINVAL),
+    (dict(temperature_scalar=float("inf")), b.RLK_EINVAL),
+    (dict(temperature_scalar=float("nan")), b.RLK_EINVAL),
+    (dict(top_p_scalar=0.0), b.RLK_EINVAL),
+    (dict(top_p_scalar=1.5), b.RLK_EINVAL),
+    (dict(top_k_scalar=0), b.RLK_EINVAL),
+    (dict(top_k_scalar=151937), b.RLK_EINVAL),
+    (dict(top_k_scalar=-2), b.RLK_EINVAL),
+    (dict(temperature=0x40001), b.RLK_EALIGN),
+])
+def test_pair_rejects_bad_arguments_on_host(lib, kw, status):
+    a = _args(**kw)
+    got = lib.rlk_logp_pair(ctypes.byref(a), OUT, OUT + 0x1000, None, None)
+    assert got == status
+    assert lib.rlk_last_error()
+
+
+def test_null_and_misaligned_outputs(lib):
+    a = _args()
+    assert lib.rlk_logp_pair(ctypes.byref(a), None, None, None, None) == b.RLK_EINVAL
+    assert lib.rlk_logp_pair(ctypes.byref(a), OUT + 2, None, None, None) == b.RLK_EALIGN
+    assert lib.rlk_logp_full(ctypes.byref(a), None, None) == b.RLK_EINVAL
+    assert lib.rlk_logp_restricted(ctypes.byref(a), None, None, None) == b.RLK_EINVAL
+    assert lib.rlk_logp_full(None, OUT, None) == b.RLK_EINVAL
+    assert lib.rlk_logp_kl(ctypes.byref(a), 0x50008, b.VOCAB_PADDED, OUT, None, None,
+                           OUT, OUT, None) == b.RLK_EALIGN
+    assert lib.rlk_logp_kl(ctypes.byref(a), 0x50000, b.VOCAB_PADDED, OUT, None, None,
+                           None, OUT, None) == b.RLK_EINVAL
+
+
+def test_full_ignores_top_p_top_k(lib):
+    # top_p/top_k are not part of the full-vocabulary call; out-of-domain values
+    # there must not be rejected (the call then fails only at the launch, on CPU).
+    a = _args(top_p_scalar=7.0, top_k_scalar=0, T=0)
+    assert lib.rlk_logp_full(ctypes.byref(a), OUT, None) == b.RLK_OK
+
+
+def test_empty_batch_is_a_noop(lib):
+    a = _args(T=0, logits=None, target=None)
+    assert lib.rlk_logp_pair(ctypes.byref(a), None, None, None, None) == b.RLK_OK
+    assert lib.rlk_logp_full(ctypes.byref(a), None, None) == b.RLK_OK
+
+
+def test_kl_ref_validation(lib):
+    a = _args()
+    assert lib.rlk_logp_kl_ref(ctypes.byref(a), None, OUT, OUT, None) == b.RLK_EINVAL
+    assert lib.rlk_logp_kl_ref(ctypes.byref(a), OUT, OUT + 1, OUT, None) == b.RLK_EALIGN
+    assert lib.rlk_logp_kl_ref(ctypes.byref(_args(T=0)), None, None, None, None) == b.RLK_OK

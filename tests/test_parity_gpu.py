@@ -1,0 +1,310 @@
+"""GPU parity: the CUDA path against the CPU oracle, element by element.
+
+Tolerance: |delta logprob| <= 2e-5 absolute on both outputs; supports equal,
+except at tie classes whose renormalised mass above them lies within 1e-6
+(relative) of p, which are counted and then scored on the support the GPU
+chose.  All calls go through the C ABI (the ctypes binding).
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rollout_consistent_vocab_gb300 as pkg
+from rollout_consistent_vocab_gb300 import workloads as W
+
+from _support import TOL, Stats, bits_of, check_row, check_rows, oracle_targets
+
+pytestmark = pytest.mark.gpu
+VR, VP = oracle.VREAL, oracle.VPAD
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from rollout_consistent_vocab_gb300.build import build_library
+    build_library()
+    pkg.load_library()
+
+
+def _t(a, dtype):
+    return torch.as_tensor(np.asarray(a), dtype=dtype, device=DEV)
+
+
+def run_pair(x, t, tau, p, k):
+    full, restr, sup = pkg.logp_pair(x, t, tau, p, k)
+    torch.cuda.synchronize()
+    return full.cpu().numpy(), restr.cpu().numpy(), sup.cpu().numpy()
+
+
+def rows_from_bits(rows_bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(rows_bits.view(np.int16).copy()).to(DEV).view(torch.bfloat16)
+
+
+# ------------------------------------------------------------------ golden
+
+def test_golden_tiny16():
+    path = os.path.join(os.path.dirname(__file__), "golden", "tiny16.json")
+    data = json.load(open(path))
+    dec = lambda v: -math.inf if v == "-inf" else float(v)
+    for case in data["cases"]:
+        row = np.full(VP, 0xFF80, dtype=np.uint16)
+        vals = np.asarray(case["values"], dtype=np.float32)
+        row[case["cols"]] = (vals.view(np.uint32) >> 16).astype(np.uint16)
+        targets = [pt[0] for pt in case["per_target"]]
+        x = rows_from_bits(np.stack([row] * len(targets)))
+        f, r, s = run_pair(x, _t(targets, torch.int32), case["tau"], case["top_p"], case["top_k"])
+        for i, (t, full, restr, sup) in enumerate(case["per_target"]):
+            assert f[i] == dec(full) or abs(f[i] - dec(full)) <= TOL, (case["tau"], t)
+            assert r[i] == dec(restr) or abs(r[i] - dec(restr)) <= TOL, (case, t)
+            assert s[i] == sup
+
+
+# ------------------------------------------------------------------ pins on the GPU
+
+def _row(fill, values=None, pad="neginf"):
+    import test_oracle_pins as P
+    return P.make_row(fill, values, pad)
+
+
+def test_pins_uniform_dominant_two_valued():
+    rows = [_row(1.5), _row(-64.0, {77: 64.0}),
+            _row(0.0, {j: 12.0 for j in range(1000, 1000 + 32 * 97, 97)})]
+    x = rows_from_bits(np.stack(rows))
+    t = _t([5, 77, 1000 + 3 * 97], torch.int32)
+    f, r, s = run_pair(x, t, _t([0.7, 1.0, 0.7], torch.float32), _t([0.95, 0.95, 0.95], torch.float32),
+                       _t([-1, -1, -1], torch.int32))
+    assert abs(f[0] - (-math.log(VR))) <= TOL and abs(r[0] - (-math.log(VR))) <= TOL and s[0] == VR
+    assert abs(f[1]) <= TOL and r[1] == 0.0 and s[1] == 1
+    hs = float(np.float32(12.0) / np.float32(0.7))
+    assert abs(f[2] - (-math.log(32 + (VR - 32) * math.exp(-hs)))) <= TOL
+    assert abs(r[2] - (-math.log(32))) <= TOL and s[2] == 32
+    # top-k 50 on the uniform row keeps every tied token
+    f, r, s = run_pair(x[:1], t[:1], 1.3, 0.99, 50)
+    assert s[0] == VR and abs(r[0] + math.log(VR)) <= TOL
+
+
+def test_pins_staircase_and_order():
+    row = _row(-128.0, {j: -float(j) for j in range(64)})
+    x = rows_from_bits(np.stack([row] * 4))
+    t = _t([0, 2, 0, 1], torch.int32)
+    f, r, s = run_pair(x, t, 1.0, _t([0.95, 0.95, 0.7, 0.75], torch.float32),
+                       _t([-1, -1, 2, 2], torch.int32))
+    assert s[0] == 3 and abs(r[0] - (-0.4076059644443804)) <= TOL
+    assert abs(f[0] - (-0.45867514538708193)) <= TOL
+    assert abs(r[1] - (-2 - math.log(1 + math.exp(-1) + math.exp(-2)))) <= TOL
+    assert s[2] == 1 and r[2] == 0.0
+    assert s[3] == 2 and abs(r[3] - (-1 - math.log(1 + math.exp(-1)))) <= TOL
+
+
+def test_pins_topk1_ties_greedy():
+    rng = np.random.default_rng(11)
+    cols = rng.choice(VR, 50, replace=False)
+    vals = {int(j): float(v) for j, v in zip(cols, np.arange(1, 51, dtype=np.float32))}
+    amax = max(vals, key=vals.get)
+    rows = [_row(0.0, vals), _row(0.0, vals),
+            _row(-20.0, {10: 3.0, 11: 2.0, 12: 1.0, 13: 1.0, 14: 1.0, 15: 1.0, 16: 1.0}),
+            _row(0.0, {500: 7.0, 90000: 7.0, 3: 6.0}), _row(0.0, {500: 7.0, 90000: 7.0, 3: 6.0}),
+            _row(0.0, {150000: 9.0, 151935: 9.0})]
+    x = rows_from_bits(np.stack(rows))
+    t = _t([amax, (amax + 1) % VR, 16, 500, 90000, 150000], torch.int32)
+    f, r, s = run_pair(x, t, _t([0.9, 0.9, 1.0, 0.0, 0.0, 0.0], torch.float32),
+                       _t([0.5, 1.0, 1.0, 0.9, 0.9, 1.0], torch.float32),
+                       _t([1, 1, 3, 50, 50, -1], torch.int32))
+    assert r[0] == 0.0 and s[0] == 1 and r[1] == -math.inf
+    assert s[2] == 7 and abs(r[2] - (1 - math.log(math.exp(3) + math.exp(2) + 5 * math.exp(1)))) <= TOL
+    assert f[3] == 0.0 and r[3] == 0.0 and f[4] == -math.inf and r[4] == -math.inf
+    assert f[5] == 0.0 and s[5] == 1
+
+
+def test_padding_is_ignored_and_nonfinite_rows():
+    base = {j: float(j % 13) for j in range(0, VR, 1237)}
+    rows = [_row(-3.0, base, "neginf"), _row(-3.0, base, "garbage")]
+    nan_row = _row(-3.0, base)
+    nan_row[777] = 0x7FC0
+    inf_row = _row(-3.0, base)
+    inf_row[151935] = 0x7F80
+    allneg = _row(float("-inf"))
+    two = _row(float("-inf"), {7: 0.0, 8: 0.0})
+    x = rows_from_bits(np.stack(rows + [nan_row, inf_row, allneg, two, two]))
+    t = _t([1237, 1237, 1237, 1237, 0, 7, 9], torch.int32)
+    f, r, s = run_pair(x, t, 0.9, 0.9, 64)
+    assert f[0] == f[1] and r[0] == r[1] and s[0] == s[1]
+    for i in (2, 3, 4):
+        assert math.isnan(f[i]) and math.isnan(r[i]) and s[i] == -1
+    assert abs(f[5] + math.log(2)) <= TOL and f[6] == -math.inf
+    # greedy on NaN rows is NaN too
+    f, r, s = run_pair(x[2:5], t[2:5], 0.0, 1.0, -1)
+    assert all(math.isnan(v) for v in f) and all(v == -1 for v in s)
+
+
+def test_invalid_per_row_parameters_are_counted():
+    x, hot, n = W.hot_logits(8, 4, 8, seed=5, device=DEV)
+    t = W.structural_targets(8, hot, n, seed=5, device=DEV)
+    t[7] = VR        # out of range target
+    tau = _t([0.7, -1.0, float("nan"), 0.7, 0.7, 0.7, 0.7, 0.7], torch.float32)
+    p = _t([0.9, 0.9, 0.9, 0.0, 1.5, 0.9, 0.9, 0.9], torch.float32)
+    k = _t([-1, -1, -1, -1, -1, 0, VR + 1, -1], torch.int32)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    f, r, s = pkg.logp_pair(x, t, tau, p, k, err_count=err)
+    torch.cuda.synchronize()
+    assert err.item() == 7
+    assert not math.isnan(f[0].item()) and s[0].item() > 0
+    assert torch.isnan(f[1:]).all() and torch.isnan(r[1:]).all() and (s[1:] == -1).all()
+
+
+# ------------------------------------------------------------------ the workloads
+
+def test_c0_spread_all_rows():
+    """64 rows of N(0,3^2), tau 0.7, p 0.95; oracle targets, 4 rows forced outside."""
+    wl = W.workload_c0(device=DEV)
+    bits = bits_of(wl.logits)
+    rng = np.random.default_rng(0)
+    forced = set(rng.choice(wl.T, 4, replace=False).tolist())
+    ones = np.ones(wl.T)
+    targets = oracle_targets(bits, 0.7 * ones, 0.95 * ones, -ones.astype(int), rng, forced)
+    f, r, s = run_pair(wl.logits, _t(targets, torch.int32), 0.7, 0.95, -1)
+    st = Stats()
+    check_rows(st, bits, 0.7 * ones, 0.95 * ones, -ones, targets, f, r, s)
+    assert sum(r[i] == -math.inf for i in forced) == 4
+    print("c0", st)
+
+
+def test_c1_microbatch_sampled_rows():
+    """T = 1024 rows on the GPU; 96 sampled rows checked (oracle targets, 5% forced out)."""
+    wl = W.workload_c1(device=DEV)
+    rng = np.random.default_rng(1)
+    rows = np.sort(rng.choice(wl.T, 96, replace=False))
+    bits = bits_of(wl.logits[torch.as_tensor(rows, device=DEV)])
+    targets = W.structural_targets(wl.T, wl.hot, wl.hot_n, seed=1, device=DEV)
+    forced = set(rng.choice(len(rows), 5, replace=False).tolist())
+    ones = np.ones(len(rows))
+    tsel = oracle_targets(bits, 0.7 * ones, 0.95 * ones, -ones.astype(int), rng, forced)
+    targets[torch.as_tensor(rows, device=DEV)] = _t(tsel, torch.int32)
+    f, r, s = run_pair(wl.logits, targets, 0.7, 0.95, -1)
+    st = Stats()
+    check_rows(st, bits, 0.7 * ones, 0.95 * ones, -ones, tsel, f[rows], r[rows], s[rows])
+    print("c1", st)
+
+
+def test_c2_pair_and_kl_sampled_rows():
+    """T = 8192, tau 1.3, p 0.99, k 128, plus the KL term against perturbed reference logits."""
+    wl = W.workload_c2(device=DEV)
+    T = wl.T
+    targets = W.structural_targets(T, wl.hot, wl.hot_n, seed=2, device=DEV)
+    full, restr, sup, full_ref, kl = pkg.logp_kl(wl.logits, wl.ref_logits, targets, 1.3, 0.99, 128)
+    f2, r2, s2 = pkg.logp_pair(wl.logits, targets, 1.3, 0.99, 128)
+    torch.cuda.synchronize()
+    assert torch.equal(full, f2) and torch.equal(restr.nan_to_num(), r2.nan_to_num()) and torch.equal(sup, s2)
+    assert torch.equal(kl, full - full_ref)
+    rng = np.random.default_rng(2)
+    rows = np.sort(rng.choice(T, 40, replace=False))
+    ridx = torch.as_tensor(rows, device=DEV)
+    bits = bits_of(wl.logits[ridx])
+    rbits = bits_of(wl.ref_logits[ridx])
+    ts = targets[ridx].cpu().numpy()
+    f, r, s = full[ridx].cpu().numpy(), restr[ridx].cpu().numpy(), sup[ridx].cpu().numpy()
+    fr, klv = full_ref[ridx].cpu().numpy(), kl[ridx].cpu().numpy()
+    st = Stats()
+    ones = np.ones(len(rows))
+    check_rows(st, bits, 1.3 * ones, 0.99 * ones, 128 * ones, ts, f, r, s)
+    for n in range(len(rows)):
+        o_ref = oracle.logp_row(rbits[n], 1.3, 1.0, -1, int(ts[n]))
+        o_pol = oracle.logp_row(bits[n], 1.3, 1.0, -1, int(ts[n]))
+        assert abs(fr[n] - o_ref.full) <= TOL
+        assert abs(klv[n] - (o_pol.full - o_ref.full)) <= 2 * TOL
+    assert (s[s >= 0] >= 1).all() and (s <= 128 + 64).all()
+    print("c2", st)
+
+
+def test_c4_mixed_parameters_sampled_rows():
+    """T = 55296 (16.9 GB of logits) with per-row tau/p/k; rows sampled per parameter combo."""
+    wl = W.workload_c4(device=DEV)
+    T = wl.T
+    targets = W.structural_targets(T, wl.hot, wl.hot_n, seed=4, device=DEV)
+    full, restr, sup = pkg.logp_pair(wl.logits, targets, wl.temperature, wl.top_p, wl.top_k)
+    torch.cuda.synchronize()
+    tau, p, k = wl.temperature.cpu().numpy(), wl.top_p.cpu().numpy(), wl.top_k.cpu().numpy()
+    rng = np.random.default_rng(4)
+    rows = []
+    for tv in np.unique(tau):
+        for pv in np.unique(p):
+            for kv in np.unique(k):
+                idx = np.nonzero((tau == tv) & (p == pv) & (k == kv))[0]
+                rows += rng.choice(idx, 3, replace=False).tolist()
+    rows = np.sort(np.asarray(rows))
+    ridx = torch.as_tensor(rows, device=DEV)
+    bits = bits_of(wl.logits[ridx])
+    st = Stats()
+    check_rows(st, bits, tau[rows], p[rows], k[rows], targets[ridx].cpu().numpy(),
+               full[ridx].cpu().numpy(), restr[ridx].cpu().numpy(), sup[ridx].cpu().numpy())
+    print("c4", st)
+    del wl, full, restr, sup
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("T", [1, 7, 300])
+def test_ragged_batches_random_parameters(T):
+    rng = np.random.default_rng(T)
+    x, hot, n = W.hot_logits(T, 1, 300, seed=100 + T, device=DEV)
+    tau = rng.choice([0.0, 0.5, 0.7, 1.0, 1.3, 2.0], T).astype(np.float32)
+    p = rng.choice([0.3, 0.8, 0.9, 0.95, 0.99, 1.0], T).astype(np.float32)
+    k = rng.choice([-1, 1, 5, 50, 128, 256, 257, 1000], T).astype(np.int32)
+    bits = bits_of(x)
+    forced = set(rng.choice(T, max(1, T // 10), replace=False).tolist())
+    tg = oracle_targets(bits, tau, p, k, rng, forced)
+    f, r, s = run_pair(x, _t(tg, torch.int32), _t(tau, torch.float32), _t(p, torch.float32),
+                       _t(k, torch.int32))
+    st = Stats()
+    check_rows(st, bits, tau, p, k, tg, f, r, s)
+    print(T, st)
+
+
+def test_entry_points_agree_bitwise():
+    x, hot, n = W.hot_logits(64, 1, 256, seed=9, device=DEV)
+    t = W.structural_targets(64, hot, n, seed=9, device=DEV)
+    f, r, s = pkg.logp_pair(x, t, 1.3, 0.99, 128)
+    f1 = pkg.logp_full(x, t, 1.3)
+    r1, s1 = pkg.logp_restricted(x, t, 1.3, 0.99, 128)
+    torch.cuda.synchronize()
+    assert torch.equal(f, f1) and torch.equal(r, r1) and torch.equal(s, s1)
+
+
+def test_row_stride_and_buffer_offset():
+    """Rows inside a wider buffer (row stride 152576 + 8j) give the same bits."""
+    x, hot, n = W.hot_logits(33, 1, 64, seed=13, device=DEV)
+    t = W.structural_targets(33, hot, n, seed=13, device=DEV)
+    f0, r0, s0 = pkg.logp_pair(x, t, 0.7, 0.95, -1)
+    for extra in (8, 64, 4096):
+        big = torch.full((33 + 3, VP + extra), float("nan"), dtype=torch.bfloat16, device=DEV)
+        big[3:, :VP] = x
+        f1, r1, s1 = pkg.logp_pair(big[3:], t, 0.7, 0.95, -1)
+        torch.cuda.synchronize()
+        assert torch.equal(f0, f1) and torch.equal(r0, r1) and torch.equal(s0, s1)
+
+
+def test_wide_support_fallback_path():
+    """Supports reaching more than 2048 order keys below the maximum take the
+    global-memory window path; still exact against the oracle."""
+    rng = np.random.default_rng(77)
+    T = 6
+    # logits centred on 0 with small spread: the nucleus crosses zero
+    x = (0.02 * rng.standard_normal((T, VP))).astype(np.float32)
+    x[:, 5] = 3.0
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)
+    bits[:, VR:] = 0xFF80
+    tau = np.array([1.0, 1.0, 0.5, 1.0, 2.0, 1.0], np.float32)
+    p = np.array([0.9, 0.5, 0.99, 1.0, 0.7, 0.99], np.float32)
+    k = np.array([-1, -1, -1, 100000, 70000, 3000], np.int32)
+    forced = {1}
+    tg = oracle_targets(bits, tau, p, k, rng, forced)
+    f, r, s = run_pair(rows_from_bits(bits), _t(tg, torch.int32), _t(tau, torch.float32),
+                       _t(p, torch.float32), _t(k, torch.int32))
+    st = Stats()
+    check_rows(st, bits, tau, p, k, tg, f, r, s)
+    print("fallback", st)
