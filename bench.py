@@ -57,6 +57,26 @@ def dist_env():
     return rank, world, local
 
 
+def rank_seed(base: int, rank: int) -> int:
+    """Seed of a rank's own rows: ranks process disjoint synthetic batches."""
+    return base + 1000 * rank
+
+
+def max_over_ranks(ms: float, device) -> float:
+    """Slowest rank's time (ms); identity when no process group is initialised."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput(world: int, rows: int, steps: int, ms: float) -> float:
+    """Whole-job rows (tokens) per second: all ranks' units over the slowest rank's time."""
+    return world * rows * steps / (ms / 1e3)
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -217,9 +237,9 @@ def run_ours(args, rank, world, local):
         dist.init_process_group("nccl", device_id=dev)
 
     # each rank owns its own 8192 rows (weak scaling)
-    x, hot, n = W.hot_logits(T_ROWS, 1, 256, seed=2 + 1000 * rank, device=dev)
-    ref = W.perturbed_copy(x, 0.05, seed=102 + 1000 * rank)
-    tg = W.structural_targets(T_ROWS, hot, n, seed=2 + 1000 * rank, device=dev)
+    x, hot, n = W.hot_logits(T_ROWS, 1, 256, seed=rank_seed(2, rank), device=dev)
+    ref = W.perturbed_copy(x, 0.05, seed=rank_seed(102, rank))
+    tg = W.structural_targets(T_ROWS, hot, n, seed=rank_seed(2, rank), device=dev)
     del hot, n
     f32 = dict(dtype=torch.float32, device=dev)
     full, restr, kl, full_ref = (torch.empty(T_ROWS, **f32) for _ in range(4))
@@ -256,11 +276,8 @@ def run_ours(args, rank, world, local):
     total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
     pair_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     ref_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
-    value = world * T_ROWS * K / (total_ms / 1e3)
+    total_ms = max_over_ranks(total_ms, dev)
+    value = throughput(world, T_ROWS, K, total_ms)
 
     # ---- end to end through the public API from pinned host buffers
     e2e = None
@@ -296,12 +313,10 @@ def run_ours(args, rank, world, local):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        et = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(et, op=dist.ReduceOp.MAX)
+        et = max_over_ranks(e0.elapsed_time(e1), dev)
         h2d = hx.numel() * 2 + hr.numel() * 2 + ht.numel() * 4
         d2h = 3 * 4 * T_ROWS + 4 * T_ROWS
-        e2e = {"value": world * T_ROWS * args.e2e_steps / (float(et.item()) / 1e3), "unit": UNIT,
+        e2e = {"value": throughput(world, T_ROWS, args.e2e_steps, et), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     cpu = None
