@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", type=int, default=T_ROWS,
+                    help="rows per GPU (default: the 8192-row workload; smaller only for profiling)")
     return ap.parse_args()
 
 
@@ -224,6 +226,8 @@ def workload_config():
 # ------------------------------------------------------------------ ours
 
 def run_ours(args, rank, world, local):
+    global T_ROWS
+    T_ROWS = args.rows
     import numpy as np
     import torch
     import torch.distributed as dist
