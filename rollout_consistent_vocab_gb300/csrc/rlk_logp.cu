@@ -58,7 +58,8 @@ constexpr int SHARD_CHUNKS = SW / 8;                        // 2384 16-byte chun
 constexpr int LAST_CHUNKS = (VREAL - (NSHARD - 1) * SW) / 8;  // 2304 real chunks
 constexpr int NTHR = 256;
 constexpr int NWARP = NTHR / 32;
-constexpr int WIN = 2048;            // histogram window, in bf16 order keys
+constexpr int MAXCH = (SHARD_CHUNKS + NTHR - 1) / NTHR;     // chunks per thread (9 or 10)
+constexpr int WIN = 1024;            // candidate window, in bf16 order keys (8 binades)
 constexpr int TMA_PIECES = 4;
 constexpr float LOG2E = 1.4426950408889634f;   // log2(e)
 constexpr float FX_SCALE = 17592186044416.0f;  // 2^44: fixed-point scale of masses
@@ -67,22 +68,30 @@ constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
 static_assert(SW % 8 == 0 && (VREAL - (NSHARD - 1) * SW) % 8 == 0, "chunking");
 static_assert(SHARD_CHUNKS % TMA_PIECES == 0 && LAST_CHUNKS % TMA_PIECES == 0, "pieces");
 
-enum : uint32_t { FLAG_TIMEOUT = 1u };
+enum : uint32_t { FLAG_TIMEOUT = 1u, FLAG_NAN = 2u };
+constexpr int KEY_NEG_INF = 0x007F;   // order key of -inf
 
-struct __align__(16) Summary {
-  float xm;        // shard maximum (a bf16 value, or -inf / +inf / NaN)
-  float l;         // sum over the shard of exp(s_j - m_r)
-  int32_t first;   // greedy: first column holding the shard maximum
-  int32_t lo;      // histogram window [lo, hi] in order keys (lo > hi: empty)
-  int32_t hi;
+// Exchanged by every CTA with every CTA before the candidate pass.
+struct __align__(16) MidSlot {
+  float xm;        // shard maximum (a bf16 value or -inf / +inf)
+  int32_t lkey;    // order key that at least ceil(k/8) of the shard's thread maxima reach (0: none)
   uint32_t flags;
-  int32_t pad0, pad1;
+  int32_t pad;
+};
+
+// Sent by every CTA to the leader at the end.
+struct __align__(16) Summary {
+  float xm;        // shard maximum
+  float l;         // sum over the shard of exp(s_j - m_r) (NaN if the shard holds a NaN)
+  int32_t first;   // greedy: first column holding the shard maximum
+  uint32_t flags;
 };
 
 struct __align__(128) Smem {
-  uint4 shard[SHARD_CHUNKS];       // 38144 B; the leader reuses it as scratch
-  uint32_t hist[WIN / 2];          // u16 counts, two per word
-  Summary slot[NSHARD];            // written by every CTA into the leader's copy
+  uint4 shard[SHARD_CHUNKS];       // 38144 B; the leader reuses it as scratch at the end
+  uint32_t merged[WIN];            // leader: per-key candidate counts of the whole row
+  MidSlot mid[NSHARD];
+  Summary slot[NSHARD];
   float red_f[NWARP];
   int32_t red_i[NWARP];
   uint32_t scan_c[NWARP];
@@ -134,14 +143,12 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
 __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};"
                :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ void red_cluster_add(uint32_t addr, uint32_t v) {
+  asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ unsigned long long global_timer() {
   unsigned long long t;
@@ -150,7 +157,7 @@ __device__ __forceinline__ unsigned long long global_timer() {
 }
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  // make the initialised barrier visible to the bulk-copy (async) proxy
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
@@ -237,9 +244,6 @@ __device__ __forceinline__ int okey_floor(float x) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__device__ __forceinline__ float fmax_nan(float a, float b) {
-  return (a != a) ? a : ((b != b) ? b : fmaxf(a, b));
-}
 __device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t w) {
   return *reinterpret_cast<__nv_bfloat162*>(&w);
 }
@@ -252,15 +256,15 @@ __device__ __forceinline__ unsigned long long qfx(float v, float M, float c) {
 
 // ------------------------------------------------------------ block helpers
 
-__device__ __forceinline__ float block_max_nan(float v, Smem& S) {
+__device__ __forceinline__ float block_max(float v, Smem& S) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmax_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   if (lane == 0) S.red_f[warp] = v;
   __syncthreads();
   float r = S.red_f[0];
 #pragma unroll
-  for (int w = 1; w < NWARP; ++w) r = fmax_nan(r, S.red_f[w]);
+  for (int w = 1; w < NWARP; ++w) r = fmaxf(r, S.red_f[w]);
   __syncthreads();
   return r;
 }
@@ -322,10 +326,11 @@ __device__ __forceinline__ void block_excl_scan(uint32_t c, unsigned long long m
   __syncthreads();
 }
 
-// k-th largest of the block's 256 per-thread keys (k <= 256), by bisection
-// on the 16-bit key with block-wide predicate counts.
-__device__ __forceinline__ int kth_largest_key(int mykey, int k, int hi_key) {
-  int lo = 0, hi = hi_key;
+// Largest key in [lo_key, hi_key] that at least k of the block's per-thread
+// keys reach (the caller ensures lo_key qualifies), by bisection with
+// block-wide predicate counts.
+__device__ __forceinline__ int kth_largest_key(int mykey, int k, int lo_key, int hi_key) {
+  int lo = lo_key, hi = hi_key;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     const int n = __syncthreads_count(mykey >= mid);
@@ -534,9 +539,9 @@ logp_kernel(const KParams P) {
 #pragma unroll
     for (int i = 0; i < TMA_PIECES; ++i) bulk_load(dst + i * piece, src + i * piece, piece, bar, pol);
   }
-  cluster_arrive_relaxed();   // every CTA of the cluster has started
-  if (sel)
-    for (int i = tid; i < WIN / 2; i += NTHR) S.hist[i] = 0u;
+  if (sel && r == 0)
+    for (int i = tid; i < WIN; i += NTHR) S.merged[i] = 0u;
+  cluster_arrive_relaxed();   // S0: every CTA of the cluster has started
   __syncthreads();
   uint32_t flags = 0;
   if (!mbar_wait_bounded(bar, 0)) {
@@ -544,39 +549,71 @@ logp_kernel(const KParams P) {
     mbar_wait_bounded(bar, 0);   // give copies in flight a second bounded chance to land
   }
 
-  // ---- 2. shard maximum (NaN-propagating so NaN rows are detected)
+  // ---- 2. shard maximum; per-chunk maxima stay in registers for the candidate pass.
+  // bf16 max ignores NaN; a NaN shows up as a NaN sum-exp (or in the scans below).
   const uint4* sh = S.shard;
-  __nv_bfloat162 m2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
-  for (int ch = tid; ch < nchunks; ch += NTHR) {
-    const uint4 v = sh[ch];
-    m2 = __hmax2_nan(m2, __hmax2_nan(__hmax2_nan(as_bf2(v.x), as_bf2(v.y)),
-                                     __hmax2_nan(as_bf2(v.z), as_bf2(v.w))));
+  const __nv_bfloat162 ninf2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+  __nv_bfloat162 cm[MAXCH];
+  __nv_bfloat162 m2 = ninf2;
+#pragma unroll
+  for (int i = 0; i < MAXCH; ++i) {
+    const int ch = tid + i * NTHR;
+    cm[i] = ninf2;
+    if (ch < nchunks) {
+      const uint4 v = sh[ch];
+      cm[i] = __hmax2(__hmax2(as_bf2(v.x), as_bf2(v.y)), __hmax2(as_bf2(v.z), as_bf2(v.w)));
+      m2 = __hmax2(m2, cm[i]);
+    }
   }
-  const float tmax = fmax_nan(__low2float(m2), __high2float(m2));
-  const float xm = block_max_nan(tmax, S);
+  const float tmax = fmaxf(__low2float(m2), __high2float(m2));
+  const float xm = block_max(tmax, S);
   const bool xm_finite = (xm > -INFINITY) && (xm < INFINITY);
 
-  float l = 0.0f;
   int first = 0x7fffffff;
-  int lo_r = 1, hi_r = 0;   // empty window
-  if (greedy) {
-    // ---- greedy: first column of this shard holding its maximum
-    if (xm == xm) {
-      for (int ch = tid; ch < nchunks && first == 0x7fffffff; ch += NTHR) {
-        const uint4 v = sh[ch];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  if (greedy || xm == -INFINITY) {
+    // greedy: first column of this shard holding its maximum; both cases: NaN scan
+    bool nan_seen = false;
+    for (int ch = tid; ch < nchunks; ch += NTHR) {
+      const uint4 v = sh[ch];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 7; j >= 0; --j) {
-          const float x = (j & 1) ? bf16_hi(w[j >> 1]) : bf16_lo(w[j >> 1]);
-          if (x == xm) first = ch * 8 + j;
-        }
+      for (int j = 7; j >= 0; --j) {
+        const float x = (j & 1) ? bf16_hi(w[j >> 1]) : bf16_lo(w[j >> 1]);
+        nan_seen |= (x != x);
+        if (x == xm) first = min(first, ch * 8 + j);
       }
     }
-    first = block_min_int(first, S);
-    if (first != 0x7fffffff) first += static_cast<int>(r) * SW;
-  } else if (xm_finite) {
-    // ---- 3. shard sum-exp, fixed tree
-    const float c = __fdiv_rn(LOG2E, tau);
+    if (__syncthreads_or(nan_seen)) flags |= FLAG_NAN;
+    if (greedy) {
+      first = block_min_int(first, S);
+      if (first != 0x7fffffff) first += static_cast<int>(r) * SW;
+    }
+  }
+
+  // ---- pooled top-k bound: every CTA certifies ceil(k/8) thread maxima at or above
+  // its lkey, so at least k real tokens reach min over CTAs of lkey.
+  int lkey = 0;
+  const int kj = (k + NSHARD - 1) / NSHARD;
+  if (sel && k_on && xm_finite && kj <= NTHR) {
+    const int hi_r = okey_of(xm);
+    const int lo_s = max(0, hi_r - (WIN - 1));
+    const int mykey = okey_of(tmax);
+    if (__syncthreads_count(mykey >= lo_s) >= kj) lkey = kth_largest_key(mykey, kj, lo_s, hi_r);
+  }
+
+  cluster_wait();              // S0 complete: peers' shared memory may be written
+  if (sel) {
+    if (tid < NSHARD)
+      st_cluster_v4(map_rank(smem_addr(&S.mid[r]), tid),
+                    make_uint4(__float_as_uint(xm), static_cast<uint32_t>(lkey), flags, 0u));
+    cluster_arrive();          // MID
+  }
+
+  // ---- 3. shard sum-exp, fixed tree
+  float l = 0.0f;
+  float c = 0.0f;
+  if (!greedy && xm_finite) {
+    c = __fdiv_rn(LOG2E, tau);
     const uint64_t nxm2 = pack2(-xm, -xm);
     const uint64_t c2 = pack2(c, c);
     uint64_t acc = pack2(0.0f, 0.0f);
@@ -594,80 +631,84 @@ logp_kernel(const KParams P) {
     float e0, e1;
     unpack2(acc, e0, e1);
     l = block_sum_fixed(e0 + e1, S);
+  }
 
-    // ---- 4. candidate window and exact per-key counts
-    if (sel) {
-      hi_r = okey_of(xm);
-      int lo = max(0, hi_r - (WIN - 1));
+  // ---- 4. candidate pass: exact per-key counts into the leader's histogram
+  int hi = 0, lo = 1;
+  float M = xm;
+  if (sel) {
+    cluster_wait();            // MID complete: all shard maxima and bounds are here
+    int L = 0x7fffffff;
+    M = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < NSHARD; ++q) {
+      M = fmaxf(M, S.mid[q].xm);
+      L = min(L, S.mid[q].lkey);
+    }
+    if (M > -INFINITY && M < INFINITY) {
+      hi = okey_of(M);
+      lo = max(0, hi - (WIN - 1));
       if (k_on) {
-        if (k <= NTHR) lo = max(lo, kth_largest_key(okey_of(tmax), k, hi_r));
+        lo = max(lo, L);
       } else {
-        // Elements below s_max + ln((1-p)/V) cannot reach the nucleus: even
-        // V of them hold less than (1-p) of the total mass.  Slack keeps the
+        // Tokens below s_max + ln((1-p)/V) cannot reach the nucleus: even all V
+        // of them would hold less than 1-p of the total mass.  The slack keeps the
         // float evaluation on the safe side.
         const float width = tau * (logf(static_cast<float>(VREAL) / (1.0f - p)) * 1.0001f + 1e-3f);
-        lo = max(lo, okey_floor(xm - width));
+        lo = max(lo, okey_floor(M - width));
       }
-      lo_r = lo;
-      const float vlo = key_value(lo_r);
-      for (int ch = tid; ch < nchunks; ch += NTHR) {
-        const uint4 v = sh[ch];
-        const __nv_bfloat162 mm = __hmax2(__hmax2(as_bf2(v.x), as_bf2(v.y)),
-                                          __hmax2(as_bf2(v.z), as_bf2(v.w)));
-        if (fmaxf(__low2float(mm), __high2float(mm)) >= vlo) {
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      lo = max(lo, KEY_NEG_INF);   // keys below that of -inf are NaN patterns
+    }
+    if (xm_finite && lo <= hi && okey_of(xm) >= lo) {
+      const float vlo_f = key_value(lo);
+      const __nv_bfloat162 vlo2 = __floats2bfloat162_rn(vlo_f, vlo_f);
+      const uint32_t dst = map_rank(smem_addr(S.merged), 0);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t b = (w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
-            if (__uint_as_float(b << 16) >= vlo) {
-              const int idx = hi_r - okey(b);
-              atomicAdd(&S.hist[idx >> 1], 1u << ((idx & 1) * 16));
-            }
+      for (int i = 0; i < MAXCH; ++i) {
+        const int ch = tid + i * NTHR;
+        if (ch < nchunks && __hge2_mask(cm[i], vlo2) != 0u) {
+          const uint4 v = sh[ch];
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          uint32_t bits = 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) bits |= (__hge2_mask(as_bf2(w[j]), vlo2) & 0x00010001u) << j;
+          while (bits) {
+            const int pos = __ffs(bits) - 1;
+            bits &= bits - 1;
+            const int j = pos & 3;
+            const uint32_t wj = (j == 0) ? w[0] : (j == 1) ? w[1] : (j == 2) ? w[2] : w[3];
+            const uint32_t b = (pos & 16) ? (wj >> 16) : (wj & 0xFFFFu);
+            red_cluster_add(dst + 4u * static_cast<uint32_t>(hi - okey(b)), 1u);
           }
         }
       }
     }
   }
 
-  // ---- 5. publish the summary into the leader's shared memory
-  cluster_wait();             // pairs with the relaxed arrive above
-  if (tid == 0) {
-    const uint32_t dst = map_rank(smem_addr(&S.slot[r]), 0);
-    st_cluster_v4(dst, make_uint4(__float_as_uint(xm), __float_as_uint(l),
-                                  static_cast<uint32_t>(first), static_cast<uint32_t>(lo_r)));
-    st_cluster_v4(dst + 16, make_uint4(static_cast<uint32_t>(hi_r), flags, 0u, 0u));
-  }
-  cluster_arrive();
+  // ---- 5. summary to the leader
+  if (tid == 0)
+    st_cluster_v4(map_rank(smem_addr(&S.slot[r]), 0),
+                  make_uint4(__float_as_uint(xm), __float_as_uint(l), static_cast<uint32_t>(first), flags));
+  cluster_arrive();            // A
+  if (r != 0) return;          // nobody reads this CTA's shared memory any more
   cluster_wait();
 
-  if (r != 0) {
-    if (sel) {                // keep the histogram alive until the leader has read it
-      cluster_arrive();
-      cluster_wait();
-    }
-    return;
-  }
-
   // ================= leader: merge in fixed shard order =================
-  float M = -INFINITY;
   bool bad = false;
+  bool timed_out = false;
+  M = -INFINITY;
 #pragma unroll
   for (int q = 0; q < NSHARD; ++q) {
-    const float v = S.slot[q].xm;
-    if (!(v == v) || v == INFINITY || (S.slot[q].flags & FLAG_TIMEOUT)) bad = true;
-    M = fmaxf(M, v);
+    const Summary& s = S.slot[q];
+    if (s.flags & FLAG_TIMEOUT) timed_out = true;
+    if ((s.flags & FLAG_NAN) || s.xm == INFINITY || s.l != s.l) bad = true;
+    M = fmaxf(M, s.xm);
   }
-  if (!(M > -INFINITY)) bad = true;
-  const bool timed_out = [&] {
-    bool f = false;
-#pragma unroll
-    for (int q = 0; q < NSHARD; ++q) f |= (S.slot[q].flags & FLAG_TIMEOUT) != 0;
-    return f;
-  }();
+  bad |= timed_out || !(M > -INFINITY);
   const float qnan = __int_as_float(0x7fc00000);
   float full = qnan, restr = qnan;
   int support = -1;
-  float c = 0.0f, Z = 0.0f, d = 0.0f;
+  float Z = 0.0f, d = 0.0f;
   if (!bad && greedy) {
     int amax = 0x7fffffff;
 #pragma unroll
@@ -692,44 +733,14 @@ logp_kernel(const KParams P) {
       support = VREAL;
     }
   }
-
-  if (sel) {
-    uint32_t* cnt0 = reinterpret_cast<uint32_t*>(S.shard);
-    uint32_t* cntB = cnt0 + WIN;
-    int hi = 0, lo = 0;
-    if (!bad) {
-      hi = okey_of(M);
-#pragma unroll
-      for (int q = 0; q < NSHARD; ++q)
-        if (S.slot[q].xm > -INFINITY) lo = max(lo, S.slot[q].lo);
-      const int n = hi - lo + 1;
-      const uint32_t hist_base = smem_addr(S.hist);
-      for (int i = tid; i < n; i += NTHR) {
-        const int K = hi - i;
-        uint32_t sum = 0;
-#pragma unroll
-        for (int q = 0; q < NSHARD; ++q) {
-          const Summary& s = S.slot[q];
-          if (s.xm > -INFINITY && K >= s.lo && K <= s.hi) {
-            const int idx = s.hi - K;
-            const uint32_t wv = ld_cluster_u32(map_rank(hist_base + 4u * (idx >> 1), q));
-            sum += (wv >> ((idx & 1) * 16)) & 0xFFFFu;
-          }
-        }
-        cnt0[i] = sum;
-      }
-    }
-    __syncthreads();
-    cluster_arrive();          // the other CTAs may now exit
-    if (!bad) {
-      const SelResult sr = select_support(S, cnt0, cntB, hi, lo, rowp, M, c, Z, p, k, k_on, p_on);
-      const float xt = __uint_as_float(static_cast<uint32_t>(__ldg(rowp + t)) << 16);
-      const bool in_s = okey_of(xt) >= sr.min_key;
-      const float zs = static_cast<float>(static_cast<double>(sr.zs) * (1.0 / 17592186044416.0));
-      restr = in_s ? d - logf(zs) : -INFINITY;
-      support = static_cast<int>(sr.support);
-    }
-    cluster_wait();
+  if (sel && !bad) {
+    uint32_t* cntB = reinterpret_cast<uint32_t*>(S.shard);
+    const SelResult sr = select_support(S, S.merged, cntB, hi, lo, rowp, M, c, Z, p, k, k_on, p_on);
+    const float xt = __uint_as_float(static_cast<uint32_t>(__ldg(rowp + t)) << 16);
+    const bool in_s = okey_of(xt) >= sr.min_key;
+    const float zs = static_cast<float>(static_cast<double>(sr.zs) * (1.0 / 17592186044416.0));
+    restr = in_s ? d - logf(zs) : -INFINITY;
+    support = static_cast<int>(sr.support);
   }
 
   if (tid == 0) {
