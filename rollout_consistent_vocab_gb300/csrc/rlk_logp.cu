@@ -74,7 +74,7 @@ constexpr int KEY_NEG_INF = 0x007F;   // order key of -inf
 // Exchanged by every CTA with every CTA before the candidate pass.
 struct __align__(16) MidSlot {
   float xm;        // shard maximum (a bf16 value or -inf / +inf)
-  int32_t lkey;    // order key that at least ceil(k/8) of the shard's thread maxima reach (0: none)
+  int32_t lkey;    // order key reached by ceil(k/64) lane maxima of every warp of the shard (0: none)
   uint32_t flags;
   int32_t pad;
 };
@@ -90,6 +90,7 @@ struct __align__(16) Summary {
 struct __align__(128) Smem {
   uint4 shard[SHARD_CHUNKS];       // 38144 B; the leader reuses it as scratch at the end
   uint32_t merged[WIN];            // leader: per-key candidate counts of the whole row
+  uint32_t hist[WIN / 2];          // this shard's per-key candidate counts (u16 pairs)
   MidSlot mid[NSHARD];
   Summary slot[NSHARD];
   float red_f[NWARP];
@@ -256,17 +257,39 @@ __device__ __forceinline__ unsigned long long qfx(float v, float M, float c) {
 
 // ------------------------------------------------------------ block helpers
 
-__device__ __forceinline__ float block_max(float v, Smem& S) {
+// Block maximum of v and block minimum of a per-warp value iw (equal on all
+// lanes of a warp), in one round through shared memory.
+__device__ __forceinline__ float block_max_min(float v, int iw, int& imin, Smem& S) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  if (lane == 0) S.red_f[warp] = v;
+  if (lane == 0) { S.red_f[warp] = v; S.red_i[warp] = iw; }
   __syncthreads();
   float r = S.red_f[0];
+  int m = S.red_i[0];
 #pragma unroll
-  for (int w = 1; w < NWARP; ++w) r = fmaxf(r, S.red_f[w]);
+  for (int w = 1; w < NWARP; ++w) { r = fmaxf(r, S.red_f[w]); m = min(m, S.red_i[w]); }
   __syncthreads();
+  imin = m;
   return r;
+}
+
+// j-th largest (1 <= j <= 32) of the warp's 32 keys, on every lane: a
+// bitonic sort over the lanes (ascending), then a broadcast.
+__device__ __forceinline__ int warp_kth_largest(int key, int j) {
+  const int lane = threadIdx.x & 31;
+  int v = key;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const int other = __shfl_xor_sync(0xffffffffu, v, stride);
+      const bool ascending = (lane & size) == 0;
+      const bool lower = (lane & stride) == 0;
+      v = (lower == ascending) ? min(v, other) : max(v, other);
+    }
+  }
+  return __shfl_sync(0xffffffffu, v, 32 - j);
 }
 
 // Fixed-order sum: butterfly inside each warp, then a left fold over warps.
@@ -326,19 +349,6 @@ __device__ __forceinline__ void block_excl_scan(uint32_t c, unsigned long long m
   __syncthreads();
 }
 
-// Largest key in [lo_key, hi_key] that at least k of the block's per-thread
-// keys reach (the caller ensures lo_key qualifies), by bisection with
-// block-wide predicate counts.
-__device__ __forceinline__ int kth_largest_key(int mykey, int k, int lo_key, int hi_key) {
-  int lo = lo_key, hi = hi_key;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    const int n = __syncthreads_count(mykey >= mid);
-    if (n >= k) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 // ------------------------------------------------------------ leader: selection
 
 // Count the row's real elements whose key lies in [wlo, whi] (global memory
@@ -394,7 +404,7 @@ __device__ __forceinline__ WinScan scan_window(const uint32_t* cnt, int n, int w
 // mass (fixed point) and the lowest kept key.
 struct SelResult { uint32_t support; unsigned long long zs; int min_key; };
 
-__device__ SelResult select_support(Smem& S, uint32_t* cnt0, uint32_t* cntB, int hi, int lo,
+__device__ __noinline__ SelResult select_support(Smem& S, uint32_t* cnt0, uint32_t* cntB, int hi, int lo,
                                     const uint16_t* rowp, float M, float c, float Z, float p,
                                     int k, bool k_on, bool p_on) {
   const int tid = threadIdx.x;
@@ -490,6 +500,91 @@ __device__ SelResult select_support(Smem& S, uint32_t* cnt0, uint32_t* cntB, int
   }
 }
 
+// Selection when the first window holds every threshold (the common case):
+// one block scan of (count, mass) over the keys hi, hi-1, ..., lo, then the
+// top-k boundary and the nucleus boundary are read off it.  Returns false if
+// a threshold may lie below the window; select_support then takes over.
+__device__ bool select_fast(Smem& S, const uint32_t* cnt, int hi, int lo, float M, float c, float Z,
+                            float p, int k, bool k_on, bool p_on, SelResult& out) {
+  constexpr int PER = WIN / NTHR;
+  const int n = hi - lo + 1;
+  const int per = (n + NTHR - 1) / NTHR;
+  const int i0 = min(n, static_cast<int>(threadIdx.x) * per);
+  const int i1 = min(n, i0 + per);
+  uint32_t ci[PER];
+  uint32_t lc = 0;
+  unsigned long long lm = 0;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int i = i0 + q;
+    ci[q] = (i < i1) ? cnt[i] : 0u;
+    if (ci[q]) { lc += ci[q]; lm += ci[q] * qfx(key_value(hi - i), M, c); }
+  }
+  if (threadIdx.x == 0) S.found_i = -1;
+  uint32_t bc, tc;
+  unsigned long long bm, tm;
+  block_excl_scan(lc, lm, bc, bm, tc, tm, S);
+
+  int imax = n - 1;
+  unsigned long long zk = __float2ull_rn(Z * FX_SCALE);
+  if (k_on) {
+    uint32_t rc = bc;
+    unsigned long long rm = bm;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int i = i0 + q;
+      if (ci[q]) {
+        const unsigned long long m = ci[q] * qfx(key_value(hi - i), M, c);
+        if (rc < static_cast<uint32_t>(k) && rc + ci[q] >= static_cast<uint32_t>(k)) {
+          S.found_i = i;
+          S.found_c = rc + ci[q];
+          S.found_m = rm + m;
+        }
+        rc += ci[q];
+        rm += m;
+      }
+    }
+    __syncthreads();
+    const int ik = S.found_i;
+    if (ik < 0) return false;                  // k-th value below the window
+    imax = ik;
+    zk = S.found_m;
+    const uint32_t sup_k = S.found_c;
+    __syncthreads();
+    if (!p_on) {
+      out = SelResult{sup_k, zk, hi - ik};
+      return true;
+    }
+    if (threadIdx.x == 0) S.found_i = -1;
+    __syncthreads();
+  }
+  // nucleus inside S_k: keep key i iff the mass strictly above it is < p * Z_k
+  const double T = static_cast<double>(p) * static_cast<double>(zk);
+  {
+    uint32_t rc = bc;
+    unsigned long long rm = bm;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int i = i0 + q;
+      const unsigned long long m = ci[q] ? ci[q] * qfx(key_value(hi - i), M, c) : 0ull;
+      if (i < i1 && i <= imax && static_cast<double>(rm) < T &&
+          (static_cast<double>(rm + m) >= T || (i == imax && k_on))) {
+        S.found_i = i;
+        S.found_c = rc + ci[q];
+        S.found_m = rm + m;
+      }
+      rc += ci[q];
+      rm += m;
+    }
+  }
+  __syncthreads();
+  const int ip = S.found_i;
+  if (ip < 0) return false;                    // nucleus reaches below the window
+  out = SelResult{S.found_c, S.found_m, hi - ip};
+  __syncthreads();
+  return true;
+}
+
 // ------------------------------------------------------------ the kernel
 
 template <bool RESTR>
@@ -539,8 +634,11 @@ logp_kernel(const KParams P) {
 #pragma unroll
     for (int i = 0; i < TMA_PIECES; ++i) bulk_load(dst + i * piece, src + i * piece, piece, bar, pol);
   }
-  if (sel && r == 0)
-    for (int i = tid; i < WIN; i += NTHR) S.merged[i] = 0u;
+  if (sel) {
+    if (r == 0)
+      for (int i = tid; i < WIN; i += NTHR) S.merged[i] = 0u;
+    for (int i = tid; i < WIN / 2; i += NTHR) S.hist[i] = 0u;
+  }
   cluster_arrive_relaxed();   // S0: every CTA of the cluster has started
   __syncthreads();
   uint32_t flags = 0;
@@ -553,20 +651,28 @@ logp_kernel(const KParams P) {
   // bf16 max ignores NaN; a NaN shows up as a NaN sum-exp (or in the scans below).
   const uint4* sh = S.shard;
   const __nv_bfloat162 ninf2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
-  __nv_bfloat162 cm[MAXCH];
+  __nv_bfloat162 cm[MAXCH - 1];   // the last chunk (threads < 80 only) is recomputed later
   __nv_bfloat162 m2 = ninf2;
 #pragma unroll
   for (int i = 0; i < MAXCH; ++i) {
     const int ch = tid + i * NTHR;
-    cm[i] = ninf2;
+    __nv_bfloat162 cmax = ninf2;
     if (ch < nchunks) {
       const uint4 v = sh[ch];
-      cm[i] = __hmax2(__hmax2(as_bf2(v.x), as_bf2(v.y)), __hmax2(as_bf2(v.z), as_bf2(v.w)));
-      m2 = __hmax2(m2, cm[i]);
+      cmax = __hmax2(__hmax2(as_bf2(v.x), as_bf2(v.y)), __hmax2(as_bf2(v.z), as_bf2(v.w)));
+      m2 = __hmax2(m2, cmax);
     }
+    if (i < MAXCH - 1) cm[i] = cmax;
   }
   const float tmax = fmaxf(__low2float(m2), __high2float(m2));
-  const float xm = block_max(tmax, S);
+  // Pooled top-k bound: warp w certifies kw = ceil(k/64) lane maxima at or above
+  // lw (its kw-th largest lane maximum), so the 64 warps of the row certify
+  // 64*kw >= k tokens at or above the minimum of lw over the cluster.
+  const int kw = (k + 63) / 64;
+  const bool k_bound = sel && k_on && kw <= 32;
+  const int lw = k_bound ? warp_kth_largest(okey_of(tmax), kw) : 0;
+  int lkey;
+  const float xm = block_max_min(tmax, lw, lkey, S);
   const bool xm_finite = (xm > -INFINITY) && (xm < INFINITY);
 
   int first = 0x7fffffff;
@@ -588,17 +694,6 @@ logp_kernel(const KParams P) {
       first = block_min_int(first, S);
       if (first != 0x7fffffff) first += static_cast<int>(r) * SW;
     }
-  }
-
-  // ---- pooled top-k bound: every CTA certifies ceil(k/8) thread maxima at or above
-  // its lkey, so at least k real tokens reach min over CTAs of lkey.
-  int lkey = 0;
-  const int kj = (k + NSHARD - 1) / NSHARD;
-  if (sel && k_on && xm_finite && kj <= NTHR) {
-    const int hi_r = okey_of(xm);
-    const int lo_s = max(0, hi_r - (WIN - 1));
-    const int mykey = okey_of(tmax);
-    if (__syncthreads_count(mykey >= lo_s) >= kj) lkey = kth_largest_key(mykey, kj, lo_s, hi_r);
   }
 
   cluster_wait();              // S0 complete: peers' shared memory may be written
@@ -662,11 +757,18 @@ logp_kernel(const KParams P) {
     if (xm_finite && lo <= hi && okey_of(xm) >= lo) {
       const float vlo_f = key_value(lo);
       const __nv_bfloat162 vlo2 = __floats2bfloat162_rn(vlo_f, vlo_f);
-      const uint32_t dst = map_rank(smem_addr(S.merged), 0);
 #pragma unroll
       for (int i = 0; i < MAXCH; ++i) {
         const int ch = tid + i * NTHR;
-        if (ch < nchunks && __hge2_mask(cm[i], vlo2) != 0u) {
+        if (ch >= nchunks) continue;
+        __nv_bfloat162 cmax;
+        if (i < MAXCH - 1) {
+          cmax = cm[i];
+        } else {
+          const uint4 v = sh[ch];
+          cmax = __hmax2(__hmax2(as_bf2(v.x), as_bf2(v.y)), __hmax2(as_bf2(v.z), as_bf2(v.w)));
+        }
+        if (__hge2_mask(cmax, vlo2) != 0u) {
           const uint4 v = sh[ch];
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
           uint32_t bits = 0;
@@ -678,10 +780,20 @@ logp_kernel(const KParams P) {
             const int j = pos & 3;
             const uint32_t wj = (j == 0) ? w[0] : (j == 1) ? w[1] : (j == 2) ? w[2] : w[3];
             const uint32_t b = (pos & 16) ? (wj >> 16) : (wj & 0xFFFFu);
-            red_cluster_add(dst + 4u * static_cast<uint32_t>(hi - okey(b)), 1u);
+            const int idx = hi - okey(b);
+            atomicAdd(&S.hist[idx >> 1], 1u << ((idx & 1) * 16));
           }
         }
       }
+    }
+    __syncthreads();
+    // push this shard's nonzero counts into the leader's histogram
+    const uint32_t dst = map_rank(smem_addr(S.merged), 0);
+    const int nwords = (hi - lo + 2) >> 1;
+    for (int i = tid; i < nwords; i += NTHR) {
+      const uint32_t w = S.hist[i];
+      if (w & 0xFFFFu) red_cluster_add(dst + 8u * i, w & 0xFFFFu);
+      if (w >> 16) red_cluster_add(dst + 8u * i + 4u, w >> 16);
     }
   }
 
@@ -735,7 +847,9 @@ logp_kernel(const KParams P) {
   }
   if (sel && !bad) {
     uint32_t* cntB = reinterpret_cast<uint32_t*>(S.shard);
-    const SelResult sr = select_support(S, S.merged, cntB, hi, lo, rowp, M, c, Z, p, k, k_on, p_on);
+    SelResult sr;
+    if (!select_fast(S, S.merged, hi, lo, M, c, Z, p, k, k_on, p_on, sr))
+      sr = select_support(S, S.merged, cntB, hi, lo, rowp, M, c, Z, p, k, k_on, p_on);
     const float xt = __uint_as_float(static_cast<uint32_t>(__ldg(rowp + t)) << 16);
     const bool in_s = okey_of(xt) >= sr.min_key;
     const float zs = static_cast<float>(static_cast<double>(sr.zs) * (1.0 / 17592186044416.0));
