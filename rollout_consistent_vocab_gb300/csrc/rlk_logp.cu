@@ -63,18 +63,19 @@ constexpr int WIN = 1024;            // candidate window, in bf16 order keys (8 
 constexpr int TMA_PIECES = 4;
 constexpr float LOG2E = 1.4426950408889634f;   // log2(e)
 constexpr float FX_SCALE = 17592186044416.0f;  // 2^44: fixed-point scale of masses
-constexpr unsigned long long TIMEOUT_NS = 2000000000ull;
+constexpr double FX_INV = 1.0 / 17592186044416.0;
+constexpr unsigned long long TIMEOUT_NS = 200000000ull;   // 0.2 s bound on every wait
+constexpr int KEY_NEG_INF = 0x007F;  // order key of -inf; smaller keys are NaN patterns
 
 static_assert(SW % 8 == 0 && (VREAL - (NSHARD - 1) * SW) % 8 == 0, "chunking");
 static_assert(SHARD_CHUNKS % TMA_PIECES == 0 && LAST_CHUNKS % TMA_PIECES == 0, "pieces");
 
 enum : uint32_t { FLAG_TIMEOUT = 1u, FLAG_NAN = 2u };
-constexpr int KEY_NEG_INF = 0x007F;   // order key of -inf
 
-// Exchanged by every CTA with every CTA before the candidate pass.
+// Sent by every CTA to every CTA before the candidate pass.
 struct __align__(16) MidSlot {
   float xm;        // shard maximum (a bf16 value or -inf / +inf)
-  int32_t lkey;    // order key reached by ceil(k/64) lane maxima of every warp of the shard (0: none)
+  int32_t lkey;    // order key reached by ceil(k/64) lane maxima of every warp of the shard
   uint32_t flags;
   int32_t pad;
 };
@@ -83,7 +84,7 @@ struct __align__(16) MidSlot {
 struct __align__(16) Summary {
   float xm;        // shard maximum
   float l;         // sum over the shard of exp(s_j - m_r) (NaN if the shard holds a NaN)
-  int32_t first;   // greedy: first column holding the shard maximum
+  uint32_t aux;    // greedy: first column holding the maximum; otherwise candidate messages sent
   uint32_t flags;
 };
 
@@ -93,15 +94,19 @@ struct __align__(128) Smem {
   uint32_t hist[WIN / 2];          // this shard's per-key candidate counts (u16 pairs)
   MidSlot mid[NSHARD];
   Summary slot[NSHARD];
-  float red_f[NWARP];
+  uint32_t red_u[NWARP];
   int32_t red_i[NWARP];
+  float red_f[NWARP];
   uint32_t scan_c[NWARP];
   unsigned long long scan_m[NWARP];
   int32_t found_i;
   uint32_t found_c;
   unsigned long long found_m;
-  unsigned long long mbar;
+  uint32_t npush;
+  unsigned long long bar_load, bar_mid, bar_sum, bar_hist;
 };
+// five CTAs per SM: 5 * (sizeof + 1 KB reserved) <= 228 KB
+static_assert(sizeof(Smem) + 1024 <= 233472 / 5, "shared memory budget of 5 CTAs per SM");
 
 struct KParams {
   const uint16_t* logits;
@@ -130,9 +135,6 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
@@ -144,12 +146,16 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};"
-               :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+// 16-byte store into a peer CTA's shared memory, completing 16 bytes of
+// transaction count on that CTA's mbarrier.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint4 v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+               :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar) : "memory");
 }
-__device__ __forceinline__ void red_cluster_add(uint32_t addr, uint32_t v) {
-  asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
+// atomic add into a peer CTA's shared memory, completing 4 bytes on its mbarrier
+__device__ __forceinline__ void red_async_add(uint32_t addr, uint32_t v, uint32_t bar) {
+  asm volatile("red.async.relaxed.cluster.shared::cluster.mbarrier::complete_tx::bytes.add.u32 [%0], %1, [%2];"
+               :: "r"(addr), "r"(v), "r"(bar) : "memory");
 }
 __device__ __forceinline__ unsigned long long global_timer() {
   unsigned long long t;
@@ -158,10 +164,9 @@ __device__ __forceinline__ unsigned long long global_timer() {
 }
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
-  // make the initialised barrier visible to the bulk-copy (async) proxy
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+// the single expected arrival of a barrier, announcing `bytes` of transactions
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                :: "r"(bar), "r"(bytes) : "memory");
 }
@@ -186,11 +191,11 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
   return ok != 0;
 }
-// Bounded wait: gives up after TIMEOUT_NS of wall time.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-  if (mbar_try(bar, parity)) return true;
+// Bounded wait on phase 0 of a barrier: gives up after TIMEOUT_NS of wall time.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar) {
+  if (mbar_try(bar, 0)) return true;
   const unsigned long long t0 = global_timer();
-  while (!mbar_try(bar, parity)) {
+  while (!mbar_try(bar, 0)) {
     if (global_timer() - t0 > TIMEOUT_NS) return false;
   }
   return true;
@@ -244,7 +249,6 @@ __device__ __forceinline__ int okey_floor(float x) {
 }
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
 __device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t w) {
   return *reinterpret_cast<__nv_bfloat162*>(&w);
 }
@@ -256,41 +260,6 @@ __device__ __forceinline__ unsigned long long qfx(float v, float M, float c) {
 }
 
 // ------------------------------------------------------------ block helpers
-
-// Block maximum of v and block minimum of a per-warp value iw (equal on all
-// lanes of a warp), in one round through shared memory.
-__device__ __forceinline__ float block_max_min(float v, int iw, int& imin, Smem& S) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  if (lane == 0) { S.red_f[warp] = v; S.red_i[warp] = iw; }
-  __syncthreads();
-  float r = S.red_f[0];
-  int m = S.red_i[0];
-#pragma unroll
-  for (int w = 1; w < NWARP; ++w) { r = fmaxf(r, S.red_f[w]); m = min(m, S.red_i[w]); }
-  __syncthreads();
-  imin = m;
-  return r;
-}
-
-// j-th largest (1 <= j <= 32) of the warp's 32 keys, on every lane: a
-// bitonic sort over the lanes (ascending), then a broadcast.
-__device__ __forceinline__ int warp_kth_largest(int key, int j) {
-  const int lane = threadIdx.x & 31;
-  int v = key;
-#pragma unroll
-  for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const int other = __shfl_xor_sync(0xffffffffu, v, stride);
-      const bool ascending = (lane & size) == 0;
-      const bool lower = (lane & stride) == 0;
-      v = (lower == ascending) ? min(v, other) : max(v, other);
-    }
-  }
-  return __shfl_sync(0xffffffffu, v, 32 - j);
-}
 
 // Fixed-order sum: butterfly inside each warp, then a left fold over warps.
 __device__ __forceinline__ float block_sum_fixed(float v, Smem& S) {
@@ -308,8 +277,7 @@ __device__ __forceinline__ float block_sum_fixed(float v, Smem& S) {
 
 __device__ __forceinline__ int block_min_int(int v, Smem& S) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  v = __reduce_min_sync(0xffffffffu, v);
   if (lane == 0) S.red_i[warp] = v;
   __syncthreads();
   int r = S.red_i[0];
@@ -317,6 +285,19 @@ __device__ __forceinline__ int block_min_int(int v, Smem& S) {
   for (int w = 1; w < NWARP; ++w) r = min(r, S.red_i[w]);
   __syncthreads();
   return r;
+}
+
+// j-th largest (1 <= j <= 32) of the warp's 32 keys, on every lane: peel off
+// the maximum value with its multiplicity until j keys are covered.
+__device__ __forceinline__ int warp_kth_largest(int key, int j) {
+  unsigned v = static_cast<unsigned>(key);
+  int covered = 0;
+  for (;;) {
+    const unsigned m = __reduce_max_sync(0xffffffffu, v);
+    covered += __popc(__ballot_sync(0xffffffffu, v == m));
+    if (covered >= j || m == 0u) return static_cast<int>(m);
+    if (v == m) v = 0u;
+  }
 }
 
 // Exclusive block scan of (count, mass); also returns the block totals.
@@ -349,7 +330,20 @@ __device__ __forceinline__ void block_excl_scan(uint32_t c, unsigned long long m
   __syncthreads();
 }
 
+// ceil(p * z) for a fixed-point mass z < 2^63 and p in (0, 1], exact in p's
+// float value: p * 2^32 is an integer for every float p >= 2^-9, and the
+// product is formed in 128 bits.
+__device__ __forceinline__ unsigned long long nucleus_bound(float p, unsigned long long z) {
+  const unsigned long long pf = __float2ull_rn(p * 4294967296.0f);
+  const unsigned long long lo = z * pf;
+  const unsigned long long hi = __umul64hi(z, pf);
+  const unsigned long long fl = (hi << 32) | (lo >> 32);
+  return fl + ((lo & 0xFFFFFFFFull) != 0ull);
+}
+
 // ------------------------------------------------------------ leader: selection
+
+struct SelResult { uint32_t support; unsigned long long zs; int min_key; };
 
 // Count the row's real elements whose key lies in [wlo, whi] (global memory
 // re-read; fallback for supports that reach below the first window).
@@ -400,13 +394,12 @@ __device__ __forceinline__ WinScan scan_window(const uint32_t* cnt, int n, int w
   return w;
 }
 
-// Selection on the merged histogram.  Returns the support size, the support
-// mass (fixed point) and the lowest kept key.
-struct SelResult { uint32_t support; unsigned long long zs; int min_key; };
-
-__device__ __noinline__ SelResult select_support(Smem& S, uint32_t* cnt0, uint32_t* cntB, int hi, int lo,
-                                    const uint16_t* rowp, float M, float c, float Z, float p,
-                                    int k, bool k_on, bool p_on) {
+// General selection over successive windows of WIN keys from the top: exact
+// for any support size.  Used when the first window does not hold every
+// threshold.
+__device__ __noinline__ SelResult select_support(Smem& S, uint32_t* cnt0, uint32_t* cntB, int hi,
+                                                 int lo, const uint16_t* rowp, float M, float c,
+                                                 float Z, float p, int k, bool k_on, bool p_on) {
   const int tid = threadIdx.x;
   int vk_key = -1;                    // lowest key of S_k (-1: top-k off)
   uint32_t sup_k = VREAL;
@@ -457,7 +450,7 @@ __device__ __noinline__ SelResult select_support(Smem& S, uint32_t* cnt0, uint32
   if (!p_on) return SelResult{sup_k, zk, vk_key};
 
   // ---- stage P: nucleus threshold inside S_k
-  const double T = static_cast<double>(p) * static_cast<double>(zk);
+  const unsigned long long T = nucleus_bound(p, zk);
   int whi = hi, wlo = lo;
   const uint32_t* cnt = cnt0;
   uint32_t carry_c = 0;
@@ -475,8 +468,7 @@ __device__ __noinline__ SelResult select_support(Smem& S, uint32_t* cnt0, uint32
     for (int i = w.i0; i < w.i1 && i <= imax; ++i) {
       const uint32_t ci = cnt[i];
       const unsigned long long mi = ci ? ci * qfx(key_value(whi - i), M, c) : 0ull;
-      if (static_cast<double>(rm) < T &&
-          (static_cast<double>(rm + mi) >= T || (i == imax && bounded))) {
+      if (rm < T && (rm + mi >= T || (i == imax && bounded))) {
         S.found_i = whi - i;
         S.found_c = rc + ci;
         S.found_m = rm + mi;
@@ -504,21 +496,22 @@ __device__ __noinline__ SelResult select_support(Smem& S, uint32_t* cnt0, uint32
 // one block scan of (count, mass) over the keys hi, hi-1, ..., lo, then the
 // top-k boundary and the nucleus boundary are read off it.  Returns false if
 // a threshold may lie below the window; select_support then takes over.
-__device__ bool select_fast(Smem& S, const uint32_t* cnt, int hi, int lo, float M, float c, float Z,
-                            float p, int k, bool k_on, bool p_on, SelResult& out) {
-  constexpr int PER = WIN / NTHR;
+// Per-key masses go to `mass` (shared scratch of WIN entries).
+__device__ bool select_fast(Smem& S, const uint32_t* cnt, unsigned long long* mass, int hi, int lo,
+                            float M, float c, float Z, float p, int k, bool k_on, bool p_on,
+                            SelResult& out) {
   const int n = hi - lo + 1;
   const int per = (n + NTHR - 1) / NTHR;
   const int i0 = min(n, static_cast<int>(threadIdx.x) * per);
   const int i1 = min(n, i0 + per);
-  uint32_t ci[PER];
   uint32_t lc = 0;
   unsigned long long lm = 0;
-#pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    const int i = i0 + q;
-    ci[q] = (i < i1) ? cnt[i] : 0u;
-    if (ci[q]) { lc += ci[q]; lm += ci[q] * qfx(key_value(hi - i), M, c); }
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t ci = cnt[i];
+    const unsigned long long mi = ci ? ci * qfx(key_value(hi - i), M, c) : 0ull;
+    mass[i] = mi;
+    lc += ci;
+    lm += mi;
   }
   if (threadIdx.x == 0) S.found_i = -1;
   uint32_t bc, tc;
@@ -528,25 +521,21 @@ __device__ bool select_fast(Smem& S, const uint32_t* cnt, int hi, int lo, float 
   int imax = n - 1;
   unsigned long long zk = __float2ull_rn(Z * FX_SCALE);
   if (k_on) {
+    if (tc < static_cast<uint32_t>(k)) return false;     // k-th value below the window
     uint32_t rc = bc;
     unsigned long long rm = bm;
-#pragma unroll
-    for (int q = 0; q < PER; ++q) {
-      const int i = i0 + q;
-      if (ci[q]) {
-        const unsigned long long m = ci[q] * qfx(key_value(hi - i), M, c);
-        if (rc < static_cast<uint32_t>(k) && rc + ci[q] >= static_cast<uint32_t>(k)) {
-          S.found_i = i;
-          S.found_c = rc + ci[q];
-          S.found_m = rm + m;
-        }
-        rc += ci[q];
-        rm += m;
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t ci = cnt[i];
+      if (rc < static_cast<uint32_t>(k) && rc + ci >= static_cast<uint32_t>(k)) {
+        S.found_i = i;
+        S.found_c = rc + ci;
+        S.found_m = rm + mass[i];
       }
+      rc += ci;
+      rm += mass[i];
     }
     __syncthreads();
     const int ik = S.found_i;
-    if (ik < 0) return false;                  // k-th value below the window
     imax = ik;
     zk = S.found_m;
     const uint32_t sup_k = S.found_c;
@@ -556,33 +545,29 @@ __device__ bool select_fast(Smem& S, const uint32_t* cnt, int hi, int lo, float 
       return true;
     }
     if (threadIdx.x == 0) S.found_i = -1;
-    __syncthreads();
   }
   // nucleus inside S_k: keep key i iff the mass strictly above it is < p * Z_k
-  const double T = static_cast<double>(p) * static_cast<double>(zk);
+  const unsigned long long T = nucleus_bound(p, zk);
+  if (!k_on && tm < T) return false;             // nucleus reaches below the window
+  __syncthreads();
   {
     uint32_t rc = bc;
     unsigned long long rm = bm;
-#pragma unroll
-    for (int q = 0; q < PER; ++q) {
-      const int i = i0 + q;
-      const unsigned long long m = ci[q] ? ci[q] * qfx(key_value(hi - i), M, c) : 0ull;
-      if (i < i1 && i <= imax && static_cast<double>(rm) < T &&
-          (static_cast<double>(rm + m) >= T || (i == imax && k_on))) {
+    for (int i = i0; i < i1 && i <= imax; ++i) {
+      const unsigned long long mi = mass[i];
+      if (rm < T && (rm + mi >= T || (i == imax && k_on))) {
         S.found_i = i;
-        S.found_c = rc + ci[q];
-        S.found_m = rm + m;
+        S.found_c = rc + cnt[i];
+        S.found_m = rm + mi;
       }
-      rc += ci[q];
-      rm += m;
+      rc += cnt[i];
+      rm += mi;
     }
   }
   __syncthreads();
   const int ip = S.found_i;
-  if (ip < 0) return false;                    // nucleus reaches below the window
   out = SelResult{S.found_c, S.found_m, hi - ip};
-  __syncthreads();
-  return true;
+  return ip >= 0;
 }
 
 // ------------------------------------------------------------ the kernel
@@ -620,35 +605,47 @@ logp_kernel(const KParams P) {
 
   const int nchunks = (r == NSHARD - 1) ? LAST_CHUNKS : SHARD_CHUNKS;
   const uint16_t* rowp = P.logits + row * P.stride;
-  const uint32_t bar = smem_addr(&S.mbar);
+  const uint32_t bar_load = smem_addr(&S.bar_load);
+  const uint32_t bar_mid = smem_addr(&S.bar_mid);
+  const uint32_t bar_sum = smem_addr(&S.bar_sum);
+  const uint32_t bar_hist = smem_addr(&S.bar_hist);
 
-  // ---- 1. bulk copy of the shard into shared memory
+  // ---- 1. barriers, and the bulk copy of the shard into shared memory
   if (tid == 0) {
-    mbar_init(bar, 1);
+    mbar_init(bar_load, 1);
+    mbar_init(bar_mid, 1);
+    mbar_init(bar_sum, 1);
+    mbar_init(bar_hist, 1);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     const uint32_t bytes = static_cast<uint32_t>(nchunks) * 16u;
-    mbar_expect_tx(bar, bytes);
+    mbar_arrive_expect_tx(bar_load, bytes);
     const uint64_t pol = evict_first_policy();
     const uint32_t piece = bytes / TMA_PIECES;
     const char* src = reinterpret_cast<const char*>(rowp + static_cast<int64_t>(r) * SW);
     const uint32_t dst = smem_addr(S.shard);
 #pragma unroll
-    for (int i = 0; i < TMA_PIECES; ++i) bulk_load(dst + i * piece, src + i * piece, piece, bar, pol);
+    for (int i = 0; i < TMA_PIECES; ++i) bulk_load(dst + i * piece, src + i * piece, piece, bar_load, pol);
+    // messages from the 7 peers: 16 bytes each
+    if (sel) mbar_arrive_expect_tx(bar_mid, (NSHARD - 1) * 16);
+    if (r == 0) mbar_arrive_expect_tx(bar_sum, (NSHARD - 1) * 16);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    S.npush = 0u;
   }
   if (sel) {
     if (r == 0)
       for (int i = tid; i < WIN; i += NTHR) S.merged[i] = 0u;
     for (int i = tid; i < WIN / 2; i += NTHR) S.hist[i] = 0u;
   }
-  cluster_arrive_relaxed();   // S0: every CTA of the cluster has started
+  cluster_arrive();            // S0: barriers initialised, leader histogram zeroed
   __syncthreads();
   uint32_t flags = 0;
-  if (!mbar_wait_bounded(bar, 0)) {
+  if (!mbar_wait_bounded(bar_load)) {
     flags |= FLAG_TIMEOUT;
-    mbar_wait_bounded(bar, 0);   // give copies in flight a second bounded chance to land
+    mbar_wait_bounded(bar_load);   // give copies in flight a second bounded chance to land
   }
 
   // ---- 2. shard maximum; per-chunk maxima stay in registers for the candidate pass.
-  // bf16 max ignores NaN; a NaN shows up as a NaN sum-exp (or in the scans below).
+  // bf16 max ignores NaN; a NaN shows up as a NaN sum-exp (or in the scan below).
   const uint4* sh = S.shard;
   const __nv_bfloat162 ninf2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
   __nv_bfloat162 cm[MAXCH - 1];   // the last chunk (threads < 80 only) is recomputed later
@@ -664,21 +661,31 @@ logp_kernel(const KParams P) {
     }
     if (i < MAXCH - 1) cm[i] = cmax;
   }
-  const float tmax = fmaxf(__low2float(m2), __high2float(m2));
+  const int tkey = okey_of(fmaxf(__low2float(m2), __high2float(m2)));
   // Pooled top-k bound: warp w certifies kw = ceil(k/64) lane maxima at or above
   // lw (its kw-th largest lane maximum), so the 64 warps of the row certify
   // 64*kw >= k tokens at or above the minimum of lw over the cluster.
   const int kw = (k + 63) / 64;
   const bool k_bound = sel && k_on && kw <= 32;
-  const int lw = k_bound ? warp_kth_largest(okey_of(tmax), kw) : 0;
-  int lkey;
-  const float xm = block_max_min(tmax, lw, lkey, S);
+  {
+    const int lane = tid & 31, warp = tid >> 5;
+    const int lw = k_bound ? warp_kth_largest(tkey, kw) : 0;
+    const unsigned wmax = __reduce_max_sync(0xffffffffu, static_cast<unsigned>(tkey));
+    if (lane == 0) { S.red_u[warp] = wmax; S.red_i[warp] = lw; }
+  }
+  __syncthreads();
+  unsigned xkey = S.red_u[0];
+  int lkey = S.red_i[0];
+#pragma unroll
+  for (int w = 1; w < NWARP; ++w) { xkey = max(xkey, S.red_u[w]); lkey = min(lkey, S.red_i[w]); }
+  const float xm = key_value(static_cast<int>(xkey));
   const bool xm_finite = (xm > -INFINITY) && (xm < INFINITY);
 
-  int first = 0x7fffffff;
+  uint32_t first = 0x7fffffffu;
   if (greedy || xm == -INFINITY) {
     // greedy: first column of this shard holding its maximum; both cases: NaN scan
     bool nan_seen = false;
+    int f = 0x7fffffff;
     for (int ch = tid; ch < nchunks; ch += NTHR) {
       const uint4 v = sh[ch];
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -686,29 +693,29 @@ logp_kernel(const KParams P) {
       for (int j = 7; j >= 0; --j) {
         const float x = (j & 1) ? bf16_hi(w[j >> 1]) : bf16_lo(w[j >> 1]);
         nan_seen |= (x != x);
-        if (x == xm) first = min(first, ch * 8 + j);
+        if (x == xm) f = min(f, ch * 8 + j);
       }
     }
     if (__syncthreads_or(nan_seen)) flags |= FLAG_NAN;
     if (greedy) {
-      first = block_min_int(first, S);
-      if (first != 0x7fffffff) first += static_cast<int>(r) * SW;
+      f = block_min_int(f, S);
+      if (f != 0x7fffffff) first = static_cast<uint32_t>(f + static_cast<int>(r) * SW);
     }
   }
 
-  cluster_wait();              // S0 complete: peers' shared memory may be written
-  if (sel) {
-    if (tid < NSHARD)
-      st_cluster_v4(map_rank(smem_addr(&S.mid[r]), tid),
-                    make_uint4(__float_as_uint(xm), static_cast<uint32_t>(lkey), flags, 0u));
-    cluster_arrive();          // MID
+  cluster_wait();              // S0 complete: peers' barriers and histogram are ready
+  if (sel && tid < NSHARD) {
+    const uint4 msg = make_uint4(__float_as_uint(xm), static_cast<uint32_t>(lkey), flags, 0u);
+    if (tid == static_cast<int>(r))
+      *reinterpret_cast<uint4*>(&S.mid[r]) = msg;
+    else
+      st_async_v4(map_rank(smem_addr(&S.mid[r]), tid), msg, map_rank(bar_mid, tid));
   }
 
   // ---- 3. shard sum-exp, fixed tree
   float l = 0.0f;
-  float c = 0.0f;
   if (!greedy && xm_finite) {
-    c = __fdiv_rn(LOG2E, tau);
+    const float c = __fdiv_rn(LOG2E, tau);
     const uint64_t nxm2 = pack2(-xm, -xm);
     const uint64_t c2 = pack2(c, c);
     uint64_t acc = pack2(0.0f, 0.0f);
@@ -730,11 +737,11 @@ logp_kernel(const KParams P) {
 
   // ---- 4. candidate pass: exact per-key counts into the leader's histogram
   int hi = 0, lo = 1;
-  float M = xm;
   if (sel) {
-    cluster_wait();            // MID complete: all shard maxima and bounds are here
+    if (!mbar_wait_bounded(bar_mid)) flags |= FLAG_TIMEOUT;
+    __syncthreads();           // this CTA's own slot, written locally, is visible too
     int L = 0x7fffffff;
-    M = -INFINITY;
+    float M = -INFINITY;
 #pragma unroll
     for (int q = 0; q < NSHARD; ++q) {
       M = fmaxf(M, S.mid[q].xm);
@@ -752,9 +759,11 @@ logp_kernel(const KParams P) {
         const float width = tau * (logf(static_cast<float>(VREAL) / (1.0f - p)) * 1.0001f + 1e-3f);
         lo = max(lo, okey_floor(M - width));
       }
-      lo = max(lo, KEY_NEG_INF);   // keys below that of -inf are NaN patterns
+      lo = max(lo, KEY_NEG_INF);
     }
-    if (xm_finite && lo <= hi && okey_of(xm) >= lo) {
+    // the leader counts straight into the merged histogram, the others locally
+    uint32_t* cnt_local = (r == 0) ? S.merged : S.hist;
+    if (xm_finite && lo <= hi && static_cast<int>(xkey) >= lo) {
       const float vlo_f = key_value(lo);
       const __nv_bfloat162 vlo2 = __floats2bfloat162_rn(vlo_f, vlo_f);
 #pragma unroll
@@ -781,52 +790,66 @@ logp_kernel(const KParams P) {
             const uint32_t wj = (j == 0) ? w[0] : (j == 1) ? w[1] : (j == 2) ? w[2] : w[3];
             const uint32_t b = (pos & 16) ? (wj >> 16) : (wj & 0xFFFFu);
             const int idx = hi - okey(b);
-            atomicAdd(&S.hist[idx >> 1], 1u << ((idx & 1) * 16));
+            if (r == 0) atomicAdd(&cnt_local[idx], 1u);
+            else atomicAdd(&cnt_local[idx >> 1], 1u << ((idx & 1) * 16));
           }
         }
       }
     }
-    __syncthreads();
-    // push this shard's nonzero counts into the leader's histogram
-    const uint32_t dst = map_rank(smem_addr(S.merged), 0);
-    const int nwords = (hi - lo + 2) >> 1;
-    for (int i = tid; i < nwords; i += NTHR) {
-      const uint32_t w = S.hist[i];
-      if (w & 0xFFFFu) red_cluster_add(dst + 8u * i, w & 0xFFFFu);
-      if (w >> 16) red_cluster_add(dst + 8u * i + 4u, w >> 16);
+    if (r != 0) {
+      __syncthreads();
+      // send this shard's nonzero counts to the leader
+      const uint32_t dst = map_rank(smem_addr(S.merged), 0);
+      const uint32_t rbar = map_rank(bar_hist, 0);
+      const int nwords = (hi - lo + 2) >> 1;
+      uint32_t sent = 0;
+      for (int i = tid; i < nwords; i += NTHR) {
+        const uint32_t w = S.hist[i];
+        if (w & 0xFFFFu) { red_async_add(dst + 8u * i, w & 0xFFFFu, rbar); ++sent; }
+        if (w >> 16) { red_async_add(dst + 8u * i + 4u, w >> 16, rbar); ++sent; }
+      }
+      if (sent) atomicAdd(&S.npush, sent);
+      __syncthreads();
     }
   }
 
   // ---- 5. summary to the leader
-  if (tid == 0)
-    st_cluster_v4(map_rank(smem_addr(&S.slot[r]), 0),
-                  make_uint4(__float_as_uint(xm), __float_as_uint(l), static_cast<uint32_t>(first), flags));
-  cluster_arrive();            // A
-  if (r != 0) return;          // nobody reads this CTA's shared memory any more
-  cluster_wait();
+  if (tid == 0) {
+    const uint4 msg = make_uint4(__float_as_uint(xm), __float_as_uint(l), sel ? S.npush : first, flags);
+    if (r == 0) *reinterpret_cast<uint4*>(&S.slot[0]) = msg;
+    else st_async_v4(map_rank(smem_addr(&S.slot[r]), 0), msg, map_rank(bar_sum, 0));
+  }
+  if (r != 0) return;          // messages carry everything the leader needs
 
   // ================= leader: merge in fixed shard order =================
+  bool timed_out = !mbar_wait_bounded(bar_sum);
+  __syncthreads();             // own slot and own counts visible to every thread
   bool bad = false;
-  bool timed_out = false;
-  M = -INFINITY;
+  float M = -INFINITY;
+  uint32_t pushed = 0;
 #pragma unroll
   for (int q = 0; q < NSHARD; ++q) {
     const Summary& s = S.slot[q];
     if (s.flags & FLAG_TIMEOUT) timed_out = true;
     if ((s.flags & FLAG_NAN) || s.xm == INFINITY || s.l != s.l) bad = true;
     M = fmaxf(M, s.xm);
+    if (q > 0) pushed += s.aux;
+  }
+  if (sel) {
+    if (tid == 0) mbar_arrive_expect_tx(bar_hist, 4u * pushed);
+    if (!mbar_wait_bounded(bar_hist)) timed_out = true;
   }
   bad |= timed_out || !(M > -INFINITY);
   const float qnan = __int_as_float(0x7fc00000);
   float full = qnan, restr = qnan;
   int support = -1;
-  float Z = 0.0f, d = 0.0f;
+  float c = 0.0f, Z = 0.0f, d = 0.0f;
   if (!bad && greedy) {
-    int amax = 0x7fffffff;
+    uint32_t amax = 0x7fffffffu;
 #pragma unroll
     for (int q = NSHARD - 1; q >= 0; --q)
-      if (S.slot[q].xm == M) amax = S.slot[q].first;
-    full = restr = (t == amax) ? 0.0f : -INFINITY;
+      if (S.slot[q].xm == M) amax = S.slot[q].aux;
+    full = restr = (static_cast<uint32_t>(t) == amax) ? 0.0f : -INFINITY;
     support = 1;
   } else if (!bad) {
     c = __fdiv_rn(LOG2E, tau);
@@ -846,13 +869,14 @@ logp_kernel(const KParams P) {
     }
   }
   if (sel && !bad) {
-    uint32_t* cntB = reinterpret_cast<uint32_t*>(S.shard);
+    unsigned long long* mass = reinterpret_cast<unsigned long long*>(S.shard);
+    uint32_t* cntB = reinterpret_cast<uint32_t*>(S.shard) + 2 * WIN;
     SelResult sr;
-    if (!select_fast(S, S.merged, hi, lo, M, c, Z, p, k, k_on, p_on, sr))
+    if (!select_fast(S, S.merged, mass, hi, lo, M, c, Z, p, k, k_on, p_on, sr))
       sr = select_support(S, S.merged, cntB, hi, lo, rowp, M, c, Z, p, k, k_on, p_on);
     const float xt = __uint_as_float(static_cast<uint32_t>(__ldg(rowp + t)) << 16);
     const bool in_s = okey_of(xt) >= sr.min_key;
-    const float zs = static_cast<float>(static_cast<double>(sr.zs) * (1.0 / 17592186044416.0));
+    const float zs = static_cast<float>(static_cast<double>(sr.zs) * FX_INV);
     restr = in_s ? d - logf(zs) : -INFINITY;
     support = static_cast<int>(sr.support);
   }
