@@ -63,7 +63,6 @@ constexpr int WIN = 1024;            // candidate window, in bf16 order keys (8 
 constexpr int TMA_PIECES = 4;
 constexpr float LOG2E = 1.4426950408889634f;   // log2(e)
 constexpr float FX_SCALE = 17592186044416.0f;  // 2^44: fixed-point scale of masses
-constexpr double FX_INV = 1.0 / 17592186044416.0;
 constexpr unsigned long long TIMEOUT_NS = 200000000ull;   // 0.2 s bound on every wait
 constexpr int KEY_NEG_INF = 0x007F;  // order key of -inf; smaller keys are NaN patterns
 
@@ -156,6 +155,10 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, uint4 v, uint32_t bar
 __device__ __forceinline__ void red_async_add(uint32_t addr, uint32_t v, uint32_t bar) {
   asm volatile("red.async.relaxed.cluster.shared::cluster.mbarrier::complete_tx::bytes.add.u32 [%0], %1, [%2];"
                :: "r"(addr), "r"(v), "r"(bar) : "memory");
+}
+// shared-memory add without a return value (nothing waits for it)
+__device__ __forceinline__ void red_shared_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.shared.add.u32 [%0], %1;" :: "r"(smem_addr(p)), "r"(v) : "memory");
 }
 __device__ __forceinline__ unsigned long long global_timer() {
   unsigned long long t;
@@ -605,6 +608,8 @@ logp_kernel(const KParams P) {
 
   const int nchunks = (r == NSHARD - 1) ? LAST_CHUNKS : SHARD_CHUNKS;
   const uint16_t* rowp = P.logits + row * P.stride;
+  // the leader needs the target's logit at the end: start the load now
+  const float xt = (r == 0) ? __uint_as_float(static_cast<uint32_t>(__ldg(rowp + t)) << 16) : 0.0f;
   const uint32_t bar_load = smem_addr(&S.bar_load);
   const uint32_t bar_mid = smem_addr(&S.bar_mid);
   const uint32_t bar_sum = smem_addr(&S.bar_sum);
@@ -790,8 +795,8 @@ logp_kernel(const KParams P) {
             const uint32_t wj = (j == 0) ? w[0] : (j == 1) ? w[1] : (j == 2) ? w[2] : w[3];
             const uint32_t b = (pos & 16) ? (wj >> 16) : (wj & 0xFFFFu);
             const int idx = hi - okey(b);
-            if (r == 0) atomicAdd(&cnt_local[idx], 1u);
-            else atomicAdd(&cnt_local[idx >> 1], 1u << ((idx & 1) * 16));
+            if (r == 0) red_shared_add(&cnt_local[idx], 1u);
+            else red_shared_add(&cnt_local[idx >> 1], 1u << ((idx & 1) * 16));
           }
         }
       }
@@ -861,7 +866,6 @@ logp_kernel(const KParams P) {
         const Summary& s = S.slot[q];
         if (s.xm > -INFINITY) Z = fmaf(s.l, ex2((s.xm - M) * c), Z);
       }
-      const float xt = __uint_as_float(static_cast<uint32_t>(__ldg(rowp + t)) << 16);
       d = __fdiv_rn(xt - M, tau);
       full = d - logf(Z);
       restr = full;
@@ -874,9 +878,8 @@ logp_kernel(const KParams P) {
     SelResult sr;
     if (!select_fast(S, S.merged, mass, hi, lo, M, c, Z, p, k, k_on, p_on, sr))
       sr = select_support(S, S.merged, cntB, hi, lo, rowp, M, c, Z, p, k, k_on, p_on);
-    const float xt = __uint_as_float(static_cast<uint32_t>(__ldg(rowp + t)) << 16);
     const bool in_s = okey_of(xt) >= sr.min_key;
-    const float zs = static_cast<float>(static_cast<double>(sr.zs) * FX_INV);
+    const float zs = __ull2float_rn(sr.zs) * (1.0f / FX_SCALE);
     restr = in_s ? d - logf(zs) : -INFINITY;
     support = static_cast<int>(sr.support);
   }
