@@ -59,8 +59,10 @@ constexpr int LAST_CHUNKS = (VREAL - (NSHARD - 1) * SW) / 8;  // 2304 real chunk
 constexpr int NTHR = 256;
 constexpr int NWARP = NTHR / 32;
 constexpr int MAXCH = (SHARD_CHUNKS + NTHR - 1) / NTHR;     // chunks per thread (9 or 10)
+constexpr int KEEPCH = 7;            // chunk maxima kept in registers; the rest are recomputed
 constexpr int WIN = 1024;            // candidate window, in bf16 order keys (8 binades)
 constexpr int TMA_PIECES = 4;
+constexpr int CLIST = 256;           // capacity of the candidate-chunk list
 constexpr float LOG2E = 1.4426950408889634f;   // log2(e)
 constexpr float FX_SCALE = 17592186044416.0f;  // 2^44: fixed-point scale of masses
 constexpr unsigned long long TIMEOUT_NS = 200000000ull;   // 0.2 s bound on every wait
@@ -91,6 +93,7 @@ struct __align__(128) Smem {
   uint4 shard[SHARD_CHUNKS];       // 38144 B; the leader reuses it as scratch at the end
   uint32_t merged[WIN];            // leader: per-key candidate counts of the whole row
   uint32_t hist[WIN / 2];          // this shard's per-key candidate counts (u16 pairs)
+  uint16_t clist[CLIST];           // chunks holding candidates, processed element-parallel
   MidSlot mid[NSHARD];
   Summary slot[NSHARD];
   uint32_t red_u[NWARP];
@@ -102,6 +105,8 @@ struct __align__(128) Smem {
   uint32_t found_c;
   unsigned long long found_m;
   uint32_t npush;
+  uint32_t nlist;
+  int32_t sel_done;
   unsigned long long bar_load, bar_mid, bar_sum, bar_hist;
 };
 // five CTAs per SM: 5 * (sizeof + 1 KB reserved) <= 228 KB
@@ -495,82 +500,78 @@ __device__ __noinline__ SelResult select_support(Smem& S, uint32_t* cnt0, uint32
   }
 }
 
-// Selection when the first window holds every threshold (the common case):
-// one block scan of (count, mass) over the keys hi, hi-1, ..., lo, then the
-// top-k boundary and the nucleus boundary are read off it.  Returns false if
-// a threshold may lie below the window; select_support then takes over.
-// Per-key masses go to `mass` (shared scratch of WIN entries).
-__device__ bool select_fast(Smem& S, const uint32_t* cnt, unsigned long long* mass, int hi, int lo,
-                            float M, float c, float Z, float p, int k, bool k_on, bool p_on,
-                            SelResult& out) {
+// Selection by one warp when the first window holds every threshold (the
+// common case): keys hi, hi-1, ..., lo in blocks of 128 (4 consecutive keys
+// per lane), warp scans of (count, mass), and ballots to find the top-k and
+// nucleus boundaries.  Returns false if a threshold may lie below the window.
+__device__ __noinline__ bool select_warp(const uint32_t* cnt, int hi, int lo, float M, float c, float Z,
+                            float p, int k, bool k_on, bool p_on, SelResult& out) {
+  const int lane = threadIdx.x & 31;
   const int n = hi - lo + 1;
-  const int per = (n + NTHR - 1) / NTHR;
-  const int i0 = min(n, static_cast<int>(threadIdx.x) * per);
-  const int i1 = min(n, i0 + per);
-  uint32_t lc = 0;
-  unsigned long long lm = 0;
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t ci = cnt[i];
-    const unsigned long long mi = ci ? ci * qfx(key_value(hi - i), M, c) : 0ull;
-    mass[i] = mi;
-    lc += ci;
-    lm += mi;
-  }
-  if (threadIdx.x == 0) S.found_i = -1;
-  uint32_t bc, tc;
-  unsigned long long bm, tm;
-  block_excl_scan(lc, lm, bc, bm, tc, tm, S);
-
   int imax = n - 1;
   unsigned long long zk = __float2ull_rn(Z * FX_SCALE);
-  if (k_on) {
-    if (tc < static_cast<uint32_t>(k)) return false;     // k-th value below the window
-    uint32_t rc = bc;
-    unsigned long long rm = bm;
-    for (int i = i0; i < i1; ++i) {
-      const uint32_t ci = cnt[i];
-      if (rc < static_cast<uint32_t>(k) && rc + ci >= static_cast<uint32_t>(k)) {
-        S.found_i = i;
-        S.found_c = rc + ci;
-        S.found_m = rm + mass[i];
+  for (int stage = k_on ? 0 : 1; stage < 2; ++stage) {
+    if (stage == 1 && !p_on) break;
+    const unsigned long long T = (stage == 1) ? nucleus_bound(p, zk) : 0ull;
+    uint32_t carry_c = 0;
+    unsigned long long carry_m = 0;
+    for (int b0 = 0; b0 <= imax; b0 += 4 * 32) {
+      uint32_t cj[4];
+      unsigned long long mj[4];
+      uint32_t lc = 0;
+      unsigned long long lm = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = b0 + 4 * lane + j;
+        cj[j] = (i <= imax) ? cnt[i] : 0u;
+        mj[j] = cj[j] ? cj[j] * qfx(key_value(hi - i), M, c) : 0ull;
+        lc += cj[j];
+        lm += mj[j];
       }
-      rc += ci;
-      rm += mass[i];
-    }
-    __syncthreads();
-    const int ik = S.found_i;
-    imax = ik;
-    zk = S.found_m;
-    const uint32_t sup_k = S.found_c;
-    __syncthreads();
-    if (!p_on) {
-      out = SelResult{sup_k, zk, hi - ik};
-      return true;
-    }
-    if (threadIdx.x == 0) S.found_i = -1;
-  }
-  // nucleus inside S_k: keep key i iff the mass strictly above it is < p * Z_k
-  const unsigned long long T = nucleus_bound(p, zk);
-  if (!k_on && tm < T) return false;             // nucleus reaches below the window
-  __syncthreads();
-  {
-    uint32_t rc = bc;
-    unsigned long long rm = bm;
-    for (int i = i0; i < i1 && i <= imax; ++i) {
-      const unsigned long long mi = mass[i];
-      if (rm < T && (rm + mi >= T || (i == imax && k_on))) {
-        S.found_i = i;
-        S.found_c = rc + cnt[i];
-        S.found_m = rm + mi;
+      uint32_t ic = lc;
+      unsigned long long im = lm;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t yc = __shfl_up_sync(0xffffffffu, ic, o);
+        const unsigned long long ym = __shfl_up_sync(0xffffffffu, im, o);
+        if (lane >= o) { ic += yc; im += ym; }
       }
-      rc += cnt[i];
-      rm += mi;
+      uint32_t rc = carry_c + ic - lc;
+      unsigned long long rm = carry_m + im - lm;
+      int fi = -1;
+      uint32_t fc = 0;
+      unsigned long long fm = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = b0 + 4 * lane + j;
+        const bool hit = (stage == 0)
+            ? (rc < static_cast<uint32_t>(k) && rc + cj[j] >= static_cast<uint32_t>(k))
+            : (i <= imax && rm < T && (rm + mj[j] >= T || (i == imax && k_on)));
+        if (fi < 0 && hit) { fi = i; fc = rc + cj[j]; fm = rm + mj[j]; }
+        rc += cj[j];
+        rm += mj[j];
+      }
+      const unsigned bal = __ballot_sync(0xffffffffu, fi >= 0);
+      if (bal) {
+        const int src = __ffs(bal) - 1;
+        fi = __shfl_sync(0xffffffffu, fi, src);
+        fc = __shfl_sync(0xffffffffu, fc, src);
+        fm = __shfl_sync(0xffffffffu, fm, src);
+        if (stage == 0) {
+          imax = fi;
+          zk = fm;
+          out = SelResult{fc, fm, hi - fi};
+        } else {
+          out = SelResult{fc, fm, hi - fi};
+        }
+        break;
+      }
+      carry_c += __shfl_sync(0xffffffffu, ic, 31);
+      carry_m += __shfl_sync(0xffffffffu, im, 31);
+      if (b0 + 4 * 32 > imax) return false;   // boundary below the window
     }
   }
-  __syncthreads();
-  const int ip = S.found_i;
-  out = SelResult{S.found_c, S.found_m, hi - ip};
-  return ip >= 0;
+  return true;
 }
 
 // ------------------------------------------------------------ the kernel
@@ -635,6 +636,7 @@ logp_kernel(const KParams P) {
     if (r == 0) mbar_arrive_expect_tx(bar_sum, (NSHARD - 1) * 16);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     S.npush = 0u;
+    S.nlist = 0u;
   }
   if (sel) {
     if (r == 0)
@@ -653,7 +655,7 @@ logp_kernel(const KParams P) {
   // bf16 max ignores NaN; a NaN shows up as a NaN sum-exp (or in the scan below).
   const uint4* sh = S.shard;
   const __nv_bfloat162 ninf2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
-  __nv_bfloat162 cm[MAXCH - 1];   // the last chunk (threads < 80 only) is recomputed later
+  __nv_bfloat162 cm[KEEPCH];      // later chunks' maxima are recomputed when needed
   __nv_bfloat162 m2 = ninf2;
 #pragma unroll
   for (int i = 0; i < MAXCH; ++i) {
@@ -664,7 +666,7 @@ logp_kernel(const KParams P) {
       cmax = __hmax2(__hmax2(as_bf2(v.x), as_bf2(v.y)), __hmax2(as_bf2(v.z), as_bf2(v.w)));
       m2 = __hmax2(m2, cmax);
     }
-    if (i < MAXCH - 1) cm[i] = cmax;
+    if (i < KEEPCH) cm[i] = cmax;
   }
   const int tkey = okey_of(fmaxf(__low2float(m2), __high2float(m2)));
   // Pooled top-k bound: warp w certifies kw = ceil(k/64) lane maxima at or above
@@ -771,33 +773,66 @@ logp_kernel(const KParams P) {
     if (xm_finite && lo <= hi && static_cast<int>(xkey) >= lo) {
       const float vlo_f = key_value(lo);
       const __nv_bfloat162 vlo2 = __floats2bfloat162_rn(vlo_f, vlo_f);
+      // chunks whose maximum reaches the window, from the register chunk maxima
+      uint32_t hitmask = 0;
 #pragma unroll
       for (int i = 0; i < MAXCH; ++i) {
         const int ch = tid + i * NTHR;
-        if (ch >= nchunks) continue;
-        __nv_bfloat162 cmax;
-        if (i < MAXCH - 1) {
-          cmax = cm[i];
-        } else {
-          const uint4 v = sh[ch];
-          cmax = __hmax2(__hmax2(as_bf2(v.x), as_bf2(v.y)), __hmax2(as_bf2(v.z), as_bf2(v.w)));
+        if (ch < nchunks) {
+          __nv_bfloat162 cmax;
+          if (i < KEEPCH) {
+            cmax = cm[i];
+          } else {
+            const uint4 v = sh[ch];
+            cmax = __hmax2(__hmax2(as_bf2(v.x), as_bf2(v.y)), __hmax2(as_bf2(v.z), as_bf2(v.w)));
+          }
+          if (__hge2_mask(cmax, vlo2) != 0u) hitmask |= 1u << i;
         }
-        if (__hge2_mask(cmax, vlo2) != 0u) {
+      }
+      // warp-aggregated append of those chunks to the CTA list
+      const int lane = tid & 31;
+      const int h = __popc(hitmask);
+      int incl = h;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int base = 0;
+      if (lane == 31 && incl > 0) base = static_cast<int>(atomicAdd(&S.nlist, static_cast<uint32_t>(incl)));
+      int pos = __shfl_sync(0xffffffffu, base, 31) + incl - h;
+      while (hitmask) {
+        const int i = __ffs(hitmask) - 1;
+        hitmask &= hitmask - 1;
+        const int ch = tid + i * NTHR;
+        if (pos < CLIST) {
+          S.clist[pos] = static_cast<uint16_t>(ch);
+        } else {
+          // list full: count this chunk here
           const uint4 v = sh[ch];
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-          uint32_t bits = 0;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) bits |= (__hge2_mask(as_bf2(w[j]), vlo2) & 0x00010001u) << j;
-          while (bits) {
-            const int pos = __ffs(bits) - 1;
-            bits &= bits - 1;
-            const int j = pos & 3;
-            const uint32_t wj = (j == 0) ? w[0] : (j == 1) ? w[1] : (j == 2) ? w[2] : w[3];
-            const uint32_t b = (pos & 16) ? (wj >> 16) : (wj & 0xFFFFu);
-            const int idx = hi - okey(b);
-            if (r == 0) red_shared_add(&cnt_local[idx], 1u);
-            else red_shared_add(&cnt_local[idx >> 1], 1u << ((idx & 1) * 16));
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t b = (w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
+            if (__uint_as_float(b << 16) >= vlo_f) {
+              const int idx = hi - okey(b);
+              if (r == 0) red_shared_add(&cnt_local[idx], 1u);
+              else red_shared_add(&cnt_local[idx >> 1], 1u << ((idx & 1) * 16));
+            }
           }
+        }
+        ++pos;
+      }
+      __syncthreads();
+      // listed chunks, one element per thread
+      const int nl = min(static_cast<int>(S.nlist), CLIST);
+      const uint16_t* elem = reinterpret_cast<const uint16_t*>(S.shard);
+      for (int e = tid >> 3; e < nl; e += NTHR / 8) {
+        const uint32_t b = elem[static_cast<int>(S.clist[e]) * 8 + (tid & 7)];
+        if (__uint_as_float(b << 16) >= vlo_f) {
+          const int idx = hi - okey(b);
+          if (r == 0) red_shared_add(&cnt_local[idx], 1u);
+          else red_shared_add(&cnt_local[idx >> 1], 1u << ((idx & 1) * 16));
         }
       }
     }
@@ -873,11 +908,14 @@ logp_kernel(const KParams P) {
     }
   }
   if (sel && !bad) {
-    unsigned long long* mass = reinterpret_cast<unsigned long long*>(S.shard);
-    uint32_t* cntB = reinterpret_cast<uint32_t*>(S.shard) + 2 * WIN;
-    SelResult sr;
-    if (!select_fast(S, S.merged, mass, hi, lo, M, c, Z, p, k, k_on, p_on, sr))
-      sr = select_support(S, S.merged, cntB, hi, lo, rowp, M, c, Z, p, k, k_on, p_on);
+    uint32_t* cntB = reinterpret_cast<uint32_t*>(S.shard);
+    SelResult sr{0u, 0ull, 0};
+    if (tid < 32) {
+      const bool ok = select_warp(S.merged, hi, lo, M, c, Z, p, k, k_on, p_on, sr);
+      if (tid == 0) S.sel_done = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (!S.sel_done) sr = select_support(S, S.merged, cntB, hi, lo, rowp, M, c, Z, p, k, k_on, p_on);
     const bool in_s = okey_of(xt) >= sr.min_key;
     const float zs = __ull2float_rn(sr.zs) * (1.0f / FX_SCALE);
     restr = in_s ? d - logf(zs) : -INFINITY;
