@@ -107,7 +107,8 @@ struct __align__(128) Smem {
   uint32_t npush;
   uint32_t nlist;
   int32_t sel_done;
-  unsigned long long bar_load, bar_mid, bar_sum, bar_hist;
+  unsigned long long bar_load[TMA_PIECES];
+  unsigned long long bar_mid, bar_sum, bar_hist;
 };
 // five CTAs per SM: 5 * (sizeof + 1 KB reserved) <= 228 KB
 static_assert(sizeof(Smem) + 1024 <= 233472 / 5, "shared memory budget of 5 CTAs per SM");
@@ -501,77 +502,144 @@ __device__ __noinline__ SelResult select_support(Smem& S, uint32_t* cnt0, uint32
 }
 
 // Selection by one warp when the first window holds every threshold (the
-// common case): keys hi, hi-1, ..., lo in blocks of 128 (4 consecutive keys
-// per lane), warp scans of (count, mass), and ballots to find the top-k and
-// nucleus boundaries.  Returns false if a threshold may lie below the window.
-__device__ __noinline__ bool select_warp(const uint32_t* cnt, int hi, int lo, float M, float c, float Z,
-                            float p, int k, bool k_on, bool p_on, SelResult& out) {
+// common case).  Keys hi, hi-1, ..., lo are taken in blocks of 128 (4
+// consecutive keys per lane): first a scan of the counts alone finds the
+// top-k boundary, then one scan of the fixed-point masses over S_k finds the
+// nucleus boundary.  Returns false if a threshold may lie below the window.
+__device__ __forceinline__ uint32_t warp_incl_scan_u32(uint32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
+}
+__device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long long v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
+}
+
+__device__ __noinline__ bool select_warp(const uint32_t* cnt, int hi, int lo, float M, float c,
+                                         float Z, float p, int k, bool k_on, bool p_on,
+                                         SelResult& out) {
+  constexpr int BLK = 4 * 32;
   const int lane = threadIdx.x & 31;
   const int n = hi - lo + 1;
   int imax = n - 1;
-  unsigned long long zk = __float2ull_rn(Z * FX_SCALE);
-  for (int stage = k_on ? 0 : 1; stage < 2; ++stage) {
-    if (stage == 1 && !p_on) break;
-    const unsigned long long T = (stage == 1) ? nucleus_bound(p, zk) : 0ull;
-    uint32_t carry_c = 0;
-    unsigned long long carry_m = 0;
-    for (int b0 = 0; b0 <= imax; b0 += 4 * 32) {
-      uint32_t cj[4];
-      unsigned long long mj[4];
-      uint32_t lc = 0;
+  uint32_t sup_k = 0;
+  // ---- top-k boundary from the counts
+  if (k_on) {
+    uint32_t carry = 0;
+    int fi = -1;
+    for (int b0 = 0; b0 < n && fi < 0; b0 += BLK) {
+      uint32_t cj[4], lc = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = b0 + 4 * lane + j;
+        cj[j] = (i < n) ? cnt[i] : 0u;
+        lc += cj[j];
+      }
+      const uint32_t ic = warp_incl_scan_u32(lc);
+      uint32_t rc = carry + ic - lc;
+      int f = -1;
+      uint32_t fc = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (f < 0 && rc < static_cast<uint32_t>(k) && rc + cj[j] >= static_cast<uint32_t>(k)) {
+          f = b0 + 4 * lane + j;
+          fc = rc + cj[j];
+        }
+        rc += cj[j];
+      }
+      const unsigned bal = __ballot_sync(0xffffffffu, f >= 0);
+      if (bal) {
+        const int src = __ffs(bal) - 1;
+        fi = __shfl_sync(0xffffffffu, f, src);
+        sup_k = __shfl_sync(0xffffffffu, fc, src);
+      }
+      carry += __shfl_sync(0xffffffffu, ic, 31);
+    }
+    if (fi < 0) return false;                  // k-th value below the window
+    imax = fi;
+  }
+  // ---- masses over S_k (all of it in one block in the common case)
+  unsigned long long zk = k_on ? 0ull : __float2ull_rn(Z * FX_SCALE);
+  const bool one_block = imax < BLK;
+  if (k_on && !one_block) {
+    for (int b0 = 0; b0 <= imax; b0 += BLK) {
       unsigned long long lm = 0;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int i = b0 + 4 * lane + j;
-        cj[j] = (i <= imax) ? cnt[i] : 0u;
-        mj[j] = cj[j] ? cj[j] * qfx(key_value(hi - i), M, c) : 0ull;
-        lc += cj[j];
-        lm += mj[j];
+        const uint32_t ci = (i <= imax) ? cnt[i] : 0u;
+        if (ci) lm += ci * qfx(key_value(hi - i), M, c);
       }
-      uint32_t ic = lc;
-      unsigned long long im = lm;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t yc = __shfl_up_sync(0xffffffffu, ic, o);
-        const unsigned long long ym = __shfl_up_sync(0xffffffffu, im, o);
-        if (lane >= o) { ic += yc; im += ym; }
-      }
-      uint32_t rc = carry_c + ic - lc;
-      unsigned long long rm = carry_m + im - lm;
-      int fi = -1;
-      uint32_t fc = 0;
-      unsigned long long fm = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int i = b0 + 4 * lane + j;
-        const bool hit = (stage == 0)
-            ? (rc < static_cast<uint32_t>(k) && rc + cj[j] >= static_cast<uint32_t>(k))
-            : (i <= imax && rm < T && (rm + mj[j] >= T || (i == imax && k_on)));
-        if (fi < 0 && hit) { fi = i; fc = rc + cj[j]; fm = rm + mj[j]; }
-        rc += cj[j];
-        rm += mj[j];
-      }
-      const unsigned bal = __ballot_sync(0xffffffffu, fi >= 0);
-      if (bal) {
-        const int src = __ffs(bal) - 1;
-        fi = __shfl_sync(0xffffffffu, fi, src);
-        fc = __shfl_sync(0xffffffffu, fc, src);
-        fm = __shfl_sync(0xffffffffu, fm, src);
-        if (stage == 0) {
-          imax = fi;
-          zk = fm;
-          out = SelResult{fc, fm, hi - fi};
-        } else {
-          out = SelResult{fc, fm, hi - fi};
-        }
-        break;
-      }
-      carry_c += __shfl_sync(0xffffffffu, ic, 31);
-      carry_m += __shfl_sync(0xffffffffu, im, 31);
-      if (b0 + 4 * 32 > imax) return false;   // boundary below the window
+      for (int o = 16; o > 0; o >>= 1) lm += __shfl_xor_sync(0xffffffffu, lm, o);
+      zk += lm;
     }
   }
-  return true;
+  if (k_on && !p_on && !one_block) {
+    out = SelResult{sup_k, zk, hi - imax};
+    return true;
+  }
+  unsigned long long T = (k_on && one_block) ? 0ull : nucleus_bound(p, zk);
+  uint32_t carry_c = 0;
+  unsigned long long carry_m = 0;
+  for (int b0 = 0; b0 <= imax; b0 += BLK) {
+    uint32_t cj[4], lc = 0;
+    unsigned long long mj[4], lm = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = b0 + 4 * lane + j;
+      cj[j] = (i <= imax) ? cnt[i] : 0u;
+      mj[j] = cj[j] ? cj[j] * qfx(key_value(hi - i), M, c) : 0ull;
+      lc += cj[j];
+      lm += mj[j];
+    }
+    const uint32_t ic = warp_incl_scan_u32(lc);
+    const unsigned long long im = warp_incl_scan_u64(lm);
+    if (k_on && one_block) {
+      zk = __shfl_sync(0xffffffffu, im, 31);   // the whole of S_k
+      if (!p_on) {
+        out = SelResult{sup_k, zk, hi - imax};
+        return true;
+      }
+      T = nucleus_bound(p, zk);
+    }
+    uint32_t rc = carry_c + ic - lc;
+    unsigned long long rm = carry_m + im - lm;
+    int f = -1;
+    uint32_t fc = 0;
+    unsigned long long fm = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = b0 + 4 * lane + j;
+      if (f < 0 && i <= imax && rm < T && (rm + mj[j] >= T || (i == imax && k_on))) {
+        f = i;
+        fc = rc + cj[j];
+        fm = rm + mj[j];
+      }
+      rc += cj[j];
+      rm += mj[j];
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, f >= 0);
+    if (bal) {
+      const int src = __ffs(bal) - 1;
+      out = SelResult{__shfl_sync(0xffffffffu, fc, src), __shfl_sync(0xffffffffu, fm, src),
+                      hi - __shfl_sync(0xffffffffu, f, src)};
+      return true;
+    }
+    carry_c += __shfl_sync(0xffffffffu, ic, 31);
+    carry_m += __shfl_sync(0xffffffffu, im, 31);
+  }
+  return false;                                  // nucleus reaches below the window
 }
 
 // ------------------------------------------------------------ the kernel
@@ -611,26 +679,31 @@ logp_kernel(const KParams P) {
   const uint16_t* rowp = P.logits + row * P.stride;
   // the leader needs the target's logit at the end: start the load now
   const float xt = (r == 0) ? __uint_as_float(static_cast<uint32_t>(__ldg(rowp + t)) << 16) : 0.0f;
-  const uint32_t bar_load = smem_addr(&S.bar_load);
   const uint32_t bar_mid = smem_addr(&S.bar_mid);
   const uint32_t bar_sum = smem_addr(&S.bar_sum);
   const uint32_t bar_hist = smem_addr(&S.bar_hist);
 
-  // ---- 1. barriers, and the bulk copy of the shard into shared memory
+  // ---- 1. barriers, and the bulk copy of the shard into shared memory in
+  //         TMA_PIECES pieces, each with its own barrier so work can start on
+  //         the first piece while the others are in flight
+  const uint32_t piece_chunks = static_cast<uint32_t>(nchunks) / TMA_PIECES;
   if (tid == 0) {
-    mbar_init(bar_load, 1);
+#pragma unroll
+    for (int q = 0; q < TMA_PIECES; ++q) mbar_init(smem_addr(&S.bar_load[q]), 1);
     mbar_init(bar_mid, 1);
     mbar_init(bar_sum, 1);
     mbar_init(bar_hist, 1);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    const uint32_t bytes = static_cast<uint32_t>(nchunks) * 16u;
-    mbar_arrive_expect_tx(bar_load, bytes);
     const uint64_t pol = evict_first_policy();
-    const uint32_t piece = bytes / TMA_PIECES;
+    const uint32_t piece = piece_chunks * 16u;
     const char* src = reinterpret_cast<const char*>(rowp + static_cast<int64_t>(r) * SW);
     const uint32_t dst = smem_addr(S.shard);
 #pragma unroll
-    for (int i = 0; i < TMA_PIECES; ++i) bulk_load(dst + i * piece, src + i * piece, piece, bar_load, pol);
+    for (int q = 0; q < TMA_PIECES; ++q) {
+      const uint32_t b = smem_addr(&S.bar_load[q]);
+      mbar_arrive_expect_tx(b, piece);
+      bulk_load(dst + q * piece, src + q * piece, piece, b, pol);
+    }
     // messages from the 7 peers: 16 bytes each
     if (sel) mbar_arrive_expect_tx(bar_mid, (NSHARD - 1) * 16);
     if (r == 0) mbar_arrive_expect_tx(bar_sum, (NSHARD - 1) * 16);
@@ -645,30 +718,68 @@ logp_kernel(const KParams P) {
   }
   cluster_arrive();            // S0: barriers initialised, leader histogram zeroed
   __syncthreads();
-  uint32_t flags = 0;
-  if (!mbar_wait_bounded(bar_load)) {
-    flags |= FLAG_TIMEOUT;
-    mbar_wait_bounded(bar_load);   // give copies in flight a second bounded chance to land
-  }
 
-  // ---- 2. shard maximum; per-chunk maxima stay in registers for the candidate pass.
-  // bf16 max ignores NaN; a NaN shows up as a NaN sum-exp (or in the scan below).
+  // ---- 2. one pass over the shard: per-thread running maximum and sum-exp.
+  // Thread t owns 16-byte chunks t, t+256, ... in that order and keeps even and
+  // odd columns in the two lanes of a packed f32x2 accumulator, relative to its
+  // running maximum (rescaled when the maximum rises).  bf16 max ignores NaN;
+  // a NaN still reaches the sum (or the all -inf chunk check) and marks the row.
   const uint4* sh = S.shard;
   const __nv_bfloat162 ninf2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+  const float c = greedy ? 0.0f : __fdiv_rn(LOG2E, tau);
+  const uint64_t c2 = pack2(c, c);
   __nv_bfloat162 cm[KEEPCH];      // later chunks' maxima are recomputed when needed
-  __nv_bfloat162 m2 = ninf2;
+  float mt = -INFINITY;
+  uint64_t acc = pack2(0.0f, 0.0f);
+  uint32_t flags = 0;
+  bool nan_seen = false;
+  int waited = -1;
 #pragma unroll
   for (int i = 0; i < MAXCH; ++i) {
     const int ch = tid + i * NTHR;
     __nv_bfloat162 cmax = ninf2;
     if (ch < nchunks) {
+      const int q = min(static_cast<int>(static_cast<uint32_t>(ch) / piece_chunks), TMA_PIECES - 1);
+      if (q > waited) {
+        for (int qq = waited + 1; qq <= q; ++qq)
+          if (!mbar_wait_bounded(smem_addr(&S.bar_load[qq]))) flags |= FLAG_TIMEOUT;
+        waited = q;
+      }
       const uint4 v = sh[ch];
       cmax = __hmax2(__hmax2(as_bf2(v.x), as_bf2(v.y)), __hmax2(as_bf2(v.z), as_bf2(v.w)));
-      m2 = __hmax2(m2, cmax);
+      const float mx = fmaxf(__low2float(cmax), __high2float(cmax));
+      if (mx == -INFINITY || greedy) {
+        // no sum-exp sees these elements: check them for NaN directly
+        nan_seen |= (__hne2_mask(as_bf2(v.x), as_bf2(v.x)) | __hne2_mask(as_bf2(v.y), as_bf2(v.y)) |
+                     __hne2_mask(as_bf2(v.z), as_bf2(v.z)) | __hne2_mask(as_bf2(v.w), as_bf2(v.w))) != 0u;
+        mt = fmaxf(mt, mx);
+      } else {
+        if (mx > mt) {
+          if (mt > -INFINITY) {
+            const float sc = ex2((mt - mx) * c);
+            acc = mul2(acc, pack2(sc, sc));
+          }
+          mt = mx;
+        }
+        const uint64_t nmt2 = pack2(-mt, -mt);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint64_t a = mul2(add2(pack2(bf16_lo(w[j]), bf16_hi(w[j])), nmt2), c2);
+          float a0, a1;
+          unpack2(a, a0, a1);
+          acc = add2(acc, pack2(ex2(a0), ex2(a1)));
+        }
+      }
     }
     if (i < KEEPCH) cm[i] = cmax;
   }
-  const int tkey = okey_of(fmaxf(__low2float(m2), __high2float(m2)));
+  if (waited < TMA_PIECES - 1) {
+    // threads without chunks in the last pieces still keep the copies' landing in view
+    for (int qq = waited + 1; qq < TMA_PIECES; ++qq)
+      if (!mbar_wait_bounded(smem_addr(&S.bar_load[qq]))) flags |= FLAG_TIMEOUT;
+  }
+  const int tkey = okey_of(mt);
   // Pooled top-k bound: warp w certifies kw = ceil(k/64) lane maxima at or above
   // lw (its kw-th largest lane maximum), so the 64 warps of the row certify
   // 64*kw >= k tokens at or above the minimum of lw over the cluster.
@@ -680,7 +791,7 @@ logp_kernel(const KParams P) {
     const unsigned wmax = __reduce_max_sync(0xffffffffu, static_cast<unsigned>(tkey));
     if (lane == 0) { S.red_u[warp] = wmax; S.red_i[warp] = lw; }
   }
-  __syncthreads();
+  if (__syncthreads_or(nan_seen)) flags |= FLAG_NAN;
   unsigned xkey = S.red_u[0];
   int lkey = S.red_i[0];
 #pragma unroll
@@ -689,25 +800,20 @@ logp_kernel(const KParams P) {
   const bool xm_finite = (xm > -INFINITY) && (xm < INFINITY);
 
   uint32_t first = 0x7fffffffu;
-  if (greedy || xm == -INFINITY) {
-    // greedy: first column of this shard holding its maximum; both cases: NaN scan
-    bool nan_seen = false;
+  if (greedy && xm_finite) {
+    // first column of this shard holding its maximum
     int f = 0x7fffffff;
-    for (int ch = tid; ch < nchunks; ch += NTHR) {
+    for (int ch = tid; ch < nchunks && f == 0x7fffffff; ch += NTHR) {
       const uint4 v = sh[ch];
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int j = 7; j >= 0; --j) {
         const float x = (j & 1) ? bf16_hi(w[j >> 1]) : bf16_lo(w[j >> 1]);
-        nan_seen |= (x != x);
-        if (x == xm) f = min(f, ch * 8 + j);
+        if (x == xm) f = ch * 8 + j;
       }
     }
-    if (__syncthreads_or(nan_seen)) flags |= FLAG_NAN;
-    if (greedy) {
-      f = block_min_int(f, S);
-      if (f != 0x7fffffff) first = static_cast<uint32_t>(f + static_cast<int>(r) * SW);
-    }
+    f = block_min_int(f, S);
+    if (f != 0x7fffffff) first = static_cast<uint32_t>(f + static_cast<int>(r) * SW);
   }
 
   cluster_wait();              // S0 complete: peers' barriers and histogram are ready
@@ -719,27 +825,14 @@ logp_kernel(const KParams P) {
       st_async_v4(map_rank(smem_addr(&S.mid[r]), tid), msg, map_rank(bar_mid, tid));
   }
 
-  // ---- 3. shard sum-exp, fixed tree
+  // ---- 3. shard sum-exp: thread sums brought to the shard maximum, then a
+  //         fixed tree (shuffle-xor butterfly, left fold over warps)
   float l = 0.0f;
   if (!greedy && xm_finite) {
-    const float c = __fdiv_rn(LOG2E, tau);
-    const uint64_t nxm2 = pack2(-xm, -xm);
-    const uint64_t c2 = pack2(c, c);
-    uint64_t acc = pack2(0.0f, 0.0f);
-    for (int ch = tid; ch < nchunks; ch += NTHR) {
-      const uint4 v = sh[ch];
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint64_t a = mul2(add2(pack2(bf16_lo(w[j]), bf16_hi(w[j])), nxm2), c2);
-        float a0, a1;
-        unpack2(a, a0, a1);
-        acc = add2(acc, pack2(ex2(a0), ex2(a1)));
-      }
-    }
     float e0, e1;
     unpack2(acc, e0, e1);
-    l = block_sum_fixed(e0 + e1, S);
+    const float lt = (mt > -INFINITY) ? (e0 + e1) * ex2((mt - xm) * c) : 0.0f;
+    l = block_sum_fixed(lt, S);
   }
 
   // ---- 4. candidate pass: exact per-key counts into the leader's histogram
@@ -883,7 +976,7 @@ logp_kernel(const KParams P) {
   const float qnan = __int_as_float(0x7fc00000);
   float full = qnan, restr = qnan;
   int support = -1;
-  float c = 0.0f, Z = 0.0f, d = 0.0f;
+  float Z = 0.0f, d = 0.0f;
   if (!bad && greedy) {
     uint32_t amax = 0x7fffffffu;
 #pragma unroll
@@ -892,7 +985,6 @@ logp_kernel(const KParams P) {
     full = restr = (static_cast<uint32_t>(t) == amax) ? 0.0f : -INFINITY;
     support = 1;
   } else if (!bad) {
-    c = __fdiv_rn(LOG2E, tau);
     if (isinf(__fdiv_rn(M, tau))) {
       bad = true;
     } else {
