@@ -750,8 +750,8 @@ logp_kernel(const KParams P) {
       const float mx = fmaxf(__low2float(cmax), __high2float(cmax));
       if (mx == -INFINITY || greedy) {
         // no sum-exp sees these elements: check them for NaN directly
-        nan_seen |= (__hne2_mask(as_bf2(v.x), as_bf2(v.x)) | __hne2_mask(as_bf2(v.y), as_bf2(v.y)) |
-                     __hne2_mask(as_bf2(v.z), as_bf2(v.z)) | __hne2_mask(as_bf2(v.w), as_bf2(v.w))) != 0u;
+        nan_seen |= (__hneu2_mask(as_bf2(v.x), as_bf2(v.x)) | __hneu2_mask(as_bf2(v.y), as_bf2(v.y)) |
+                     __hneu2_mask(as_bf2(v.z), as_bf2(v.z)) | __hneu2_mask(as_bf2(v.w), as_bf2(v.w))) != 0u;
         mt = fmaxf(mt, mx);
       } else {
         if (mx > mt) {

@@ -131,15 +131,21 @@ def test_padding_is_ignored_and_nonfinite_rows():
     inf_row[151935] = 0x7F80
     allneg = _row(float("-inf"))
     two = _row(float("-inf"), {7: 0.0, 8: 0.0})
-    x = rows_from_bits(np.stack(rows + [nan_row, inf_row, allneg, two, two]))
-    t = _t([1237, 1237, 1237, 1237, 0, 7, 9], torch.int32)
+    nan_chunk = _row(-3.0, base)
+    nan_chunk[800:808] = 0x7FC1          # a whole 16-byte chunk of NaN
+    x = rows_from_bits(np.stack(rows + [nan_row, inf_row, allneg, two, two, nan_chunk]))
+    t = _t([1237, 1237, 1237, 1237, 0, 7, 9, 1237], torch.int32)
     f, r, s = run_pair(x, t, 0.9, 0.9, 64)
     assert f[0] == f[1] and r[0] == r[1] and s[0] == s[1]
-    for i in (2, 3, 4):
-        assert math.isnan(f[i]) and math.isnan(r[i]) and s[i] == -1
+    for i in (2, 3, 4, 7):
+        assert math.isnan(f[i]) and math.isnan(r[i]) and s[i] == -1, i
     assert abs(f[5] + math.log(2)) <= TOL and f[6] == -math.inf
-    # greedy on NaN rows is NaN too
-    f, r, s = run_pair(x[2:5], t[2:5], 0.0, 1.0, -1)
+    # full-only and greedy on NaN rows are NaN too
+    f1 = pkg.logp_full(x, t, 0.9)
+    torch.cuda.synchronize()
+    assert all(math.isnan(f1[i].item()) for i in (2, 3, 4, 7))
+    sel = [2, 3, 4, 7]
+    f, r, s = run_pair(x[sel], t[sel], 0.0, 1.0, -1)
     assert all(math.isnan(v) for v in f) and all(v == -1 for v in s)
 
 
