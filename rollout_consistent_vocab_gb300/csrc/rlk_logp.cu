@@ -107,8 +107,7 @@ struct __align__(128) Smem {
   uint32_t npush;
   uint32_t nlist;
   int32_t sel_done;
-  unsigned long long bar_load[TMA_PIECES];
-  unsigned long long bar_mid, bar_sum, bar_hist;
+  unsigned long long bar_load, bar_mid, bar_sum, bar_hist;
 };
 // five CTAs per SM: 5 * (sizeof + 1 KB reserved) <= 228 KB
 static_assert(sizeof(Smem) + 1024 <= 233472 / 5, "shared memory budget of 5 CTAs per SM");
@@ -679,31 +678,26 @@ logp_kernel(const KParams P) {
   const uint16_t* rowp = P.logits + row * P.stride;
   // the leader needs the target's logit at the end: start the load now
   const float xt = (r == 0) ? __uint_as_float(static_cast<uint32_t>(__ldg(rowp + t)) << 16) : 0.0f;
+  const uint32_t bar_load = smem_addr(&S.bar_load);
   const uint32_t bar_mid = smem_addr(&S.bar_mid);
   const uint32_t bar_sum = smem_addr(&S.bar_sum);
   const uint32_t bar_hist = smem_addr(&S.bar_hist);
 
-  // ---- 1. barriers, and the bulk copy of the shard into shared memory in
-  //         TMA_PIECES pieces, each with its own barrier so work can start on
-  //         the first piece while the others are in flight
-  const uint32_t piece_chunks = static_cast<uint32_t>(nchunks) / TMA_PIECES;
+  // ---- 1. barriers, and the bulk copy of the shard into shared memory
   if (tid == 0) {
-#pragma unroll
-    for (int q = 0; q < TMA_PIECES; ++q) mbar_init(smem_addr(&S.bar_load[q]), 1);
+    mbar_init(bar_load, 1);
     mbar_init(bar_mid, 1);
     mbar_init(bar_sum, 1);
     mbar_init(bar_hist, 1);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    const uint32_t bytes = static_cast<uint32_t>(nchunks) * 16u;
+    mbar_arrive_expect_tx(bar_load, bytes);
     const uint64_t pol = evict_first_policy();
-    const uint32_t piece = piece_chunks * 16u;
+    const uint32_t piece = bytes / TMA_PIECES;
     const char* src = reinterpret_cast<const char*>(rowp + static_cast<int64_t>(r) * SW);
     const uint32_t dst = smem_addr(S.shard);
 #pragma unroll
-    for (int q = 0; q < TMA_PIECES; ++q) {
-      const uint32_t b = smem_addr(&S.bar_load[q]);
-      mbar_arrive_expect_tx(b, piece);
-      bulk_load(dst + q * piece, src + q * piece, piece, b, pol);
-    }
+    for (int i = 0; i < TMA_PIECES; ++i) bulk_load(dst + i * piece, src + i * piece, piece, bar_load, pol);
     // messages from the 7 peers: 16 bytes each
     if (sel) mbar_arrive_expect_tx(bar_mid, (NSHARD - 1) * 16);
     if (r == 0) mbar_arrive_expect_tx(bar_sum, (NSHARD - 1) * 16);
@@ -718,68 +712,30 @@ logp_kernel(const KParams P) {
   }
   cluster_arrive();            // S0: barriers initialised, leader histogram zeroed
   __syncthreads();
+  uint32_t flags = 0;
+  if (!mbar_wait_bounded(bar_load)) {
+    flags |= FLAG_TIMEOUT;
+    mbar_wait_bounded(bar_load);   // give copies in flight a second bounded chance to land
+  }
 
-  // ---- 2. one pass over the shard: per-thread running maximum and sum-exp.
-  // Thread t owns 16-byte chunks t, t+256, ... in that order and keeps even and
-  // odd columns in the two lanes of a packed f32x2 accumulator, relative to its
-  // running maximum (rescaled when the maximum rises).  bf16 max ignores NaN;
-  // a NaN still reaches the sum (or the all -inf chunk check) and marks the row.
+  // ---- 2. shard maximum; per-chunk maxima stay in registers for the candidate pass.
+  // bf16 max ignores NaN; a NaN shows up as a NaN sum-exp (or in the scan below).
   const uint4* sh = S.shard;
   const __nv_bfloat162 ninf2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
-  const float c = greedy ? 0.0f : __fdiv_rn(LOG2E, tau);
-  const uint64_t c2 = pack2(c, c);
   __nv_bfloat162 cm[KEEPCH];      // later chunks' maxima are recomputed when needed
-  float mt = -INFINITY;
-  uint64_t acc = pack2(0.0f, 0.0f);
-  uint32_t flags = 0;
-  bool nan_seen = false;
-  int waited = -1;
+  __nv_bfloat162 m2 = ninf2;
 #pragma unroll
   for (int i = 0; i < MAXCH; ++i) {
     const int ch = tid + i * NTHR;
     __nv_bfloat162 cmax = ninf2;
     if (ch < nchunks) {
-      const int q = min(static_cast<int>(static_cast<uint32_t>(ch) / piece_chunks), TMA_PIECES - 1);
-      if (q > waited) {
-        for (int qq = waited + 1; qq <= q; ++qq)
-          if (!mbar_wait_bounded(smem_addr(&S.bar_load[qq]))) flags |= FLAG_TIMEOUT;
-        waited = q;
-      }
       const uint4 v = sh[ch];
       cmax = __hmax2(__hmax2(as_bf2(v.x), as_bf2(v.y)), __hmax2(as_bf2(v.z), as_bf2(v.w)));
-      const float mx = fmaxf(__low2float(cmax), __high2float(cmax));
-      if (mx == -INFINITY || greedy) {
-        // no sum-exp sees these elements: check them for NaN directly
-        nan_seen |= (__hneu2_mask(as_bf2(v.x), as_bf2(v.x)) | __hneu2_mask(as_bf2(v.y), as_bf2(v.y)) |
-                     __hneu2_mask(as_bf2(v.z), as_bf2(v.z)) | __hneu2_mask(as_bf2(v.w), as_bf2(v.w))) != 0u;
-        mt = fmaxf(mt, mx);
-      } else {
-        if (mx > mt) {
-          if (mt > -INFINITY) {
-            const float sc = ex2((mt - mx) * c);
-            acc = mul2(acc, pack2(sc, sc));
-          }
-          mt = mx;
-        }
-        const uint64_t nmt2 = pack2(-mt, -mt);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint64_t a = mul2(add2(pack2(bf16_lo(w[j]), bf16_hi(w[j])), nmt2), c2);
-          float a0, a1;
-          unpack2(a, a0, a1);
-          acc = add2(acc, pack2(ex2(a0), ex2(a1)));
-        }
-      }
+      m2 = __hmax2(m2, cmax);
     }
     if (i < KEEPCH) cm[i] = cmax;
   }
-  if (waited < TMA_PIECES - 1) {
-    // threads without chunks in the last pieces still keep the copies' landing in view
-    for (int qq = waited + 1; qq < TMA_PIECES; ++qq)
-      if (!mbar_wait_bounded(smem_addr(&S.bar_load[qq]))) flags |= FLAG_TIMEOUT;
-  }
-  const int tkey = okey_of(mt);
+  const int tkey = okey_of(fmaxf(__low2float(m2), __high2float(m2)));
   // Pooled top-k bound: warp w certifies kw = ceil(k/64) lane maxima at or above
   // lw (its kw-th largest lane maximum), so the 64 warps of the row certify
   // 64*kw >= k tokens at or above the minimum of lw over the cluster.
@@ -791,7 +747,7 @@ logp_kernel(const KParams P) {
     const unsigned wmax = __reduce_max_sync(0xffffffffu, static_cast<unsigned>(tkey));
     if (lane == 0) { S.red_u[warp] = wmax; S.red_i[warp] = lw; }
   }
-  if (__syncthreads_or(nan_seen)) flags |= FLAG_NAN;
+  __syncthreads();
   unsigned xkey = S.red_u[0];
   int lkey = S.red_i[0];
 #pragma unroll
@@ -800,20 +756,25 @@ logp_kernel(const KParams P) {
   const bool xm_finite = (xm > -INFINITY) && (xm < INFINITY);
 
   uint32_t first = 0x7fffffffu;
-  if (greedy && xm_finite) {
-    // first column of this shard holding its maximum
+  if (greedy || xm == -INFINITY) {
+    // greedy: first column of this shard holding its maximum; both cases: NaN scan
+    bool nan_seen = false;
     int f = 0x7fffffff;
-    for (int ch = tid; ch < nchunks && f == 0x7fffffff; ch += NTHR) {
+    for (int ch = tid; ch < nchunks; ch += NTHR) {
       const uint4 v = sh[ch];
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int j = 7; j >= 0; --j) {
         const float x = (j & 1) ? bf16_hi(w[j >> 1]) : bf16_lo(w[j >> 1]);
-        if (x == xm) f = ch * 8 + j;
+        nan_seen |= (x != x);
+        if (x == xm) f = min(f, ch * 8 + j);
       }
     }
-    f = block_min_int(f, S);
-    if (f != 0x7fffffff) first = static_cast<uint32_t>(f + static_cast<int>(r) * SW);
+    if (__syncthreads_or(nan_seen)) flags |= FLAG_NAN;
+    if (greedy) {
+      f = block_min_int(f, S);
+      if (f != 0x7fffffff) first = static_cast<uint32_t>(f + static_cast<int>(r) * SW);
+    }
   }
 
   cluster_wait();              // S0 complete: peers' barriers and histogram are ready
@@ -825,14 +786,27 @@ logp_kernel(const KParams P) {
       st_async_v4(map_rank(smem_addr(&S.mid[r]), tid), msg, map_rank(bar_mid, tid));
   }
 
-  // ---- 3. shard sum-exp: thread sums brought to the shard maximum, then a
-  //         fixed tree (shuffle-xor butterfly, left fold over warps)
+  // ---- 3. shard sum-exp, fixed tree
   float l = 0.0f;
   if (!greedy && xm_finite) {
+    const float c = __fdiv_rn(LOG2E, tau);
+    const uint64_t nxm2 = pack2(-xm, -xm);
+    const uint64_t c2 = pack2(c, c);
+    uint64_t acc = pack2(0.0f, 0.0f);
+    for (int ch = tid; ch < nchunks; ch += NTHR) {
+      const uint4 v = sh[ch];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint64_t a = mul2(add2(pack2(bf16_lo(w[j]), bf16_hi(w[j])), nxm2), c2);
+        float a0, a1;
+        unpack2(a, a0, a1);
+        acc = add2(acc, pack2(ex2(a0), ex2(a1)));
+      }
+    }
     float e0, e1;
     unpack2(acc, e0, e1);
-    const float lt = (mt > -INFINITY) ? (e0 + e1) * ex2((mt - xm) * c) : 0.0f;
-    l = block_sum_fixed(lt, S);
+    l = block_sum_fixed(e0 + e1, S);
   }
 
   // ---- 4. candidate pass: exact per-key counts into the leader's histogram
@@ -977,6 +951,7 @@ logp_kernel(const KParams P) {
   float full = qnan, restr = qnan;
   int support = -1;
   float Z = 0.0f, d = 0.0f;
+  const float c = greedy ? 0.0f : __fdiv_rn(LOG2E, tau);
   if (!bad && greedy) {
     uint32_t amax = 0x7fffffffu;
 #pragma unroll
