@@ -62,7 +62,6 @@ constexpr int MAXCH = (SHARD_CHUNKS + NTHR - 1) / NTHR;     // chunks per thread
 constexpr int KEEPCH = 7;            // chunk maxima kept in registers; the rest are recomputed
 constexpr int WIN = 1024;            // candidate window, in bf16 order keys (8 binades)
 constexpr int TMA_PIECES = 4;
-constexpr int CLIST = 256;           // capacity of the candidate-chunk list
 constexpr float LOG2E = 1.4426950408889634f;   // log2(e)
 constexpr float FX_SCALE = 17592186044416.0f;  // 2^44: fixed-point scale of masses
 constexpr unsigned long long TIMEOUT_NS = 200000000ull;   // 0.2 s bound on every wait
@@ -93,7 +92,7 @@ struct __align__(128) Smem {
   uint4 shard[SHARD_CHUNKS];       // 38144 B; the leader reuses it as scratch at the end
   uint32_t merged[WIN];            // leader: per-key candidate counts of the whole row
   uint32_t hist[WIN / 2];          // this shard's per-key candidate counts (u16 pairs)
-  uint16_t clist[CLIST];           // chunks holding candidates, processed element-parallel
+  uint16_t clist[NWARP * 32];      // per-warp lists of chunks holding candidates
   MidSlot mid[NSHARD];
   Summary slot[NSHARD];
   uint32_t red_u[NWARP];
@@ -105,7 +104,6 @@ struct __align__(128) Smem {
   uint32_t found_c;
   unsigned long long found_m;
   uint32_t npush;
-  uint32_t nlist;
   int32_t sel_done;
   unsigned long long bar_load, bar_mid, bar_sum, bar_hist;
 };
@@ -652,43 +650,16 @@ logp_kernel(const KParams P) {
   const uint32_t r = cluster_rank();
   const int64_t row = blockIdx.x / NSHARD;
 
-  // ---- row parameters (every CTA of the cluster takes the same decisions)
-  const float tau = P.tau_arr ? P.tau_arr[row] : P.tau_s;
-  const float p = RESTR ? (P.p_arr ? P.p_arr[row] : P.p_s) : 1.0f;
-  const int k = RESTR ? (P.k_arr ? P.k_arr[row] : P.k_s) : -1;
-  const int t = P.target[row];
-  const bool valid = (tau >= 0.0f) && (tau <= 3.402823466e38f) && (p > 0.0f) && (p <= 1.0f) &&
-                     (k == -1 || (k >= 1 && k <= VREAL)) && (t >= 0) && (t < VREAL);
-  if (!valid) {
-    if (r == 0 && tid == 0) {
-      if (P.out_full) P.out_full[row] = __int_as_float(0x7fc00000);
-      if (RESTR && P.out_restr) P.out_restr[row] = __int_as_float(0x7fc00000);
-      if (RESTR && P.out_support) P.out_support[row] = -1;
-      if (P.out_kl) P.out_kl[row] = __int_as_float(0x7fc00000);
-      if (P.err) atomicAdd(P.err, 1);
-    }
-    return;
-  }
-  const bool greedy = (tau == 0.0f);
-  const bool k_on = (k != -1) && (k < VREAL);
-  const bool p_on = (p < 1.0f);
-  const bool sel = RESTR && !greedy && (k_on || p_on);
-
   const int nchunks = (r == NSHARD - 1) ? LAST_CHUNKS : SHARD_CHUNKS;
   const uint16_t* rowp = P.logits + row * P.stride;
-  // the leader needs the target's logit at the end: start the load now
-  const float xt = (r == 0) ? __uint_as_float(static_cast<uint32_t>(__ldg(rowp + t)) << 16) : 0.0f;
   const uint32_t bar_load = smem_addr(&S.bar_load);
   const uint32_t bar_mid = smem_addr(&S.bar_mid);
   const uint32_t bar_sum = smem_addr(&S.bar_sum);
   const uint32_t bar_hist = smem_addr(&S.bar_hist);
 
-  // ---- 1. barriers, and the bulk copy of the shard into shared memory
+  // ---- 1. the bulk copy of the shard into shared memory goes out first
   if (tid == 0) {
     mbar_init(bar_load, 1);
-    mbar_init(bar_mid, 1);
-    mbar_init(bar_sum, 1);
-    mbar_init(bar_hist, 1);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     const uint32_t bytes = static_cast<uint32_t>(nchunks) * 16u;
     mbar_arrive_expect_tx(bar_load, bytes);
@@ -698,12 +669,46 @@ logp_kernel(const KParams P) {
     const uint32_t dst = smem_addr(S.shard);
 #pragma unroll
     for (int i = 0; i < TMA_PIECES; ++i) bulk_load(dst + i * piece, src + i * piece, piece, bar_load, pol);
+  }
+
+  // ---- row parameters (every CTA of the cluster takes the same decisions)
+  const float tau = P.tau_arr ? P.tau_arr[row] : P.tau_s;
+  const float p = RESTR ? (P.p_arr ? P.p_arr[row] : P.p_s) : 1.0f;
+  const int k = RESTR ? (P.k_arr ? P.k_arr[row] : P.k_s) : -1;
+  const int t = P.target[row];
+  const bool valid = (tau >= 0.0f) && (tau <= 3.402823466e38f) && (p > 0.0f) && (p <= 1.0f) &&
+                     (k == -1 || (k >= 1 && k <= VREAL)) && (t >= 0) && (t < VREAL);
+  if (!valid) {
+    if (tid == 0) {
+      // the copy writes this CTA's shared memory: let it land before leaving
+      mbar_wait_bounded(bar_load);
+      if (r == 0) {
+        if (P.out_full) P.out_full[row] = __int_as_float(0x7fc00000);
+        if (RESTR && P.out_restr) P.out_restr[row] = __int_as_float(0x7fc00000);
+        if (RESTR && P.out_support) P.out_support[row] = -1;
+        if (P.out_kl) P.out_kl[row] = __int_as_float(0x7fc00000);
+        if (P.err) atomicAdd(P.err, 1);
+      }
+    }
+    return;
+  }
+  const bool greedy = (tau == 0.0f);
+  const bool k_on = (k != -1) && (k < VREAL);
+  const bool p_on = (p < 1.0f);
+  const bool sel = RESTR && !greedy && (k_on || p_on);
+  // the leader needs the target's logit at the end: start the load now
+  const float xt = (r == 0) ? __uint_as_float(static_cast<uint32_t>(__ldg(rowp + t)) << 16) : 0.0f;
+
+  // ---- barriers that peers signal, and the leader's histogram
+  if (tid == 0) {
+    mbar_init(bar_mid, 1);
+    mbar_init(bar_sum, 1);
+    mbar_init(bar_hist, 1);
     // messages from the 7 peers: 16 bytes each
     if (sel) mbar_arrive_expect_tx(bar_mid, (NSHARD - 1) * 16);
     if (r == 0) mbar_arrive_expect_tx(bar_sum, (NSHARD - 1) * 16);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     S.npush = 0u;
-    S.nlist = 0u;
   }
   if (sel) {
     if (r == 0)
@@ -856,7 +861,8 @@ logp_kernel(const KParams P) {
           if (__hge2_mask(cmax, vlo2) != 0u) hitmask |= 1u << i;
         }
       }
-      // warp-aggregated append of those chunks to the CTA list
+      // this warp's chunks with candidates go to the warp's own list (32 slots;
+      // more are counted directly), then 8 lanes take one listed chunk each round
       const int lane = tid & 31;
       const int h = __popc(hitmask);
       int incl = h;
@@ -865,17 +871,16 @@ logp_kernel(const KParams P) {
         const int y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
-      int base = 0;
-      if (lane == 31 && incl > 0) base = static_cast<int>(atomicAdd(&S.nlist, static_cast<uint32_t>(incl)));
-      int pos = __shfl_sync(0xffffffffu, base, 31) + incl - h;
+      const int wtot = __shfl_sync(0xffffffffu, incl, 31);
+      uint16_t* wl = S.clist + (tid >> 5) * 32;
+      int pos = incl - h;
       while (hitmask) {
         const int i = __ffs(hitmask) - 1;
         hitmask &= hitmask - 1;
         const int ch = tid + i * NTHR;
-        if (pos < CLIST) {
-          S.clist[pos] = static_cast<uint16_t>(ch);
+        if (pos < 32) {
+          wl[pos] = static_cast<uint16_t>(ch);
         } else {
-          // list full: count this chunk here
           const uint4 v = sh[ch];
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -890,12 +895,11 @@ logp_kernel(const KParams P) {
         }
         ++pos;
       }
-      __syncthreads();
-      // listed chunks, one element per thread
-      const int nl = min(static_cast<int>(S.nlist), CLIST);
+      __syncwarp();
+      const int nl = min(wtot, 32);
       const uint16_t* elem = reinterpret_cast<const uint16_t*>(S.shard);
-      for (int e = tid >> 3; e < nl; e += NTHR / 8) {
-        const uint32_t b = elem[static_cast<int>(S.clist[e]) * 8 + (tid & 7)];
+      for (int e = lane >> 3; e < nl; e += 4) {
+        const uint32_t b = elem[static_cast<int>(wl[e]) * 8 + (lane & 7)];
         if (__uint_as_float(b << 16) >= vlo_f) {
           const int idx = hi - okey(b);
           if (r == 0) red_shared_add(&cnt_local[idx], 1u);
