@@ -522,7 +522,7 @@ __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long l
   return v;
 }
 
-__device__ __noinline__ bool select_warp(const uint32_t* cnt, int hi, int lo, float M, float c,
+__device__ __forceinline__ bool select_warp(const uint32_t* cnt, int hi, int lo, float M, float c,
                                          float Z, float p, int k, bool k_on, bool p_on,
                                          SelResult& out) {
   constexpr int BLK = 4 * 32;
