@@ -137,8 +137,8 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -188,13 +188,16 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+// One test of a barrier phase; a thread whose phase is not complete sleeps
+// (up to 20 us) instead of spinning, so waiting warps leave the issue slots
+// to working ones.
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+      : "=r"(ok) : "r"(bar), "r"(parity), "r"(20000u) : "memory");
   return ok != 0;
 }
 // Bounded wait on phase 0 of a barrier: gives up after TIMEOUT_NS of wall time.
@@ -707,7 +710,6 @@ logp_kernel(const KParams P) {
     // messages from the 7 peers: 16 bytes each
     if (sel) mbar_arrive_expect_tx(bar_mid, (NSHARD - 1) * 16);
     if (r == 0) mbar_arrive_expect_tx(bar_sum, (NSHARD - 1) * 16);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     S.npush = 0u;
   }
   if (sel) {
@@ -715,8 +717,15 @@ logp_kernel(const KParams P) {
       for (int i = tid; i < WIN; i += NTHR) S.merged[i] = 0u;
     for (int i = tid; i < WIN / 2; i += NTHR) S.hist[i] = 0u;
   }
-  cluster_arrive();            // S0: barriers initialised, leader histogram zeroed
   __syncthreads();
+  // S0: barriers initialised and the leader's histogram zeroed.  One thread
+  // publishes all of it to the cluster (the block barrier above orders the
+  // other threads' stores before its fence); everyone arrives relaxed.
+  if (tid == 0) {
+    if (sel && r == 0) asm volatile("fence.acq_rel.cluster;" ::: "memory");
+    else asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  cluster_arrive_relaxed();
   uint32_t flags = 0;
   if (!mbar_wait_bounded(bar_load)) {
     flags |= FLAG_TIMEOUT;
