@@ -59,7 +59,7 @@ constexpr int LAST_CHUNKS = (VREAL - (NSHARD - 1) * SW) / 8;  // 2304 real chunk
 constexpr int NTHR = 256;
 constexpr int NWARP = NTHR / 32;
 constexpr int MAXCH = (SHARD_CHUNKS + NTHR - 1) / NTHR;     // chunks per thread (9 or 10)
-constexpr int KEEPCH = 7;            // chunk maxima kept in registers; the rest are recomputed
+constexpr int KEEPCH = MAXCH;        // chunk maxima kept in registers
 constexpr int WIN = 1024;            // candidate window, in bf16 order keys (8 binades)
 constexpr int TMA_PIECES = 4;
 constexpr float LOG2E = 1.4426950408889634f;   // log2(e)
@@ -104,6 +104,7 @@ struct __align__(128) Smem {
   uint32_t found_c;
   unsigned long long found_m;
   uint32_t npush;
+  int32_t win[4];
   int32_t sel_done;
   unsigned long long bar_load, bar_mid, bar_sum, bar_hist;
 };
@@ -800,55 +801,42 @@ logp_kernel(const KParams P) {
       st_async_v4(map_rank(smem_addr(&S.mid[r]), tid), msg, map_rank(bar_mid, tid));
   }
 
-  // ---- 3. shard sum-exp, fixed tree
-  float l = 0.0f;
-  if (!greedy && xm_finite) {
-    const float c = __fdiv_rn(LOG2E, tau);
-    const uint64_t nxm2 = pack2(-xm, -xm);
-    const uint64_t c2 = pack2(c, c);
-    uint64_t acc = pack2(0.0f, 0.0f);
-    for (int ch = tid; ch < nchunks; ch += NTHR) {
-      const uint4 v = sh[ch];
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint64_t a = mul2(add2(pack2(bf16_lo(w[j]), bf16_hi(w[j])), nxm2), c2);
-        float a0, a1;
-        unpack2(a, a0, a1);
-        acc = add2(acc, pack2(ex2(a0), ex2(a1)));
-      }
-    }
-    float e0, e1;
-    unpack2(acc, e0, e1);
-    l = block_sum_fixed(e0 + e1, S);
-  }
-
-  // ---- 4. candidate pass: exact per-key counts into the leader's histogram
+  // ---- 3/4. candidate pass: exact per-key counts into the leader's histogram
   int hi = 0, lo = 1;
   if (sel) {
-    if (!mbar_wait_bounded(bar_mid)) flags |= FLAG_TIMEOUT;
-    __syncthreads();           // this CTA's own slot, written locally, is visible too
-    int L = 0x7fffffff;
-    float M = -INFINITY;
+    if (tid == 0) {
+      // the window of candidate keys, the same in every CTA of the cluster
+      if (!mbar_wait_bounded(bar_mid)) flags |= FLAG_TIMEOUT;
+      int L = 0x7fffffff;
+      float M = -INFINITY;
 #pragma unroll
-    for (int q = 0; q < NSHARD; ++q) {
-      M = fmaxf(M, S.mid[q].xm);
-      L = min(L, S.mid[q].lkey);
-    }
-    if (M > -INFINITY && M < INFINITY) {
-      hi = okey_of(M);
-      lo = max(0, hi - (WIN - 1));
-      if (k_on) {
-        lo = max(lo, L);
-      } else {
-        // Tokens below s_max + ln((1-p)/V) cannot reach the nucleus: even all V
-        // of them would hold less than 1-p of the total mass.  The slack keeps the
-        // float evaluation on the safe side.
-        const float width = tau * (logf(static_cast<float>(VREAL) / (1.0f - p)) * 1.0001f + 1e-3f);
-        lo = max(lo, okey_floor(M - width));
+      for (int q = 0; q < NSHARD; ++q) {
+        M = fmaxf(M, S.mid[q].xm);
+        L = min(L, S.mid[q].lkey);
       }
-      lo = max(lo, KEY_NEG_INF);
+      int whi = 0, wlo = 1;
+      if (M > -INFINITY && M < INFINITY) {
+        whi = okey_of(M);
+        wlo = max(0, whi - (WIN - 1));
+        if (k_on) {
+          wlo = max(wlo, L);
+        } else {
+          // Tokens below s_max + ln((1-p)/V) cannot reach the nucleus: even all V
+          // of them would hold less than 1-p of the total mass.  The slack keeps the
+          // float evaluation on the safe side.
+          const float width = tau * (logf(static_cast<float>(VREAL) / (1.0f - p)) * 1.0001f + 1e-3f);
+          wlo = max(wlo, okey_floor(M - width));
+        }
+        wlo = max(wlo, KEY_NEG_INF);
+      }
+      S.win[0] = whi;
+      S.win[1] = wlo;
+      S.win[2] = static_cast<int>(flags);
     }
+    __syncthreads();
+    hi = S.win[0];
+    lo = S.win[1];
+    flags = static_cast<uint32_t>(S.win[2]);
     // the leader counts straight into the merged histogram, the others locally
     uint32_t* cnt_local = (r == 0) ? S.merged : S.hist;
     if (xm_finite && lo <= hi && static_cast<int>(xkey) >= lo) {
@@ -933,7 +921,30 @@ logp_kernel(const KParams P) {
     }
   }
 
-  // ---- 5. summary to the leader
+  // ---- 5. shard sum-exp, fixed tree
+  float l = 0.0f;
+  if (!greedy && xm_finite) {
+    const float c = __fdiv_rn(LOG2E, tau);
+    const uint64_t nxm2 = pack2(-xm, -xm);
+    const uint64_t c2 = pack2(c, c);
+    uint64_t acc = pack2(0.0f, 0.0f);
+    for (int ch = tid; ch < nchunks; ch += NTHR) {
+      const uint4 v = sh[ch];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint64_t a = mul2(add2(pack2(bf16_lo(w[j]), bf16_hi(w[j])), nxm2), c2);
+        float a0, a1;
+        unpack2(a, a0, a1);
+        acc = add2(acc, pack2(ex2(a0), ex2(a1)));
+      }
+    }
+    float e0, e1;
+    unpack2(acc, e0, e1);
+    l = block_sum_fixed(e0 + e1, S);
+  }
+
+  // ---- 6. summary to the leader
   if (tid == 0) {
     const uint4 msg = make_uint4(__float_as_uint(xm), __float_as_uint(l), sel ? S.npush : first, flags);
     if (r == 0) *reinterpret_cast<uint4*>(&S.slot[0]) = msg;
