@@ -91,8 +91,6 @@ struct __align__(16) Summary {
 struct __align__(128) Smem {
   uint4 shard[SHARD_CHUNKS];       // 38144 B; the leader reuses it as scratch at the end
   uint32_t merged[WIN];            // leader: per-key candidate counts of the whole row
-  uint32_t hist[WIN / 2];          // this shard's per-key candidate counts (u16 pairs)
-  uint16_t clist[NWARP * 32];      // per-warp lists of chunks holding candidates
   MidSlot mid[NSHARD];
   Summary slot[NSHARD];
   uint32_t red_u[NWARP];
@@ -716,7 +714,6 @@ logp_kernel(const KParams P) {
   if (sel) {
     if (r == 0)
       for (int i = tid; i < WIN; i += NTHR) S.merged[i] = 0u;
-    for (int i = tid; i < WIN / 2; i += NTHR) S.hist[i] = 0u;
   }
   __syncthreads();
   // S0: barriers initialised and the leader's histogram zeroed.  One thread
@@ -743,7 +740,7 @@ logp_kernel(const KParams P) {
   for (int i = 0; i < MAXCH; ++i) {
     const int ch = tid + i * NTHR;
     __nv_bfloat162 cmax = ninf2;
-    if (ch < nchunks) {
+    if (i < MAXCH - 1 || ch < nchunks) {   // chunks 0..8 of every thread always exist
       const uint4 v = sh[ch];
       cmax = __hmax2(__hmax2(as_bf2(v.x), as_bf2(v.y)), __hmax2(as_bf2(v.z), as_bf2(v.w)));
       m2 = __hmax2(m2, cmax);
@@ -801,7 +798,8 @@ logp_kernel(const KParams P) {
       st_async_v4(map_rank(smem_addr(&S.mid[r]), tid), msg, map_rank(bar_mid, tid));
   }
 
-  // ---- 3/4. candidate pass: exact per-key counts into the leader's histogram
+  // ---- 3/4. candidate pass: every element of the window is counted straight
+  //           into the leader's histogram (one shared-memory add per element)
   int hi = 0, lo = 1;
   if (sel) {
     if (tid == 0) {
@@ -837,88 +835,44 @@ logp_kernel(const KParams P) {
     hi = S.win[0];
     lo = S.win[1];
     flags = static_cast<uint32_t>(S.win[2]);
-    // the leader counts straight into the merged histogram, the others locally
-    uint32_t* cnt_local = (r == 0) ? S.merged : S.hist;
+    uint32_t sent = 0;
     if (xm_finite && lo <= hi && static_cast<int>(xkey) >= lo) {
       const float vlo_f = key_value(lo);
       const __nv_bfloat162 vlo2 = __floats2bfloat162_rn(vlo_f, vlo_f);
+      const uint32_t dst = map_rank(smem_addr(S.merged), 0);
+      const uint32_t rbar = map_rank(bar_hist, 0);
       // chunks whose maximum reaches the window, from the register chunk maxima
       uint32_t hitmask = 0;
 #pragma unroll
-      for (int i = 0; i < MAXCH; ++i) {
-        const int ch = tid + i * NTHR;
-        if (ch < nchunks) {
-          __nv_bfloat162 cmax;
-          if (i < KEEPCH) {
-            cmax = cm[i];
-          } else {
-            const uint4 v = sh[ch];
-            cmax = __hmax2(__hmax2(as_bf2(v.x), as_bf2(v.y)), __hmax2(as_bf2(v.z), as_bf2(v.w)));
-          }
-          if (__hge2_mask(cmax, vlo2) != 0u) hitmask |= 1u << i;
-        }
-      }
-      // this warp's chunks with candidates go to the warp's own list (32 slots;
-      // more are counted directly), then 8 lanes take one listed chunk each round
-      const int lane = tid & 31;
-      const int h = __popc(hitmask);
-      int incl = h;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const int wtot = __shfl_sync(0xffffffffu, incl, 31);
-      uint16_t* wl = S.clist + (tid >> 5) * 32;
-      int pos = incl - h;
+      for (int i = 0; i < MAXCH; ++i)
+        if (__hge2_mask(cm[i], vlo2) != 0u) hitmask |= 1u << i;
       while (hitmask) {
         const int i = __ffs(hitmask) - 1;
         hitmask &= hitmask - 1;
-        const int ch = tid + i * NTHR;
-        if (pos < 32) {
-          wl[pos] = static_cast<uint16_t>(ch);
-        } else {
-          const uint4 v = sh[ch];
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const uint4 v = sh[tid + i * NTHR];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t bits = 0;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t b = (w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
-            if (__uint_as_float(b << 16) >= vlo_f) {
-              const int idx = hi - okey(b);
-              if (r == 0) red_shared_add(&cnt_local[idx], 1u);
-              else red_shared_add(&cnt_local[idx >> 1], 1u << ((idx & 1) * 16));
-            }
+        for (int j = 0; j < 4; ++j) bits |= (__hge2_mask(as_bf2(w[j]), vlo2) & 0x00010001u) << j;
+        while (bits) {
+          const int pos = __ffs(bits) - 1;
+          bits &= bits - 1;
+          const int j = pos & 3;
+          const uint32_t wj = (j == 0) ? w[0] : (j == 1) ? w[1] : (j == 2) ? w[2] : w[3];
+          const uint32_t b = (pos & 16) ? (wj >> 16) : (wj & 0xFFFFu);
+          const int idx = hi - okey(b);
+          if (r == 0) {
+            red_shared_add(&S.merged[idx], 1u);
+          } else {
+            red_async_add(dst + 4u * static_cast<uint32_t>(idx), 1u, rbar);
+            ++sent;
           }
         }
-        ++pos;
-      }
-      __syncwarp();
-      const int nl = min(wtot, 32);
-      const uint16_t* elem = reinterpret_cast<const uint16_t*>(S.shard);
-      for (int e = lane >> 3; e < nl; e += 4) {
-        const uint32_t b = elem[static_cast<int>(wl[e]) * 8 + (lane & 7)];
-        if (__uint_as_float(b << 16) >= vlo_f) {
-          const int idx = hi - okey(b);
-          if (r == 0) red_shared_add(&cnt_local[idx], 1u);
-          else red_shared_add(&cnt_local[idx >> 1], 1u << ((idx & 1) * 16));
-        }
       }
     }
-    if (r != 0) {
-      __syncthreads();
-      // send this shard's nonzero counts to the leader
-      const uint32_t dst = map_rank(smem_addr(S.merged), 0);
-      const uint32_t rbar = map_rank(bar_hist, 0);
-      const int nwords = (hi - lo + 2) >> 1;
-      uint32_t sent = 0;
-      for (int i = tid; i < nwords; i += NTHR) {
-        const uint32_t w = S.hist[i];
-        if (w & 0xFFFFu) { red_async_add(dst + 8u * i, w & 0xFFFFu, rbar); ++sent; }
-        if (w >> 16) { red_async_add(dst + 8u * i + 4u, w >> 16, rbar); ++sent; }
-      }
-      if (sent) atomicAdd(&S.npush, sent);
-      __syncthreads();
-    }
+    // the leader learns how many adds each peer sent from its summary
+    sent = __reduce_add_sync(0xffffffffu, sent);
+    if ((tid & 31) == 0 && sent) atomicAdd(&S.npush, sent);
   }
 
   // ---- 5. shard sum-exp, fixed tree
@@ -928,20 +882,26 @@ logp_kernel(const KParams P) {
     const uint64_t nxm2 = pack2(-xm, -xm);
     const uint64_t c2 = pack2(c, c);
     uint64_t acc = pack2(0.0f, 0.0f);
-    for (int ch = tid; ch < nchunks; ch += NTHR) {
-      const uint4 v = sh[ch];
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint64_t a = mul2(add2(pack2(bf16_lo(w[j]), bf16_hi(w[j])), nxm2), c2);
-        float a0, a1;
-        unpack2(a, a0, a1);
-        acc = add2(acc, pack2(ex2(a0), ex2(a1)));
+    for (int i = 0; i < MAXCH; ++i) {
+      const int ch = tid + i * NTHR;
+      if (i < MAXCH - 1 || ch < nchunks) {   // chunks 0..8 of every thread always exist
+        const uint4 v = sh[ch];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint64_t a = mul2(add2(pack2(bf16_lo(w[j]), bf16_hi(w[j])), nxm2), c2);
+          float a0, a1;
+          unpack2(a, a0, a1);
+          acc = add2(acc, pack2(ex2(a0), ex2(a1)));
+        }
       }
     }
     float e0, e1;
     unpack2(acc, e0, e1);
-    l = block_sum_fixed(e0 + e1, S);
+    l = block_sum_fixed(e0 + e1, S);   // its barriers also complete the npush adds
+  } else if (sel) {
+    __syncthreads();
   }
 
   // ---- 6. summary to the leader
@@ -953,24 +913,30 @@ logp_kernel(const KParams P) {
   if (r != 0) return;          // messages carry everything the leader needs
 
   // ================= leader: merge in fixed shard order =================
-  bool timed_out = !mbar_wait_bounded(bar_sum);
-  __syncthreads();             // own slot and own counts visible to every thread
-  bool bad = false;
+  // One thread waits for the peers' messages; warp 0 merges and selects; the
+  // whole block joins only for the general (wide-support) selection.
+  if (tid == 0) {
+    bool timed_out = !mbar_wait_bounded(bar_sum);
+    uint32_t pushed = 0;
+#pragma unroll
+    for (int q = 1; q < NSHARD; ++q) pushed += S.slot[q].aux;
+    if (sel) {
+      mbar_arrive_expect_tx(bar_hist, 4u * pushed);
+      if (!mbar_wait_bounded(bar_hist)) timed_out = true;
+    }
+    S.win[3] = timed_out ? 1 : 0;
+  }
+  __syncthreads();
+  const bool timed_out = S.win[3] != 0;
+  bool bad = timed_out;
   float M = -INFINITY;
-  uint32_t pushed = 0;
 #pragma unroll
   for (int q = 0; q < NSHARD; ++q) {
     const Summary& s = S.slot[q];
-    if (s.flags & FLAG_TIMEOUT) timed_out = true;
-    if ((s.flags & FLAG_NAN) || s.xm == INFINITY || s.l != s.l) bad = true;
+    if ((s.flags & (FLAG_NAN | FLAG_TIMEOUT)) || s.xm == INFINITY || s.l != s.l) bad = true;
     M = fmaxf(M, s.xm);
-    if (q > 0) pushed += s.aux;
   }
-  if (sel) {
-    if (tid == 0) mbar_arrive_expect_tx(bar_hist, 4u * pushed);
-    if (!mbar_wait_bounded(bar_hist)) timed_out = true;
-  }
-  bad |= timed_out || !(M > -INFINITY);
+  bad |= !(M > -INFINITY);
   const float qnan = __int_as_float(0x7fc00000);
   float full = qnan, restr = qnan;
   int support = -1;
@@ -999,14 +965,16 @@ logp_kernel(const KParams P) {
     }
   }
   if (sel && !bad) {
-    uint32_t* cntB = reinterpret_cast<uint32_t*>(S.shard);
     SelResult sr{0u, 0ull, 0};
     if (tid < 32) {
       const bool ok = select_warp(S.merged, hi, lo, M, c, Z, p, k, k_on, p_on, sr);
       if (tid == 0) S.sel_done = ok ? 1 : 0;
     }
     __syncthreads();
-    if (!S.sel_done) sr = select_support(S, S.merged, cntB, hi, lo, rowp, M, c, Z, p, k, k_on, p_on);
+    if (!S.sel_done) {
+      uint32_t* cntB = reinterpret_cast<uint32_t*>(S.shard);
+      sr = select_support(S, S.merged, cntB, hi, lo, rowp, M, c, Z, p, k, k_on, p_on);
+    }
     const bool in_s = okey_of(xt) >= sr.min_key;
     const float zs = __ull2float_rn(sr.zs) * (1.0f / FX_SCALE);
     restr = in_s ? d - logf(zs) : -INFINITY;
