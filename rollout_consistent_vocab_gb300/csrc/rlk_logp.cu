@@ -62,6 +62,7 @@ constexpr int MAXCH = (SHARD_CHUNKS + NTHR - 1) / NTHR;     // chunks per thread
 constexpr int KEEPCH = MAXCH;        // chunk maxima kept in registers
 constexpr int WIN = 1024;            // candidate window, in bf16 order keys (8 binades)
 constexpr int TMA_PIECES = 4;
+constexpr int BUSY_HITS = 16;        // candidate chunks per warp above which it counts locally
 constexpr float LOG2E = 1.4426950408889634f;   // log2(e)
 constexpr float FX_SCALE = 17592186044416.0f;  // 2^44: fixed-point scale of masses
 constexpr unsigned long long TIMEOUT_NS = 200000000ull;   // 0.2 s bound on every wait
@@ -91,6 +92,7 @@ struct __align__(16) Summary {
 struct __align__(128) Smem {
   uint4 shard[SHARD_CHUNKS];       // 38144 B; the leader reuses it as scratch at the end
   uint32_t merged[WIN];            // leader: per-key candidate counts of the whole row
+  uint32_t hist[WIN / 2];          // busy warps' per-key counts (u16 pairs), pushed once
   MidSlot mid[NSHARD];
   Summary slot[NSHARD];
   uint32_t red_u[NWARP];
@@ -103,6 +105,7 @@ struct __align__(128) Smem {
   unsigned long long found_m;
   uint32_t npush;
   int32_t win[4];
+  float bc_f[4];
   int32_t sel_done;
   unsigned long long bar_load, bar_mid, bar_sum, bar_hist;
 };
@@ -714,6 +717,8 @@ logp_kernel(const KParams P) {
   if (sel) {
     if (r == 0)
       for (int i = tid; i < WIN; i += NTHR) S.merged[i] = 0u;
+    else
+      for (int i = tid; i < WIN / 2; i += NTHR) S.hist[i] = 0u;
   }
   __syncthreads();
   // S0: barriers initialised and the leader's histogram zeroed.  One thread
@@ -846,6 +851,11 @@ logp_kernel(const KParams P) {
 #pragma unroll
       for (int i = 0; i < MAXCH; ++i)
         if (__hge2_mask(cm[i], vlo2) != 0u) hitmask |= 1u << i;
+      // warps with many candidate chunks count locally and push per key;
+      // the others send one add per element
+      const bool busy = (r != 0) && __reduce_add_sync(0xffffffffu, __popc(hitmask)) > BUSY_HITS;
+      // with a positive window every candidate is positive: its key is b | 0x8000
+      const bool pos_window = vlo_f > 0.0f;
       while (hitmask) {
         const int i = __ffs(hitmask) - 1;
         hitmask &= hitmask - 1;
@@ -860,13 +870,24 @@ logp_kernel(const KParams P) {
           const int j = pos & 3;
           const uint32_t wj = (j == 0) ? w[0] : (j == 1) ? w[1] : (j == 2) ? w[2] : w[3];
           const uint32_t b = (pos & 16) ? (wj >> 16) : (wj & 0xFFFFu);
-          const int idx = hi - okey(b);
+          const int idx = hi - (pos_window ? static_cast<int>(b | 0x8000u) : okey(b));
           if (r == 0) {
             red_shared_add(&S.merged[idx], 1u);
+          } else if (busy) {
+            red_shared_add(&S.hist[idx >> 1], 1u << ((idx & 1) * 16));
           } else {
             red_async_add(dst + 4u * static_cast<uint32_t>(idx), 1u, rbar);
             ++sent;
           }
+        }
+      }
+      if (__syncthreads_or(busy)) {
+        // push the busy warps' counts, one add per nonzero key
+        const int nwords = (hi - lo + 2) >> 1;
+        for (int iw = tid; iw < nwords; iw += NTHR) {
+          const uint32_t hw = S.hist[iw];
+          if (hw & 0xFFFFu) { red_async_add(dst + 8u * iw, hw & 0xFFFFu, rbar); ++sent; }
+          if (hw >> 16) { red_async_add(dst + 8u * iw + 4u, hw >> 16, rbar); ++sent; }
         }
       }
     }
@@ -928,57 +949,66 @@ logp_kernel(const KParams P) {
   }
   __syncthreads();
   const bool timed_out = S.win[3] != 0;
+  if (tid >= 32 && !sel) return;   // only warp 0 finishes rows without a support search
   bool bad = timed_out;
   float M = -INFINITY;
-#pragma unroll
-  for (int q = 0; q < NSHARD; ++q) {
-    const Summary& s = S.slot[q];
-    if ((s.flags & (FLAG_NAN | FLAG_TIMEOUT)) || s.xm == INFINITY || s.l != s.l) bad = true;
-    M = fmaxf(M, s.xm);
-  }
-  bad |= !(M > -INFINITY);
-  const float qnan = __int_as_float(0x7fc00000);
-  float full = qnan, restr = qnan;
+  float full = __int_as_float(0x7fc00000), restr = full;
   int support = -1;
   float Z = 0.0f, d = 0.0f;
   const float c = greedy ? 0.0f : __fdiv_rn(LOG2E, tau);
-  if (!bad && greedy) {
-    uint32_t amax = 0x7fffffffu;
+  bool done = true;
+  SelResult sr{0u, 0ull, 0};
+  if (tid < 32) {
 #pragma unroll
-    for (int q = NSHARD - 1; q >= 0; --q)
-      if (S.slot[q].xm == M) amax = S.slot[q].aux;
-    full = restr = (static_cast<uint32_t>(t) == amax) ? 0.0f : -INFINITY;
-    support = 1;
-  } else if (!bad) {
-    if (isinf(__fdiv_rn(M, tau))) {
-      bad = true;
-    } else {
+    for (int q = 0; q < NSHARD; ++q) {
+      const Summary& s = S.slot[q];
+      if ((s.flags & (FLAG_NAN | FLAG_TIMEOUT)) || s.xm == INFINITY || s.l != s.l) bad = true;
+      M = fmaxf(M, s.xm);
+    }
+    bad |= !(M > -INFINITY);
+    if (!bad && greedy) {
+      uint32_t amax = 0x7fffffffu;
 #pragma unroll
-      for (int q = 0; q < NSHARD; ++q) {
-        const Summary& s = S.slot[q];
-        if (s.xm > -INFINITY) Z = fmaf(s.l, ex2((s.xm - M) * c), Z);
+      for (int q = NSHARD - 1; q >= 0; --q)
+        if (S.slot[q].xm == M) amax = S.slot[q].aux;
+      full = restr = (static_cast<uint32_t>(t) == amax) ? 0.0f : -INFINITY;
+      support = 1;
+    } else if (!bad) {
+      if (isinf(__fdiv_rn(M, tau))) {
+        bad = true;
+      } else {
+#pragma unroll
+        for (int q = 0; q < NSHARD; ++q) {
+          const Summary& s = S.slot[q];
+          if (s.xm > -INFINITY) Z = fmaf(s.l, ex2((s.xm - M) * c), Z);
+        }
+        d = __fdiv_rn(xt - M, tau);
+        full = d - logf(Z);
+        restr = full;
+        support = VREAL;
       }
-      d = __fdiv_rn(xt - M, tau);
-      full = d - logf(Z);
-      restr = full;
-      support = VREAL;
+    }
+    if (sel && !bad) done = select_warp(S.merged, hi, lo, M, c, Z, p, k, k_on, p_on, sr);
+    if (sel && tid == 0) {
+      S.sel_done = done ? 1 : 0;
+      S.bc_f[0] = M;
+      S.bc_f[1] = Z;
     }
   }
-  if (sel && !bad) {
-    SelResult sr{0u, 0ull, 0};
-    if (tid < 32) {
-      const bool ok = select_warp(S.merged, hi, lo, M, c, Z, p, k, k_on, p_on, sr);
-      if (tid == 0) S.sel_done = ok ? 1 : 0;
-    }
+  if (sel) {
     __syncthreads();
     if (!S.sel_done) {
+      // wide support: the whole block scans further windows
       uint32_t* cntB = reinterpret_cast<uint32_t*>(S.shard);
-      sr = select_support(S, S.merged, cntB, hi, lo, rowp, M, c, Z, p, k, k_on, p_on);
+      sr = select_support(S, S.merged, cntB, hi, lo, rowp, S.bc_f[0], c, S.bc_f[1], p, k, k_on, p_on);
     }
-    const bool in_s = okey_of(xt) >= sr.min_key;
-    const float zs = __ull2float_rn(sr.zs) * (1.0f / FX_SCALE);
-    restr = in_s ? d - logf(zs) : -INFINITY;
-    support = static_cast<int>(sr.support);
+    if (tid != 0) return;
+    if (!bad) {
+      const bool in_s = okey_of(xt) >= sr.min_key;
+      const float zs = __ull2float_rn(sr.zs) * (1.0f / FX_SCALE);
+      restr = in_s ? d - logf(zs) : -INFINITY;
+      support = static_cast<int>(sr.support);
+    }
   }
 
   if (tid == 0) {
