@@ -79,7 +79,10 @@ struct __align__(16) MidSlot {
   int32_t lkey;    // order key reached by ceil(k/64) lane maxima of every warp of the shard
   uint32_t flags;
   int32_t pad;
+  uint16_t top[4 * NWARP];   // the 4 largest lane maxima (order keys) of each warp
 };
+constexpr int MID_BYTES = static_cast<int>(sizeof(MidSlot));   // 80
+static_assert(MID_BYTES % 16 == 0, "exchange message in 16-byte pieces");
 
 // Sent by every CTA to the leader at the end.
 struct __align__(16) Summary {
@@ -94,6 +97,7 @@ struct __align__(128) Smem {
   uint32_t merged[WIN];            // leader: per-key candidate counts of the whole row
   uint32_t hist[WIN / 2];          // busy warps' per-key counts (u16 pairs), pushed once
   MidSlot mid[NSHARD];
+  uint16_t top[4 * NWARP];         // this CTA's warps' top-4 lane maxima, staged for sending
   Summary slot[NSHARD];
   uint32_t red_u[NWARP];
   int32_t red_i[NWARP];
@@ -309,6 +313,54 @@ __device__ __forceinline__ int warp_kth_largest(int key, int j) {
     if (covered >= j || m == 0u) return static_cast<int>(m);
     if (v == m) v = 0u;
   }
+}
+
+// The 4 largest of the warp's 32 keys (with multiplicity), written by lane 0.
+__device__ __forceinline__ void warp_top4(int key, uint16_t* out4) {
+  unsigned v = static_cast<unsigned>(key);
+  unsigned vals[4] = {0u, 0u, 0u, 0u};
+  int filled = 0;
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const unsigned m = __reduce_max_sync(0xffffffffu, v);
+    const int c = __popc(__ballot_sync(0xffffffffu, v == m));
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (q >= filled && q < filled + c) vals[q] = m;
+    filled += c;
+    if (v == m) v = 0u;
+  }
+  if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) out4[q] = static_cast<uint16_t>(vals[q]);
+  }
+}
+
+// k-th largest (k <= 256) of the 256 exchanged keys (8 CTAs x 32), by one
+// warp: 8 keys per lane, bisection on the key with warp-wide counts.
+__device__ __forceinline__ int union_kth_largest(const Smem& S, int k) {
+  const int lane = threadIdx.x & 31;
+  const uint4 kv = *reinterpret_cast<const uint4*>(&S.mid[lane >> 2].top[(lane & 3) * 8]);
+  const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+  int key[8];
+  int kmin = 0xFFFF, kmax = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    key[j] = static_cast<int>((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
+    kmin = min(kmin, key[j]);
+    kmax = max(kmax, key[j]);
+  }
+  int lo = __reduce_min_sync(0xffffffffu, kmin);
+  int hi = __reduce_max_sync(0xffffffffu, kmax);
+  // invariant: at least k keys are >= lo (all 256 are >= the minimum)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) c += (key[j] >= mid);
+    if (__reduce_add_sync(0xffffffffu, c) >= k) lo = mid; else hi = mid - 1;
+  }
+  return lo;
 }
 
 // Exclusive block scan of (count, mass); also returns the block totals.
@@ -710,7 +762,7 @@ logp_kernel(const KParams P) {
     mbar_init(bar_sum, 1);
     mbar_init(bar_hist, 1);
     // messages from the 7 peers: 16 bytes each
-    if (sel) mbar_arrive_expect_tx(bar_mid, (NSHARD - 1) * 16);
+    if (sel) mbar_arrive_expect_tx(bar_mid, (NSHARD - 1) * MID_BYTES);
     if (r == 0) mbar_arrive_expect_tx(bar_sum, (NSHARD - 1) * 16);
     S.npush = 0u;
   }
@@ -756,12 +808,15 @@ logp_kernel(const KParams P) {
   // Pooled top-k bound: warp w certifies kw = ceil(k/64) lane maxima at or above
   // lw (its kw-th largest lane maximum), so the 64 warps of the row certify
   // 64*kw >= k tokens at or above the minimum of lw over the cluster.
+  // For k <= 256 a tighter bound comes from the union of every warp's 4
+  // largest lane maxima (256 distinct tokens per row): its k-th largest.
   const int kw = (k + 63) / 64;
   const bool k_bound = sel && k_on && kw <= 32;
   {
     const int lane = tid & 31, warp = tid >> 5;
-    const int lw = k_bound ? warp_kth_largest(tkey, kw) : 0;
+    const int lw = (k_bound && k > 4 * NWARP * NSHARD) ? warp_kth_largest(tkey, kw) : 0;
     const unsigned wmax = __reduce_max_sync(0xffffffffu, static_cast<unsigned>(tkey));
+    if (k_bound && k <= 4 * NWARP * NSHARD) warp_top4(tkey, &S.top[warp * 4]);
     if (lane == 0) { S.red_u[warp] = wmax; S.red_i[warp] = lw; }
   }
   __syncthreads();
@@ -796,20 +851,32 @@ logp_kernel(const KParams P) {
 
   cluster_wait();              // S0 complete: peers' barriers and histogram are ready
   if (sel && tid < NSHARD) {
-    const uint4 msg = make_uint4(__float_as_uint(xm), static_cast<uint32_t>(lkey), flags, 0u);
-    if (tid == static_cast<int>(r))
-      *reinterpret_cast<uint4*>(&S.mid[r]) = msg;
-    else
-      st_async_v4(map_rank(smem_addr(&S.mid[r]), tid), msg, map_rank(bar_mid, tid));
+    // the 80-byte exchange message, in five 16-byte pieces, to CTA `tid`
+    uint4 msg[MID_BYTES / 16];
+    msg[0] = make_uint4(__float_as_uint(xm), static_cast<uint32_t>(lkey), flags, 0u);
+    const uint4* topv = reinterpret_cast<const uint4*>(S.top);
+#pragma unroll
+    for (int q = 1; q < MID_BYTES / 16; ++q) msg[q] = topv[q - 1];
+    uint4* mine = reinterpret_cast<uint4*>(&S.mid[r]);
+    if (tid == static_cast<int>(r)) {
+#pragma unroll
+      for (int q = 0; q < MID_BYTES / 16; ++q) mine[q] = msg[q];
+    } else {
+      const uint32_t dst = map_rank(smem_addr(mine), tid);
+      const uint32_t rb = map_rank(bar_mid, tid);
+#pragma unroll
+      for (int q = 0; q < MID_BYTES / 16; ++q) st_async_v4(dst + 16u * q, msg[q], rb);
+    }
   }
 
   // ---- 3/4. candidate pass: every element of the window is counted straight
   //           into the leader's histogram (one shared-memory add per element)
   int hi = 0, lo = 1;
   if (sel) {
-    if (tid == 0) {
+    if (tid < 32) {
       // the window of candidate keys, the same in every CTA of the cluster
-      if (!mbar_wait_bounded(bar_mid)) flags |= FLAG_TIMEOUT;
+      if (tid == 0 && !mbar_wait_bounded(bar_mid)) flags |= FLAG_TIMEOUT;
+      __syncwarp();
       int L = 0x7fffffff;
       float M = -INFINITY;
 #pragma unroll
@@ -817,6 +884,7 @@ logp_kernel(const KParams P) {
         M = fmaxf(M, S.mid[q].xm);
         L = min(L, S.mid[q].lkey);
       }
+      if (k_bound && k <= 4 * NWARP * NSHARD) L = union_kth_largest(S, k);
       int whi = 0, wlo = 1;
       if (M > -INFINITY && M < INFINITY) {
         whi = okey_of(M);
@@ -832,9 +900,11 @@ logp_kernel(const KParams P) {
         }
         wlo = max(wlo, KEY_NEG_INF);
       }
-      S.win[0] = whi;
-      S.win[1] = wlo;
-      S.win[2] = static_cast<int>(flags);
+      if (tid == 0) {
+        S.win[0] = whi;
+        S.win[1] = wlo;
+        S.win[2] = static_cast<int>(flags);
+      }
     }
     __syncthreads();
     hi = S.win[0];
