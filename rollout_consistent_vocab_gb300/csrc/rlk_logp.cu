@@ -56,8 +56,13 @@ constexpr int NSHARD = RLK_NUM_SHARDS;
 constexpr int SW = RLK_SHARD_WIDTH;
 constexpr int SHARD_CHUNKS = SW / 8;                        // 2384 16-byte chunks
 constexpr int LAST_CHUNKS = (VREAL - (NSHARD - 1) * SW) / 8;  // 2304 real chunks
-constexpr int NTHR = 256;
+#ifndef RLK_NTHR
+#define RLK_NTHR 256
+#endif
+constexpr int NTHR = RLK_NTHR;       // threads per CTA
 constexpr int NWARP = NTHR / 32;
+constexpr int ROW_WARPS = NSHARD * NWARP;
+constexpr int CTAS_PER_SM = 5;
 constexpr int MAXCH = (SHARD_CHUNKS + NTHR - 1) / NTHR;     // chunks per thread (9 or 10)
 constexpr int KEEPCH = MAXCH;        // chunk maxima kept in registers
 constexpr int WIN = 1024;            // candidate window, in bf16 order keys (8 binades)
@@ -69,6 +74,7 @@ constexpr unsigned long long TIMEOUT_NS = 200000000ull;   // 0.2 s bound on ever
 constexpr int KEY_NEG_INF = 0x007F;  // order key of -inf; smaller keys are NaN patterns
 
 static_assert(SW % 8 == 0 && (VREAL - (NSHARD - 1) * SW) % 8 == 0, "chunking");
+static_assert((MAXCH - 1) * NTHR <= LAST_CHUNKS, "every thread owns MAXCH-1 chunks in every shard");
 static_assert(SHARD_CHUNKS % TMA_PIECES == 0 && LAST_CHUNKS % TMA_PIECES == 0, "pieces");
 
 enum : uint32_t { FLAG_TIMEOUT = 1u, FLAG_NAN = 2u };
@@ -79,10 +85,7 @@ struct __align__(16) MidSlot {
   int32_t lkey;    // order key reached by ceil(k/64) lane maxima of every warp of the shard
   uint32_t flags;
   int32_t pad;
-  uint16_t top[4 * NWARP];   // the 4 largest lane maxima (order keys) of each warp
 };
-constexpr int MID_BYTES = static_cast<int>(sizeof(MidSlot));   // 80
-static_assert(MID_BYTES % 16 == 0, "exchange message in 16-byte pieces");
 
 // Sent by every CTA to the leader at the end.
 struct __align__(16) Summary {
@@ -97,7 +100,6 @@ struct __align__(128) Smem {
   uint32_t merged[WIN];            // leader: per-key candidate counts of the whole row
   uint32_t hist[WIN / 2];          // busy warps' per-key counts (u16 pairs), pushed once
   MidSlot mid[NSHARD];
-  uint16_t top[4 * NWARP];         // this CTA's warps' top-4 lane maxima, staged for sending
   Summary slot[NSHARD];
   uint32_t red_u[NWARP];
   int32_t red_i[NWARP];
@@ -114,7 +116,7 @@ struct __align__(128) Smem {
   unsigned long long bar_load, bar_mid, bar_sum, bar_hist;
 };
 // five CTAs per SM: 5 * (sizeof + 1 KB reserved) <= 228 KB
-static_assert(sizeof(Smem) + 1024 <= 233472 / 5, "shared memory budget of 5 CTAs per SM");
+static_assert(sizeof(Smem) + 1024 <= 233472 / CTAS_PER_SM, "shared memory budget of 5 CTAs per SM");
 
 struct KParams {
   const uint16_t* logits;
@@ -313,54 +315,6 @@ __device__ __forceinline__ int warp_kth_largest(int key, int j) {
     if (covered >= j || m == 0u) return static_cast<int>(m);
     if (v == m) v = 0u;
   }
-}
-
-// The 4 largest of the warp's 32 keys (with multiplicity), written by lane 0.
-__device__ __forceinline__ void warp_top4(int key, uint16_t* out4) {
-  unsigned v = static_cast<unsigned>(key);
-  unsigned vals[4] = {0u, 0u, 0u, 0u};
-  int filled = 0;
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const unsigned m = __reduce_max_sync(0xffffffffu, v);
-    const int c = __popc(__ballot_sync(0xffffffffu, v == m));
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (q >= filled && q < filled + c) vals[q] = m;
-    filled += c;
-    if (v == m) v = 0u;
-  }
-  if ((threadIdx.x & 31) == 0) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) out4[q] = static_cast<uint16_t>(vals[q]);
-  }
-}
-
-// k-th largest (k <= 256) of the 256 exchanged keys (8 CTAs x 32), by one
-// warp: 8 keys per lane, bisection on the key with warp-wide counts.
-__device__ __forceinline__ int union_kth_largest(const Smem& S, int k) {
-  const int lane = threadIdx.x & 31;
-  const uint4 kv = *reinterpret_cast<const uint4*>(&S.mid[lane >> 2].top[(lane & 3) * 8]);
-  const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
-  int key[8];
-  int kmin = 0xFFFF, kmax = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    key[j] = static_cast<int>((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
-    kmin = min(kmin, key[j]);
-    kmax = max(kmax, key[j]);
-  }
-  int lo = __reduce_min_sync(0xffffffffu, kmin);
-  int hi = __reduce_max_sync(0xffffffffu, kmax);
-  // invariant: at least k keys are >= lo (all 256 are >= the minimum)
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    int c = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) c += (key[j] >= mid);
-    if (__reduce_add_sync(0xffffffffu, c) >= k) lo = mid; else hi = mid - 1;
-  }
-  return lo;
 }
 
 // Exclusive block scan of (count, mass); also returns the block totals.
@@ -699,7 +653,7 @@ __device__ __forceinline__ bool select_warp(const uint32_t* cnt, int hi, int lo,
 // ------------------------------------------------------------ the kernel
 
 template <bool RESTR>
-__global__ void __cluster_dims__(NSHARD, 1, 1) __launch_bounds__(NTHR, 5)
+__global__ void __cluster_dims__(NSHARD, 1, 1) __launch_bounds__(NTHR, CTAS_PER_SM)
 logp_kernel(const KParams P) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
@@ -762,7 +716,7 @@ logp_kernel(const KParams P) {
     mbar_init(bar_sum, 1);
     mbar_init(bar_hist, 1);
     // messages from the 7 peers: 16 bytes each
-    if (sel) mbar_arrive_expect_tx(bar_mid, (NSHARD - 1) * MID_BYTES);
+    if (sel) mbar_arrive_expect_tx(bar_mid, (NSHARD - 1) * 16);
     if (r == 0) mbar_arrive_expect_tx(bar_sum, (NSHARD - 1) * 16);
     S.npush = 0u;
   }
@@ -797,7 +751,7 @@ logp_kernel(const KParams P) {
   for (int i = 0; i < MAXCH; ++i) {
     const int ch = tid + i * NTHR;
     __nv_bfloat162 cmax = ninf2;
-    if (i < MAXCH - 1 || ch < nchunks) {   // chunks 0..8 of every thread always exist
+    if (i < MAXCH - 1 || ch < nchunks) {   // all but the last chunk of every thread exist
       const uint4 v = sh[ch];
       cmax = __hmax2(__hmax2(as_bf2(v.x), as_bf2(v.y)), __hmax2(as_bf2(v.z), as_bf2(v.w)));
       m2 = __hmax2(m2, cmax);
@@ -805,18 +759,15 @@ logp_kernel(const KParams P) {
     if (i < KEEPCH) cm[i] = cmax;
   }
   const int tkey = okey_of(fmaxf(__low2float(m2), __high2float(m2)));
-  // Pooled top-k bound: warp w certifies kw = ceil(k/64) lane maxima at or above
-  // lw (its kw-th largest lane maximum), so the 64 warps of the row certify
-  // 64*kw >= k tokens at or above the minimum of lw over the cluster.
-  // For k <= 256 a tighter bound comes from the union of every warp's 4
-  // largest lane maxima (256 distinct tokens per row): its k-th largest.
-  const int kw = (k + 63) / 64;
+  // Pooled top-k bound: warp w certifies kw = ceil(k/W) lane maxima at or above
+  // lw (its kw-th largest lane maximum), so the W warps of the row certify
+  // W*kw >= k tokens at or above the minimum of lw over the cluster.
+  const int kw = (k + ROW_WARPS - 1) / ROW_WARPS;
   const bool k_bound = sel && k_on && kw <= 32;
   {
     const int lane = tid & 31, warp = tid >> 5;
-    const int lw = (k_bound && k > 4 * NWARP * NSHARD) ? warp_kth_largest(tkey, kw) : 0;
+    const int lw = k_bound ? warp_kth_largest(tkey, kw) : 0;
     const unsigned wmax = __reduce_max_sync(0xffffffffu, static_cast<unsigned>(tkey));
-    if (k_bound && k <= 4 * NWARP * NSHARD) warp_top4(tkey, &S.top[warp * 4]);
     if (lane == 0) { S.red_u[warp] = wmax; S.red_i[warp] = lw; }
   }
   __syncthreads();
@@ -851,32 +802,20 @@ logp_kernel(const KParams P) {
 
   cluster_wait();              // S0 complete: peers' barriers and histogram are ready
   if (sel && tid < NSHARD) {
-    // the 80-byte exchange message, in five 16-byte pieces, to CTA `tid`
-    uint4 msg[MID_BYTES / 16];
-    msg[0] = make_uint4(__float_as_uint(xm), static_cast<uint32_t>(lkey), flags, 0u);
-    const uint4* topv = reinterpret_cast<const uint4*>(S.top);
-#pragma unroll
-    for (int q = 1; q < MID_BYTES / 16; ++q) msg[q] = topv[q - 1];
-    uint4* mine = reinterpret_cast<uint4*>(&S.mid[r]);
-    if (tid == static_cast<int>(r)) {
-#pragma unroll
-      for (int q = 0; q < MID_BYTES / 16; ++q) mine[q] = msg[q];
-    } else {
-      const uint32_t dst = map_rank(smem_addr(mine), tid);
-      const uint32_t rb = map_rank(bar_mid, tid);
-#pragma unroll
-      for (int q = 0; q < MID_BYTES / 16; ++q) st_async_v4(dst + 16u * q, msg[q], rb);
-    }
+    const uint4 msg = make_uint4(__float_as_uint(xm), static_cast<uint32_t>(lkey), flags, 0u);
+    if (tid == static_cast<int>(r))
+      *reinterpret_cast<uint4*>(&S.mid[r]) = msg;
+    else
+      st_async_v4(map_rank(smem_addr(&S.mid[r]), tid), msg, map_rank(bar_mid, tid));
   }
 
   // ---- 3/4. candidate pass: every element of the window is counted straight
   //           into the leader's histogram (one shared-memory add per element)
   int hi = 0, lo = 1;
   if (sel) {
-    if (tid < 32) {
+    if (tid == 0) {
       // the window of candidate keys, the same in every CTA of the cluster
-      if (tid == 0 && !mbar_wait_bounded(bar_mid)) flags |= FLAG_TIMEOUT;
-      __syncwarp();
+      if (!mbar_wait_bounded(bar_mid)) flags |= FLAG_TIMEOUT;
       int L = 0x7fffffff;
       float M = -INFINITY;
 #pragma unroll
@@ -884,7 +823,6 @@ logp_kernel(const KParams P) {
         M = fmaxf(M, S.mid[q].xm);
         L = min(L, S.mid[q].lkey);
       }
-      if (k_bound && k <= 4 * NWARP * NSHARD) L = union_kth_largest(S, k);
       int whi = 0, wlo = 1;
       if (M > -INFINITY && M < INFINITY) {
         whi = okey_of(M);
@@ -900,11 +838,9 @@ logp_kernel(const KParams P) {
         }
         wlo = max(wlo, KEY_NEG_INF);
       }
-      if (tid == 0) {
-        S.win[0] = whi;
-        S.win[1] = wlo;
-        S.win[2] = static_cast<int>(flags);
-      }
+      S.win[0] = whi;
+      S.win[1] = wlo;
+      S.win[2] = static_cast<int>(flags);
     }
     __syncthreads();
     hi = S.win[0];
@@ -976,7 +912,7 @@ logp_kernel(const KParams P) {
 #pragma unroll
     for (int i = 0; i < MAXCH; ++i) {
       const int ch = tid + i * NTHR;
-      if (i < MAXCH - 1 || ch < nchunks) {   // chunks 0..8 of every thread always exist
+      if (i < MAXCH - 1 || ch < nchunks) {   // all but the last chunk of every thread exist
         const uint4 v = sh[ch];
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
