@@ -57,7 +57,7 @@ constexpr int SW = RLK_SHARD_WIDTH;
 constexpr int SHARD_CHUNKS = SW / 8;                        // 2384 16-byte chunks
 constexpr int LAST_CHUNKS = (VREAL - (NSHARD - 1) * SW) / 8;  // 2304 real chunks
 #ifndef RLK_NTHR
-#define RLK_NTHR 256
+#define RLK_NTHR 128
 #endif
 constexpr int NTHR = RLK_NTHR;       // threads per CTA
 constexpr int NWARP = NTHR / 32;
@@ -809,7 +809,34 @@ logp_kernel(const KParams P) {
       st_async_v4(map_rank(smem_addr(&S.mid[r]), tid), msg, map_rank(bar_mid, tid));
   }
 
-  // ---- 3/4. candidate pass: every element of the window is counted straight
+  // ---- 3. shard sum-exp, fixed tree (while the peers' messages travel)
+  float l = 0.0f;
+  if (!greedy && xm_finite) {
+    const float c = __fdiv_rn(LOG2E, tau);
+    const uint64_t nxm2 = pack2(-xm, -xm);
+    const uint64_t c2 = pack2(c, c);
+    uint64_t acc = pack2(0.0f, 0.0f);
+#pragma unroll
+    for (int i = 0; i < MAXCH; ++i) {
+      const int ch = tid + i * NTHR;
+      if (i < MAXCH - 1 || ch < nchunks) {   // all but the last chunk of every thread exist
+        const uint4 v = sh[ch];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint64_t a = mul2(add2(pack2(bf16_lo(w[j]), bf16_hi(w[j])), nxm2), c2);
+          float a0, a1;
+          unpack2(a, a0, a1);
+          acc = add2(acc, pack2(ex2(a0), ex2(a1)));
+        }
+      }
+    }
+    float e0, e1;
+    unpack2(acc, e0, e1);
+    l = block_sum_fixed(e0 + e1, S);
+  }
+
+  // ---- 4. candidate pass: every element of the window is counted straight
   //           into the leader's histogram (one shared-memory add per element)
   int hi = 0, lo = 1;
   if (sel) {
@@ -900,38 +927,10 @@ logp_kernel(const KParams P) {
     // the leader learns how many adds each peer sent from its summary
     sent = __reduce_add_sync(0xffffffffu, sent);
     if ((tid & 31) == 0 && sent) atomicAdd(&S.npush, sent);
-  }
-
-  // ---- 5. shard sum-exp, fixed tree
-  float l = 0.0f;
-  if (!greedy && xm_finite) {
-    const float c = __fdiv_rn(LOG2E, tau);
-    const uint64_t nxm2 = pack2(-xm, -xm);
-    const uint64_t c2 = pack2(c, c);
-    uint64_t acc = pack2(0.0f, 0.0f);
-#pragma unroll
-    for (int i = 0; i < MAXCH; ++i) {
-      const int ch = tid + i * NTHR;
-      if (i < MAXCH - 1 || ch < nchunks) {   // all but the last chunk of every thread exist
-        const uint4 v = sh[ch];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint64_t a = mul2(add2(pack2(bf16_lo(w[j]), bf16_hi(w[j])), nxm2), c2);
-          float a0, a1;
-          unpack2(a, a0, a1);
-          acc = add2(acc, pack2(ex2(a0), ex2(a1)));
-        }
-      }
-    }
-    float e0, e1;
-    unpack2(acc, e0, e1);
-    l = block_sum_fixed(e0 + e1, S);   // its barriers also complete the npush adds
-  } else if (sel) {
     __syncthreads();
   }
 
-  // ---- 6. summary to the leader
+  // ---- 5. summary to the leader
   if (tid == 0) {
     const uint4 msg = make_uint4(__float_as_uint(xm), __float_as_uint(l), sel ? S.npush : first, flags);
     if (r == 0) *reinterpret_cast<uint4*>(&S.slot[0]) = msg;
