@@ -10,8 +10,9 @@
  *   first 151936 columns; the 640 padded columns are never read.
  *
  *   "Reproduce and profile the Qwen3-8B TP4/CP2 experiment", section "How
- *   non-default CUDA topology reuses TP4/CP2": logp emits per-shard vocabulary
- *   summaries and merges them in fixed global-vocabulary order.  Here each of
+ *   non-default CUDA topology reuses TP4/CP2": every vocabulary shard yields a
+ *   summary, and the summaries combine in one fixed order of vocabulary
+ *   position.  Here each of
  *   the 8 shards of 19072 columns emits a (max, sum-exp) pair built in a fixed
  *   reduction tree and the pairs merge as a left fold over shard index 0..7.
  *

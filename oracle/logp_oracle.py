@@ -10,11 +10,11 @@ section):
 * "Configurable H100 consistency runs", sampling-flags paragraph: logits are
   the BF16 model logits, scaled by the temperature in float32; temperature 0
   selects greedy sampling; top-p lies in (0, 1]; top-k is -1 (off) or
-  1..real vocabulary size and is independent of top-p and temperature; the
-  top-p/top-k support is computed over the real vocabulary.
-* same page, KL-reference paragraph: the KL reference logprob is
-  temperature-scaled over the *full* vocabulary (not truncated), while the
-  policy logprob keeps its actual top-p/top-k sampling support.
+  1..real vocabulary size and is set separately from top-p and the
+  temperature; the support of both filters spans the whole real vocabulary.
+* same page, KL-reference paragraph: the reference side of the KL term uses
+  the temperature-scaled distribution over all real tokens, with no
+  truncation; only the policy side is restricted to its sampling support.
 * same page, topology paragraph: a padded vocabulary of 152576 columns is
   used; the real vocabulary (151936 columns) is the part the support is
   computed over.  Columns at or beyond the real size are ignored whatever
@@ -90,8 +90,8 @@ def validate(tau: float, top_p: float, top_k: int, target: int, vreal: int = VRE
 def scaled_logits(bits_row: np.ndarray, tau: float, vreal: int = VREAL) -> np.ndarray:
     """s_j = float32(x_j) / float32(tau), IEEE float32 division, widened to fp64.
 
-    "Both sides use float32 temperature scaling after the same BF16 model
-    logits" (Configurable H100 consistency runs, sampling flags).
+    The temperature divides the BF16 logits in float32 on both the training
+    and the rollout side (Configurable H100 consistency runs, sampling flags).
     """
     x = bf16_bits_to_f32(bits_row[:vreal])
     with np.errstate(over="ignore", invalid="ignore", divide="ignore"):
@@ -259,10 +259,11 @@ def logp_batch(bits: np.ndarray, tau, top_p, top_k, target, rows=None):
 def shard_summaries(bits_row: np.ndarray, tau: float):
     """Per-virtual-shard (max, sum-exp) of the scaled logits, fp64.
 
-    "logp emits ... vocabulary summaries and merges them in fixed global-vocab
-    order" (Reproduce and profile the Qwen3-8B TP4/CP2 experiment, section
-    "How non-default CUDA topology reuses TP4/CP2"), with the fixed virtual
-    TP8 partition of the padded vocabulary.  Padded columns are excluded.
+    Each vocabulary shard yields one summary and the summaries combine in a
+    fixed order of vocabulary position (Reproduce and profile the Qwen3-8B
+    TP4/CP2 experiment, section "How non-default CUDA topology reuses
+    TP4/CP2"); the shards are the fixed virtual TP8 partition of the padded
+    vocabulary.  Padded columns are excluded.
     Returns arrays m[8], l[8] (l_r = sum over shard r of exp(s_j - m_r)).
     """
     s_real = scaled_logits(np.asarray(bits_row, dtype=np.uint16), tau)

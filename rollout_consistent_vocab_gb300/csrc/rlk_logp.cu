@@ -24,10 +24,10 @@
 //   5. the CTA stores its summary (m_r, l_r, window) into the leader CTA's
 //      shared memory over DSMEM and arrives on the cluster barrier.
 //
-// The leader (rank 0) merges the summaries as a left fold over shard index
-// ("logp emits ... vocabulary summaries and merges them in fixed
-// global-vocab order", Reproduce and profile the Qwen3-8B TP4/CP2
-// experiment, "How non-default CUDA topology reuses TP4/CP2"), sums the 8
+// The leader (rank 0) merges the summaries as a left fold over shard index:
+// each vocabulary shard contributes one summary and the summaries combine in
+// one fixed order of vocabulary position (Reproduce and profile the Qwen3-8B
+// TP4/CP2 experiment, "How non-default CUDA topology reuses TP4/CP2"), sums the 8
 // histograms over DSMEM, and finds the top-k and top-p thresholds on the
 // merged histogram.  Masses there are per-key exp values times integer
 // counts in 2^-44 fixed point, so every sum is an exact integer sum and the
