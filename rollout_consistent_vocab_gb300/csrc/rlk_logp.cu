@@ -82,9 +82,9 @@ enum : uint32_t { FLAG_TIMEOUT = 1u, FLAG_NAN = 2u };
 // Sent by every CTA to every CTA before the candidate pass.
 struct __align__(16) MidSlot {
   float xm;        // shard maximum (a bf16 value or -inf / +inf)
-  int32_t lkey;    // order key reached by ceil(k/64) lane maxima of every warp of the shard
+  int32_t lkey;    // order key reached by ceil(k/W) lane maxima of every warp of the shard
   uint32_t flags;
-  int32_t pad;
+  float l;         // top-p-only rows: the shard's sum-exp (0 otherwise)
 };
 
 // Sent by every CTA to the leader at the end.
@@ -650,6 +650,18 @@ __device__ __forceinline__ bool select_warp(const uint32_t* cnt, int hi, int lo,
   return false;                                  // nucleus reaches below the window
 }
 
+// The 16-byte exchange message of this CTA (rank r) to CTA `to` (a local
+// store when `to` is this CTA).
+__device__ __forceinline__ void send_mid(Smem& S, uint32_t r, int to, float xm, int lkey,
+                                         uint32_t flags, float l, uint32_t bar_mid) {
+  const uint4 msg = make_uint4(__float_as_uint(xm), static_cast<uint32_t>(lkey), flags,
+                               __float_as_uint(l));
+  if (to == static_cast<int>(r))
+    *reinterpret_cast<uint4*>(&S.mid[r]) = msg;
+  else
+    st_async_v4(map_rank(smem_addr(&S.mid[r]), to), msg, map_rank(bar_mid, to));
+}
+
 // ------------------------------------------------------------ the kernel
 
 template <bool RESTR>
@@ -801,13 +813,11 @@ logp_kernel(const KParams P) {
   }
 
   cluster_wait();              // S0 complete: peers' barriers and histogram are ready
-  if (sel && tid < NSHARD) {
-    const uint4 msg = make_uint4(__float_as_uint(xm), static_cast<uint32_t>(lkey), flags, 0u);
-    if (tid == static_cast<int>(r))
-      *reinterpret_cast<uint4*>(&S.mid[r]) = msg;
-    else
-      st_async_v4(map_rank(smem_addr(&S.mid[r]), tid), msg, map_rank(bar_mid, tid));
-  }
+  // Rows with top-k send their maximum and bound now and overlap the exchange
+  // with the sum-exp pass; top-p-only rows also send their sum-exp, which
+  // tightens the candidate window, so they send after that pass.
+  const bool late_mid = sel && !k_on;
+  if (sel && !late_mid && tid < NSHARD) send_mid(S, r, tid, xm, lkey, flags, 0.0f, bar_mid);
 
   // ---- 3. shard sum-exp, fixed tree (while the peers' messages travel)
   float l = 0.0f;
@@ -835,6 +845,7 @@ logp_kernel(const KParams P) {
     unpack2(acc, e0, e1);
     l = block_sum_fixed(e0 + e1, S);
   }
+  if (late_mid && tid < NSHARD) send_mid(S, r, tid, xm, lkey, flags, l, bar_mid);
 
   // ---- 4. candidate pass: every element of the window is counted straight
   //           into the leader's histogram (one shared-memory add per element)
@@ -857,10 +868,19 @@ logp_kernel(const KParams P) {
         if (k_on) {
           wlo = max(wlo, L);
         } else {
-          // Tokens below s_max + ln((1-p)/V) cannot reach the nucleus: even all V
-          // of them would hold less than 1-p of the total mass.  The slack keeps the
-          // float evaluation on the safe side.
-          const float width = tau * (logf(static_cast<float>(VREAL) / (1.0f - p)) * 1.0001f + 1e-3f);
+          // Tokens with s <= s_max + ln((1-p) Z / V) cannot reach the nucleus:
+          // even all V of them would hold at most 1-p of the total mass Z
+          // (relative to the maximum), so the mass strictly above any of them is
+          // at least p Z.  Z is merged here exactly as the leader merges it; the
+          // slack keeps the float evaluation on the safe side.
+          const float cz = __fdiv_rn(LOG2E, tau);
+          float Z = 0.0f;
+#pragma unroll
+          for (int q = 0; q < NSHARD; ++q)
+            if (S.mid[q].xm > -INFINITY) Z = fmaf(S.mid[q].l, ex2((S.mid[q].xm - M) * cz), Z);
+          const float lnz = fmaxf(0.0f, logf(Z * 0.9999f));
+          const float width =
+              tau * (logf(static_cast<float>(VREAL) / (1.0f - p)) * 1.0001f + 1e-3f - lnz);
           wlo = max(wlo, okey_floor(M - width));
         }
         wlo = max(wlo, KEY_NEG_INF);
