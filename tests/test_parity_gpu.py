@@ -259,7 +259,7 @@ def test_ragged_batches_random_parameters(T):
     rng = np.random.default_rng(T)
     x, hot, n = W.hot_logits(T, 1, 300, seed=100 + T, device=DEV)
     tau = rng.choice([0.0, 0.5, 0.7, 1.0, 1.3, 2.0], T).astype(np.float32)
-    p = rng.choice([0.3, 0.8, 0.9, 0.95, 0.99, 1.0], T).astype(np.float32)
+    p = rng.choice([0.3, 0.8, 0.9, 0.95, 0.99, 0.9999, 1.0], T).astype(np.float32)
     k = rng.choice([-1, 1, 5, 50, 128, 256, 257, 1000], T).astype(np.int32)
     bits = bits_of(x)
     forced = set(rng.choice(T, max(1, T // 10), replace=False).tolist())
@@ -292,6 +292,26 @@ def test_row_stride_and_buffer_offset():
         f1, r1, s1 = pkg.logp_pair(big[3:], t, 0.7, 0.95, -1)
         torch.cuda.synchronize()
         assert torch.equal(f0, f1) and torch.equal(r0, r1) and torch.equal(s0, s1)
+
+
+def test_top_p_only_deep_nucleus():
+    """Top-p without top-k, p close to 1, on spread and on hot rows: the candidate
+    window derived from the total mass must still hold the whole nucleus."""
+    rng = np.random.default_rng(55)
+    xs = W.spread_logits(6, 2.0, seed=55, device=DEV)
+    xh, hot, n = W.hot_logits(6, 1, 64, seed=56, device=DEV)
+    x = torch.cat([xs, xh])
+    T = x.shape[0]
+    tau = rng.choice([0.7, 1.0, 1.3], T).astype(np.float32)
+    p = rng.choice([0.99, 0.999, 0.9999, 0.99999], T).astype(np.float32)
+    k = np.full(T, -1, np.int32)
+    bits = bits_of(x)
+    tg = oracle_targets(bits, tau, p, k, rng, {0, 7})
+    f, r, s = run_pair(x, _t(tg, torch.int32), _t(tau, torch.float32), _t(p, torch.float32),
+                       _t(k, torch.int32))
+    st = Stats()
+    check_rows(st, bits, tau, p, k, tg, f, r, s)
+    print("deep nucleus", st)
 
 
 def test_wide_support_fallback_path():
