@@ -34,7 +34,9 @@ UNIT = "tokens/s"
 VPAD, VREAL = 152576, 151936
 T_ROWS, TAU, TOP_P, TOP_K = 8192, 1.3, 0.99, 128
 WORKLOAD = "c2_hot1-256_T8192_policy+ref_kl"
-KERNEL_SRC = os.path.join(ROOT, "rollout_consistent_vocab_gb300", "csrc", "rlk_logp.cu")
+# the fused kernel's sources: its own file and the device code it includes
+KERNEL_SRCS = [os.path.join(ROOT, "rollout_consistent_vocab_gb300", "csrc", f)
+               for f in ("rlk_logp.cu", "rlk_device.cuh")]
 NCU_SUMMARY = os.path.join(ROOT, "profiles", "logp_pair_kernel_c2.md")
 
 
@@ -89,8 +91,11 @@ def measured_peak():
 
 
 def kernel_sha() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic():

@@ -57,8 +57,8 @@
  *   - Per-row parameter arrays cannot be checked on the host without a
  *     synchronisation: a row whose tau, top_p, top_k or target is out of
  *     domain gets NaN outputs, support -1, and increments *err_count (an
- *     optional device int32).  A shard load that does not complete within
- *     about two seconds is treated the same way.
+ *     optional device int32).  A shard load or exchange that does not
+ *     complete within 0.2 s is treated the same way.
  *   - rlk_last_error() returns a message for the last non-OK status of the
  *     calling host thread.
  */
@@ -137,6 +137,88 @@ rlk_status rlk_logp_kl(const rlk_logp_args* policy, const void* ref_logits,
  * out_kl are required device float[T]. */
 rlk_status rlk_logp_kl_ref(const rlk_logp_args* ref, const float* full_policy,
                            float* out_full_ref, float* out_kl, void* stream);
+
+/* ---------------------------------------------------------------------
+ * Vocabulary-sharded form: the fixed virtual TP8 partition with each shard
+ * in its own buffer, as a tensor-parallel rank would hold it ("Reproduce and
+ * profile the Qwen3-8B TP4/CP2 experiment", section "How non-default CUDA
+ * topology reuses TP4/CP2": every shard yields a summary and the summaries
+ * combine in one fixed vocabulary order).
+ *
+ * Round 1: rlk_logp_shard_summary on each shard (on whichever device holds
+ * it); gather the [T] outputs of the 8 shards into shard-major [8][T] arrays
+ * (the summary exchange of the tensor-parallel setting); rlk_logp_merge then
+ * gives the full logprob, bit-identical to rlk_logp_full/pair on the whole
+ * row.  Round 2 (restricted side): rlk_logp_shard_counts on each shard with
+ * the gathered summaries, then rlk_logp_merge with the counts of all shards
+ * gives the restricted logprob and support, bit-identical to rlk_logp_pair
+ * for every row whose support lies within 1024 order keys of the row maximum
+ * (8 binades of bf16); other rows get NaN and support -2 (the fused entry
+ * points resolve them by re-reading the row).
+ *
+ * Rows are validated as in rlk_logp_pair.  A rejected row gets NaN summaries
+ * and NaN outputs with support -1; only shard 0 increments err_count, so one
+ * pass over the 8 shards counts each rejected row once.
+ * ------------------------------------------------------------------- */
+
+typedef struct rlk_shard_args {
+  /* bf16 [T, row_stride]: the shard's columns; column 0 is vocabulary column
+   * 19072*shard.  Shards 0..6 read 19072 columns, shard 7 its 18432 real
+   * ones.  Base 16-byte aligned. */
+  const void* logits;
+  int64_t T;                 /* rows, < 2^31 */
+  int64_t row_stride;        /* elements; >= 19072, % 8 == 0 */
+  int32_t shard;             /* 0..7 */
+  const int32_t* target;     /* [T] target column in the whole vocabulary */
+  const float* temperature;  float temperature_scalar;
+  const float* top_p;        float top_p_scalar;
+  const int32_t* top_k;      int32_t top_k_scalar;
+  int32_t* err_count;        /* optional; counted by shard 0 only */
+} rlk_shard_args;
+
+/* Per-row summary of one shard, each output a device [T] array:
+ *   out_max     the shard maximum of the logits (a bf16 value; -inf if all
+ *               -inf; NaN for a rejected row);
+ *   out_sumexp  sum over the shard of exp((x_j - out_max) / tau) in the fixed
+ *               tree of the fused kernel (NaN if the shard holds a NaN or for
+ *               a rejected row, 0 for greedy rows);
+ *   out_aux     greedy rows: first vocabulary column holding the shard
+ *               maximum; rows with 1 <= k <= 1024: the shard's top-k witness
+ *               (an order key); otherwise 0;
+ *   out_target_logit  the target's logit, written only for rows whose target
+ *               lies in this shard (other entries are left untouched). */
+rlk_status rlk_logp_shard_summary(const rlk_shard_args* args, float* out_max, float* out_sumexp,
+                                  int32_t* out_aux, float* out_target_logit, void* stream);
+
+/* Per-row exact counts of this shard's tokens on the row's candidate window
+ * (at most 1024 order keys below the row maximum, derived from the 8
+ * summaries exactly as the fused kernel derives it).  maxes, sumexps, aux
+ * are the gathered shard-major [8][T] round-1 outputs.  out_counts: device
+ * uint32 [T][1024], 16-byte aligned; entry i counts the tokens whose bf16
+ * order key is the row maximum's key minus i (zero beyond the window and for
+ * rows without a top-k or top-p filter). */
+rlk_status rlk_logp_shard_counts(const rlk_shard_args* args, const float* maxes,
+                                 const float* sumexps, const int32_t* aux, uint32_t* out_counts,
+                                 void* stream);
+
+/* Merge of the 8 summaries of every row in fixed shard order.
+ *   maxes, sumexps, aux: shard-major [8][T]; target_logit: [T] (from the
+ *   shard holding each target); target, temperature/top_p/top_k as in
+ *   rlk_shard_args (per-row array or scalar).
+ *   out_full: [T] full logprob (required).
+ *   counts == NULL: full logprob only (top_p/top_k ignored).  Otherwise
+ *   count_shards (1 or 8) count arrays of [T][1024] each, summed here (pass
+ *   1 if they were already summed across shards), and out_restr /
+ *   out_support (at least one given) receive the restricted logprob and the
+ *   support size. */
+rlk_status rlk_logp_merge(const float* maxes, const float* sumexps, const int32_t* aux,
+                          const float* target_logit, int64_t T, const int32_t* target,
+                          const float* temperature, float temperature_scalar,
+                          const float* top_p, float top_p_scalar,
+                          const int32_t* top_k, int32_t top_k_scalar,
+                          const uint32_t* counts, int32_t count_shards,
+                          float* out_full, float* out_restr, int32_t* out_support,
+                          void* stream);
 
 /* Static message for a status code. */
 const char* rlk_status_string(rlk_status status);

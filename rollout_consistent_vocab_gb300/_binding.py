@@ -45,8 +45,26 @@ class LogpArgs(ctypes.Structure):
     ]
 
 
-EXPORTS = ("rlk_logp_full", "rlk_logp_restricted", "rlk_logp_pair", "rlk_logp_kl", "rlk_logp_kl_ref",
-           "rlk_status_string", "rlk_last_error", "rlk_abi_version")
+class ShardArgs(ctypes.Structure):
+    _fields_ = [
+        ("logits", ctypes.c_void_p),
+        ("T", ctypes.c_int64),
+        ("row_stride", ctypes.c_int64),
+        ("shard", ctypes.c_int32),
+        ("target", ctypes.c_void_p),
+        ("temperature", ctypes.c_void_p),
+        ("temperature_scalar", ctypes.c_float),
+        ("top_p", ctypes.c_void_p),
+        ("top_p_scalar", ctypes.c_float),
+        ("top_k", ctypes.c_void_p),
+        ("top_k_scalar", ctypes.c_int32),
+        ("err_count", ctypes.c_void_p),
+    ]
+
+
+COMPUTE = ("rlk_logp_full", "rlk_logp_restricted", "rlk_logp_pair", "rlk_logp_kl", "rlk_logp_kl_ref",
+           "rlk_logp_shard_summary", "rlk_logp_shard_counts", "rlk_logp_merge")
+EXPORTS = COMPUTE + ("rlk_status_string", "rlk_last_error", "rlk_abi_version")
 
 _lib = None
 
@@ -67,8 +85,13 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     lib.rlk_logp_pair.argtypes = [A, VP, VP, VP, VP]
     lib.rlk_logp_kl.argtypes = [A, VP, ctypes.c_int64, VP, VP, VP, VP, VP, VP]
     lib.rlk_logp_kl_ref.argtypes = [A, VP, VP, VP, VP]
-    for f in ("rlk_logp_full", "rlk_logp_restricted", "rlk_logp_pair", "rlk_logp_kl",
-              "rlk_logp_kl_ref"):
+    SA = P(ShardArgs)
+    lib.rlk_logp_shard_summary.argtypes = [SA, VP, VP, VP, VP, VP]
+    lib.rlk_logp_shard_counts.argtypes = [SA, VP, VP, VP, VP, VP]
+    f32, i32 = ctypes.c_float, ctypes.c_int32
+    lib.rlk_logp_merge.argtypes = [VP, VP, VP, VP, ctypes.c_int64, VP, VP, f32, VP, f32, VP, i32,
+                                   VP, i32, VP, VP, VP, VP]
+    for f in COMPUTE:
         getattr(lib, f).restype = ctypes.c_int
     lib.rlk_status_string.argtypes = [ctypes.c_int]
     lib.rlk_status_string.restype = ctypes.c_char_p
@@ -212,3 +235,96 @@ def logp_kl_ref(ref_logits, target, full_policy, temperature=1.0, *, out_full_re
     check(lib.rlk_logp_kl_ref(ctypes.byref(a), _ptr(full_policy), _ptr(out_full_ref), _ptr(out_kl),
                               _stream(stream)))
     return out_full_ref, out_kl
+
+
+# ------------------------------------------------------------ vocabulary-sharded form
+
+def make_shard_args(shard_logits, shard, target, temperature=1.0, top_p=1.0, top_k=-1,
+                    err_count=None) -> ShardArgs:
+    torch = _torch()
+    if shard_logits.dtype != torch.bfloat16 or shard_logits.dim() != 2 or shard_logits.stride(1) != 1:
+        raise ValueError("shard logits must be a bf16 [T, >=19072] tensor with unit column stride")
+    if shard_logits.shape[1] < SHARD_WIDTH:
+        raise ValueError(f"shard logits must have at least {SHARD_WIDTH} columns")
+    T = shard_logits.shape[0]
+    if target.dtype != torch.int32 or target.shape != (T,) or not target.is_contiguous():
+        raise ValueError("target must be a contiguous int32 tensor of shape [T]")
+    a = ShardArgs()
+    a.logits = shard_logits.data_ptr() if T else None
+    a.T = T
+    a.row_stride = shard_logits.stride(0) if T else SHARD_WIDTH
+    a.shard = shard
+    a.target = _ptr(target) if T else None
+    a.temperature, a.temperature_scalar = _param(temperature, T, torch.float32, "temperature")
+    a.top_p, a.top_p_scalar = _param(top_p, T, torch.float32, "top_p")
+    a.top_k, a.top_k_scalar = _param(top_k, T, torch.int32, "top_k")
+    a.err_count = _ptr(err_count)
+    return a
+
+
+def shard_summary(shard_logits, shard, target, temperature=1.0, top_p=1.0, top_k=-1, *,
+                  out_max, out_sumexp, out_aux, out_target_logit, err_count=None, stream=None):
+    """Round 1 on one shard: per-row (max, sum-exp, aux) into the given [T]
+    views, and the target logit for rows whose target lies in this shard."""
+    lib = load_library()
+    a = make_shard_args(shard_logits, shard, target, temperature, top_p, top_k, err_count)
+    check(lib.rlk_logp_shard_summary(ctypes.byref(a), _ptr(out_max), _ptr(out_sumexp), _ptr(out_aux),
+                                     _ptr(out_target_logit), _stream(stream)))
+
+
+def shard_counts(shard_logits, shard, target, maxes, sumexps, aux, temperature=1.0, top_p=1.0,
+                 top_k=-1, *, out_counts, stream=None):
+    """Round 2 on one shard: exact per-key counts [T, 1024] on each row's window."""
+    lib = load_library()
+    a = make_shard_args(shard_logits, shard, target, temperature, top_p, top_k, None)
+    check(lib.rlk_logp_shard_counts(ctypes.byref(a), _ptr(maxes), _ptr(sumexps), _ptr(aux),
+                                    _ptr(out_counts), _stream(stream)))
+
+
+def logp_merge(maxes, sumexps, aux, target_logit, target, temperature=1.0, top_p=1.0, top_k=-1, *,
+               counts=None, out_full=None, out_restr=None, out_support=None, stream=None):
+    """Merge of the gathered [8, T] summaries: full logprob, and with counts
+    ([1 or 8, T, 1024]) the restricted logprob and support."""
+    lib = load_library()
+    torch = _torch()
+    T = target.shape[0]
+    tp, ts = _param(temperature, T, torch.float32, "temperature")
+    pp, ps = _param(top_p, T, torch.float32, "top_p")
+    kp, ks = _param(top_k, T, torch.int32, "top_k")
+    out_full = _empty(T, torch.float32, maxes) if out_full is None else out_full
+    if counts is not None:
+        out_restr = _empty(T, torch.float32, maxes) if out_restr is None else out_restr
+        out_support = _empty(T, torch.int32, maxes) if out_support is None else out_support
+    nc = 0 if counts is None else counts.shape[0]
+    check(lib.rlk_logp_merge(_ptr(maxes), _ptr(sumexps), _ptr(aux), _ptr(target_logit), T,
+                             _ptr(target), tp, ts, pp, ps, kp, ks, _ptr(counts), nc,
+                             _ptr(out_full), _ptr(out_restr), _ptr(out_support), _stream(stream)))
+    return (out_full,) if counts is None else (out_full, out_restr, out_support)
+
+
+def logp_sharded(shards, target, temperature=1.0, top_p=1.0, top_k=-1, *, restricted=True,
+                 err_count=None, stream=None):
+    """All rounds over 8 shard buffers (shard r holds vocabulary columns
+    [19072 r, 19072 (r+1))): summaries, then counts when restricted, then the
+    merge.  Returns (full,) or (full, restricted, support)."""
+    torch = _torch()
+    if len(shards) != NUM_SHARDS:
+        raise ValueError(f"expected {NUM_SHARDS} shard tensors")
+    T = target.shape[0]
+    dev = shards[0].device
+    maxes = torch.empty((NUM_SHARDS, T), dtype=torch.float32, device=dev)
+    sumexps = torch.empty_like(maxes)
+    aux = torch.empty((NUM_SHARDS, T), dtype=torch.int32, device=dev)
+    xt = torch.empty((T,), dtype=torch.float32, device=dev)
+    pk = (top_p, top_k) if restricted else (1.0, -1)
+    for r, sh in enumerate(shards):
+        shard_summary(sh, r, target, temperature, *pk, out_max=maxes[r], out_sumexp=sumexps[r],
+                      out_aux=aux[r], out_target_logit=xt, err_count=err_count, stream=stream)
+    counts = None
+    if restricted:
+        counts = torch.empty((NUM_SHARDS, T, 1024), dtype=torch.int32, device=dev)
+        for r, sh in enumerate(shards):
+            shard_counts(sh, r, target, maxes, sumexps, aux, temperature, top_p, top_k,
+                         out_counts=counts[r], stream=stream)
+    return logp_merge(maxes, sumexps, aux, xt, target, temperature, *pk, counts=counts,
+                      stream=stream)

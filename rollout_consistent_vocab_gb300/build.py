@@ -8,7 +8,9 @@ import subprocess
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SRC = os.path.join(PKG, "csrc", "rlk_logp.cu")
+CSRC = os.path.join(PKG, "csrc")
+SOURCES = [os.path.join(CSRC, "rlk_logp.cu"), os.path.join(CSRC, "rlk_shard.cu")]
+HEADERS = [os.path.join(CSRC, "rlk_device.cuh"), os.path.join(CSRC, "rlk_host.h")]
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIB_DIR, "librlk_logp.so")
@@ -31,7 +33,7 @@ def needs_build() -> bool:
     if not os.path.exists(LIB):
         return True
     lib_t = os.path.getmtime(LIB)
-    deps = [SRC, os.path.join(INCLUDE, "rlk_logp.h")]
+    deps = [*SOURCES, *HEADERS, os.path.join(INCLUDE, "rlk_logp.h")]
     return any(os.path.getmtime(d) > lib_t for d in deps)
 
 
@@ -40,7 +42,8 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
         return LIB
     os.makedirs(LIB_DIR, exist_ok=True)
     tmp = LIB + ".tmp"
-    cmd = [nvcc_path(), *NVCC_FLAGS, "-I", INCLUDE, "-o", tmp, SRC]
+    # one nvcc call; --threads compiles the translation units in parallel
+    cmd = [nvcc_path(), *NVCC_FLAGS, "--threads", "0", "-I", INCLUDE, "-o", tmp, *SOURCES]
     if verbose:
         print(" ".join(cmd))
     subprocess.run(cmd, check=True)

@@ -1,0 +1,522 @@
+// rlk_shard.cu -- the vocabulary-sharded form of the strict token logprob.
+//
+// Each shard of the fixed virtual TP8 partition sits in its own buffer, as a
+// tensor-parallel rank would hold it.  Every shard yields a summary and the
+// summaries combine in one fixed order of vocabulary position (Reproduce and
+// profile the Qwen3-8B TP4/CP2 experiment, "How non-default CUDA topology
+// reuses TP4/CP2"):
+//
+//   round 1  shard_summary_kernel, one CTA per row of one shard: the same
+//            max pass, top-k witness, greedy/NaN scan and fixed-tree sum-exp
+//            as a CTA of the fused kernel, so the (max, sum-exp) pair has the
+//            same bits;
+//   round 2  shard_counts_kernel: the row's candidate window from the 8
+//            gathered summaries (candidate_window, as in the fused kernel)
+//            and the exact per-key counts of this shard's tokens in it;
+//   merge    merge_kernel, one warp per row: the left fold over shard index
+//            of the fused kernel's leader, then the same warp selection on
+//            the summed counts.
+//
+// The fused kernel resolves a support that reaches below the window by
+// re-reading the row; a shard cannot, so such rows are reported (support -2).
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "rlk_logp.h"
+#include "rlk_device.cuh"
+#include "rlk_host.h"
+
+namespace rlk {
+
+struct __align__(128) ShardSmem {
+  uint4 shard[SHARD_CHUNKS];
+  uint32_t hist[WIN];              // counts kernel: per-key counts of this shard
+  uint32_t red_u[NWARP];
+  int32_t red_i[NWARP];
+  float red_f[NWARP];
+  unsigned long long bar_load;
+};
+static_assert(sizeof(ShardSmem) + 1024 <= 233472 / CTAS_PER_SM, "shared memory budget of 5 CTAs per SM");
+
+struct ShardParams {
+  const uint16_t* logits;
+  int64_t stride;
+  int64_t T;
+  int shard;
+  const int32_t* target;
+  const float* tau_arr;
+  const float* p_arr;
+  const int32_t* k_arr;
+  float tau_s, p_s;
+  int32_t k_s;
+  // round 1 outputs
+  float* out_max;
+  float* out_sumexp;
+  int32_t* out_aux;
+  float* out_xt;
+  // round 2: gathered summaries in, counts out
+  const float* g_max;
+  const float* g_sumexp;
+  const int32_t* g_aux;
+  uint32_t* out_counts;
+  int32_t* err;
+};
+
+struct RowParams {
+  float tau, p;
+  int k, t;
+  bool valid, greedy, k_on, p_on;
+};
+
+// The row's parameters and the validity rule of the fused kernel.
+__device__ __forceinline__ RowParams row_params(const float* tau_arr, float tau_s, const float* p_arr,
+                                                float p_s, const int32_t* k_arr, int32_t k_s,
+                                                const int32_t* target, int64_t row) {
+  RowParams rp;
+  rp.tau = tau_arr ? tau_arr[row] : tau_s;
+  rp.p = p_arr ? p_arr[row] : p_s;
+  rp.k = k_arr ? k_arr[row] : k_s;
+  rp.t = target[row];
+  rp.valid = (rp.tau >= 0.0f) && (rp.tau <= 3.402823466e38f) && (rp.p > 0.0f) && (rp.p <= 1.0f) &&
+             (rp.k == -1 || (rp.k >= 1 && rp.k <= VREAL)) && (rp.t >= 0) && (rp.t < VREAL);
+  rp.greedy = (rp.tau == 0.0f);
+  rp.k_on = (rp.k != -1) && (rp.k < VREAL);
+  rp.p_on = (rp.p < 1.0f);
+  return rp;
+}
+
+// Thread 0 starts the bulk copy of one shard row into shared memory.
+__device__ __forceinline__ void load_shard_row(ShardSmem& S, const uint16_t* rowp, int nchunks) {
+  if (threadIdx.x == 0) {
+    const uint32_t bar = smem_addr(&S.bar_load);
+    mbar_init(bar, 1);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    const uint32_t bytes = static_cast<uint32_t>(nchunks) * 16u;
+    mbar_arrive_expect_tx(bar, bytes);
+    const uint64_t pol = evict_first_policy();
+    const uint32_t piece = bytes / TMA_PIECES;
+    const char* src = reinterpret_cast<const char*>(rowp);
+    const uint32_t dst = smem_addr(S.shard);
+#pragma unroll
+    for (int i = 0; i < TMA_PIECES; ++i) bulk_load(dst + i * piece, src + i * piece, piece, bar, pol);
+  }
+}
+
+// ------------------------------------------------------------ round 1
+
+__global__ void __launch_bounds__(NTHR, CTAS_PER_SM) shard_summary_kernel(const ShardParams P) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  ShardSmem& S = *reinterpret_cast<ShardSmem*>(smem_raw);
+  const int tid = threadIdx.x;
+  const int64_t row = blockIdx.x;
+  const int r = P.shard;
+  const int nchunks = (r == NSHARD - 1) ? LAST_CHUNKS : SHARD_CHUNKS;
+  const uint32_t bar = smem_addr(&S.bar_load);
+  load_shard_row(S, P.logits + row * P.stride, nchunks);
+
+  const RowParams rp = row_params(P.tau_arr, P.tau_s, P.p_arr, P.p_s, P.k_arr, P.k_s, P.target, row);
+  const float qnan = __int_as_float(0x7fc00000);
+  if (!rp.valid) {
+    if (tid == 0) {
+      mbar_wait_bounded(bar);   // the copy writes this CTA's shared memory: let it land
+      P.out_max[row] = qnan;
+      P.out_sumexp[row] = qnan;
+      P.out_aux[row] = 0;
+      if (r == 0 && P.err) atomicAdd(P.err, 1);
+    }
+    return;
+  }
+  __syncthreads();              // barrier initialised before anyone waits on it
+  bool bad = false;
+  if (!mbar_wait_bounded(bar)) {
+    bad = true;
+    mbar_wait_bounded(bar);     // give copies in flight a second bounded chance to land
+  }
+
+  const uint4* sh = S.shard;
+  __nv_bfloat162 cm[MAXCH];
+  const int tkey = pass_max(sh, tid, nchunks, cm);
+  const int kw = (rp.k + ROW_WARPS - 1) / ROW_WARPS;
+  const bool k_bound = !rp.greedy && rp.k_on && kw <= 32;
+  stage_max_bound(tkey, k_bound ? kw : 0, S);
+  __syncthreads();
+  unsigned xkey = S.red_u[0];
+  int lkey = S.red_i[0];
+#pragma unroll
+  for (int w = 1; w < NWARP; ++w) { xkey = max(xkey, S.red_u[w]); lkey = min(lkey, S.red_i[w]); }
+  const float xm = key_value(static_cast<int>(xkey));
+  const bool xm_finite = (xm > -INFINITY) && (xm < INFINITY);
+  if (xm != xm) bad = true;     // a thread whose every element is NaN
+
+  uint32_t first = 0x7fffffffu;
+  if (rp.greedy || xm == -INFINITY) {
+    // greedy: first column of this shard holding its maximum; both: NaN scan
+    bool nan_seen = false;
+    int f = 0x7fffffff;
+    for (int ch = tid; ch < nchunks; ch += NTHR) {
+      const uint4 v = sh[ch];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 7; j >= 0; --j) {
+        const float x = (j & 1) ? bf16_hi(w[j >> 1]) : bf16_lo(w[j >> 1]);
+        nan_seen |= (x != x);
+        if (x == xm) f = min(f, ch * 8 + j);
+      }
+    }
+    if (__syncthreads_or(nan_seen)) bad = true;
+    if (rp.greedy) {
+      f = block_min_int(f, S);
+      if (f != 0x7fffffff) first = static_cast<uint32_t>(f + r * SW);
+    }
+  }
+  float l = 0.0f;
+  if (!rp.greedy && xm_finite) l = block_sum_fixed(pass_sumexp(sh, tid, nchunks, xm, __fdiv_rn(LOG2E, rp.tau)), S);
+  if (tid == 0) {
+    P.out_max[row] = xm;
+    P.out_sumexp[row] = bad ? qnan : l;
+    P.out_aux[row] = rp.greedy ? static_cast<int32_t>(first) : (k_bound ? lkey : 0);
+    const int local_t = rp.t - r * SW;
+    if (local_t >= 0 && local_t < nchunks * 8) {
+      const uint16_t* elem = reinterpret_cast<const uint16_t*>(S.shard);
+      P.out_xt[row] = __uint_as_float(static_cast<uint32_t>(elem[local_t]) << 16);
+    }
+  }
+}
+
+// ------------------------------------------------------------ round 2
+
+// The row's candidate window from the gathered summaries: maximum and top-k
+// witness folded over the shards, and for top-p-only rows the total mass Z
+// folded in shard order exactly as the fused kernel folds the exchanged
+// sum-exps.  Also returns M.
+__device__ __forceinline__ void gathered_window(const float* g_max, const float* g_sumexp,
+                                                const int32_t* g_aux, int64_t T, int64_t row,
+                                                const RowParams& rp, float& M, int& hi, int& lo) {
+  int L = 0x7fffffff;
+  M = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < NSHARD; ++q) {
+    M = fmaxf(M, g_max[q * T + row]);
+    L = min(L, g_aux[q * T + row]);
+  }
+  float Z = 0.0f;
+  if (!rp.k_on) {
+    const float cz = __fdiv_rn(LOG2E, rp.tau);
+#pragma unroll
+    for (int q = 0; q < NSHARD; ++q) {
+      const float xq = g_max[q * T + row];
+      if (xq > -INFINITY) Z = fmaf(g_sumexp[q * T + row], ex2((xq - M) * cz), Z);
+    }
+  }
+  candidate_window(M, L, Z, rp.tau, rp.p, rp.k_on, hi, lo);
+}
+
+__global__ void __launch_bounds__(NTHR, CTAS_PER_SM) shard_counts_kernel(const ShardParams P) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  ShardSmem& S = *reinterpret_cast<ShardSmem*>(smem_raw);
+  const int tid = threadIdx.x;
+  const int64_t row = blockIdx.x;
+  const int r = P.shard;
+  const int nchunks = (r == NSHARD - 1) ? LAST_CHUNKS : SHARD_CHUNKS;
+  const RowParams rp = row_params(P.tau_arr, P.tau_s, P.p_arr, P.p_s, P.k_arr, P.k_s, P.target, row);
+  const bool sel = rp.valid && !rp.greedy && (rp.k_on || rp.p_on);
+  for (int i = tid; i < WIN; i += NTHR) S.hist[i] = 0u;
+  if (sel) {
+    float M;
+    int hi, lo;
+    gathered_window(P.g_max, P.g_sumexp, P.g_aux, P.T, row, rp, M, hi, lo);
+    // the fused kernel's CTA counts only if its shard maximum is finite and
+    // reaches the window
+    const float xm = P.g_max[static_cast<int64_t>(r) * P.T + row];
+    const bool count = (xm > -INFINITY) && (xm < INFINITY) && lo <= hi && okey_of(xm) >= lo;
+    if (count) {
+      const uint32_t bar = smem_addr(&S.bar_load);
+      load_shard_row(S, P.logits + row * P.stride, nchunks);
+      __syncthreads();          // barrier initialised and histogram zeroed
+      if (!mbar_wait_bounded(bar)) mbar_wait_bounded(bar);
+      __nv_bfloat162 cm[MAXCH];
+      pass_max(S.shard, tid, nchunks, cm);
+      const float vlo_f = key_value(lo);
+      const __nv_bfloat162 vlo2 = __floats2bfloat162_rn(vlo_f, vlo_f);
+#pragma unroll
+      for (int i = 0; i < MAXCH; ++i) {
+        if (__hge2_mask(cm[i], vlo2) == 0u) continue;
+        const uint4 v = S.shard[tid + i * NTHR];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t b = (w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
+          if (__uint_as_float(b << 16) >= vlo_f) red_shared_add(&S.hist[hi - okey(b)], 1u);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(P.out_counts + row * WIN);
+  const uint4* src = reinterpret_cast<const uint4*>(S.hist);
+  for (int i = tid; i < WIN / 4; i += NTHR) dst[i] = src[i];
+}
+
+// ------------------------------------------------------------ merge
+
+struct MergeParams {
+  const float* g_max;
+  const float* g_sumexp;
+  const int32_t* g_aux;
+  const float* xt;
+  int64_t T;
+  const int32_t* target;
+  const float* tau_arr;
+  const float* p_arr;
+  const int32_t* k_arr;
+  float tau_s, p_s;
+  int32_t k_s;
+  const uint32_t* counts;
+  int count_shards;
+  float* out_full;
+  float* out_restr;
+  int32_t* out_support;
+};
+
+constexpr int MERGE_ROWS = NTHR / 32;   // one warp per row
+
+template <bool RESTR>
+__global__ void __launch_bounds__(NTHR) merge_kernel(const MergeParams P) {
+  __shared__ uint32_t cnt[MERGE_ROWS][WIN];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * MERGE_ROWS + warp;
+  if (row >= P.T) return;
+  const int64_t T = P.T;
+  const RowParams rp = row_params(P.tau_arr, P.tau_s, P.p_arr, P.p_s, P.k_arr, P.k_s, P.target, row);
+  const float qnan = __int_as_float(0x7fc00000);
+  float full = qnan, restr = qnan;
+  int support = -1;
+  if (rp.valid) {
+    const bool sel = RESTR && !rp.greedy && (rp.k_on || rp.p_on);
+    bool bad = false;
+    float M = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < NSHARD; ++q) {
+      const float xq = P.g_max[q * T + row];
+      const float lq = P.g_sumexp[q * T + row];
+      if (xq == INFINITY || xq != xq || lq != lq) bad = true;
+      M = fmaxf(M, xq);
+    }
+    bad |= !(M > -INFINITY);
+    const float c = rp.greedy ? 0.0f : __fdiv_rn(LOG2E, rp.tau);
+    float Z = 0.0f, d = 0.0f;
+    const float xt = P.xt[row];
+    if (!bad && rp.greedy) {
+      uint32_t amax = 0x7fffffffu;
+#pragma unroll
+      for (int q = NSHARD - 1; q >= 0; --q)
+        if (P.g_max[q * T + row] == M) amax = static_cast<uint32_t>(P.g_aux[q * T + row]);
+      full = restr = (static_cast<uint32_t>(rp.t) == amax) ? 0.0f : -INFINITY;
+      support = 1;
+    } else if (!bad) {
+      if (isinf(__fdiv_rn(M, rp.tau))) {
+        bad = true;
+      } else {
+#pragma unroll
+        for (int q = 0; q < NSHARD; ++q) {
+          const float xq = P.g_max[q * T + row];
+          if (xq > -INFINITY) Z = fmaf(P.g_sumexp[q * T + row], ex2((xq - M) * c), Z);
+        }
+        d = __fdiv_rn(xt - M, rp.tau);
+        full = d - logf(Z);
+        restr = full;
+        support = VREAL;
+      }
+    }
+    if (sel && !bad) {
+      float Mw;
+      int hi, lo;
+      gathered_window(P.g_max, P.g_sumexp, P.g_aux, T, row, rp, Mw, hi, lo);
+      const int n = hi - lo + 1;
+      for (int i = lane; i < n; i += 32) {
+        uint32_t sum = 0;
+        for (int q = 0; q < P.count_shards; ++q) sum += P.counts[(q * T + row) * WIN + i];
+        cnt[warp][i] = sum;
+      }
+      __syncwarp();
+      SelResult sr{0u, 0ull, 0};
+      if (n > 0 && select_warp(cnt[warp], hi, lo, M, c, Z, rp.p, rp.k, rp.k_on, rp.p_on, sr)) {
+        const bool in_s = okey_of(xt) >= sr.min_key;
+        const float zs = __ull2float_rn(sr.zs) * (1.0f / FX_SCALE);
+        restr = in_s ? d - logf(zs) : -INFINITY;
+        support = static_cast<int>(sr.support);
+      } else {
+        restr = qnan;           // the support reaches below the exchanged window
+        support = -2;
+      }
+    }
+  }
+  if (lane == 0) {
+    P.out_full[row] = full;
+    if (RESTR) {
+      if (P.out_restr) P.out_restr[row] = restr;
+      if (P.out_support) P.out_support[row] = support;
+    }
+  }
+}
+
+// ------------------------------------------------------------ host side
+
+rlk_status check_shard_args(const rlk_shard_args* a) {
+  if (!a) return fail(RLK_EINVAL, "args is NULL");
+  if (a->T < 0 || a->T >= (int64_t(1) << 31)) return fail(RLK_EINVAL, "T = %lld out of range [0, 2^31)", (long long)a->T);
+  if (a->shard < 0 || a->shard >= NSHARD) return fail(RLK_EINVAL, "shard %d must be 0..%d", a->shard, NSHARD - 1);
+  if (a->T == 0) return RLK_OK;
+  if (!a->logits) return fail(RLK_EINVAL, "logits is NULL");
+  if (a->row_stride < SW) return fail(RLK_EINVAL, "row_stride %lld < %d", (long long)a->row_stride, SW);
+  if (!aligned(a->logits, 16)) return fail(RLK_EALIGN, "logits base is not 16-byte aligned");
+  if (a->row_stride % 8 != 0) return fail(RLK_EALIGN, "row_stride %lld is not a multiple of 8", (long long)a->row_stride);
+  if (!a->target) return fail(RLK_EINVAL, "target is NULL");
+  if (!aligned(a->target, 4)) return fail(RLK_EALIGN, "target is not 4-byte aligned");
+  rlk_status s;
+  if ((s = check_tau(a->temperature, a->temperature_scalar)) != RLK_OK) return s;
+  if ((s = check_top_p(a->top_p, a->top_p_scalar)) != RLK_OK) return s;
+  if ((s = check_top_k(a->top_k, a->top_k_scalar)) != RLK_OK) return s;
+  if (a->err_count && !aligned(a->err_count, 4)) return fail(RLK_EALIGN, "err_count is not 4-byte aligned");
+  return RLK_OK;
+}
+
+ShardParams make_shard_params(const rlk_shard_args* a) {
+  ShardParams P;
+  memset(&P, 0, sizeof(P));
+  P.logits = static_cast<const uint16_t*>(a->logits);
+  P.stride = a->row_stride;
+  P.T = a->T;
+  P.shard = a->shard;
+  P.target = a->target;
+  P.tau_arr = a->temperature;
+  P.p_arr = a->top_p;
+  P.k_arr = a->top_k;
+  P.tau_s = a->temperature_scalar;
+  P.p_s = a->top_p_scalar;
+  P.k_s = a->top_k_scalar;
+  P.err = a->err_count;
+  return P;
+}
+
+template <int WHICH>
+rlk_status launch_shard(void (*kernel)(ShardParams), const ShardParams& P, cudaStream_t stream) {
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(sizeof(ShardSmem)));
+    if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    configured[dev] = true;
+  }
+  kernel<<<static_cast<unsigned>(P.T), NTHR, sizeof(ShardSmem), stream>>>(P);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(RLK_ECUDA, "kernel launch: %s", cudaGetErrorString(e));
+  return RLK_OK;
+}
+
+}  // namespace rlk
+
+using namespace rlk;
+
+extern "C" {
+
+rlk_status rlk_logp_shard_summary(const rlk_shard_args* args, float* out_max, float* out_sumexp,
+                                  int32_t* out_aux, float* out_target_logit, void* stream) {
+  rlk_status s = check_shard_args(args);
+  if (s != RLK_OK || args->T == 0) return s;
+  if ((s = check_out(out_max, "out_max", true)) != RLK_OK) return s;
+  if ((s = check_out(out_sumexp, "out_sumexp", true)) != RLK_OK) return s;
+  if ((s = check_out(out_aux, "out_aux", true)) != RLK_OK) return s;
+  if ((s = check_out(out_target_logit, "out_target_logit", true)) != RLK_OK) return s;
+  ShardParams P = make_shard_params(args);
+  P.out_max = out_max;
+  P.out_sumexp = out_sumexp;
+  P.out_aux = out_aux;
+  P.out_xt = out_target_logit;
+  return launch_shard<0>(shard_summary_kernel, P, static_cast<cudaStream_t>(stream));
+}
+
+rlk_status rlk_logp_shard_counts(const rlk_shard_args* args, const float* maxes,
+                                 const float* sumexps, const int32_t* aux, uint32_t* out_counts,
+                                 void* stream) {
+  rlk_status s = check_shard_args(args);
+  if (s != RLK_OK || args->T == 0) return s;
+  if ((s = check_out(maxes, "maxes", true)) != RLK_OK) return s;
+  if ((s = check_out(sumexps, "sumexps", true)) != RLK_OK) return s;
+  if ((s = check_out(aux, "aux", true)) != RLK_OK) return s;
+  if (!out_counts) return fail(RLK_EINVAL, "out_counts is NULL");
+  if (!aligned(out_counts, 16)) return fail(RLK_EALIGN, "out_counts is not 16-byte aligned");
+  ShardParams P = make_shard_params(args);
+  P.g_max = maxes;
+  P.g_sumexp = sumexps;
+  P.g_aux = aux;
+  P.out_counts = out_counts;
+  return launch_shard<1>(shard_counts_kernel, P, static_cast<cudaStream_t>(stream));
+}
+
+rlk_status rlk_logp_merge(const float* maxes, const float* sumexps, const int32_t* aux,
+                          const float* target_logit, int64_t T, const int32_t* target,
+                          const float* temperature, float temperature_scalar,
+                          const float* top_p, float top_p_scalar,
+                          const int32_t* top_k, int32_t top_k_scalar,
+                          const uint32_t* counts, int32_t count_shards,
+                          float* out_full, float* out_restr, int32_t* out_support,
+                          void* stream) {
+  if (T < 0 || T >= (int64_t(1) << 31)) return fail(RLK_EINVAL, "T = %lld out of range [0, 2^31)", (long long)T);
+  if (T == 0) return RLK_OK;
+  rlk_status s;
+  if ((s = check_out(maxes, "maxes", true)) != RLK_OK) return s;
+  if ((s = check_out(sumexps, "sumexps", true)) != RLK_OK) return s;
+  if ((s = check_out(aux, "aux", true)) != RLK_OK) return s;
+  if ((s = check_out(target_logit, "target_logit", true)) != RLK_OK) return s;
+  if ((s = check_out(target, "target", true)) != RLK_OK) return s;
+  if ((s = check_out(out_full, "out_full", true)) != RLK_OK) return s;
+  if ((s = check_tau(temperature, temperature_scalar)) != RLK_OK) return s;
+  const bool restr = counts != nullptr;
+  if (restr) {
+    if (count_shards != 1 && count_shards != NSHARD)
+      return fail(RLK_EINVAL, "count_shards %d must be 1 or %d", count_shards, NSHARD);
+    if (!aligned(counts, 4)) return fail(RLK_EALIGN, "counts is not 4-byte aligned");
+    if ((s = check_top_p(top_p, top_p_scalar)) != RLK_OK) return s;
+    if ((s = check_top_k(top_k, top_k_scalar)) != RLK_OK) return s;
+    if (!out_restr && !out_support) return fail(RLK_EINVAL, "out_restr and out_support are both NULL");
+    if ((s = check_out(out_restr, "out_restr", false)) != RLK_OK) return s;
+    if ((s = check_out(out_support, "out_support", false)) != RLK_OK) return s;
+  }
+  MergeParams P;
+  memset(&P, 0, sizeof(P));
+  P.g_max = maxes;
+  P.g_sumexp = sumexps;
+  P.g_aux = aux;
+  P.xt = target_logit;
+  P.T = T;
+  P.target = target;
+  P.tau_arr = temperature;
+  P.tau_s = temperature_scalar;
+  P.p_arr = restr ? top_p : nullptr;
+  P.p_s = restr ? top_p_scalar : 1.0f;
+  P.k_arr = restr ? top_k : nullptr;
+  P.k_s = restr ? top_k_scalar : -1;
+  P.counts = counts;
+  P.count_shards = count_shards;
+  P.out_full = out_full;
+  P.out_restr = out_restr;
+  P.out_support = out_support;
+  const unsigned grid = static_cast<unsigned>((T + MERGE_ROWS - 1) / MERGE_ROWS);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (restr) merge_kernel<true><<<grid, NTHR, 0, st>>>(P);
+  else merge_kernel<false><<<grid, NTHR, 0, st>>>(P);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(RLK_ECUDA, "kernel launch: %s", cudaGetErrorString(e));
+  return RLK_OK;
+}
+
+}  // extern "C"

@@ -125,3 +125,83 @@ def test_kl_ref_validation(lib):
     assert lib.rlk_logp_kl_ref(ctypes.byref(a), None, OUT, OUT, None) == b.RLK_EINVAL
     assert lib.rlk_logp_kl_ref(ctypes.byref(a), OUT, OUT + 1, OUT, None) == b.RLK_EALIGN
     assert lib.rlk_logp_kl_ref(ctypes.byref(_args(T=0)), None, None, None, None) == b.RLK_OK
+
+
+# ------------------------------------------------------------ vocabulary-sharded entry points
+
+def _sargs(**kw):
+    a = b.ShardArgs()
+    a.logits = 0x10000
+    a.T = 4
+    a.row_stride = b.SHARD_WIDTH
+    a.shard = 3
+    a.target = 0x20000
+    a.temperature = None
+    a.temperature_scalar = 0.7
+    a.top_p = None
+    a.top_p_scalar = 0.95
+    a.top_k = None
+    a.top_k_scalar = -1
+    a.err_count = None
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=-1), b.RLK_EINVAL),
+    (dict(T=1 << 31), b.RLK_EINVAL),
+    (dict(shard=-1), b.RLK_EINVAL),
+    (dict(shard=8), b.RLK_EINVAL),
+    (dict(logits=None), b.RLK_EINVAL),
+    (dict(target=None), b.RLK_EINVAL),
+    (dict(row_stride=19064), b.RLK_EINVAL),
+    (dict(logits=0x10004), b.RLK_EALIGN),
+    (dict(row_stride=19076), b.RLK_EALIGN),
+    (dict(target=0x20001), b.RLK_EALIGN),
+    (dict(temperature_scalar=-1.0), b.RLK_EINVAL),
+    (dict(top_p_scalar=0.0), b.RLK_EINVAL),
+    (dict(top_k_scalar=0), b.RLK_EINVAL),
+    (dict(top_k=0x40002), b.RLK_EALIGN),
+    (dict(err_count=0x40002), b.RLK_EALIGN),
+])
+def test_shard_entry_points_reject_bad_arguments_on_host(lib, kw, status):
+    a = _sargs(**kw)
+    assert lib.rlk_logp_shard_summary(ctypes.byref(a), OUT, OUT, OUT, OUT, None) == status
+    assert lib.rlk_logp_shard_counts(ctypes.byref(a), OUT, OUT, OUT, OUT, None) == status
+    assert lib.rlk_last_error()
+
+
+def test_shard_outputs_checked(lib):
+    a = _sargs()
+    assert lib.rlk_logp_shard_summary(ctypes.byref(a), None, OUT, OUT, OUT, None) == b.RLK_EINVAL
+    assert lib.rlk_logp_shard_summary(ctypes.byref(a), OUT, OUT, OUT, OUT + 2, None) == b.RLK_EALIGN
+    assert lib.rlk_logp_shard_counts(ctypes.byref(a), OUT, OUT, OUT, None, None) == b.RLK_EINVAL
+    # the count rows are copied out as 16-byte vectors
+    assert lib.rlk_logp_shard_counts(ctypes.byref(a), OUT, OUT, OUT, OUT + 4, None) == b.RLK_EALIGN
+    assert lib.rlk_logp_shard_counts(ctypes.byref(a), None, OUT, OUT, OUT, None) == b.RLK_EINVAL
+    z = _sargs(T=0, logits=None, target=None)
+    assert lib.rlk_logp_shard_summary(ctypes.byref(z), None, None, None, None, None) == b.RLK_OK
+    assert lib.rlk_logp_shard_counts(ctypes.byref(z), None, None, None, None, None) == b.RLK_OK
+
+
+def _merge(lib, T=4, tau=0.7, p=0.95, k=-1, counts=OUT, nc=8, full=OUT, restr=OUT, sup=OUT,
+           maxes=OUT, target=OUT):
+    return lib.rlk_logp_merge(maxes, OUT, OUT, OUT, T, target, None, tau, None, p, None, k,
+                              counts, nc, full, restr, sup, None)
+
+
+def test_merge_validation(lib):
+    assert _merge(lib, T=-1) == b.RLK_EINVAL
+    assert _merge(lib, T=0, maxes=None, target=None, full=None) == b.RLK_OK
+    assert _merge(lib, maxes=None) == b.RLK_EINVAL
+    assert _merge(lib, target=OUT + 2) == b.RLK_EALIGN
+    assert _merge(lib, full=None) == b.RLK_EINVAL
+    assert _merge(lib, tau=float("nan")) == b.RLK_EINVAL
+    assert _merge(lib, nc=2) == b.RLK_EINVAL
+    assert _merge(lib, nc=0) == b.RLK_EINVAL
+    assert _merge(lib, p=1.5) == b.RLK_EINVAL
+    assert _merge(lib, k=151937) == b.RLK_EINVAL
+    assert _merge(lib, restr=None, sup=None) == b.RLK_EINVAL
+    assert _merge(lib, counts=OUT + 2) == b.RLK_EALIGN
+    assert _merge(lib, restr=OUT + 1) == b.RLK_EALIGN

@@ -315,7 +315,7 @@ def test_top_p_only_deep_nucleus():
 
 
 def test_wide_support_fallback_path():
-    """Supports reaching more than 2048 order keys below the maximum take the
+    """Supports reaching more than 1024 order keys below the maximum take the
     global-memory window path; still exact against the oracle."""
     rng = np.random.default_rng(77)
     T = 6
