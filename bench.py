@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sharded-steps", type=int, default=50,
+                    help="steps of the vocabulary-sharded form timed beside the fused pass (0: skip)")
     ap.add_argument("--rows", type=int, default=T_ROWS,
                     help="rows per GPU (default: the 8192-row workload; smaller only for profiling)")
     return ap.parse_args()
@@ -328,6 +330,55 @@ def run_ours(args, rank, world, local):
         e2e = {"value": throughput(world, T_ROWS, args.e2e_steps, et), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
+    # ---- the vocabulary-sharded form of the policy pair pass (8 shard buffers):
+    #      8 summary launches, 8 count launches, one merge
+    sharded = None
+    if args.sharded_steps > 0:
+        SW = pkg.SHARD_WIDTH
+        shards = [x[:, r * SW:(r + 1) * SW].contiguous() for r in range(8)]
+        maxes = torch.empty((8, T_ROWS), **f32)
+        sumexps = torch.empty_like(maxes)
+        aux = torch.empty((8, T_ROWS), dtype=torch.int32, device=dev)
+        xt = torch.empty(T_ROWS, **f32)
+        counts = torch.empty((8, T_ROWS, 1024), dtype=torch.int32, device=dev)
+        s_full, s_restr = torch.empty(T_ROWS, **f32), torch.empty(T_ROWS, **f32)
+        s_sup = torch.empty(T_ROWS, dtype=torch.int32, device=dev)
+
+        def sharded_step(evs=None):
+            if evs: evs[0].record(stream)
+            for r in range(8):
+                pkg.shard_summary(shards[r], r, tg, TAU, TOP_P, TOP_K, out_max=maxes[r],
+                                  out_sumexp=sumexps[r], out_aux=aux[r], out_target_logit=xt,
+                                  stream=stream)
+            if evs: evs[1].record(stream)
+            for r in range(8):
+                pkg.shard_counts(shards[r], r, tg, maxes, sumexps, aux, TAU, TOP_P, TOP_K,
+                                 out_counts=counts[r], stream=stream)
+            if evs: evs[2].record(stream)
+            pkg.logp_merge(maxes, sumexps, aux, xt, tg, TAU, TOP_P, TOP_K, counts=counts,
+                           out_full=s_full, out_restr=s_restr, out_support=s_sup, stream=stream)
+            if evs: evs[3].record(stream)
+
+        for _ in range(3):
+            sharded_step()
+        torch.cuda.synchronize()
+        Ks = args.sharded_steps
+        sev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(Ks)]
+        for i in range(Ks):
+            sharded_step(sev[i])
+        torch.cuda.synchronize()
+        phase = [statistics.mean(sev[i][j].elapsed_time(sev[i][j + 1]) for i in range(Ks))
+                 for j in range(3)]
+        tot = sum(phase)
+        same = bool(torch.equal(s_full.view(torch.int32), full.view(torch.int32)) and
+                    torch.equal(s_sup[s_sup != -2], sup[s_sup != -2]))
+        sharded = {"ms_per_step": tot, "tokens_per_s": T_ROWS / (tot / 1e3),
+                   "summary_ms": phase[0], "counts_ms": phase[1], "merge_ms": phase[2],
+                   "summary_gbs": T_ROWS * VPAD * 2 / (phase[0] / 1e3) / 1e9,
+                   "rows_outside_window": int((s_sup == -2).sum().item()),
+                   "bitwise_equal_to_fused": same, "gpu_launches_per_step": 17}
+        del shards, counts
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample_rows = np.arange(0, T_ROWS, 7)
@@ -362,6 +413,7 @@ def run_ours(args, rank, world, local):
             "gpu_launches": 2 * K,
             "clocks": clk.summary(),
             "e2e": e2e,
+            "sharded": sharded,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

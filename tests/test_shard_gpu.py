@@ -78,7 +78,10 @@ def compare(x, t, tau, p, k, err=None, err_sharded=None):
 def test_sharded_matches_fused_mixed_parameters():
     x, t, tau, p, k = mixed_rows(300, seed=21)
     s0, s1 = compare(x, t, tau, p, k)
-    assert (s1 == -2).sum() == 0, "hot rows keep their support inside the window"
+    # only deep supports (p = 0.9999, k = 3000: far more tokens than the largest
+    # hot set of 300) may reach below the window
+    wide = s1 == -2
+    assert wide.sum() <= len(s1) // 20 and (s0[wide] > 300).all(), s0[wide]
 
 
 def test_sharded_full_only_matches_logp_full():
@@ -118,12 +121,23 @@ def test_sharded_nonfinite_and_invalid_rows():
     assert not math.isnan(f[3].item()) and not math.isnan(f[5].item())
 
 
-def test_sharded_wide_supports_are_reported():
-    """Spread rows (N(0,3^2), tau 0.7, p 0.95): supports far below the maximum."""
+def test_sharded_spread_rows_and_wide_supports():
+    """Spread rows (N(0,3^2), tau 0.7, p 0.95) keep their nucleus inside the
+    window; rows centred on 0 with a small spread, whose nucleus crosses zero
+    (many binades below the maximum), are reported with support -2."""
     wl = W.workload_c0(device=DEV, T=32)
     t = W.structural_targets(32, None, None, seed=24, device=DEV)
     s0, s1 = compare(wl.logits, t, 0.7, 0.95, -1)
-    assert (s1 == -2).sum() > 0
+    assert (s1 != -2).all()
+    g = torch.Generator(device=DEV).manual_seed(24)
+    x = (0.02 * torch.randn((6, VP), generator=g, device=DEV)).to(torch.bfloat16)
+    x[:, 5] = 3.0
+    x[:, VR:] = float("-inf")
+    t = torch.full((6,), 5, dtype=torch.int32, device=DEV)
+    p = _t([0.9, 0.5, 0.99, 1.0, 0.7, 0.99], torch.float32)
+    k = _t([-1, -1, -1, 100000, 70000, 3000], torch.int32)
+    s0, s1 = compare(x, t, 1.0, p, k)
+    assert (s1 == -2).sum() >= 4
 
 
 def test_presummed_counts_and_stride():
