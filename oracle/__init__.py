@@ -6,9 +6,10 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 from .logp_oracle import (VPAD, VREAL, NSHARD, SHARD_W, InvalidArgument, RowResult,
                           bf16_bits_to_f32, validate, scaled_logits, logp_row,
                           row_logprobs_all, restr_for_support_size, logp_batch,
-                          shard_summaries, merge_summaries, top_k_mask, top_p_mask)
+                          shard_summaries, merge_summaries, top_k_mask, top_p_mask,
+                          logp_grad_row)
 
 __all__ = ["VPAD", "VREAL", "NSHARD", "SHARD_W", "InvalidArgument", "RowResult",
            "bf16_bits_to_f32", "validate", "scaled_logits", "logp_row", "row_logprobs_all",
            "restr_for_support_size", "logp_batch", "shard_summaries", "merge_summaries",
-           "top_k_mask", "top_p_mask"]
+           "top_k_mask", "top_p_mask", "logp_grad_row"]

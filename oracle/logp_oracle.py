@@ -256,6 +256,55 @@ def logp_batch(bits: np.ndarray, tau, top_p, top_k, target, rows=None):
     return full, restr, sup
 
 
+def logp_grad_row(bits_row: np.ndarray, tau: float, top_p: float, top_k: int, target: int,
+                  g_full: float, g_restr: float, vreal: int = VREAL, vpad: int = VPAD) -> np.ndarray:
+    """Gradient of g_full * full + g_restr * restr with respect to the BF16 logits, fp64.
+
+    The training side differentiates the same logprobs the rollout side
+    scores ("H100 canonical CP backward validation": gradients must come out
+    identical whatever the training topology).  With s_j = x_j / tau,
+    p = softmax(s) over the real vocabulary and q = softmax(s) over the
+    support S (zero outside it):
+
+      d full  / d x_j = (1[j == t] - p_j) / tau
+      d restr / d x_j = 1[j in S] (1[j == t] - q_j) / tau     if t in S
+
+    The support is locally constant, so no gradient flows through the
+    thresholds.  Readings for the cases the definition leaves open: when
+    t is not in S the restricted logprob is the constant -inf and contributes
+    nothing; temperature 0 (greedy) gives a piecewise-constant output and a
+    zero gradient; padded columns get 0; a row whose outputs are NaN gets NaN
+    on every real column.  Returns an array of ``vpad`` values.
+    """
+    validate(tau, top_p, top_k, target, vreal)
+    bits_row = np.asarray(bits_row, dtype=np.uint16)
+    grad = np.zeros(vpad)
+    x = bf16_bits_to_f32(bits_row[:vreal])
+    if np.any(np.isnan(x)) or np.any(np.isposinf(x)) or np.all(np.isneginf(x)):
+        grad[:vreal] = math.nan
+        return grad
+    if tau == 0.0:
+        return grad
+    s = scaled_logits(bits_row, tau, vreal)
+    m = float(np.max(s))
+    if not math.isfinite(m):
+        grad[:vreal] = math.nan
+        return grad
+    with np.errstate(under="ignore"):
+        w = np.exp(s - m)
+    onehot = np.zeros(vreal)
+    onehot[target] = 1.0
+    g = g_full * (onehot - w / math.fsum(w))
+    if g_restr != 0.0:
+        sk = top_k_mask(s, top_k)
+        S = top_p_mask(s, sk, top_p)[0] if top_p < 1.0 else sk
+        if S[target]:
+            q = np.where(S, w, 0.0) / math.fsum(w[S])
+            g = g + g_restr * (onehot - q)
+    grad[:vreal] = g / float(np.float32(tau))
+    return grad
+
+
 def shard_summaries(bits_row: np.ndarray, tau: float):
     """Per-virtual-shard (max, sum-exp) of the scaled logits, fp64.
 
