@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward-steps", type=int, default=50,
+                    help="launches of the backward pass timed beside the forward (0: skip)")
     ap.add_argument("--sharded-steps", type=int, default=50,
                     help="steps of the vocabulary-sharded form timed beside the fused pass (0: skip)")
     ap.add_argument("--rows", type=int, default=T_ROWS,
@@ -379,6 +381,46 @@ def run_ours(args, rank, world, local):
                    "bitwise_equal_to_fused": same, "gpu_launches_per_step": 17}
         del shards, counts
 
+    # ---- the backward pass (gradient of g_full * full + g_restr * restr, bf16
+    #      [T, 152576] written): the streaming pass from the record saved by the
+    #      forward, and the single pass that recomputes the forward
+    backward = None
+    if args.backward_steps > 0:
+        gen = torch.Generator(device=dev).manual_seed(rank_seed(7, rank))
+        g_full = torch.randn(T_ROWS, generator=gen, device=dev)
+        g_restr = torch.randn(T_ROWS, generator=gen, device=dev)
+        grad = torch.empty((T_ROWS, VPAD), dtype=torch.bfloat16, device=dev)
+        _, _, _, stats = pkg.logp_pair_save(x, tg, TAU, TOP_P, TOP_K)
+
+        def timed(fn, n):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+            evs[0].record(stream)
+            for i in range(n):
+                fn()
+                evs[i + 1].record(stream)
+            torch.cuda.synchronize()
+            return statistics.mean(evs[i].elapsed_time(evs[i + 1]) for i in range(n))
+
+        saved_ms = timed(lambda: pkg.logp_backward_saved(x, tg, stats, TAU, grad_full=g_full,
+                                                         grad_restr=g_restr, out=grad,
+                                                         stream=stream), args.backward_steps)
+        fused_ms = timed(lambda: pkg.logp_backward(x, tg, TAU, TOP_P, TOP_K, grad_full=g_full,
+                                                   grad_restr=g_restr, out=grad, stream=stream),
+                         args.backward_steps)
+        b_bytes = 2 * T_ROWS * VPAD * 2
+        peak_b, _ = measured_peak()
+        backward = {"kernel": "grad_kernel (streaming, from the saved per-row record)",
+                    "avg_launch_ms": saved_ms, "tokens_per_s": T_ROWS / (saved_ms / 1e3),
+                    "algorithmic_bytes_per_launch": b_bytes,
+                    "achieved_gbs": b_bytes / (saved_ms / 1e3) / 1e9,
+                    "frac": b_bytes / (saved_ms / 1e3) / 1e9 / peak_b,
+                    "single_pass_ms": fused_ms,
+                    "single_pass_frac": b_bytes / (fused_ms / 1e3) / 1e9 / peak_b}
+        del grad, stats
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample_rows = np.arange(0, T_ROWS, 7)
@@ -414,6 +456,7 @@ def run_ours(args, rank, world, local):
             "clocks": clk.summary(),
             "e2e": e2e,
             "sharded": sharded,
+            "backward": backward,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

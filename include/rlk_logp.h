@@ -101,6 +101,25 @@ typedef struct rlk_logp_args {
   int32_t* err_count;        /* optional device counter of rejected rows */
 } rlk_logp_args;
 
+/* Per-row record of a resolved row, written by rlk_logp_pair_save and read
+ * by rlk_logp_backward_saved (16 bytes, device memory, opaque to most
+ * callers):
+ *   max_logit      row maximum M of the real logits (a bf16 value);
+ *   inv_z          1 / sum_j exp((x_j - M) / tau) over the real vocabulary;
+ *                  NaN for a row whose outputs are NaN; 0 for greedy rows;
+ *   inv_z_support  1 / the same sum over the support S when the target is in
+ *                  S, else 0 (the restricted logprob is then -inf and has no
+ *                  gradient);
+ *   min_key        lowest bf16 order key in S (0 when S is the whole
+ *                  vocabulary).  The order key of a bf16 bit pattern b is
+ *                  b | 0x8000 for b >= 0 (and for -0), ~b & 0xFFFF for b < 0. */
+typedef struct rlk_row_stats {
+  float max_logit;
+  float inv_z;
+  float inv_z_support;
+  int32_t min_key;
+} rlk_row_stats;
+
 /* Full-vocabulary logprob of the target (the KL-reference side).
  * out_full: device float[T], required. */
 rlk_status rlk_logp_full(const rlk_logp_args* args, float* out_full, void* stream);
@@ -137,6 +156,57 @@ rlk_status rlk_logp_kl(const rlk_logp_args* policy, const void* ref_logits,
  * out_kl are required device float[T]. */
 rlk_status rlk_logp_kl_ref(const rlk_logp_args* ref, const float* full_policy,
                            float* out_full_ref, float* out_kl, void* stream);
+
+/* Backward: the gradient of  g_full[i] * full[i] + g_restr[i] * restr[i]
+ * with respect to the logits, in one pass that also recomputes the forward
+ * (the training side differentiates the very logprobs the rollout side
+ * scored; "H100 canonical CP backward validation" asks for gradients that are
+ * identical whatever the training topology, and this one is a function of
+ * the row alone).  With p the softmax of x / tau over the real vocabulary
+ * and q the softmax over the support S (0 outside it):
+ *   grad[i, j] = ( g_full (1[j == t] - p_j)
+ *                + g_restr 1[j in S] (1[j == t] - q_j) ) / tau
+ * The support is locally constant: no gradient flows through the
+ * thresholds.  The restricted term is 0 when t is not in S (restr is the
+ * constant -inf there).  Greedy rows (tau == 0) get a zero gradient; padded
+ * columns get 0; a row whose outputs are NaN (non-finite logits, rejected
+ * parameters, timeout) gets NaN on every real column.
+ *   grad_full, grad_restr: device float[T] upstream gradients; either may be
+ *     NULL (read as 0) but not both.
+ *   grad_logits: device [T, grad_row_stride] of grad_dtype, 16-byte aligned,
+ *     grad_row_stride >= 152576 with rows a multiple of 16 bytes apart; all
+ *     152576 columns of each row are written.  It may not overlap the logits.
+ *   out_full / out_restr / out_support: optional forward outputs (NULL to
+ *     skip).  top_p / top_k are used (and validated) when grad_restr,
+ *     out_restr or out_support is given; otherwise the pass is full-only.
+ * One launch on `stream`; reads the logits once and writes the gradient
+ * once. */
+typedef enum { RLK_GRAD_BF16 = 0, RLK_GRAD_F32 = 1 } rlk_grad_dtype;
+
+rlk_status rlk_logp_backward(const rlk_logp_args* args, const float* grad_full,
+                             const float* grad_restr, void* grad_logits, int64_t grad_row_stride,
+                             int32_t grad_dtype, float* out_full, float* out_restr,
+                             int32_t* out_support, void* stream);
+
+/* rlk_logp_pair plus the per-row record a later backward needs (the usual
+ * training order: the forward runs first, the backward later).  out_stats:
+ * device rlk_row_stats[T], 16-byte aligned, required; the other outputs as in
+ * rlk_logp_pair (at least one of out_full/out_restr). */
+rlk_status rlk_logp_pair_save(const rlk_logp_args* args, float* out_full, float* out_restr,
+                              int32_t* out_support, rlk_row_stats* out_stats, void* stream);
+
+/* The same gradient as rlk_logp_backward, bit for bit, from a saved record:
+ * a streaming pass that reads the logits once and writes the gradient once.
+ * args carries the logits, targets and temperatures of the saved forward
+ * (top_p/top_k are not read: the support is in the record).  stats: device
+ * rlk_row_stats[T] from rlk_logp_pair_save on the same logits and
+ * parameters, 16-byte aligned.  grad_full, grad_restr, grad_logits,
+ * grad_row_stride and grad_dtype as in rlk_logp_backward.  A row whose record
+ * is NaN (a rejected or non-finite row) gets NaN on every real column. */
+rlk_status rlk_logp_backward_saved(const rlk_logp_args* args, const rlk_row_stats* stats,
+                                   const float* grad_full, const float* grad_restr,
+                                   void* grad_logits, int64_t grad_row_stride, int32_t grad_dtype,
+                                   void* stream);
 
 /* ---------------------------------------------------------------------
  * Vocabulary-sharded form: the fixed virtual TP8 partition with each shard

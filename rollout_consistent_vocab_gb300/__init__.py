@@ -6,9 +6,12 @@ declared in ``include/rlk_logp.h``); this package is its thin Python binding.
 
 from ._binding import (VOCAB_PADDED, VOCAB_REAL, NUM_SHARDS, SHARD_WIDTH, RlkError, LogpArgs,
                        ShardArgs, EXPORTS, load_library, logp_full, logp_pair, logp_restricted,
-                       logp_kl, logp_kl_ref, shard_summary, shard_counts, logp_merge, logp_sharded)
+                       logp_kl, logp_kl_ref, logp_backward, logp_pair_save, logp_backward_saved,
+                       logp_autograd, shard_summary,
+                       shard_counts, logp_merge, logp_sharded)
 
 __all__ = ["VOCAB_PADDED", "VOCAB_REAL", "NUM_SHARDS", "SHARD_WIDTH", "RlkError", "LogpArgs",
            "ShardArgs",
            "EXPORTS", "load_library", "logp_full", "logp_pair", "logp_restricted", "logp_kl", "logp_kl_ref",
-           "shard_summary", "shard_counts", "logp_merge", "logp_sharded"]
+           "logp_backward", "logp_pair_save", "logp_backward_saved", "logp_autograd", "shard_summary", "shard_counts", "logp_merge",
+           "logp_sharded"]

@@ -63,7 +63,9 @@ class ShardArgs(ctypes.Structure):
 
 
 COMPUTE = ("rlk_logp_full", "rlk_logp_restricted", "rlk_logp_pair", "rlk_logp_kl", "rlk_logp_kl_ref",
+           "rlk_logp_backward", "rlk_logp_pair_save", "rlk_logp_backward_saved",
            "rlk_logp_shard_summary", "rlk_logp_shard_counts", "rlk_logp_merge")
+RLK_GRAD_BF16, RLK_GRAD_F32 = 0, 1
 EXPORTS = COMPUTE + ("rlk_status_string", "rlk_last_error", "rlk_abi_version")
 
 _lib = None
@@ -85,6 +87,9 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     lib.rlk_logp_pair.argtypes = [A, VP, VP, VP, VP]
     lib.rlk_logp_kl.argtypes = [A, VP, ctypes.c_int64, VP, VP, VP, VP, VP, VP]
     lib.rlk_logp_kl_ref.argtypes = [A, VP, VP, VP, VP]
+    lib.rlk_logp_backward.argtypes = [A, VP, VP, VP, ctypes.c_int64, ctypes.c_int32, VP, VP, VP, VP]
+    lib.rlk_logp_pair_save.argtypes = [A, VP, VP, VP, VP, VP]
+    lib.rlk_logp_backward_saved.argtypes = [A, VP, VP, VP, VP, ctypes.c_int64, ctypes.c_int32, VP]
     SA = P(ShardArgs)
     lib.rlk_logp_shard_summary.argtypes = [SA, VP, VP, VP, VP, VP]
     lib.rlk_logp_shard_counts.argtypes = [SA, VP, VP, VP, VP, VP]
@@ -328,3 +333,115 @@ def logp_sharded(shards, target, temperature=1.0, top_p=1.0, top_k=-1, *, restri
                          out_counts=counts[r], stream=stream)
     return logp_merge(maxes, sumexps, aux, xt, target, temperature, *pk, counts=counts,
                       stream=stream)
+
+
+# ------------------------------------------------------------ backward
+
+def logp_backward(logits, target, temperature=1.0, top_p=1.0, top_k=-1, *, grad_full=None,
+                  grad_restr=None, dtype=None, out=None, out_full=None, out_restr=None,
+                  out_support=None, err_count=None, stream=None):
+    """Gradient of grad_full * full + grad_restr * restr with respect to the
+    logits ([T, 152576], bf16 unless ``dtype`` is torch.float32), recomputing
+    the forward in the same pass (optional forward outputs)."""
+    lib = load_library()
+    torch = _torch()
+    a = make_args(logits, target, temperature, top_p, top_k, err_count)
+    for g, name in ((grad_full, "grad_full"), (grad_restr, "grad_restr")):
+        if g is not None and (g.dtype != torch.float32 or g.shape != (a.T,) or not g.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous float32 tensor of shape [T]")
+    if out is None:
+        dtype = torch.bfloat16 if dtype is None else dtype
+        out = torch.empty((a.T, VOCAB_PADDED), dtype=dtype, device=logits.device)
+    if out.dtype not in (torch.bfloat16, torch.float32) or out.dim() != 2 or out.stride(1) != 1:
+        raise ValueError("out must be a bf16 or float32 [T, >=152576] tensor with unit column stride")
+    gd = RLK_GRAD_F32 if out.dtype == torch.float32 else RLK_GRAD_BF16
+    check(lib.rlk_logp_backward(ctypes.byref(a), _ptr(grad_full), _ptr(grad_restr),
+                                out.data_ptr() if a.T else None,
+                                out.stride(0) if a.T else VOCAB_PADDED, gd, _ptr(out_full),
+                                _ptr(out_restr), _ptr(out_support), _stream(stream)))
+    return out
+
+
+def logp_pair_save(logits, target, temperature=1.0, top_p=1.0, top_k=-1, *, out_full=None,
+                   out_restr=None, out_support=None, out_stats=None, err_count=None, stream=None):
+    """logp_pair plus the per-row record for a later backward: returns
+    (full, restricted, support, stats), stats a float32 [T, 4] tensor holding
+    rlk_row_stats (column 3 is the int32 min_key, stored bitwise)."""
+    lib = load_library()
+    torch = _torch()
+    a = make_args(logits, target, temperature, top_p, top_k, err_count)
+    out_full = _empty(a.T, torch.float32, logits) if out_full is None else out_full
+    out_restr = _empty(a.T, torch.float32, logits) if out_restr is None else out_restr
+    out_support = _empty(a.T, torch.int32, logits) if out_support is None else out_support
+    if out_stats is None:
+        out_stats = torch.empty((a.T, 4), dtype=torch.float32, device=logits.device)
+    check(lib.rlk_logp_pair_save(ctypes.byref(a), _ptr(out_full), _ptr(out_restr), _ptr(out_support),
+                                 _ptr(out_stats), _stream(stream)))
+    return out_full, out_restr, out_support, out_stats
+
+
+def logp_backward_saved(logits, target, stats, temperature=1.0, *, grad_full=None, grad_restr=None,
+                        dtype=None, out=None, stream=None):
+    """The backward from a record saved by logp_pair_save (same logits, targets
+    and temperatures): a streaming pass, bit-identical to logp_backward."""
+    lib = load_library()
+    torch = _torch()
+    a = make_args(logits, target, temperature, 1.0, -1, None)
+    if stats.dtype != torch.float32 or stats.shape != (a.T, 4) or not stats.is_contiguous():
+        raise ValueError("stats must be the contiguous float32 [T, 4] record of logp_pair_save")
+    for g, name in ((grad_full, "grad_full"), (grad_restr, "grad_restr")):
+        if g is not None and (g.dtype != torch.float32 or g.shape != (a.T,) or not g.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous float32 tensor of shape [T]")
+    if out is None:
+        dtype = torch.bfloat16 if dtype is None else dtype
+        out = torch.empty((a.T, VOCAB_PADDED), dtype=dtype, device=logits.device)
+    if out.dtype not in (torch.bfloat16, torch.float32) or out.dim() != 2 or out.stride(1) != 1:
+        raise ValueError("out must be a bf16 or float32 [T, >=152576] tensor with unit column stride")
+    gd = RLK_GRAD_F32 if out.dtype == torch.float32 else RLK_GRAD_BF16
+    check(lib.rlk_logp_backward_saved(ctypes.byref(a), _ptr(stats), _ptr(grad_full), _ptr(grad_restr),
+                                      out.data_ptr() if a.T else None,
+                                      out.stride(0) if a.T else VOCAB_PADDED, gd, _stream(stream)))
+    return out
+
+
+def _autograd_function():
+    torch = _torch()
+
+    class _Logp(torch.autograd.Function):
+        """(full, restr) of each row's target, differentiable with respect to
+        the logits.  The forward saves a 16-byte record per row; the backward
+        is one streaming call of rlk_logp_backward_saved."""
+
+        @staticmethod
+        def forward(ctx, logits, target, temperature, top_p, top_k):
+            full, restr, _, stats = logp_pair_save(logits, target, temperature, top_p, top_k)
+            ctx.save_for_backward(logits, target, stats)
+            ctx.temperature = temperature
+            return full, restr
+
+        @staticmethod
+        def backward(ctx, g_full, g_restr):
+            logits, target, stats = ctx.saved_tensors
+            gf = None if g_full is None else g_full.float().contiguous()
+            gr = None if g_restr is None else g_restr.float().contiguous()
+            if gf is None and gr is None:
+                return None, None, None, None, None
+            grad = torch.empty_like(logits)
+            if logits.shape[1] > VOCAB_PADDED:
+                grad[:, VOCAB_PADDED:] = 0
+            logp_backward_saved(logits, target, stats, ctx.temperature, grad_full=gf,
+                                grad_restr=gr, out=grad)
+            return grad, None, None, None, None
+
+    return _Logp
+
+
+_LOGP_FN = None
+
+
+def logp_autograd(logits, target, temperature=1.0, top_p=1.0, top_k=-1):
+    """(full, restr) as differentiable torch outputs (see logp_backward)."""
+    global _LOGP_FN
+    if _LOGP_FN is None:
+        _LOGP_FN = _autograd_function()
+    return _LOGP_FN.apply(logits, target, temperature, top_p, top_k)

@@ -658,4 +658,117 @@ __device__ __forceinline__ bool select_warp(const uint32_t* cnt, int hi, int lo,
   return false;                                  // nucleus reaches below the window
 }
 
+// ------------------------------------------------------------ backward
+
+// The gradient of g_full * full + g_restr * restr at column j of a resolved
+// row is  -e_j * (key_j >= min_key ? a_in : a_out) + (j == t ? b : 0)  with
+// e_j = exp((x_j - M) / tau), a_out = g_full / (Z tau), a_in = a_out +
+// g_restr / (Z_S tau) and b = (g_full + g_restr) / tau, the restricted terms
+// dropped when the target is outside the support (inv_z_support == 0).
+// Products and sums are explicitly rounded (no contraction), so every kernel
+// that forms a gradient from the same record gets the same bits.
+enum : uint32_t { GRAD_VALUES = 0u, GRAD_ZERO = 1u, GRAD_NAN = 2u };
+struct GradCoeffs {
+  float M, c, a_in, a_out, b;
+  int min_key;
+  uint32_t mode;
+};
+
+__device__ __forceinline__ rlk_row_stats nan_stats() {
+  rlk_row_stats st;
+  st.max_logit = __int_as_float(0x7fc00000);
+  st.inv_z = __int_as_float(0x7fc00000);
+  st.inv_z_support = 0.0f;
+  st.min_key = 0;
+  return st;
+}
+
+__device__ __forceinline__ GradCoeffs nan_coeffs() {
+  GradCoeffs g{};
+  g.mode = GRAD_NAN;
+  return g;
+}
+
+__device__ __forceinline__ GradCoeffs grad_coeffs(const rlk_row_stats& st, float tau, float gf,
+                                                  float gr) {
+  GradCoeffs g{};
+  if (st.inv_z != st.inv_z) {
+    g.mode = GRAD_NAN;
+  } else if (tau == 0.0f) {
+    g.mode = GRAD_ZERO;               // greedy: the logprobs are piecewise constant
+  } else {
+    const float rt = __fdiv_rn(1.0f, tau);
+    const float grs = st.inv_z_support != 0.0f ? gr : 0.0f;
+    g.mode = GRAD_VALUES;
+    g.M = st.max_logit;
+    g.c = __fdiv_rn(LOG2E, tau);
+    g.a_out = __fmul_rn(__fmul_rn(gf, st.inv_z), rt);
+    g.a_in = __fadd_rn(g.a_out, __fmul_rn(__fmul_rn(grs, st.inv_z_support), rt));
+    g.b = __fmul_rn(__fadd_rn(gf, grs), rt);
+    g.min_key = st.min_key;
+  }
+  return g;
+}
+
+// Store 8 gradient values of chunk ch (columns 8ch .. 8ch+7 of the shard),
+// streaming (evict-first) stores.
+__device__ __forceinline__ void store_grad8(char* gshard, int ch, bool f32, const float (&g)[8]) {
+  if (f32) {
+    uint4* dst = reinterpret_cast<uint4*>(gshard + static_cast<int64_t>(ch) * 32);
+    __stcs(dst, make_uint4(__float_as_uint(g[0]), __float_as_uint(g[1]), __float_as_uint(g[2]),
+                           __float_as_uint(g[3])));
+    __stcs(dst + 1, make_uint4(__float_as_uint(g[4]), __float_as_uint(g[5]), __float_as_uint(g[6]),
+                               __float_as_uint(g[7])));
+  } else {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(g[2 * j], g[2 * j + 1]);
+      w[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    __stcs(reinterpret_cast<uint4*>(gshard + static_cast<int64_t>(ch) * 16),
+           make_uint4(w[0], w[1], w[2], w[3]));
+  }
+}
+
+// One shard of a gradient row: the shard's real columns from its logits
+// (shared memory, or global memory when src_global), zeros on the padded
+// columns of the last shard.  col0 is the shard's first vocabulary column.
+__device__ __forceinline__ void write_grad_shard(const uint4* src, bool src_global, int nchunks,
+                                                 int col0, int t, const GradCoeffs& m,
+                                                 char* gshard, bool f32) {
+  const uint64_t nxm2 = pack2(-m.M, -m.M);
+  const uint64_t c2 = pack2(m.c, m.c);
+  for (int ch = threadIdx.x; ch < SHARD_CHUNKS; ch += NTHR) {
+    float g[8];
+    if (ch >= nchunks || m.mode == GRAD_ZERO) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) g[j] = 0.0f;
+    } else if (m.mode == GRAD_NAN) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) g[j] = __int_as_float(0x7fc00000);
+    } else {
+      const uint4 v = src_global ? __ldg(src + ch) : src[ch];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint64_t a = mul2(add2(pack2(bf16_lo(w[j]), bf16_hi(w[j])), nxm2), c2);
+        float a0, a1;
+        unpack2(a, a0, a1);
+        const float k0 = okey(w[j] & 0xFFFFu) >= m.min_key ? m.a_in : m.a_out;
+        const float k1 = okey(w[j] >> 16) >= m.min_key ? m.a_in : m.a_out;
+        g[2 * j] = __fmul_rn(-ex2(a0), k0);
+        g[2 * j + 1] = __fmul_rn(-ex2(a1), k1);
+      }
+      const int lt = t - col0 - ch * 8;
+      if (lt >= 0 && lt < 8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (j == lt) g[j] = __fadd_rn(g[j], m.b);
+      }
+    }
+    store_grad8(gshard, ch, f32, g);
+  }
+}
+
 }  // namespace rlk

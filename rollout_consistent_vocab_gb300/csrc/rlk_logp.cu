@@ -83,7 +83,8 @@ struct __align__(128) Smem {
   int32_t win[4];
   float bc_f[4];
   int32_t sel_done;
-  unsigned long long bar_load, bar_mid, bar_sum, bar_hist;
+  alignas(16) rlk_row_stats bwd;   // backward: the leader's resolution of the row
+  unsigned long long bar_load, bar_mid, bar_sum, bar_hist, bar_bwd;
 };
 // five CTAs per SM: 5 * (sizeof + 1 KB reserved) <= 228 KB
 static_assert(sizeof(Smem) + 1024 <= 233472 / CTAS_PER_SM, "shared memory budget of 5 CTAs per SM");
@@ -103,6 +104,13 @@ struct KParams {
   const float* kl_policy_full;  // reference pass: out_kl = kl_policy_full - full
   float* out_kl;
   int32_t* err;
+  rlk_row_stats* out_stats;     // optional per-row record for a later backward
+  // backward
+  const float* g_full;          // upstream gradients (NULL: 0)
+  const float* g_restr;
+  char* grad;                   // [T, grad_stride] bf16 or f32
+  int64_t grad_stride;          // elements
+  int grad_f32;
 };
 
 // The 16-byte exchange message of this CTA (rank r) to CTA `to` (a local
@@ -119,7 +127,7 @@ __device__ __forceinline__ void send_mid(Smem& S, uint32_t r, int to, float xm, 
 
 // ------------------------------------------------------------ the kernel
 
-template <bool RESTR>
+template <bool RESTR, bool BWD>
 __global__ void __cluster_dims__(NSHARD, 1, 1) __launch_bounds__(NTHR, CTAS_PER_SM)
 logp_kernel(const KParams P) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -134,6 +142,10 @@ logp_kernel(const KParams P) {
   const uint32_t bar_mid = smem_addr(&S.bar_mid);
   const uint32_t bar_sum = smem_addr(&S.bar_sum);
   const uint32_t bar_hist = smem_addr(&S.bar_hist);
+  const uint32_t bar_bwd = smem_addr(&S.bar_bwd);
+  char* const gshard = BWD ? P.grad + (row * P.grad_stride + static_cast<int64_t>(r) * SW) *
+                                          (P.grad_f32 ? 4 : 2)
+                           : nullptr;
 
   // ---- 1. the bulk copy of the shard into shared memory goes out first
   if (tid == 0) {
@@ -165,9 +177,13 @@ logp_kernel(const KParams P) {
         if (RESTR && P.out_restr) P.out_restr[row] = __int_as_float(0x7fc00000);
         if (RESTR && P.out_support) P.out_support[row] = -1;
         if (P.out_kl) P.out_kl[row] = __int_as_float(0x7fc00000);
+        if (P.out_stats) P.out_stats[row] = nan_stats();
         if (P.err) atomicAdd(P.err, 1);
       }
     }
+    if (BWD)
+      write_grad_shard(nullptr, false, nchunks, static_cast<int>(r) * SW, -1, nan_coeffs(), gshard,
+                       P.grad_f32 != 0);
     return;
   }
   const bool greedy = (tau == 0.0f);
@@ -185,6 +201,10 @@ logp_kernel(const KParams P) {
     // messages from the 7 peers: 16 bytes each
     if (sel) mbar_arrive_expect_tx(bar_mid, (NSHARD - 1) * 16);
     if (r == 0) mbar_arrive_expect_tx(bar_sum, (NSHARD - 1) * 16);
+    if (BWD && r != 0) {
+      mbar_init(bar_bwd, 1);
+      mbar_arrive_expect_tx(bar_bwd, sizeof(rlk_row_stats));
+    }
     S.npush = 0u;
   }
   if (sel) {
@@ -358,7 +378,17 @@ logp_kernel(const KParams P) {
     if (r == 0) *reinterpret_cast<uint4*>(&S.slot[0]) = msg;
     else st_async_v4(map_rank(smem_addr(&S.slot[r]), 0), msg, map_rank(bar_sum, 0));
   }
-  if (r != 0) return;          // messages carry everything the leader needs
+  if (r != 0) {                // messages carry everything the leader needs
+    if (BWD) {
+      // the leader's resolution of the row, then this shard's gradient
+      const bool ok = mbar_wait_bounded(bar_bwd);
+      const GradCoeffs m = ok ? grad_coeffs(S.bwd, tau, P.g_full ? P.g_full[row] : 0.0f,
+                                            (RESTR && P.g_restr) ? P.g_restr[row] : 0.0f)
+                              : nan_coeffs();
+      write_grad_shard(sh, false, nchunks, static_cast<int>(r) * SW, t, m, gshard, P.grad_f32 != 0);
+    }
+    return;
+  }
 
   // ================= leader: merge in fixed shard order =================
   // One thread waits for the peers' messages; warp 0 merges and selects; the
@@ -376,7 +406,7 @@ logp_kernel(const KParams P) {
   }
   __syncthreads();
   const bool timed_out = S.win[3] != 0;
-  if (tid >= 32 && !sel) return;   // only warp 0 finishes rows without a support search
+  if (!BWD && tid >= 32 && !sel) return;   // only warp 0 finishes rows without a support search
   bool bad = timed_out;
   float M = -INFINITY;
   float full = __int_as_float(0x7fc00000), restr = full;
@@ -422,17 +452,21 @@ logp_kernel(const KParams P) {
       S.bc_f[1] = Z;
     }
   }
+  bool shard_reused = false;      // the leader's shard copy became scratch
+  bool in_s = true;               // target in the support (every token is when !sel)
+  float zs = Z;
   if (sel) {
     __syncthreads();
     if (!S.sel_done) {
       // wide support: the whole block scans further windows
       uint32_t* cntB = reinterpret_cast<uint32_t*>(S.shard);
       sr = select_support(S, S.merged, cntB, hi, lo, rowp, S.bc_f[0], c, S.bc_f[1], p, k, k_on, p_on);
+      shard_reused = true;
     }
-    if (tid != 0) return;
-    if (!bad) {
-      const bool in_s = okey_of(xt) >= sr.min_key;
-      const float zs = __ull2float_rn(sr.zs) * (1.0f / FX_SCALE);
+    if (!BWD && tid != 0) return;
+    if (tid == 0 && !bad) {
+      in_s = okey_of(xt) >= sr.min_key;
+      zs = __ull2float_rn(sr.zs) * (1.0f / FX_SCALE);
       restr = in_s ? d - logf(zs) : -INFINITY;
       support = static_cast<int>(sr.support);
     }
@@ -445,38 +479,36 @@ logp_kernel(const KParams P) {
     if (P.out_kl) P.out_kl[row] = P.kl_policy_full[row] - full;
     if (timed_out && P.err) atomicAdd(P.err, 1);
   }
+
+  if (BWD || P.out_stats) {
+    // the row's resolution as a per-row record: saved for a later backward,
+    // and sent to the 7 peers for this pass's gradient
+    if (tid == 0) {
+      rlk_row_stats st;
+      st.max_logit = M;
+      st.inv_z = bad ? __int_as_float(0x7fc00000) : (greedy ? 0.0f : __fdiv_rn(1.0f, Z));
+      st.inv_z_support = (bad || greedy || !in_s) ? 0.0f : __fdiv_rn(1.0f, zs);
+      st.min_key = sel ? sr.min_key : 0;
+      if (P.out_stats) P.out_stats[row] = st;
+      if (BWD) {
+        S.bwd = st;
+        const uint4 v = *reinterpret_cast<const uint4*>(&st);
+#pragma unroll
+        for (int q = 1; q < NSHARD; ++q)
+          st_async_v4(map_rank(smem_addr(&S.bwd), q), v, map_rank(bar_bwd, q));
+      }
+    }
+  }
+  if (BWD) {
+    __syncthreads();
+    const GradCoeffs m = grad_coeffs(S.bwd, tau, P.g_full ? P.g_full[row] : 0.0f,
+                                     (RESTR && P.g_restr) ? P.g_restr[row] : 0.0f);
+    write_grad_shard(shard_reused ? reinterpret_cast<const uint4*>(rowp) : sh, shard_reused, nchunks,
+                     0, t, m, gshard, P.grad_f32 != 0);
+  }
 }
 
 // ------------------------------------------------------------ host side
-
-rlk_status check_logits(const void* logits, int64_t T, int64_t stride, const char* what) {
-  if (!logits) return fail(RLK_EINVAL, "%s is NULL", what);
-  if (stride < VPAD) return fail(RLK_EINVAL, "%s row_stride %lld < %d", what, (long long)stride, VPAD);
-  if (!aligned(logits, 16)) return fail(RLK_EALIGN, "%s base is not 16-byte aligned", what);
-  if (stride % 8 != 0) return fail(RLK_EALIGN, "%s row_stride %lld is not a multiple of 8", what, (long long)stride);
-  (void)T;
-  return RLK_OK;
-}
-
-rlk_status check_args(const rlk_logp_args* a, bool restr) {
-  if (!a) return fail(RLK_EINVAL, "args is NULL");
-  if (a->T < 0) return fail(RLK_EINVAL, "T = %lld < 0", (long long)a->T);
-  if (a->T >= (int64_t(1) << 28)) return fail(RLK_EINVAL, "T = %lld: at most 2^28 - 1 rows per call", (long long)a->T);
-  if (a->vocab_real != VREAL || a->vocab_padded != VPAD)
-    return fail(RLK_EINVAL, "vocab sizes must be %d/%d, got %d/%d", VREAL, VPAD, a->vocab_real, a->vocab_padded);
-  if (a->T == 0) return RLK_OK;
-  rlk_status s = check_logits(a->logits, a->T, a->row_stride, "logits");
-  if (s != RLK_OK) return s;
-  if (!a->target) return fail(RLK_EINVAL, "target is NULL");
-  if (!aligned(a->target, 4)) return fail(RLK_EALIGN, "target is not 4-byte aligned");
-  if ((s = check_tau(a->temperature, a->temperature_scalar)) != RLK_OK) return s;
-  if (restr) {
-    if ((s = check_top_p(a->top_p, a->top_p_scalar)) != RLK_OK) return s;
-    if ((s = check_top_k(a->top_k, a->top_k_scalar)) != RLK_OK) return s;
-  }
-  if (a->err_count && !aligned(a->err_count, 4)) return fail(RLK_EALIGN, "err_count is not 4-byte aligned");
-  return RLK_OK;
-}
 
 KParams make_params(const rlk_logp_args* a) {
   KParams P;
@@ -494,22 +526,22 @@ KParams make_params(const rlk_logp_args* a) {
   return P;
 }
 
-template <bool RESTR>
+template <bool RESTR, bool BWD = false>
 rlk_status launch(const KParams& P, int64_t T, cudaStream_t stream) {
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(logp_kernel<RESTR>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    e = cudaFuncSetAttribute(logp_kernel<RESTR, BWD>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    e = cudaFuncSetAttribute(logp_kernel<RESTR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(logp_kernel<RESTR, BWD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sizeof(Smem)));
     if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     configured[dev] = true;
   }
   const dim3 grid(static_cast<unsigned>(T * NSHARD));
-  logp_kernel<RESTR><<<grid, NTHR, sizeof(Smem), stream>>>(P);
+  logp_kernel<RESTR, BWD><<<grid, NTHR, sizeof(Smem), stream>>>(P);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(RLK_ECUDA, "kernel launch: %s", cudaGetErrorString(e));
   return RLK_OK;
@@ -542,6 +574,24 @@ rlk_status rlk_logp_pair(const rlk_logp_args* args, float* out_full, float* out_
   P.out_full = out_full;
   P.out_restr = out_restr;
   P.out_support = out_support;
+  return launch<true>(P, args->T, static_cast<cudaStream_t>(stream));
+}
+
+rlk_status rlk_logp_pair_save(const rlk_logp_args* args, float* out_full, float* out_restr,
+                              int32_t* out_support, rlk_row_stats* out_stats, void* stream) {
+  rlk_status s = check_args(args, true);
+  if (s != RLK_OK || args->T == 0) return s;
+  if (!out_full && !out_restr) return fail(RLK_EINVAL, "out_full and out_restr are both NULL");
+  if ((s = check_out(out_full, "out_full", false)) != RLK_OK) return s;
+  if ((s = check_out(out_restr, "out_restr", false)) != RLK_OK) return s;
+  if ((s = check_out(out_support, "out_support", false)) != RLK_OK) return s;
+  if (!out_stats) return fail(RLK_EINVAL, "out_stats is NULL");
+  if (!aligned(out_stats, 16)) return fail(RLK_EALIGN, "out_stats is not 16-byte aligned");
+  KParams P = make_params(args);
+  P.out_full = out_full;
+  P.out_restr = out_restr;
+  P.out_support = out_support;
+  P.out_stats = out_stats;
   return launch<true>(P, args->T, static_cast<cudaStream_t>(stream));
 }
 
@@ -590,6 +640,31 @@ rlk_status rlk_logp_kl_ref(const rlk_logp_args* ref, const float* full_policy,
   R.kl_policy_full = full_policy;
   R.out_kl = out_kl;
   return launch<false>(R, ref->T, static_cast<cudaStream_t>(stream));
+}
+
+rlk_status rlk_logp_backward(const rlk_logp_args* args, const float* grad_full,
+                             const float* grad_restr, void* grad_logits, int64_t grad_row_stride,
+                             int32_t grad_dtype, float* out_full, float* out_restr,
+                             int32_t* out_support, void* stream) {
+  const bool restr = grad_restr || out_restr || out_support;
+  rlk_status s = check_args(args, restr);
+  if (s != RLK_OK || args->T == 0) return s;
+  if ((s = check_grad_args(grad_full, grad_restr, grad_logits, grad_row_stride, grad_dtype)) != RLK_OK)
+    return s;
+  if ((s = check_out(out_full, "out_full", false)) != RLK_OK) return s;
+  if ((s = check_out(out_restr, "out_restr", false)) != RLK_OK) return s;
+  if ((s = check_out(out_support, "out_support", false)) != RLK_OK) return s;
+  KParams P = make_params(args);
+  P.out_full = out_full;
+  P.out_restr = out_restr;
+  P.out_support = out_support;
+  P.g_full = grad_full;
+  P.g_restr = grad_restr;
+  P.grad = static_cast<char*>(grad_logits);
+  P.grad_stride = grad_row_stride;
+  P.grad_f32 = grad_dtype == RLK_GRAD_F32 ? 1 : 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return restr ? launch<true, true>(P, args->T, st) : launch<false, true>(P, args->T, st);
 }
 
 const char* rlk_status_string(rlk_status status) {

@@ -205,3 +205,47 @@ def test_merge_validation(lib):
     assert _merge(lib, restr=None, sup=None) == b.RLK_EINVAL
     assert _merge(lib, counts=OUT + 2) == b.RLK_EALIGN
     assert _merge(lib, restr=OUT + 1) == b.RLK_EALIGN
+
+
+# ------------------------------------------------------------ backward
+
+def _bwd(lib, a=None, gf=OUT, gr=None, grad=0x60000, stride=b.VOCAB_PADDED, dtype=0,
+         full=None, restr=None, sup=None):
+    a = _args() if a is None else a
+    return lib.rlk_logp_backward(ctypes.byref(a), gf, gr, grad, stride, dtype, full, restr, sup, None)
+
+
+def test_backward_validation(lib):
+    assert _bwd(lib, gf=None, gr=None) == b.RLK_EINVAL
+    assert _bwd(lib, grad=None) == b.RLK_EINVAL
+    assert _bwd(lib, grad=0x60008) == b.RLK_EALIGN
+    assert _bwd(lib, stride=b.VOCAB_PADDED - 8) == b.RLK_EINVAL
+    assert _bwd(lib, stride=b.VOCAB_PADDED + 4) == b.RLK_EALIGN          # bf16 rows 8 bytes apart
+    assert _bwd(lib, stride=b.VOCAB_PADDED + 2, dtype=1) == b.RLK_EALIGN   # f32 rows 8 bytes apart
+    assert _bwd(lib, dtype=2) == b.RLK_EINVAL
+    assert _bwd(lib, gf=OUT + 2) == b.RLK_EALIGN
+    assert _bwd(lib, full=OUT + 1) == b.RLK_EALIGN
+    # top_p / top_k are validated only when the restricted side is requested
+    bad_p = _args(top_p_scalar=3.0, T=0)
+    assert _bwd(lib, a=bad_p) == b.RLK_OK
+    assert _bwd(lib, a=_args(top_p_scalar=3.0), gr=OUT) == b.RLK_EINVAL
+    assert _bwd(lib, a=_args(top_k_scalar=0), restr=OUT) == b.RLK_EINVAL
+    assert _bwd(lib, a=_args(T=0, logits=None, target=None), gf=None, gr=None, grad=None) == b.RLK_OK
+
+
+def test_pair_save_and_backward_saved_validation(lib):
+    a = _args()
+    assert lib.rlk_logp_pair_save(ctypes.byref(a), OUT, OUT, OUT, None, None) == b.RLK_EINVAL
+    assert lib.rlk_logp_pair_save(ctypes.byref(a), OUT, OUT, OUT, 0x70008, None) == b.RLK_EALIGN
+    assert lib.rlk_logp_pair_save(ctypes.byref(a), None, None, OUT, 0x70000, None) == b.RLK_EINVAL
+    assert lib.rlk_logp_pair_save(ctypes.byref(_args(top_k_scalar=0)), OUT, OUT, OUT, 0x70000, None) == b.RLK_EINVAL
+    bs = lambda a=a, st=0x70000, gf=OUT, gr=None, grad=0x60000, stride=b.VOCAB_PADDED, dt=0: \
+        lib.rlk_logp_backward_saved(ctypes.byref(a), st, gf, gr, grad, stride, dt, None)
+    assert bs(st=None) == b.RLK_EINVAL
+    assert bs(st=0x70004) == b.RLK_EALIGN
+    assert bs(gf=None) == b.RLK_EINVAL
+    assert bs(grad=0x60002) == b.RLK_EALIGN
+    assert bs(dt=5) == b.RLK_EINVAL
+    # top_p / top_k are not read by the saved backward
+    assert bs(a=_args(top_p_scalar=9.0, T=0)) == b.RLK_OK
+    assert bs(a=_args(T=0, logits=None, target=None), st=None, gf=None, grad=None) == b.RLK_OK
