@@ -305,6 +305,90 @@ def logp_grad_row(bits_row: np.ndarray, tau: float, top_p: float, top_k: int, ta
     return grad
 
 
+# ----------------------------------------------------------------- sampling
+
+_PHILOX_M = (0xD2511F53, 0xCD9E8D57)   # round multipliers
+_PHILOX_W = (0x9E3779B9, 0xBB67AE85)   # key schedule increments
+_U32 = 0xFFFFFFFF
+
+
+def philox4x32_10(counter, key):
+    """Philox4x32 with 10 rounds, from its published definition (Salmon, Moraes,
+    Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011): each
+    round multiplies words 0 and 2 by the two constants, swaps and xors the
+    high halves with words 1 and 3 and the round key; the key is bumped by the
+    Weyl increments between rounds.  counter: 4 words, key: 2 words."""
+    c0, c1, c2, c3 = (int(v) & _U32 for v in counter)
+    k0, k1 = (int(v) & _U32 for v in key)
+    for rnd in range(10):
+        if rnd > 0:
+            k0 = (k0 + _PHILOX_W[0]) & _U32
+            k1 = (k1 + _PHILOX_W[1]) & _U32
+        p0 = _PHILOX_M[0] * c0
+        p1 = _PHILOX_M[1] * c2
+        c0, c1, c2, c3 = ((p1 >> 32) ^ c1 ^ k0) & _U32, p1 & _U32, ((p0 >> 32) ^ c3 ^ k1) & _U32, p0 & _U32
+    return c0, c1, c2, c3
+
+
+def philox_uniform_bits(seed: int, counter: int) -> int:
+    """The sampler's 32 random bits for one row: word 0 of Philox4x32-10 with
+    key (seed low, seed high) and counter (counter low, counter high, 0, 0)."""
+    seed, counter = int(seed), int(counter)
+    return philox4x32_10((counter & _U32, (counter >> 32) & _U32, 0, 0),
+                         (seed & _U32, (seed >> 32) & _U32))[0]
+
+
+@dataclass
+class SampleResult:
+    token: int               # sampled column (-1 for a NaN row)
+    restr: float             # restricted logprob of the sampled token
+    full: float              # full logprob of the sampled token
+    support: int
+    lo_edge: float = math.nan   # cumulative mass (relative to Z_S) before the token
+    hi_edge: float = math.nan   # and after it; the draw U lies in [lo_edge, hi_edge)
+    u: float = math.nan
+
+
+def sample_row(bits_row: np.ndarray, tau: float, top_p: float, top_k: int, u_bits: int,
+               vreal: int = VREAL) -> SampleResult:
+    """Draw one token from the restricted distribution of a row.
+
+    The rollout side samples from the temperature-scaled, top-k-then-top-p
+    distribution ("Configurable H100 consistency runs", sampling flags;
+    temperature 0 is greedy).  Reading: inverse-CDF sampling with the support
+    in ascending column order.  With U = u_bits / 2^32 and q the renormalised
+    distribution over S, the token is the smallest column a in S with
+    sum_{j in S, j <= a} q_j > U.  Greedy rows give the argmax (lowest index on
+    ties).  The logprobs returned are those of ``logp_row`` for target a.
+    """
+    validate(tau, top_p, top_k, 0, vreal)
+    bits_row = np.asarray(bits_row, dtype=np.uint16)
+    x = bf16_bits_to_f32(bits_row[:vreal])
+    if np.any(np.isnan(x)) or np.any(np.isposinf(x)) or np.all(np.isneginf(x)):
+        return SampleResult(-1, math.nan, math.nan, -1)
+    if tau == 0.0:
+        a = int(np.argmax(x))
+        return SampleResult(a, 0.0, 0.0, 1)
+    s = scaled_logits(bits_row, tau, vreal)
+    m = float(np.max(s))
+    if not math.isfinite(m):
+        return SampleResult(-1, math.nan, math.nan, -1)
+    with np.errstate(under="ignore"):
+        w = np.exp(s - m)
+    sk = top_k_mask(s, top_k)
+    S = top_p_mask(s, sk, top_p)[0] if top_p < 1.0 else sk
+    cols = np.nonzero(S)[0]
+    z_s = math.fsum(w[cols])
+    u = int(u_bits) / 2.0 ** 32
+    cum = np.cumsum(w[cols]) / z_s
+    pos = int(np.searchsorted(cum, u, side="right"))
+    pos = min(pos, len(cols) - 1)
+    a = int(cols[pos])
+    r = logp_row(bits_row, tau, top_p, top_k, a, vreal)
+    lo = float(cum[pos - 1]) if pos > 0 else 0.0
+    return SampleResult(a, r.restr, r.full, r.support, lo, float(cum[pos]), u)
+
+
 def shard_summaries(bits_row: np.ndarray, tau: float):
     """Per-virtual-shard (max, sum-exp) of the scaled logits, fp64.
 
