@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sampler-steps", type=int, default=50,
+                    help="launches of the sampler timed beside the forward (0: skip)")
     ap.add_argument("--backward-steps", type=int, default=50,
                     help="launches of the backward pass timed beside the forward (0: skip)")
     ap.add_argument("--sharded-steps", type=int, default=50,
@@ -421,6 +423,37 @@ def run_ours(args, rank, world, local):
                     "single_pass_frac": b_bytes / (fused_ms / 1e3) / 1e9 / peak_b}
         del grad, stats
 
+    # ---- the sampler (one token per row from the restricted distribution,
+    #      Philox words keyed by a per-row counter)
+    sampler = None
+    if args.sampler_steps > 0:
+        ctr = torch.arange(T_ROWS, device=dev, dtype=torch.int64) + rank * T_ROWS
+        tok = torch.empty(T_ROWS, dtype=torch.int32, device=dev)
+        s_restr, s_full = torch.empty(T_ROWS, **f32), torch.empty(T_ROWS, **f32)
+        s_sup = torch.empty(T_ROWS, dtype=torch.int32, device=dev)
+
+        def sample_step():
+            pkg.sample(x, TAU, TOP_P, TOP_K, seed=1234, counter=ctr, out_token=tok, out_restr=s_restr,
+                       out_full=s_full, out_support=s_sup, stream=stream)
+
+        for _ in range(3):
+            sample_step()
+        torch.cuda.synchronize()
+        Ks = args.sampler_steps
+        sev = [torch.cuda.Event(enable_timing=True) for _ in range(Ks + 1)]
+        sev[0].record(stream)
+        for i in range(Ks):
+            sample_step()
+            sev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        s_ms = statistics.mean(sev[i].elapsed_time(sev[i + 1]) for i in range(Ks))
+        peak_s, _ = measured_peak()
+        s_bytes = T_ROWS * VPAD * 2
+        sampler = {"kernel": "logp_kernel<true, sample>", "avg_launch_ms": s_ms,
+                   "tokens_per_s": T_ROWS / (s_ms / 1e3),
+                   "achieved_gbs": s_bytes / (s_ms / 1e3) / 1e9,
+                   "frac": s_bytes / (s_ms / 1e3) / 1e9 / peak_s}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample_rows = np.arange(0, T_ROWS, 7)
@@ -457,6 +490,7 @@ def run_ours(args, rank, world, local):
             "e2e": e2e,
             "sharded": sharded,
             "backward": backward,
+            "sampler": sampler,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

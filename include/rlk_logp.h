@@ -208,6 +208,36 @@ rlk_status rlk_logp_backward_saved(const rlk_logp_args* args, const rlk_row_stat
                                    void* grad_logits, int64_t grad_row_stride, int32_t grad_dtype,
                                    void* stream);
 
+/* Sampler: draw one token per row from the same restricted distribution the
+ * logprobs use (the rollout side; "Configurable H100 consistency runs",
+ * sampling flags: temperature 0 is greedy, top-k then top-p over the real
+ * vocabulary), so that the sampled token's restricted logprob is the one the
+ * training side later recomputes.  The draw is inverse-CDF sampling with the
+ * support in ascending column order: with U = u / 2^32 for a 32-bit random
+ * word u, the token is the smallest column a in S whose cumulative
+ * renormalised mass exceeds U (the masses are the exact fixed-point integers
+ * of the support selection, so the draw is a function of the row and u
+ * alone).  Greedy rows give the argmax (lowest column on ties).
+ *   args: logits and per-row temperature / top_p / top_k as for
+ *     rlk_logp_pair; args->target is not read (may be NULL).
+ *   u per row: uniform[i] if uniform is not NULL, else word 0 of
+ *     Philox4x32-10 (Salmon et al., SC 2011) with key (seed low, seed high)
+ *     and counter (counter[i] low, counter[i] high, 0, 0).  Give each
+ *     (request, position) its own counter and the draw does not depend on
+ *     the batch.  counter: device uint64[T], 8-byte aligned; uniform: device
+ *     uint32[T]; at least one of them.
+ *   out_token: device int32[T], required: the sampled column; -1 for a row
+ *     whose outputs are NaN (rejected parameters, non-finite logits).
+ *   out_restr / out_full: optional float[T]: the sampled token's restricted
+ *     and full logprobs, bit-identical to rlk_logp_pair with target = token.
+ *   out_support: optional int32[T], as in rlk_logp_pair.
+ * A row whose support reaches below the 1024-key window is resolved exactly
+ * (slower path), as in rlk_logp_pair.  One launch on `stream`. */
+rlk_status rlk_sample(const rlk_logp_args* args, unsigned long long seed,
+                      const unsigned long long* counter, const uint32_t* uniform,
+                      int32_t* out_token, float* out_restr, float* out_full,
+                      int32_t* out_support, void* stream);
+
 /* ---------------------------------------------------------------------
  * Vocabulary-sharded form: the fixed virtual TP8 partition with each shard
  * in its own buffer, as a tensor-parallel rank would hold it ("Reproduce and

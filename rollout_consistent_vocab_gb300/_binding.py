@@ -63,7 +63,7 @@ class ShardArgs(ctypes.Structure):
 
 
 COMPUTE = ("rlk_logp_full", "rlk_logp_restricted", "rlk_logp_pair", "rlk_logp_kl", "rlk_logp_kl_ref",
-           "rlk_logp_backward", "rlk_logp_pair_save", "rlk_logp_backward_saved",
+           "rlk_logp_backward", "rlk_logp_pair_save", "rlk_logp_backward_saved", "rlk_sample",
            "rlk_logp_shard_summary", "rlk_logp_shard_counts", "rlk_logp_merge")
 RLK_GRAD_BF16, RLK_GRAD_F32 = 0, 1
 EXPORTS = COMPUTE + ("rlk_status_string", "rlk_last_error", "rlk_abi_version")
@@ -89,6 +89,7 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     lib.rlk_logp_kl_ref.argtypes = [A, VP, VP, VP, VP]
     lib.rlk_logp_backward.argtypes = [A, VP, VP, VP, ctypes.c_int64, ctypes.c_int32, VP, VP, VP, VP]
     lib.rlk_logp_pair_save.argtypes = [A, VP, VP, VP, VP, VP]
+    lib.rlk_sample.argtypes = [A, ctypes.c_uint64, VP, VP, VP, VP, VP, VP, VP]
     lib.rlk_logp_backward_saved.argtypes = [A, VP, VP, VP, VP, ctypes.c_int64, ctypes.c_int32, VP]
     SA = P(ShardArgs)
     lib.rlk_logp_shard_summary.argtypes = [SA, VP, VP, VP, VP, VP]
@@ -140,13 +141,15 @@ def _param(v, T, dtype, name):
 
 
 def make_args(logits, target, temperature=1.0, top_p=1.0, top_k=-1, err_count=None) -> LogpArgs:
+    """target may be None only for the sampler (which has no target)."""
     torch = _torch()
     if logits.dtype != torch.bfloat16 or logits.dim() != 2 or logits.stride(1) != 1:
         raise ValueError("logits must be a bf16 [T, >=152576] tensor with unit column stride")
     if logits.shape[1] < VOCAB_PADDED:
         raise ValueError(f"logits must have at least {VOCAB_PADDED} columns")
     T = logits.shape[0]
-    if target.dtype != torch.int32 or target.shape != (T,) or not target.is_contiguous():
+    if target is not None and (target.dtype != torch.int32 or target.shape != (T,)
+                               or not target.is_contiguous()):
         raise ValueError("target must be a contiguous int32 tensor of shape [T]")
     a = LogpArgs()
     a.logits = logits.data_ptr() if T else None
@@ -154,7 +157,7 @@ def make_args(logits, target, temperature=1.0, top_p=1.0, top_k=-1, err_count=No
     a.row_stride = logits.stride(0) if T else VOCAB_PADDED
     a.vocab_real = VOCAB_REAL
     a.vocab_padded = VOCAB_PADDED
-    a.target = _ptr(target) if T else None
+    a.target = _ptr(target) if T and target is not None else None
     a.temperature, a.temperature_scalar = _param(temperature, T, torch.float32, "temperature")
     a.top_p, a.top_p_scalar = _param(top_p, T, torch.float32, "top_p")
     a.top_k, a.top_k_scalar = _param(top_k, T, torch.int32, "top_k")
@@ -445,3 +448,31 @@ def logp_autograd(logits, target, temperature=1.0, top_p=1.0, top_k=-1):
     if _LOGP_FN is None:
         _LOGP_FN = _autograd_function()
     return _LOGP_FN.apply(logits, target, temperature, top_p, top_k)
+
+
+# ------------------------------------------------------------ sampler
+
+def sample(logits, temperature=1.0, top_p=1.0, top_k=-1, *, seed=0, counter=None, uniform=None,
+           out_token=None, out_restr=None, out_full=None, out_support=None, err_count=None,
+           stream=None):
+    """Draw one token per row from the restricted distribution (inverse CDF in
+    column order).  Random words: ``uniform`` (uint32 bits in an int32 [T]
+    tensor) or Philox4x32-10 of ``seed`` over ``counter`` (int64 [T]).
+    Returns (token, restricted logprob, full logprob, support)."""
+    lib = load_library()
+    torch = _torch()
+    a = make_args(logits, None, temperature, top_p, top_k, err_count)
+    T = a.T
+    for v, name, dt in ((counter, "counter", torch.int64), (uniform, "uniform", torch.int32)):
+        if v is not None and (v.dtype != dt or v.shape != (T,) or not v.is_contiguous() or not v.is_cuda):
+            raise ValueError(f"{name} must be a contiguous {dt} CUDA tensor of shape [T]")
+    if counter is None and uniform is None:
+        raise ValueError("give counter (with seed) or uniform")
+    out_token = _empty(T, torch.int32, logits) if out_token is None else out_token
+    out_restr = _empty(T, torch.float32, logits) if out_restr is None else out_restr
+    out_full = _empty(T, torch.float32, logits) if out_full is None else out_full
+    out_support = _empty(T, torch.int32, logits) if out_support is None else out_support
+    check(lib.rlk_sample(ctypes.byref(a), int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(counter), _ptr(uniform),
+                         _ptr(out_token), _ptr(out_restr), _ptr(out_full), _ptr(out_support),
+                         _stream(stream)))
+    return out_token, out_restr, out_full, out_support

@@ -17,6 +17,9 @@
 #ifndef RLK_NTHR
 #define RLK_NTHR 128
 #endif
+#ifndef RLK_WAIT_HINT_NS
+#define RLK_WAIT_HINT_NS 20000   // suspend-time hint of a barrier test (ns)
+#endif
 
 namespace rlk {
 
@@ -115,7 +118,7 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       "{\n .reg .pred p;\n"
       " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok) : "r"(bar), "r"(parity), "r"(20000u) : "memory");
+      : "=r"(ok) : "r"(bar), "r"(parity), "r"(static_cast<uint32_t>(RLK_WAIT_HINT_NS)) : "memory");
   return ok != 0;
 }
 // Bounded wait on phase 0 of a barrier: gives up after TIMEOUT_NS of wall time.
@@ -769,6 +772,58 @@ __device__ __forceinline__ void write_grad_shard(const uint4* src, bool src_glob
     }
     store_grad8(gshard, ch, f32, g);
   }
+}
+
+// ------------------------------------------------------------ sampling
+
+// Word 0 of Philox4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, "Parallel
+// random numbers: as easy as 1, 2, 3", SC 2011): key (seed low, seed high),
+// counter (ctr low, ctr high, 0, 0).  Each round multiplies words 0 and 2 by
+// the round constants, xors the high halves with words 1 and 3 and the round
+// key, and the key steps by the Weyl increments between rounds.
+__device__ __forceinline__ uint32_t philox_word0(unsigned long long seed, unsigned long long ctr) {
+  uint32_t c0 = static_cast<uint32_t>(ctr), c1 = static_cast<uint32_t>(ctr >> 32), c2 = 0u, c3 = 0u;
+  uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+#pragma unroll
+  for (int rnd = 0; rnd < 10; ++rnd) {
+    if (rnd > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+    c0 = hi1 ^ c1 ^ k0;
+    c1 = lo1;
+    c2 = hi0 ^ c3 ^ k1;
+    c3 = lo0;
+  }
+  return c0;
+}
+
+// floor(u * z / 2^32) for a 32-bit draw u and a fixed-point mass z < 2^63.
+__device__ __forceinline__ unsigned long long scale_draw(uint32_t u, unsigned long long z) {
+  const unsigned long long lo = z * static_cast<unsigned long long>(u);
+  const unsigned long long hi = __umul64hi(z, static_cast<unsigned long long>(u));
+  return (hi << 32) | (lo >> 32);
+}
+
+// Fixed-point mass (2^-44 units, the selection's per-key values) of the
+// elements of one 16-byte chunk whose order key is >= min_key.
+__device__ __forceinline__ unsigned long long chunk_support_mass(uint4 v, int min_key, float M, float c) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  unsigned long long m = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t b = (w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
+    if (okey(b) >= min_key) m += qfx(__uint_as_float(b << 16), M, c);
+  }
+  return m;
+}
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
 }
 
 }  // namespace rlk

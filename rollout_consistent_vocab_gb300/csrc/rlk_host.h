@@ -60,7 +60,7 @@ inline rlk_status check_logits(const void* logits, int64_t T, int64_t stride, co
   return RLK_OK;
 }
 
-inline rlk_status check_args(const rlk_logp_args* a, bool restr) {
+inline rlk_status check_args(const rlk_logp_args* a, bool restr, bool need_target = true) {
   if (!a) return fail(RLK_EINVAL, "args is NULL");
   if (a->T < 0) return fail(RLK_EINVAL, "T = %lld < 0", (long long)a->T);
   if (a->T >= (int64_t(1) << 28)) return fail(RLK_EINVAL, "T = %lld: at most 2^28 - 1 rows per call", (long long)a->T);
@@ -69,8 +69,10 @@ inline rlk_status check_args(const rlk_logp_args* a, bool restr) {
   if (a->T == 0) return RLK_OK;
   rlk_status s = check_logits(a->logits, a->T, a->row_stride, "logits");
   if (s != RLK_OK) return s;
-  if (!a->target) return fail(RLK_EINVAL, "target is NULL");
-  if (!aligned(a->target, 4)) return fail(RLK_EALIGN, "target is not 4-byte aligned");
+  if (need_target) {
+    if (!a->target) return fail(RLK_EINVAL, "target is NULL");
+    if (!aligned(a->target, 4)) return fail(RLK_EALIGN, "target is not 4-byte aligned");
+  }
   if ((s = check_tau(a->temperature, a->temperature_scalar)) != RLK_OK) return s;
   if (restr) {
     if ((s = check_top_p(a->top_p, a->top_p_scalar)) != RLK_OK) return s;

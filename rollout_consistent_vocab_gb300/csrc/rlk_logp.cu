@@ -83,8 +83,11 @@ struct __align__(128) Smem {
   int32_t win[4];
   float bc_f[4];
   int32_t sel_done;
-  alignas(16) rlk_row_stats bwd;   // backward: the leader's resolution of the row
-  unsigned long long bar_load, bar_mid, bar_sum, bar_hist, bar_bwd;
+  alignas(16) uint4 lead;          // backward / sampler: the leader's resolution of the row
+  uint4 zr[NSHARD];                 // sampler: every shard's fixed-point support mass
+  unsigned long long samp_res;      // sampler: residual draw inside the owning row of chunks
+  int32_t samp_i;
+  unsigned long long bar_load, bar_mid, bar_sum, bar_hist, bar_lead, bar_zr;
 };
 // five CTAs per SM: 5 * (sizeof + 1 KB reserved) <= 228 KB
 static_assert(sizeof(Smem) + 1024 <= 233472 / CTAS_PER_SM, "shared memory budget of 5 CTAs per SM");
@@ -111,6 +114,21 @@ struct KParams {
   char* grad;                   // [T, grad_stride] bf16 or f32
   int64_t grad_stride;          // elements
   int grad_f32;
+  // sampler
+  const uint32_t* uniform;      // per-row random words, or NULL for Philox
+  const unsigned long long* counter;
+  unsigned long long seed;
+  int32_t* out_token;
+};
+
+enum { MODE_FWD = 0, MODE_BWD = 1, MODE_SAMPLE = 2 };
+
+// Sampler message from the leader (16 bytes).
+enum : uint32_t { SAMP_DRAW = 1u, SAMP_SEL = 2u };
+struct __align__(16) SampMsg {
+  float M, Z;
+  int32_t min_key;
+  uint32_t flags;                  // SAMP_DRAW: the row draws (not greedy / NaN); SAMP_SEL: filtered
 };
 
 // The 16-byte exchange message of this CTA (rank r) to CTA `to` (a local
@@ -127,9 +145,138 @@ __device__ __forceinline__ void send_mid(Smem& S, uint32_t r, int to, float xm, 
 
 // ------------------------------------------------------------ the kernel
 
-template <bool RESTR, bool BWD>
+// The sampler's draw after every shard knows its own support mass: each CTA
+// sends its mass to the 7 others; the shard holding the drawn mass scans its
+// chunks in column order and writes the token and its logprobs.  src is the
+// shard's logits (shared memory, or global memory when src_global); cm are
+// the chunk maxima of the max pass.
+template <class SM>
+__device__ __forceinline__ void sample_shard(SM& S, const KParams& P, int64_t row, uint32_t r,
+                                             const uint4* src, bool src_global, int nchunks,
+                                             const __nv_bfloat162 (&cm)[MAXCH], const SampMsg& m,
+                                             float tau, uint32_t bar_zr) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float c = __fdiv_rn(LOG2E, tau);
+  // keys at or below -inf's are the whole vocabulary (min_key 0 when unfiltered;
+  // key_value of keys below -inf's would be a NaN pattern)
+  const float vmin_f = m.min_key <= KEY_NEG_INF ? -INFINITY : key_value(m.min_key);
+  const __nv_bfloat162 vmin2 = __floats2bfloat162_rn(vmin_f, vmin_f);
+  // ---- this shard's support mass
+  unsigned long long acc = 0;
+#pragma unroll
+  for (int i = 0; i < MAXCH; ++i) {
+    const int ch = tid + i * NTHR;
+    if (ch < nchunks && __hge2_mask(cm[i], vmin2) != 0u)
+      acc += chunk_support_mass(src_global ? __ldg(src + ch) : src[ch], m.min_key, m.M, c);
+  }
+  acc = warp_sum_u64(acc);
+  unsigned long long* wsum = reinterpret_cast<unsigned long long*>(S.hist);   // free by now
+  if (lane == 0) wsum[warp] = acc;
+  __syncthreads();
+  if (tid == 0) {
+    unsigned long long zr = 0;
+#pragma unroll
+    for (int w = 0; w < NWARP; ++w) zr += wsum[w];
+    const uint4 v = make_uint4(static_cast<uint32_t>(zr), static_cast<uint32_t>(zr >> 32), 0u, 0u);
+    S.zr[r] = v;
+#pragma unroll
+    for (int q = 0; q < NSHARD; ++q)
+      if (q != static_cast<int>(r)) st_async_v4(map_rank(smem_addr(&S.zr[r]), q), v, map_rank(bar_zr, q));
+    // one thread waits for the 7 peers' masses; the block barrier publishes them
+    S.samp_i = mbar_wait_bounded(bar_zr) ? 1 : 0;
+  }
+  __syncthreads();
+  // ---- the drawn mass, and the shard that holds it
+  const bool ok = S.samp_i != 0;
+  unsigned long long zs = 0, before = 0, mine = 0;
+#pragma unroll
+  for (int q = 0; q < NSHARD; ++q) {
+    const unsigned long long zq = (static_cast<unsigned long long>(S.zr[q].y) << 32) | S.zr[q].x;
+    if (q < static_cast<int>(r)) before += zq;
+    if (q == static_cast<int>(r)) mine = zq;
+    zs += zq;
+  }
+  if (!ok) {
+    if (tid == 0) {
+      P.out_token[row] = -1;
+      if (P.err) atomicAdd(P.err, 1);
+    }
+    return;
+  }
+  const uint32_t u = P.uniform ? P.uniform[row] : philox_word0(P.seed, P.counter[row]);
+  const unsigned long long draw = scale_draw(u, zs);
+  if (draw < before || draw - before >= mine) return;      // another shard holds it
+  const unsigned long long rr = draw - before;
+  // ---- per row of chunks (chunk index = i * NTHR + tid), then within the row
+  __syncthreads();                  // every thread has read S.samp_i
+#pragma unroll
+  for (int i = 0; i < MAXCH; ++i) {
+    const int ch = tid + i * NTHR;
+    unsigned long long mi = 0;
+    if (ch < nchunks && __hge2_mask(cm[i], vmin2) != 0u)
+      mi = chunk_support_mass(src_global ? __ldg(src + ch) : src[ch], m.min_key, m.M, c);
+    mi = warp_sum_u64(mi);
+    if (lane == 0) wsum[NWARP + i * NWARP + warp] = mi;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    unsigned long long cum = 0;
+    int istar = MAXCH - 1;
+    unsigned long long res = 0;
+    for (int i = 0; i < MAXCH; ++i) {
+      unsigned long long tot = 0;
+      for (int w = 0; w < NWARP; ++w) tot += wsum[NWARP + i * NWARP + w];
+      if (rr - cum < tot) { istar = i; res = rr - cum; break; }
+      cum += tot;
+    }
+    S.samp_i = istar;
+    S.samp_res = res;
+  }
+  __syncthreads();
+  const int istar = S.samp_i;
+  const unsigned long long res = S.samp_res;
+  const int ch = tid + istar * NTHR;
+  unsigned long long mt = 0;
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if (ch < nchunks) {
+    v = src_global ? __ldg(src + ch) : src[ch];
+    mt = chunk_support_mass(v, m.min_key, m.M, c);
+  }
+  unsigned long long excl = warp_incl_scan_u64(mt) - mt;
+  for (int w = 0; w < warp; ++w) excl += wsum[NWARP + istar * NWARP + w];
+  if (mt == 0 || res < excl || res - excl >= mt) return;
+  // this thread's chunk holds the draw: walk its 8 columns in order
+  unsigned long long left = res - excl;
+  const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+  int jstar = -1;
+  uint32_t bits = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t b = (w4[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
+    if (jstar < 0 && okey(b) >= m.min_key) {
+      const unsigned long long q = qfx(__uint_as_float(b << 16), m.M, c);
+      if (left < q) {
+        jstar = j;
+        bits = b;
+      } else {
+        left -= q;
+      }
+    }
+  }
+  const float xa = __uint_as_float(bits << 16);
+  const float d = __fdiv_rn(xa - m.M, tau);
+  const float full = d - logf(m.Z);
+  const float restr = (m.flags & SAMP_SEL) ? d - logf(__ull2float_rn(zs) * (1.0f / FX_SCALE)) : full;
+  P.out_token[row] = static_cast<int32_t>(r) * SW + ch * 8 + jstar;
+  if (P.out_full) P.out_full[row] = full;
+  if (P.out_restr) P.out_restr[row] = restr;
+}
+
+template <bool RESTR, int MODE>
 __global__ void __cluster_dims__(NSHARD, 1, 1) __launch_bounds__(NTHR, CTAS_PER_SM)
 logp_kernel(const KParams P) {
+  constexpr bool BWD = MODE == MODE_BWD;
+  constexpr bool SAMPLE = MODE == MODE_SAMPLE;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
@@ -142,7 +289,8 @@ logp_kernel(const KParams P) {
   const uint32_t bar_mid = smem_addr(&S.bar_mid);
   const uint32_t bar_sum = smem_addr(&S.bar_sum);
   const uint32_t bar_hist = smem_addr(&S.bar_hist);
-  const uint32_t bar_bwd = smem_addr(&S.bar_bwd);
+  const uint32_t bar_lead = smem_addr(&S.bar_lead);
+  const uint32_t bar_zr = smem_addr(&S.bar_zr);
   char* const gshard = BWD ? P.grad + (row * P.grad_stride + static_cast<int64_t>(r) * SW) *
                                           (P.grad_f32 ? 4 : 2)
                            : nullptr;
@@ -165,7 +313,7 @@ logp_kernel(const KParams P) {
   const float tau = P.tau_arr ? P.tau_arr[row] : P.tau_s;
   const float p = RESTR ? (P.p_arr ? P.p_arr[row] : P.p_s) : 1.0f;
   const int k = RESTR ? (P.k_arr ? P.k_arr[row] : P.k_s) : -1;
-  const int t = P.target[row];
+  const int t = SAMPLE ? 0 : P.target[row];     // the sampler has no target
   const bool valid = (tau >= 0.0f) && (tau <= 3.402823466e38f) && (p > 0.0f) && (p <= 1.0f) &&
                      (k == -1 || (k >= 1 && k <= VREAL)) && (t >= 0) && (t < VREAL);
   if (!valid) {
@@ -178,6 +326,7 @@ logp_kernel(const KParams P) {
         if (RESTR && P.out_support) P.out_support[row] = -1;
         if (P.out_kl) P.out_kl[row] = __int_as_float(0x7fc00000);
         if (P.out_stats) P.out_stats[row] = nan_stats();
+        if (SAMPLE) P.out_token[row] = -1;
         if (P.err) atomicAdd(P.err, 1);
       }
     }
@@ -191,7 +340,7 @@ logp_kernel(const KParams P) {
   const bool p_on = (p < 1.0f);
   const bool sel = RESTR && !greedy && (k_on || p_on);
   // the leader needs the target's logit at the end: start the load now
-  const float xt = (r == 0) ? __uint_as_float(static_cast<uint32_t>(__ldg(rowp + t)) << 16) : 0.0f;
+  const float xt = (r == 0 && !SAMPLE) ? __uint_as_float(static_cast<uint32_t>(__ldg(rowp + t)) << 16) : 0.0f;
 
   // ---- barriers that peers signal, and the leader's histogram
   if (tid == 0) {
@@ -201,9 +350,13 @@ logp_kernel(const KParams P) {
     // messages from the 7 peers: 16 bytes each
     if (sel) mbar_arrive_expect_tx(bar_mid, (NSHARD - 1) * 16);
     if (r == 0) mbar_arrive_expect_tx(bar_sum, (NSHARD - 1) * 16);
-    if (BWD && r != 0) {
-      mbar_init(bar_bwd, 1);
-      mbar_arrive_expect_tx(bar_bwd, sizeof(rlk_row_stats));
+    if ((BWD || SAMPLE) && r != 0) {
+      mbar_init(bar_lead, 1);
+      mbar_arrive_expect_tx(bar_lead, 16);
+    }
+    if (SAMPLE) {
+      mbar_init(bar_zr, 1);
+      mbar_arrive_expect_tx(bar_zr, (NSHARD - 1) * 16);
     }
     S.npush = 0u;
   }
@@ -379,10 +532,25 @@ logp_kernel(const KParams P) {
     else st_async_v4(map_rank(smem_addr(&S.slot[r]), 0), msg, map_rank(bar_sum, 0));
   }
   if (r != 0) {                // messages carry everything the leader needs
+    if (SAMPLE) {
+      // the leader's resolution of the row, then this shard's part of the draw
+      if (tid == 0) S.win[3] = mbar_wait_bounded(bar_lead) ? 1 : 0;
+      __syncthreads();
+      if (!S.win[3]) {
+        if (tid == 0) {
+          P.out_token[row] = -1;
+          if (P.err) atomicAdd(P.err, 1);
+        }
+        return;
+      }
+      const SampMsg m = *reinterpret_cast<const SampMsg*>(&S.lead);
+      if (m.flags & SAMP_DRAW) sample_shard(S, P, row, r, sh, false, nchunks, cm, m, tau, bar_zr);
+    }
     if (BWD) {
       // the leader's resolution of the row, then this shard's gradient
-      const bool ok = mbar_wait_bounded(bar_bwd);
-      const GradCoeffs m = ok ? grad_coeffs(S.bwd, tau, P.g_full ? P.g_full[row] : 0.0f,
+      const bool ok = mbar_wait_bounded(bar_lead);
+      const GradCoeffs m = ok ? grad_coeffs(*reinterpret_cast<const rlk_row_stats*>(&S.lead), tau,
+                                            P.g_full ? P.g_full[row] : 0.0f,
                                             (RESTR && P.g_restr) ? P.g_restr[row] : 0.0f)
                               : nan_coeffs();
       write_grad_shard(sh, false, nchunks, static_cast<int>(r) * SW, t, m, gshard, P.grad_f32 != 0);
@@ -406,12 +574,13 @@ logp_kernel(const KParams P) {
   }
   __syncthreads();
   const bool timed_out = S.win[3] != 0;
-  if (!BWD && tid >= 32 && !sel) return;   // only warp 0 finishes rows without a support search
+  if (!BWD && !SAMPLE && tid >= 32 && !sel) return;   // only warp 0 finishes rows without a support search
   bool bad = timed_out;
   float M = -INFINITY;
   float full = __int_as_float(0x7fc00000), restr = full;
   int support = -1;
   float Z = 0.0f, d = 0.0f;
+  uint32_t amax = 0x7fffffffu;    // greedy rows: first column holding the maximum
   const float c = greedy ? 0.0f : __fdiv_rn(LOG2E, tau);
   bool done = true;
   SelResult sr{0u, 0ull, 0};
@@ -424,7 +593,6 @@ logp_kernel(const KParams P) {
     }
     bad |= !(M > -INFINITY);
     if (!bad && greedy) {
-      uint32_t amax = 0x7fffffffu;
 #pragma unroll
       for (int q = NSHARD - 1; q >= 0; --q)
         if (S.slot[q].xm == M) amax = S.slot[q].aux;
@@ -463,7 +631,7 @@ logp_kernel(const KParams P) {
       sr = select_support(S, S.merged, cntB, hi, lo, rowp, S.bc_f[0], c, S.bc_f[1], p, k, k_on, p_on);
       shard_reused = true;
     }
-    if (!BWD && tid != 0) return;
+    if (!BWD && !SAMPLE && tid != 0) return;
     if (tid == 0 && !bad) {
       in_s = okey_of(xt) >= sr.min_key;
       zs = __ull2float_rn(sr.zs) * (1.0f / FX_SCALE);
@@ -472,7 +640,7 @@ logp_kernel(const KParams P) {
     }
   }
 
-  if (tid == 0) {
+  if (tid == 0 && !SAMPLE) {
     if (P.out_full) P.out_full[row] = full;
     if (RESTR && P.out_restr) P.out_restr[row] = restr;
     if (RESTR && P.out_support) P.out_support[row] = support;
@@ -491,20 +659,54 @@ logp_kernel(const KParams P) {
       st.min_key = sel ? sr.min_key : 0;
       if (P.out_stats) P.out_stats[row] = st;
       if (BWD) {
-        S.bwd = st;
         const uint4 v = *reinterpret_cast<const uint4*>(&st);
+        S.lead = v;
 #pragma unroll
         for (int q = 1; q < NSHARD; ++q)
-          st_async_v4(map_rank(smem_addr(&S.bwd), q), v, map_rank(bar_bwd, q));
+          st_async_v4(map_rank(smem_addr(&S.lead), q), v, map_rank(bar_lead, q));
       }
     }
   }
   if (BWD) {
     __syncthreads();
-    const GradCoeffs m = grad_coeffs(S.bwd, tau, P.g_full ? P.g_full[row] : 0.0f,
+    const GradCoeffs m = grad_coeffs(*reinterpret_cast<const rlk_row_stats*>(&S.lead), tau,
+                                     P.g_full ? P.g_full[row] : 0.0f,
                                      (RESTR && P.g_restr) ? P.g_restr[row] : 0.0f);
     write_grad_shard(shard_reused ? reinterpret_cast<const uint4*>(rowp) : sh, shard_reused, nchunks,
                      0, t, m, gshard, P.grad_f32 != 0);
+  }
+
+  if (SAMPLE) {
+    // the draw: tell the peers the row's resolution, write what the leader
+    // alone knows, then take part in the draw as shard 0
+    if (tid == 0) {
+      SampMsg m{};
+      m.M = M;
+      m.Z = Z;
+      m.min_key = sel ? sr.min_key : 0;
+      m.flags = (!bad && !greedy ? SAMP_DRAW : 0u) | (sel ? SAMP_SEL : 0u);
+      const uint4 v = *reinterpret_cast<const uint4*>(&m);
+      S.lead = v;
+#pragma unroll
+      for (int q = 1; q < NSHARD; ++q)
+        st_async_v4(map_rank(smem_addr(&S.lead), q), v, map_rank(bar_lead, q));
+      if (P.out_support) P.out_support[row] = support;
+      if (bad) {
+        P.out_token[row] = -1;
+        if (P.out_full) P.out_full[row] = __int_as_float(0x7fc00000);
+        if (P.out_restr) P.out_restr[row] = __int_as_float(0x7fc00000);
+      } else if (greedy) {
+        P.out_token[row] = static_cast<int32_t>(amax);
+        if (P.out_full) P.out_full[row] = 0.0f;
+        if (P.out_restr) P.out_restr[row] = 0.0f;
+      }
+      if (timed_out && P.err) atomicAdd(P.err, 1);
+    }
+    __syncthreads();
+    const SampMsg m = *reinterpret_cast<const SampMsg*>(&S.lead);
+    if (m.flags & SAMP_DRAW)
+      sample_shard(S, P, row, 0, shard_reused ? reinterpret_cast<const uint4*>(rowp) : sh, shard_reused,
+                   nchunks, cm, m, tau, bar_zr);
   }
 }
 
@@ -526,22 +728,22 @@ KParams make_params(const rlk_logp_args* a) {
   return P;
 }
 
-template <bool RESTR, bool BWD = false>
+template <bool RESTR, int MODE = MODE_FWD>
 rlk_status launch(const KParams& P, int64_t T, cudaStream_t stream) {
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(logp_kernel<RESTR, BWD>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    e = cudaFuncSetAttribute(logp_kernel<RESTR, MODE>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    e = cudaFuncSetAttribute(logp_kernel<RESTR, BWD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(logp_kernel<RESTR, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sizeof(Smem)));
     if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     configured[dev] = true;
   }
   const dim3 grid(static_cast<unsigned>(T * NSHARD));
-  logp_kernel<RESTR, BWD><<<grid, NTHR, sizeof(Smem), stream>>>(P);
+  logp_kernel<RESTR, MODE><<<grid, NTHR, sizeof(Smem), stream>>>(P);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(RLK_ECUDA, "kernel launch: %s", cudaGetErrorString(e));
   return RLK_OK;
@@ -664,7 +866,32 @@ rlk_status rlk_logp_backward(const rlk_logp_args* args, const float* grad_full,
   P.grad_stride = grad_row_stride;
   P.grad_f32 = grad_dtype == RLK_GRAD_F32 ? 1 : 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return restr ? launch<true, true>(P, args->T, st) : launch<false, true>(P, args->T, st);
+  return restr ? launch<true, MODE_BWD>(P, args->T, st) : launch<false, MODE_BWD>(P, args->T, st);
+}
+
+rlk_status rlk_sample(const rlk_logp_args* args, unsigned long long seed,
+                      const unsigned long long* counter, const uint32_t* uniform,
+                      int32_t* out_token, float* out_restr, float* out_full,
+                      int32_t* out_support, void* stream) {
+  rlk_status s = check_args(args, true, false);
+  if (s != RLK_OK || args->T == 0) return s;
+  if (!counter && !uniform) return fail(RLK_EINVAL, "counter and uniform are both NULL");
+  if (counter && !aligned(counter, 8)) return fail(RLK_EALIGN, "counter is not 8-byte aligned");
+  if ((s = check_out(uniform, "uniform", false)) != RLK_OK) return s;
+  if ((s = check_out(out_token, "out_token", true)) != RLK_OK) return s;
+  if ((s = check_out(out_restr, "out_restr", false)) != RLK_OK) return s;
+  if ((s = check_out(out_full, "out_full", false)) != RLK_OK) return s;
+  if ((s = check_out(out_support, "out_support", false)) != RLK_OK) return s;
+  KParams P = make_params(args);
+  P.target = nullptr;
+  P.out_full = out_full;
+  P.out_restr = out_restr;
+  P.out_support = out_support;
+  P.out_token = out_token;
+  P.uniform = uniform;
+  P.counter = counter;
+  P.seed = seed;
+  return launch<true, MODE_SAMPLE>(P, args->T, static_cast<cudaStream_t>(stream));
 }
 
 const char* rlk_status_string(rlk_status status) {

@@ -249,3 +249,15 @@ def test_pair_save_and_backward_saved_validation(lib):
     # top_p / top_k are not read by the saved backward
     assert bs(a=_args(top_p_scalar=9.0, T=0)) == b.RLK_OK
     assert bs(a=_args(T=0, logits=None, target=None), st=None, gf=None, grad=None) == b.RLK_OK
+
+
+def test_sample_validation(lib):
+    a = _args(target=None)           # the sampler has no target
+    smp = lambda a=a, ctr=0x80000, uni=None, tok=OUT: lib.rlk_sample(
+        ctypes.byref(a), 7, ctr, uni, tok, None, None, None, None)
+    assert smp(ctr=None, uni=None) == b.RLK_EINVAL
+    assert smp(ctr=0x80004) == b.RLK_EALIGN
+    assert smp(ctr=None, uni=0x80002) == b.RLK_EALIGN
+    assert smp(tok=None) == b.RLK_EINVAL
+    assert smp(a=_args(target=None, top_p_scalar=0.0)) == b.RLK_EINVAL
+    assert smp(a=_args(target=None, T=0, logits=None), ctr=None, tok=None) == b.RLK_OK
