@@ -231,12 +231,20 @@ rlk_status rlk_logp_backward_saved(const rlk_logp_args* args, const rlk_row_stat
  *   out_restr / out_full: optional float[T]: the sampled token's restricted
  *     and full logprobs, bit-identical to rlk_logp_pair with target = token.
  *   out_support: optional int32[T], as in rlk_logp_pair.
+ *   workspace: device scratch of RLK_SAMPLE_WORKSPACE_BYTES(T) bytes,
+ *     16-byte aligned, owned by the caller: the pair pass leaves a 16-byte
+ *     record per row there for the draw.  Its contents on entry do not
+ *     matter; calls that share a workspace must not overlap on the GPU.
  * A row whose support reaches below the 1024-key window is resolved exactly
- * (slower path), as in rlk_logp_pair.  One launch on `stream`. */
+ * (slower path), as in rlk_logp_pair.  Two launches on `stream`: the pair
+ * pass that resolves every row (greedy and NaN rows finish there), then one
+ * cluster per drawing row that re-reads the row and draws. */
+#define RLK_SAMPLE_WORKSPACE_BYTES(T) ((size_t)(T) * 16u)
+
 rlk_status rlk_sample(const rlk_logp_args* args, unsigned long long seed,
                       const unsigned long long* counter, const uint32_t* uniform,
                       int32_t* out_token, float* out_restr, float* out_full,
-                      int32_t* out_support, void* stream);
+                      int32_t* out_support, void* workspace, void* stream);
 
 /* ---------------------------------------------------------------------
  * Vocabulary-sharded form: the fixed virtual TP8 partition with each shard

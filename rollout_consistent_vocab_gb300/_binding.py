@@ -89,7 +89,7 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     lib.rlk_logp_kl_ref.argtypes = [A, VP, VP, VP, VP]
     lib.rlk_logp_backward.argtypes = [A, VP, VP, VP, ctypes.c_int64, ctypes.c_int32, VP, VP, VP, VP]
     lib.rlk_logp_pair_save.argtypes = [A, VP, VP, VP, VP, VP]
-    lib.rlk_sample.argtypes = [A, ctypes.c_uint64, VP, VP, VP, VP, VP, VP, VP]
+    lib.rlk_sample.argtypes = [A, ctypes.c_uint64, VP, VP, VP, VP, VP, VP, VP, VP]
     lib.rlk_logp_backward_saved.argtypes = [A, VP, VP, VP, VP, ctypes.c_int64, ctypes.c_int32, VP]
     SA = P(ShardArgs)
     lib.rlk_logp_shard_summary.argtypes = [SA, VP, VP, VP, VP, VP]
@@ -453,11 +453,12 @@ def logp_autograd(logits, target, temperature=1.0, top_p=1.0, top_k=-1):
 # ------------------------------------------------------------ sampler
 
 def sample(logits, temperature=1.0, top_p=1.0, top_k=-1, *, seed=0, counter=None, uniform=None,
-           out_token=None, out_restr=None, out_full=None, out_support=None, err_count=None,
-           stream=None):
+           out_token=None, out_restr=None, out_full=None, out_support=None, workspace=None,
+           err_count=None, stream=None):
     """Draw one token per row from the restricted distribution (inverse CDF in
     column order).  Random words: ``uniform`` (uint32 bits in an int32 [T]
     tensor) or Philox4x32-10 of ``seed`` over ``counter`` (int64 [T]).
+    ``workspace``: int32 [T, 4] scratch (allocated here if not given).
     Returns (token, restricted logprob, full logprob, support)."""
     lib = load_library()
     torch = _torch()
@@ -472,7 +473,11 @@ def sample(logits, temperature=1.0, top_p=1.0, top_k=-1, *, seed=0, counter=None
     out_restr = _empty(T, torch.float32, logits) if out_restr is None else out_restr
     out_full = _empty(T, torch.float32, logits) if out_full is None else out_full
     out_support = _empty(T, torch.int32, logits) if out_support is None else out_support
+    if workspace is None:
+        workspace = torch.empty((T, 4), dtype=torch.int32, device=logits.device)
+    if workspace.numel() * workspace.element_size() < 16 * T or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor of at least 16 * T bytes")
     check(lib.rlk_sample(ctypes.byref(a), int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(counter), _ptr(uniform),
                          _ptr(out_token), _ptr(out_restr), _ptr(out_full), _ptr(out_support),
-                         _stream(stream)))
+                         workspace.data_ptr() if T else None, _stream(stream)))
     return out_token, out_restr, out_full, out_support

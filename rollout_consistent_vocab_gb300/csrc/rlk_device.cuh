@@ -807,15 +807,30 @@ __device__ __forceinline__ unsigned long long scale_draw(uint32_t u, unsigned lo
   return (hi << 32) | (lo >> 32);
 }
 
-// Fixed-point mass (2^-44 units, the selection's per-key values) of the
-// elements of one 16-byte chunk whose order key is >= min_key.
-__device__ __forceinline__ unsigned long long chunk_support_mass(uint4 v, int min_key, float M, float c) {
+// Support elements of one 16-byte chunk: those >= vmin (the value of the
+// support's lowest key; -inf when the support is the whole vocabulary), as a
+// mask with bit j for column 2j and bit 16 + j for column 2j + 1 of the chunk.
+__device__ __forceinline__ uint32_t chunk_support_bits(uint4 v, __nv_bfloat162 vmin2) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  unsigned long long m = 0;
+  uint32_t bits = 0;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t b = (w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
-    if (okey(b) >= min_key) m += qfx(__uint_as_float(b << 16), M, c);
+  for (int j = 0; j < 4; ++j) bits |= (__hge2_mask(as_bf2(w[j]), vmin2) & 0x00010001u) << j;
+  return bits;
+}
+
+// Fixed-point mass (2^-44 units, the selection's per-key values) of a chunk's
+// support elements; the exponentials are evaluated for those elements only.
+__device__ __forceinline__ unsigned long long chunk_support_mass(uint4 v, __nv_bfloat162 vmin2, float M,
+                                                                 float c) {
+  uint32_t bits = chunk_support_bits(v, vmin2);
+  unsigned long long m = 0;
+  while (bits) {
+    const int pos = __ffs(bits) - 1;
+    bits &= bits - 1;
+    const int j = pos & 3;
+    const uint32_t wj = (j == 0) ? v.x : (j == 1) ? v.y : (j == 2) ? v.z : v.w;
+    const uint32_t b = (pos & 16) ? (wj >> 16) : (wj & 0xFFFFu);
+    m += qfx(__uint_as_float(b << 16), M, c);
   }
   return m;
 }

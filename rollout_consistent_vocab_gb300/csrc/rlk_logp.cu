@@ -83,12 +83,20 @@ struct __align__(128) Smem {
   int32_t win[4];
   float bc_f[4];
   int32_t sel_done;
-  alignas(16) uint4 lead;          // backward / sampler: the leader's resolution of the row
-  uint4 zr[NSHARD];                 // sampler: every shard's fixed-point support mass
-  unsigned long long samp_res;      // sampler: residual draw inside the owning row of chunks
-  int32_t samp_i;
-  unsigned long long bar_load, bar_mid, bar_sum, bar_hist, bar_lead, bar_zr;
+  alignas(16) uint4 lead;          // backward: the leader's resolution of the row
+  unsigned long long bar_load, bar_mid, bar_sum, bar_hist, bar_lead;
 };
+
+// Shared memory of the draw kernel.
+struct __align__(128) SampSmem {
+  uint4 shard[SHARD_CHUNKS];
+  uint32_t hist[WIN / 2];           // per-warp partial masses of the draw (u64 pairs)
+  uint4 zr[NSHARD];                 // every shard's fixed-point support mass
+  unsigned long long samp_res;      // residual draw inside the owning row of chunks
+  int32_t samp_i;
+  unsigned long long bar_load, bar_zr;
+};
+static_assert(sizeof(SampSmem) + 1024 <= 233472 / CTAS_PER_SM, "shared memory budget of 5 CTAs per SM");
 // five CTAs per SM: 5 * (sizeof + 1 KB reserved) <= 228 KB
 static_assert(sizeof(Smem) + 1024 <= 233472 / CTAS_PER_SM, "shared memory budget of 5 CTAs per SM");
 
@@ -119,11 +127,14 @@ struct KParams {
   const unsigned long long* counter;
   unsigned long long seed;
   int32_t* out_token;
+  struct SampMsg* out_samp;     // resolution pass: per-row record for the draw
+  const struct SampMsg* in_samp;
 };
 
 enum { MODE_FWD = 0, MODE_BWD = 1, MODE_SAMPLE = 2 };
 
-// Sampler message from the leader (16 bytes).
+// Sampler: per-row record of the resolved row, written by the leader of the
+// pair pass and read by the draw kernel (16 bytes).
 enum : uint32_t { SAMP_DRAW = 1u, SAMP_SEL = 2u };
 struct __align__(16) SampMsg {
   float M, Z;
@@ -145,15 +156,14 @@ __device__ __forceinline__ void send_mid(Smem& S, uint32_t r, int to, float xm, 
 
 // ------------------------------------------------------------ the kernel
 
-// The sampler's draw after every shard knows its own support mass: each CTA
-// sends its mass to the 7 others; the shard holding the drawn mass scans its
-// chunks in column order and writes the token and its logprobs.  src is the
-// shard's logits (shared memory, or global memory when src_global); cm are
-// the chunk maxima of the max pass.
+// The draw once the row is resolved: every shard sums the fixed-point mass
+// of its support tokens (each thread keeps its chunks' masses in registers)
+// and sends it to the 7 others; the shard holding the drawn mass finds the
+// row of chunks, the chunk and the column, in column order, and writes the
+// token and its logprobs.
 template <class SM>
 __device__ __forceinline__ void sample_shard(SM& S, const KParams& P, int64_t row, uint32_t r,
-                                             const uint4* src, bool src_global, int nchunks,
-                                             const __nv_bfloat162 (&cm)[MAXCH], const SampMsg& m,
+                                             const uint4* src, int nchunks, const SampMsg& m,
                                              float tau, uint32_t bar_zr) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float c = __fdiv_rn(LOG2E, tau);
@@ -161,25 +171,24 @@ __device__ __forceinline__ void sample_shard(SM& S, const KParams& P, int64_t ro
   // key_value of keys below -inf's would be a NaN pattern)
   const float vmin_f = m.min_key <= KEY_NEG_INF ? -INFINITY : key_value(m.min_key);
   const __nv_bfloat162 vmin2 = __floats2bfloat162_rn(vmin_f, vmin_f);
+  unsigned long long* wsum = reinterpret_cast<unsigned long long*>(S.hist);
   // ---- this shard's support mass
+  unsigned long long mi[MAXCH];
   unsigned long long acc = 0;
 #pragma unroll
   for (int i = 0; i < MAXCH; ++i) {
     const int ch = tid + i * NTHR;
-    if (ch < nchunks && __hge2_mask(cm[i], vmin2) != 0u)
-      acc += chunk_support_mass(src_global ? __ldg(src + ch) : src[ch], m.min_key, m.M, c);
+    mi[i] = (i < MAXCH - 1 || ch < nchunks) ? chunk_support_mass(src[ch], vmin2, m.M, c) : 0ull;
+    acc += mi[i];
   }
   acc = warp_sum_u64(acc);
-  unsigned long long* wsum = reinterpret_cast<unsigned long long*>(S.hist);   // free by now
   if (lane == 0) wsum[warp] = acc;
   __syncthreads();
   if (tid == 0) {
     unsigned long long zr = 0;
-#pragma unroll
     for (int w = 0; w < NWARP; ++w) zr += wsum[w];
     const uint4 v = make_uint4(static_cast<uint32_t>(zr), static_cast<uint32_t>(zr >> 32), 0u, 0u);
     S.zr[r] = v;
-#pragma unroll
     for (int q = 0; q < NSHARD; ++q)
       if (q != static_cast<int>(r)) st_async_v4(map_rank(smem_addr(&S.zr[r]), q), v, map_rank(bar_zr, q));
     // one thread waits for the 7 peers' masses; the block barrier publishes them
@@ -189,7 +198,6 @@ __device__ __forceinline__ void sample_shard(SM& S, const KParams& P, int64_t ro
   // ---- the drawn mass, and the shard that holds it
   const bool ok = S.samp_i != 0;
   unsigned long long zs = 0, before = 0, mine = 0;
-#pragma unroll
   for (int q = 0; q < NSHARD; ++q) {
     const unsigned long long zq = (static_cast<unsigned long long>(S.zr[q].y) << 32) | S.zr[q].x;
     if (q < static_cast<int>(r)) before += zq;
@@ -211,12 +219,8 @@ __device__ __forceinline__ void sample_shard(SM& S, const KParams& P, int64_t ro
   __syncthreads();                  // every thread has read S.samp_i
 #pragma unroll
   for (int i = 0; i < MAXCH; ++i) {
-    const int ch = tid + i * NTHR;
-    unsigned long long mi = 0;
-    if (ch < nchunks && __hge2_mask(cm[i], vmin2) != 0u)
-      mi = chunk_support_mass(src_global ? __ldg(src + ch) : src[ch], m.min_key, m.M, c);
-    mi = warp_sum_u64(mi);
-    if (lane == 0) wsum[NWARP + i * NWARP + warp] = mi;
+    const unsigned long long w = warp_sum_u64(mi[i]);
+    if (lane == 0) wsum[NWARP + i * NWARP + warp] = w;
   }
   __syncthreads();
   if (tid == 0) {
@@ -235,17 +239,17 @@ __device__ __forceinline__ void sample_shard(SM& S, const KParams& P, int64_t ro
   __syncthreads();
   const int istar = S.samp_i;
   const unsigned long long res = S.samp_res;
-  const int ch = tid + istar * NTHR;
   unsigned long long mt = 0;
-  uint4 v = make_uint4(0u, 0u, 0u, 0u);
-  if (ch < nchunks) {
-    v = src_global ? __ldg(src + ch) : src[ch];
-    mt = chunk_support_mass(v, m.min_key, m.M, c);
-  }
+#pragma unroll
+  for (int i = 0; i < MAXCH; ++i)
+    if (i == istar) mt = mi[i];
   unsigned long long excl = warp_incl_scan_u64(mt) - mt;
   for (int w = 0; w < warp; ++w) excl += wsum[NWARP + istar * NWARP + w];
   if (mt == 0 || res < excl || res - excl >= mt) return;
-  // this thread's chunk holds the draw: walk its 8 columns in order
+  // this thread's chunk holds the draw: walk its support columns in order
+  const int ch = tid + istar * NTHR;
+  const uint4 v = src[ch];
+  const uint32_t sb = chunk_support_bits(v, vmin2);
   unsigned long long left = res - excl;
   const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
   int jstar = -1;
@@ -253,7 +257,7 @@ __device__ __forceinline__ void sample_shard(SM& S, const KParams& P, int64_t ro
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const uint32_t b = (w4[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
-    if (jstar < 0 && okey(b) >= m.min_key) {
+    if (jstar < 0 && ((sb >> ((j >> 1) + 16 * (j & 1))) & 1u)) {
       const unsigned long long q = qfx(__uint_as_float(b << 16), m.M, c);
       if (left < q) {
         jstar = j;
@@ -290,7 +294,6 @@ logp_kernel(const KParams P) {
   const uint32_t bar_sum = smem_addr(&S.bar_sum);
   const uint32_t bar_hist = smem_addr(&S.bar_hist);
   const uint32_t bar_lead = smem_addr(&S.bar_lead);
-  const uint32_t bar_zr = smem_addr(&S.bar_zr);
   char* const gshard = BWD ? P.grad + (row * P.grad_stride + static_cast<int64_t>(r) * SW) *
                                           (P.grad_f32 ? 4 : 2)
                            : nullptr;
@@ -313,7 +316,7 @@ logp_kernel(const KParams P) {
   const float tau = P.tau_arr ? P.tau_arr[row] : P.tau_s;
   const float p = RESTR ? (P.p_arr ? P.p_arr[row] : P.p_s) : 1.0f;
   const int k = RESTR ? (P.k_arr ? P.k_arr[row] : P.k_s) : -1;
-  const int t = SAMPLE ? 0 : P.target[row];     // the sampler has no target
+  const int t = SAMPLE ? 0 : P.target[row];     // the sampler's pass has no target
   const bool valid = (tau >= 0.0f) && (tau <= 3.402823466e38f) && (p > 0.0f) && (p <= 1.0f) &&
                      (k == -1 || (k >= 1 && k <= VREAL)) && (t >= 0) && (t < VREAL);
   if (!valid) {
@@ -326,7 +329,10 @@ logp_kernel(const KParams P) {
         if (RESTR && P.out_support) P.out_support[row] = -1;
         if (P.out_kl) P.out_kl[row] = __int_as_float(0x7fc00000);
         if (P.out_stats) P.out_stats[row] = nan_stats();
-        if (SAMPLE) P.out_token[row] = -1;
+        if (SAMPLE) {
+          P.out_token[row] = -1;
+          P.out_samp[row] = SampMsg{};     // nothing to draw
+        }
         if (P.err) atomicAdd(P.err, 1);
       }
     }
@@ -350,13 +356,9 @@ logp_kernel(const KParams P) {
     // messages from the 7 peers: 16 bytes each
     if (sel) mbar_arrive_expect_tx(bar_mid, (NSHARD - 1) * 16);
     if (r == 0) mbar_arrive_expect_tx(bar_sum, (NSHARD - 1) * 16);
-    if ((BWD || SAMPLE) && r != 0) {
+    if (BWD && r != 0) {
       mbar_init(bar_lead, 1);
       mbar_arrive_expect_tx(bar_lead, 16);
-    }
-    if (SAMPLE) {
-      mbar_init(bar_zr, 1);
-      mbar_arrive_expect_tx(bar_zr, (NSHARD - 1) * 16);
     }
     S.npush = 0u;
   }
@@ -532,20 +534,6 @@ logp_kernel(const KParams P) {
     else st_async_v4(map_rank(smem_addr(&S.slot[r]), 0), msg, map_rank(bar_sum, 0));
   }
   if (r != 0) {                // messages carry everything the leader needs
-    if (SAMPLE) {
-      // the leader's resolution of the row, then this shard's part of the draw
-      if (tid == 0) S.win[3] = mbar_wait_bounded(bar_lead) ? 1 : 0;
-      __syncthreads();
-      if (!S.win[3]) {
-        if (tid == 0) {
-          P.out_token[row] = -1;
-          if (P.err) atomicAdd(P.err, 1);
-        }
-        return;
-      }
-      const SampMsg m = *reinterpret_cast<const SampMsg*>(&S.lead);
-      if (m.flags & SAMP_DRAW) sample_shard(S, P, row, r, sh, false, nchunks, cm, m, tau, bar_zr);
-    }
     if (BWD) {
       // the leader's resolution of the row, then this shard's gradient
       const bool ok = mbar_wait_bounded(bar_lead);
@@ -574,7 +562,7 @@ logp_kernel(const KParams P) {
   }
   __syncthreads();
   const bool timed_out = S.win[3] != 0;
-  if (!BWD && !SAMPLE && tid >= 32 && !sel) return;   // only warp 0 finishes rows without a support search
+  if (!BWD && tid >= 32 && !sel) return;   // only warp 0 finishes rows without a support search
   bool bad = timed_out;
   float M = -INFINITY;
   float full = __int_as_float(0x7fc00000), restr = full;
@@ -631,7 +619,7 @@ logp_kernel(const KParams P) {
       sr = select_support(S, S.merged, cntB, hi, lo, rowp, S.bc_f[0], c, S.bc_f[1], p, k, k_on, p_on);
       shard_reused = true;
     }
-    if (!BWD && !SAMPLE && tid != 0) return;
+    if (!BWD && tid != 0) return;
     if (tid == 0 && !bad) {
       in_s = okey_of(xt) >= sr.min_key;
       zs = __ull2float_rn(sr.zs) * (1.0f / FX_SCALE);
@@ -676,38 +664,66 @@ logp_kernel(const KParams P) {
                      0, t, m, gshard, P.grad_f32 != 0);
   }
 
-  if (SAMPLE) {
-    // the draw: tell the peers the row's resolution, write what the leader
-    // alone knows, then take part in the draw as shard 0
-    if (tid == 0) {
-      SampMsg m{};
-      m.M = M;
-      m.Z = Z;
-      m.min_key = sel ? sr.min_key : 0;
-      m.flags = (!bad && !greedy ? SAMP_DRAW : 0u) | (sel ? SAMP_SEL : 0u);
-      const uint4 v = *reinterpret_cast<const uint4*>(&m);
-      S.lead = v;
-#pragma unroll
-      for (int q = 1; q < NSHARD; ++q)
-        st_async_v4(map_rank(smem_addr(&S.lead), q), v, map_rank(bar_lead, q));
-      if (P.out_support) P.out_support[row] = support;
-      if (bad) {
-        P.out_token[row] = -1;
-        if (P.out_full) P.out_full[row] = __int_as_float(0x7fc00000);
-        if (P.out_restr) P.out_restr[row] = __int_as_float(0x7fc00000);
-      } else if (greedy) {
-        P.out_token[row] = static_cast<int32_t>(amax);
-        if (P.out_full) P.out_full[row] = 0.0f;
-        if (P.out_restr) P.out_restr[row] = 0.0f;
-      }
-      if (timed_out && P.err) atomicAdd(P.err, 1);
+  if (SAMPLE && tid == 0) {
+    // the row's resolution for the draw kernel; rows without a draw finish here
+    SampMsg m{};
+    m.M = M;
+    m.Z = Z;
+    m.min_key = sel ? sr.min_key : 0;
+    m.flags = (!bad && !greedy ? SAMP_DRAW : 0u) | (sel ? SAMP_SEL : 0u);
+    P.out_samp[row] = m;
+    if (P.out_support) P.out_support[row] = support;
+    if (bad) {
+      P.out_token[row] = -1;
+      if (P.out_full) P.out_full[row] = __int_as_float(0x7fc00000);
+      if (P.out_restr) P.out_restr[row] = __int_as_float(0x7fc00000);
+    } else if (greedy) {
+      P.out_token[row] = static_cast<int32_t>(amax);
+      if (P.out_full) P.out_full[row] = 0.0f;
+      if (P.out_restr) P.out_restr[row] = 0.0f;
     }
-    __syncthreads();
-    const SampMsg m = *reinterpret_cast<const SampMsg*>(&S.lead);
-    if (m.flags & SAMP_DRAW)
-      sample_shard(S, P, row, 0, shard_reused ? reinterpret_cast<const uint4*>(rowp) : sh, shard_reused,
-                   nchunks, cm, m, tau, bar_zr);
+    if (timed_out && P.err) atomicAdd(P.err, 1);
   }
+}
+
+// ------------------------------------------------------------ the draw
+
+// One cluster of 8 CTAs per row, after the pair pass resolved every row:
+// each CTA streams its shard into shared memory and takes part in the draw
+// (sample_shard).  Rows without a draw (greedy, NaN, rejected) exit at once.
+__global__ void __cluster_dims__(NSHARD, 1, 1) __launch_bounds__(NTHR, CTAS_PER_SM)
+sample_kernel(const KParams P) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  SampSmem& S = *reinterpret_cast<SampSmem*>(smem_raw);
+  const int tid = threadIdx.x;
+  const uint32_t r = cluster_rank();
+  const int64_t row = blockIdx.x / NSHARD;
+  const SampMsg m = P.in_samp[row];
+  if (!(m.flags & SAMP_DRAW)) return;         // the same decision in every CTA of the cluster
+  const int nchunks = (r == NSHARD - 1) ? LAST_CHUNKS : SHARD_CHUNKS;
+  const uint32_t bar_load = smem_addr(&S.bar_load);
+  const uint32_t bar_zr = smem_addr(&S.bar_zr);
+  if (tid == 0) {
+    mbar_init(bar_load, 1);
+    mbar_init(bar_zr, 1);
+    mbar_arrive_expect_tx(bar_zr, (NSHARD - 1) * 16);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    const uint32_t bytes = static_cast<uint32_t>(nchunks) * 16u;
+    mbar_arrive_expect_tx(bar_load, bytes);
+    const uint64_t pol = evict_first_policy();
+    const uint32_t piece = bytes / TMA_PIECES;
+    const char* src = reinterpret_cast<const char*>(P.logits + row * P.stride + static_cast<int64_t>(r) * SW);
+    const uint32_t dst = smem_addr(S.shard);
+#pragma unroll
+    for (int i = 0; i < TMA_PIECES; ++i) bulk_load(dst + i * piece, src + i * piece, piece, bar_load, pol);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  const float tau = P.tau_arr ? P.tau_arr[row] : P.tau_s;
+  __syncthreads();
+  cluster_arrive_relaxed();
+  if (!mbar_wait_bounded(bar_load)) mbar_wait_bounded(bar_load);
+  cluster_wait();                             // every peer's barrier is ready for the masses
+  sample_shard(S, P, row, r, S.shard, nchunks, m, tau, bar_zr);
 }
 
 // ------------------------------------------------------------ host side
@@ -872,7 +888,7 @@ rlk_status rlk_logp_backward(const rlk_logp_args* args, const float* grad_full,
 rlk_status rlk_sample(const rlk_logp_args* args, unsigned long long seed,
                       const unsigned long long* counter, const uint32_t* uniform,
                       int32_t* out_token, float* out_restr, float* out_full,
-                      int32_t* out_support, void* stream) {
+                      int32_t* out_support, void* workspace, void* stream) {
   rlk_status s = check_args(args, true, false);
   if (s != RLK_OK || args->T == 0) return s;
   if (!counter && !uniform) return fail(RLK_EINVAL, "counter and uniform are both NULL");
@@ -882,6 +898,8 @@ rlk_status rlk_sample(const rlk_logp_args* args, unsigned long long seed,
   if ((s = check_out(out_restr, "out_restr", false)) != RLK_OK) return s;
   if ((s = check_out(out_full, "out_full", false)) != RLK_OK) return s;
   if ((s = check_out(out_support, "out_support", false)) != RLK_OK) return s;
+  if (!workspace) return fail(RLK_EINVAL, "workspace is NULL");
+  if (!aligned(workspace, 16)) return fail(RLK_EALIGN, "workspace is not 16-byte aligned");
   KParams P = make_params(args);
   P.target = nullptr;
   P.out_full = out_full;
@@ -891,7 +909,26 @@ rlk_status rlk_sample(const rlk_logp_args* args, unsigned long long seed,
   P.uniform = uniform;
   P.counter = counter;
   P.seed = seed;
-  return launch<true, MODE_SAMPLE>(P, args->T, static_cast<cudaStream_t>(stream));
+  P.out_samp = static_cast<SampMsg*>(workspace);
+  P.in_samp = static_cast<const SampMsg*>(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((s = launch<true, MODE_SAMPLE>(P, args->T, st)) != RLK_OK) return s;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(sizeof(SampSmem)));
+    if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    configured[dev] = true;
+  }
+  sample_kernel<<<static_cast<unsigned>(args->T * NSHARD), NTHR, sizeof(SampSmem), st>>>(P);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(RLK_ECUDA, "kernel launch: %s", cudaGetErrorString(e));
+  return RLK_OK;
 }
 
 const char* rlk_status_string(rlk_status status) {

@@ -253,11 +253,13 @@ def test_pair_save_and_backward_saved_validation(lib):
 
 def test_sample_validation(lib):
     a = _args(target=None)           # the sampler has no target
-    smp = lambda a=a, ctr=0x80000, uni=None, tok=OUT: lib.rlk_sample(
-        ctypes.byref(a), 7, ctr, uni, tok, None, None, None, None)
+    smp = lambda a=a, ctr=0x80000, uni=None, tok=OUT, ws=0x90000: lib.rlk_sample(
+        ctypes.byref(a), 7, ctr, uni, tok, None, None, None, ws, None)
     assert smp(ctr=None, uni=None) == b.RLK_EINVAL
     assert smp(ctr=0x80004) == b.RLK_EALIGN
     assert smp(ctr=None, uni=0x80002) == b.RLK_EALIGN
     assert smp(tok=None) == b.RLK_EINVAL
     assert smp(a=_args(target=None, top_p_scalar=0.0)) == b.RLK_EINVAL
-    assert smp(a=_args(target=None, T=0, logits=None), ctr=None, tok=None) == b.RLK_OK
+    assert smp(ws=None) == b.RLK_EINVAL
+    assert smp(ws=0x90008) == b.RLK_EALIGN
+    assert smp(a=_args(target=None, T=0, logits=None), ctr=None, tok=None, ws=None) == b.RLK_OK
