@@ -246,6 +246,30 @@ rlk_status rlk_sample(const rlk_logp_args* args, unsigned long long seed,
                       int32_t* out_token, float* out_restr, float* out_full,
                       int32_t* out_support, void* workspace, void* stream);
 
+/* rlk_sample without a workspace argument, for callers that cannot allocate
+ * device memory when they call (their memory belongs to a framework
+ * allocator or a fixed plan, e.g. an inference-engine plugin at enqueue
+ * time, where a cudaMalloc would bypass the plan and may synchronise the
+ * device).  The pages have no counterpart: this is a packaging of
+ * rlk_sample, with the same arguments (minus workspace) and results.
+ *   Scratch: a fixed array inside the library, RLK_SAMPLE_NOALLOC_MAX_ROWS x
+ *     16 bytes (1 MiB) of device memory on every GPU that loads the library,
+ *     held until the process exits.  T above RLK_SAMPLE_NOALLOC_MAX_ROWS is
+ *     rejected with RLK_EINVAL (split the batch, or use rlk_sample).
+ *   Set-up: the first call on each device (with that device current) looks
+ *     up the array's device address; make that first call before any stream
+ *     capture.  Nothing is allocated by this or any later call.
+ *   Sharing: every call on a device uses the same array.  Each call writes
+ *     every record it reads, so leftovers from an earlier call never matter,
+ *     but calls that overlap on the GPU (different streams, or host threads
+ *     sharing a device) race on the array: order them. */
+#define RLK_SAMPLE_NOALLOC_MAX_ROWS 65536
+
+rlk_status rlk_sample_noalloc(const rlk_logp_args* args, unsigned long long seed,
+                              const unsigned long long* counter, const uint32_t* uniform,
+                              int32_t* out_token, float* out_restr, float* out_full,
+                              int32_t* out_support, void* stream);
+
 /* ---------------------------------------------------------------------
  * Vocabulary-sharded form: the fixed virtual TP8 partition with each shard
  * in its own buffer, as a tensor-parallel rank would hold it ("Reproduce and

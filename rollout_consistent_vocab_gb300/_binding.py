@@ -64,6 +64,7 @@ class ShardArgs(ctypes.Structure):
 
 COMPUTE = ("rlk_logp_full", "rlk_logp_restricted", "rlk_logp_pair", "rlk_logp_kl", "rlk_logp_kl_ref",
            "rlk_logp_backward", "rlk_logp_pair_save", "rlk_logp_backward_saved", "rlk_sample",
+           "rlk_sample_noalloc",
            "rlk_logp_shard_summary", "rlk_logp_shard_counts", "rlk_logp_merge")
 RLK_GRAD_BF16, RLK_GRAD_F32 = 0, 1
 EXPORTS = COMPUTE + ("rlk_status_string", "rlk_last_error", "rlk_abi_version")
@@ -90,6 +91,7 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     lib.rlk_logp_backward.argtypes = [A, VP, VP, VP, ctypes.c_int64, ctypes.c_int32, VP, VP, VP, VP]
     lib.rlk_logp_pair_save.argtypes = [A, VP, VP, VP, VP, VP]
     lib.rlk_sample.argtypes = [A, ctypes.c_uint64, VP, VP, VP, VP, VP, VP, VP, VP]
+    lib.rlk_sample_noalloc.argtypes = [A, ctypes.c_uint64, VP, VP, VP, VP, VP, VP, VP]
     lib.rlk_logp_backward_saved.argtypes = [A, VP, VP, VP, VP, ctypes.c_int64, ctypes.c_int32, VP]
     SA = P(ShardArgs)
     lib.rlk_logp_shard_summary.argtypes = [SA, VP, VP, VP, VP, VP]
