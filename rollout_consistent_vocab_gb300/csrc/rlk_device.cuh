@@ -183,7 +183,24 @@ __device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t w) {
   return *reinterpret_cast<__nv_bfloat162*>(&w);
 }
 
-// fixed-point mass of one element at key value v: exp(s - M) * 2^44
+// Round a float q in [0, 2^44] to the nearest integer, ties to even, without
+// the float -> u64 converter (it runs on the FP64 pipe, which is narrow on
+// this GPU).  Below 2^23 one IEEE add of 2^23 rounds q to an integer, read
+// from the sum's bits (bits(2^23) = 0x4B000000; a sum that rounds up to 2^24
+// reads as 2^23, also right); from 2^23 up q is an integer, mantissa <<
+// (exponent - 150).  Equal to round-half-even for every float in [0, 2^44]
+// (checked exhaustively).  Branch-free.
+__device__ __forceinline__ unsigned long long fx_round(float q) {
+  const uint32_t b = __float_as_uint(q);
+  const uint32_t small = __float_as_uint(__fadd_rn(q, 8388608.0f)) - 0x4B000000u;
+  const uint32_t sh = min(max(b >> 23, 150u) - 150u, 21u);
+  const unsigned long long big = static_cast<unsigned long long>((b & 0x7FFFFFu) | 0x800000u) << sh;
+  return q < 8388608.0f ? static_cast<unsigned long long>(small) : big;
+}
+
+// fixed-point mass of one element at key value v: exp(s - M) * 2^44, rounded
+// to the nearest integer.  The selection's few per-key masses are latency-bound
+// and keep the hardware conversion; the dense sampler path uses fx_round.
 __device__ __forceinline__ unsigned long long qfx(float v, float M, float c) {
   const float q = ex2((v - M) * c);
   return __float2ull_rn(q * FX_SCALE);
@@ -824,6 +841,21 @@ __device__ __forceinline__ unsigned long long chunk_support_mass(uint4 v, __nv_b
                                                                  float c) {
   uint32_t bits = chunk_support_bits(v, vmin2);
   unsigned long long m = 0;
+  if (bits == 0x000F000Fu) {
+    // every element in the support: the same per-element values as qfx (IEEE
+    // round-to-nearest subtract and multiply, ex2.approx, exact 2^44 scaling),
+    // two columns at a time
+    const uint64_t nm2 = pack2(-M, -M), c2 = pack2(c, c), s2 = pack2(FX_SCALE, FX_SCALE);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float a0, a1, q0, q1;
+      unpack2(mul2(add2(pack2(bf16_lo(w[j]), bf16_hi(w[j])), nm2), c2), a0, a1);
+      unpack2(mul2(pack2(ex2(a0), ex2(a1)), s2), q0, q1);
+      m += fx_round(q0) + fx_round(q1);
+    }
+    return m;
+  }
   while (bits) {
     const int pos = __ffs(bits) - 1;
     bits &= bits - 1;
