@@ -17,6 +17,9 @@
 #ifndef RLK_NTHR
 #define RLK_NTHR 128
 #endif
+#ifndef RLK_SEL_KPL
+#define RLK_SEL_KPL 4            // keys per lane per step of the warp selection
+#endif
 #ifndef RLK_WAIT_HINT_NS
 #define RLK_WAIT_HINT_NS 20000   // suspend-time hint of a barrier test (ns)
 #endif
@@ -538,8 +541,9 @@ __device__ __noinline__ SelResult select_support(SM& S, uint32_t* cnt0, uint32_t
 }
 
 // Selection by one warp when the first window holds every threshold (the
-// common case).  Keys hi, hi-1, ..., lo are taken in blocks of 128 (4
-// consecutive keys per lane): first a scan of the counts alone finds the
+// common case).  Keys hi, hi-1, ..., lo are taken in blocks of 32 x
+// RLK_SEL_KPL (consecutive keys per lane; 4 measured fastest, 8 slower): first
+// a scan of the counts alone finds the
 // top-k boundary, then one scan of the fixed-point masses over S_k finds the
 // nucleus boundary.  Returns false if a threshold may lie below the window.
 __device__ __forceinline__ uint32_t warp_incl_scan_u32(uint32_t v) {
@@ -564,7 +568,8 @@ __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long l
 __device__ __forceinline__ bool select_warp(const uint32_t* cnt, int hi, int lo, float M, float c,
                                          float Z, float p, int k, bool k_on, bool p_on,
                                          SelResult& out) {
-  constexpr int BLK = 4 * 32;
+  constexpr int KPL = RLK_SEL_KPL;   // consecutive keys per lane in a block
+  constexpr int BLK = KPL * 32;
   const int lane = threadIdx.x & 31;
   const int n = hi - lo + 1;
   int imax = n - 1;
@@ -574,10 +579,10 @@ __device__ __forceinline__ bool select_warp(const uint32_t* cnt, int hi, int lo,
     uint32_t carry = 0;
     int fi = -1;
     for (int b0 = 0; b0 < n && fi < 0; b0 += BLK) {
-      uint32_t cj[4], lc = 0;
+      uint32_t cj[KPL], lc = 0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int i = b0 + 4 * lane + j;
+      for (int j = 0; j < KPL; ++j) {
+        const int i = b0 + KPL * lane + j;
         cj[j] = (i < n) ? cnt[i] : 0u;
         lc += cj[j];
       }
@@ -586,9 +591,9 @@ __device__ __forceinline__ bool select_warp(const uint32_t* cnt, int hi, int lo,
       int f = -1;
       uint32_t fc = 0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < KPL; ++j) {
         if (f < 0 && rc < static_cast<uint32_t>(k) && rc + cj[j] >= static_cast<uint32_t>(k)) {
-          f = b0 + 4 * lane + j;
+          f = b0 + KPL * lane + j;
           fc = rc + cj[j];
         }
         rc += cj[j];
@@ -611,8 +616,8 @@ __device__ __forceinline__ bool select_warp(const uint32_t* cnt, int hi, int lo,
     for (int b0 = 0; b0 <= imax; b0 += BLK) {
       unsigned long long lm = 0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int i = b0 + 4 * lane + j;
+      for (int j = 0; j < KPL; ++j) {
+        const int i = b0 + KPL * lane + j;
         const uint32_t ci = (i <= imax) ? cnt[i] : 0u;
         if (ci) lm += ci * qfx(key_value(hi - i), M, c);
       }
@@ -629,11 +634,11 @@ __device__ __forceinline__ bool select_warp(const uint32_t* cnt, int hi, int lo,
   uint32_t carry_c = 0;
   unsigned long long carry_m = 0;
   for (int b0 = 0; b0 <= imax; b0 += BLK) {
-    uint32_t cj[4], lc = 0;
-    unsigned long long mj[4], lm = 0;
+    uint32_t cj[KPL], lc = 0;
+    unsigned long long mj[KPL], lm = 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int i = b0 + 4 * lane + j;
+    for (int j = 0; j < KPL; ++j) {
+      const int i = b0 + KPL * lane + j;
       cj[j] = (i <= imax) ? cnt[i] : 0u;
       mj[j] = cj[j] ? cj[j] * qfx(key_value(hi - i), M, c) : 0ull;
       lc += cj[j];
@@ -655,8 +660,8 @@ __device__ __forceinline__ bool select_warp(const uint32_t* cnt, int hi, int lo,
     uint32_t fc = 0;
     unsigned long long fm = 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int i = b0 + 4 * lane + j;
+    for (int j = 0; j < KPL; ++j) {
+      const int i = b0 + KPL * lane + j;
       if (f < 0 && i <= imax && rm < T && (rm + mj[j] >= T || (i == imax && k_on))) {
         f = i;
         fc = rc + cj[j];

@@ -345,9 +345,6 @@ logp_kernel(const KParams P) {
   const bool k_on = (k != -1) && (k < VREAL);
   const bool p_on = (p < 1.0f);
   const bool sel = RESTR && !greedy && (k_on || p_on);
-  // the leader needs the target's logit at the end: start the load now
-  const float xt = (r == 0 && !SAMPLE) ? __uint_as_float(static_cast<uint32_t>(__ldg(rowp + t)) << 16) : 0.0f;
-
   // ---- barriers that peers signal, and the leader's histogram
   if (tid == 0) {
     mbar_init(bar_mid, 1);
@@ -377,6 +374,9 @@ logp_kernel(const KParams P) {
     else asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   cluster_arrive_relaxed();
+  // the leader needs the target's logit at the end: start the load now, after
+  // the cluster fence above (a fence would wait for it)
+  const float xt = (r == 0 && !SAMPLE) ? __uint_as_float(static_cast<uint32_t>(__ldg(rowp + t)) << 16) : 0.0f;
   uint32_t flags = 0;
   if (!mbar_wait_bounded(bar_load)) {
     flags |= FLAG_TIMEOUT;
