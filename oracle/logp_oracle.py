@@ -305,6 +305,33 @@ def logp_grad_row(bits_row: np.ndarray, tau: float, top_p: float, top_k: int, ta
     return grad
 
 
+# ------------------------------------------------------ fused LM head + logprob
+
+def linear_logp_row(h_bits: np.ndarray, w_bits: np.ndarray, tau: float, target: int,
+                    vreal: int = VREAL) -> float:
+    """Full-vocabulary logprob of ``target`` when the logits are the LM head's
+    output h . W^T, formed exactly (fp64 products of bf16 values, fp64 sums).
+
+    The KL reference is the temperature-scaled logprob over the whole real
+    vocabulary ("Configurable H100 consistency runs", KL-reference
+    paragraph); here the logits are not stored first but come straight from
+    the hidden state h [H] and the padded weight W [>= vreal, H] (bf16 bits),
+    whose rows at or beyond ``vreal`` are padding and ignored.  Reading: the
+    logits keep full precision (they are not rounded to bf16), s = logits /
+    tau, full = s_t - logsumexp(s).  tau > 0.
+    """
+    if not (math.isfinite(tau) and tau > 0.0):
+        raise InvalidArgument(f"temperature must be finite and > 0, got {tau}")
+    if not (0 <= target < vreal):
+        raise InvalidArgument(f"target must be in [0, {vreal}), got {target}")
+    h = bf16_bits_to_f32(np.asarray(h_bits, dtype=np.uint16)).astype(np.float64)
+    w = bf16_bits_to_f32(np.asarray(w_bits, dtype=np.uint16)[:vreal]).astype(np.float64)
+    x = w @ h                                   # exact to fp64 rounding of the sums
+    s = x / float(np.float32(tau))
+    m = float(np.max(s))
+    return (float(s[target]) - m) - math.log(math.fsum(np.exp(s - m)))
+
+
 # ----------------------------------------------------------------- sampling
 
 _PHILOX_M = (0xD2511F53, 0xCD9E8D57)   # round multipliers
