@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--linear-steps", type=int, default=10,
+                    help="launches of the fused LM-head logprob timed beside the forward (0: skip)")
     ap.add_argument("--sampler-steps", type=int, default=50,
                     help="launches of the sampler timed beside the forward (0: skip)")
     ap.add_argument("--backward-steps", type=int, default=50,
@@ -456,6 +458,44 @@ def run_ours(args, rank, world, local):
                    "achieved_gbs": s_bytes / (s_ms / 1e3) / 1e9,
                    "frac": s_bytes / (s_ms / 1e3) / 1e9 / peak_s}
 
+    # ---- the LM head fused with the full logprob (tensor cores): hidden
+    #      [T, 4096] (the Qwen3-8B hidden size) and a random padded head
+    #      [152576, 4096], logits never stored
+    linear = None
+    if args.linear_steps > 0:
+        H = 4096
+        gen = torch.Generator(device=dev).manual_seed(rank_seed(9, rank))
+        hid = torch.randn((T_ROWS, H), generator=gen, device=dev).to(torch.bfloat16)
+        wgt = (4.0 / H ** 0.5 * torch.randn((VPAD, H), generator=gen, device=dev)).to(torch.bfloat16)
+        lin_out = torch.empty(T_ROWS, **f32)
+        lin_ws = torch.empty(pkg._binding.linear_workspace_bytes(T_ROWS), dtype=torch.uint8, device=dev)
+
+        def lin_step():
+            pkg.linear_logp(hid, wgt, tg, TAU, out=lin_out, workspace=lin_ws, stream=stream)
+
+        for _ in range(3):
+            lin_step()
+        torch.cuda.synchronize()
+        Kl = args.linear_steps
+        lev = [torch.cuda.Event(enable_timing=True) for _ in range(Kl + 1)]
+        lev[0].record(stream)
+        for i in range(Kl):
+            lin_step()
+            lev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        l_ms = statistics.mean(lev[i].elapsed_time(lev[i + 1]) for i in range(Kl))
+        flops = 2.0 * T_ROWS * H * VPAD
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fpk:
+                bf16_peak, bf16_kind = float(json.load(fpk)["bf16_tflops"]), "measured"
+        except Exception:
+            bf16_peak, bf16_kind = 1900.0, "fallback"
+        linear = {"kernel": "linear_kernel (tcgen05 GEMM + per-tile summaries) + merge",
+                  "hidden": H, "avg_ms": l_ms, "tokens_per_s": T_ROWS / (l_ms / 1e3),
+                  "tflops": flops / (l_ms / 1e3) / 1e12, "bound": "tensor", "peak_tflops": bf16_peak,
+                  "peak_kind": bf16_kind, "frac": flops / (l_ms / 1e3) / 1e12 / bf16_peak}
+        del hid, wgt, lin_ws
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample_rows = np.arange(0, T_ROWS, 7)
@@ -493,6 +533,7 @@ def run_ours(args, rank, world, local):
             "sharded": sharded,
             "backward": backward,
             "sampler": sampler,
+            "linear": linear,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

@@ -270,6 +270,33 @@ rlk_status rlk_sample_noalloc(const rlk_logp_args* args, unsigned long long seed
                               int32_t* out_token, float* out_restr, float* out_full,
                               int32_t* out_support, void* stream);
 
+/* Full-vocabulary logprob straight from the LM head, without storing the
+ * logits (the KL-reference side, "Configurable H100 consistency runs",
+ * KL-reference paragraph: the reference is scaled over the whole real
+ * vocabulary).  x = h . W^T is formed on the tensor cores (bf16 products,
+ * fp32 accumulation in a fixed K order), each 128-row x 256-column tile of x
+ * is reduced to one (max, sum-exp) pair per row, and the 596 tiles of a row
+ * are folded in a fixed order:  full[i] = (x_it - M_i) / tau_i - ln Z_i.
+ * The logits keep fp32 precision (they are not rounded to bf16), so results
+ * differ from rlk_logp_full on bf16 logits by that rounding.
+ *   hidden: bf16 [T, hidden_stride], H columns used; weight: bf16
+ *     [152576, weight_stride] (the padded LM head; rows >= 151936 ignored).
+ *     Both 16-byte aligned, strides multiples of 8 elements; H a multiple of
+ *     64.
+ *   target: int32 [T]; temperature: per-row float [T] or the scalar (> 0).
+ *   out_full: float [T].
+ *   workspace: RLK_LINEAR_WORKSPACE_BYTES(T) bytes of device scratch,
+ *     16-byte aligned (per-row tile summaries and the target's logit).
+ *   Rows with a rejected temperature or target get NaN and count in
+ *     err_count (optional).
+ * Two launches on `stream`. */
+#define RLK_LINEAR_WORKSPACE_BYTES(T) ((size_t)(T) * (596u * 8u + 4u))
+
+rlk_status rlk_linear_logp(const void* hidden, int64_t T, int64_t H, int64_t hidden_stride,
+                           const void* weight, int64_t weight_stride, const int32_t* target,
+                           const float* temperature, float temperature_scalar, float* out_full,
+                           void* workspace, int32_t* err_count, void* stream);
+
 /* ---------------------------------------------------------------------
  * Vocabulary-sharded form: the fixed virtual TP8 partition with each shard
  * in its own buffer, as a tensor-parallel rank would hold it ("Reproduce and

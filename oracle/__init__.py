@@ -8,10 +8,11 @@ from .logp_oracle import (VPAD, VREAL, NSHARD, SHARD_W, InvalidArgument, RowResu
                           row_logprobs_all, restr_for_support_size, logp_batch,
                           shard_summaries, merge_summaries, top_k_mask, top_p_mask,
                           logp_grad_row, philox4x32_10, philox_uniform_bits, sample_row,
-                          SampleResult, linear_logp_row)
+                          SampleResult, linear_logp_row,
+                          linear_logp_rows)
 
 __all__ = ["VPAD", "VREAL", "NSHARD", "SHARD_W", "InvalidArgument", "RowResult",
            "bf16_bits_to_f32", "validate", "scaled_logits", "logp_row", "row_logprobs_all",
            "restr_for_support_size", "logp_batch", "shard_summaries", "merge_summaries",
            "top_k_mask", "top_p_mask", "logp_grad_row", "philox4x32_10", "philox_uniform_bits",
-           "sample_row", "SampleResult", "linear_logp_row"]
+           "sample_row", "SampleResult", "linear_logp_row", "linear_logp_rows"]

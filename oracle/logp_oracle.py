@@ -332,6 +332,25 @@ def linear_logp_row(h_bits: np.ndarray, w_bits: np.ndarray, tau: float, target: 
     return (float(s[target]) - m) - math.log(math.fsum(np.exp(s - m)))
 
 
+def linear_logp_rows(h_bits: np.ndarray, w_bits: np.ndarray, tau, targets, vreal: int = VREAL):
+    """linear_logp_row for several rows (h_bits [n, H]) with the weight widened
+    once: the same definition, row by row."""
+    w = bf16_bits_to_f32(np.asarray(w_bits, dtype=np.uint16)[:vreal]).astype(np.float64)
+    out = np.empty(h_bits.shape[0])
+    for i in range(h_bits.shape[0]):
+        t_i = float(tau[i]) if np.ndim(tau) else float(tau)
+        tgt = int(targets[i])
+        if not (math.isfinite(t_i) and t_i > 0.0):
+            raise InvalidArgument(f"temperature must be finite and > 0, got {t_i}")
+        if not (0 <= tgt < vreal):
+            raise InvalidArgument(f"target must be in [0, {vreal}), got {tgt}")
+        h = bf16_bits_to_f32(np.asarray(h_bits[i], dtype=np.uint16)).astype(np.float64)
+        s = (w @ h) / float(np.float32(t_i))
+        m = float(np.max(s))
+        out[i] = (float(s[tgt]) - m) - math.log(math.fsum(np.exp(s - m)))
+    return out
+
+
 # ----------------------------------------------------------------- sampling
 
 _PHILOX_M = (0xD2511F53, 0xCD9E8D57)   # round multipliers

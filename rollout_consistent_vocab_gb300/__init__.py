@@ -8,10 +8,10 @@ from ._binding import (VOCAB_PADDED, VOCAB_REAL, NUM_SHARDS, SHARD_WIDTH, RlkErr
                        ShardArgs, EXPORTS, load_library, logp_full, logp_pair, logp_restricted,
                        logp_kl, logp_kl_ref, logp_backward, logp_pair_save, logp_backward_saved,
                        logp_autograd, shard_summary,
-                       shard_counts, logp_merge, logp_sharded, sample)
+                       shard_counts, logp_merge, logp_sharded, sample, linear_logp)
 
 __all__ = ["VOCAB_PADDED", "VOCAB_REAL", "NUM_SHARDS", "SHARD_WIDTH", "RlkError", "LogpArgs",
            "ShardArgs",
            "EXPORTS", "load_library", "logp_full", "logp_pair", "logp_restricted", "logp_kl", "logp_kl_ref",
            "logp_backward", "logp_pair_save", "logp_backward_saved", "logp_autograd", "shard_summary", "shard_counts", "logp_merge",
-           "logp_sharded", "sample"]
+           "logp_sharded", "sample", "linear_logp"]

@@ -64,7 +64,7 @@ class ShardArgs(ctypes.Structure):
 
 COMPUTE = ("rlk_logp_full", "rlk_logp_restricted", "rlk_logp_pair", "rlk_logp_kl", "rlk_logp_kl_ref",
            "rlk_logp_backward", "rlk_logp_pair_save", "rlk_logp_backward_saved", "rlk_sample",
-           "rlk_sample_noalloc",
+           "rlk_sample_noalloc", "rlk_linear_logp",
            "rlk_logp_shard_summary", "rlk_logp_shard_counts", "rlk_logp_merge")
 RLK_GRAD_BF16, RLK_GRAD_F32 = 0, 1
 EXPORTS = COMPUTE + ("rlk_status_string", "rlk_last_error", "rlk_abi_version")
@@ -92,6 +92,8 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     lib.rlk_logp_pair_save.argtypes = [A, VP, VP, VP, VP, VP]
     lib.rlk_sample.argtypes = [A, ctypes.c_uint64, VP, VP, VP, VP, VP, VP, VP, VP]
     lib.rlk_sample_noalloc.argtypes = [A, ctypes.c_uint64, VP, VP, VP, VP, VP, VP, VP]
+    i64 = ctypes.c_int64
+    lib.rlk_linear_logp.argtypes = [VP, i64, i64, i64, VP, i64, VP, VP, ctypes.c_float, VP, VP, VP, VP]
     lib.rlk_logp_backward_saved.argtypes = [A, VP, VP, VP, VP, ctypes.c_int64, ctypes.c_int32, VP]
     SA = P(ShardArgs)
     lib.rlk_logp_shard_summary.argtypes = [SA, VP, VP, VP, VP, VP]
@@ -483,3 +485,34 @@ def sample(logits, temperature=1.0, top_p=1.0, top_k=-1, *, seed=0, counter=None
                          _ptr(out_token), _ptr(out_restr), _ptr(out_full), _ptr(out_support),
                          workspace.data_ptr() if T else None, _stream(stream)))
     return out_token, out_restr, out_full, out_support
+
+
+# ------------------------------------------------------------ fused LM head
+
+def linear_workspace_bytes(T: int) -> int:
+    return T * (596 * 8 + 4)
+
+
+def linear_logp(hidden, weight, target, temperature=1.0, *, out=None, workspace=None, err_count=None,
+                stream=None):
+    """Full-vocabulary logprob of each row's target with logits = hidden . weight^T
+    formed on the tensor cores and never stored (hidden: bf16 [T, H]; weight:
+    bf16 [152576, H], the padded LM head)."""
+    lib = load_library()
+    torch = _torch()
+    T, H = hidden.shape
+    for t, name in ((hidden, "hidden"), (weight, "weight")):
+        if t.dtype != torch.bfloat16 or t.dim() != 2 or t.stride(1) != 1 or not t.is_cuda:
+            raise ValueError(f"{name} must be a bf16 CUDA matrix with unit column stride")
+    if weight.shape[0] != VOCAB_PADDED or weight.shape[1] != H:
+        raise ValueError(f"weight must be [{VOCAB_PADDED}, {H}]")
+    if target.dtype != torch.int32 or target.shape != (T,) or not target.is_contiguous():
+        raise ValueError("target must be a contiguous int32 tensor of shape [T]")
+    tp, ts = _param(temperature, T, torch.float32, "temperature")
+    out = _empty(T, torch.float32, hidden) if out is None else out
+    if workspace is None:
+        workspace = torch.empty(max(1, linear_workspace_bytes(T)), dtype=torch.uint8, device=hidden.device)
+    check(lib.rlk_linear_logp(hidden.data_ptr() if T else None, T, H, hidden.stride(0) if T else H,
+                              weight.data_ptr(), weight.stride(0), _ptr(target), tp, ts, _ptr(out),
+                              workspace.data_ptr(), _ptr(err_count), _stream(stream)))
+    return out

@@ -263,3 +263,21 @@ def test_sample_validation(lib):
     assert smp(ws=None) == b.RLK_EINVAL
     assert smp(ws=0x90008) == b.RLK_EALIGN
     assert smp(a=_args(target=None, T=0, logits=None), ctr=None, tok=None, ws=None) == b.RLK_OK
+
+
+def test_linear_logp_validation(lib):
+    L = lambda T=4, H=256, hs=256, w=0xA0000, ws_=256, tg=OUT, tau=1.0, out=OUT, ws=0xB0000, h=0xC0000: \
+        lib.rlk_linear_logp(h, T, H, hs, w, ws_, tg, None, tau, out, ws, None, None)
+    assert L(T=-1) == b.RLK_EINVAL
+    assert L(T=0, h=None, w=None, tg=None, out=None, ws=None) == b.RLK_OK
+    assert L(H=100) == b.RLK_EINVAL             # not a multiple of 64
+    assert L(H=0) == b.RLK_EINVAL
+    assert L(hs=128) == b.RLK_EINVAL            # stride < H
+    assert L(hs=260) == b.RLK_EALIGN            # rows 520 bytes apart
+    assert L(h=0xC0008) == b.RLK_EALIGN
+    assert L(w=None) == b.RLK_EINVAL
+    assert L(tau=0.0) == b.RLK_EINVAL           # greedy is not a full-vocabulary logprob here
+    assert L(tau=float("inf")) == b.RLK_EINVAL
+    assert L(ws=None) == b.RLK_EINVAL
+    assert L(ws=0xB0004) == b.RLK_EALIGN
+    assert L(out=None) == b.RLK_EINVAL
