@@ -8,10 +8,11 @@
 // one (max, sum-exp) pair per row, summaries of fixed column tiles combined in
 // a fixed vocabulary order afterwards.
 //
-// linear_kernel: one CTA per (128-row, 256-column) output tile.
+// linear_kernel: persistent, one CTA per SM over (128-row, 256-column)
+// output tiles.
 //   warp 0, one thread   TMA producer: A (h, 128 x 64 bf16) and B (W, 256 x 64
 //                        bf16) tiles, 128-byte swizzle, into a 4-stage ring;
-//   warp 1               TMEM allocation (256 columns, the fp32 accumulator);
+//   warp 1               TMEM allocation (512 columns: two fp32 accumulators);
 //                        one thread issues tcgen05.mma (M 128, N 256, K 16,
 //                        bf16 in, fp32 accumulate) and commits each stage
 //                        back to the producer, then the tile to the epilogue;
@@ -143,6 +144,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 
 // ------------------------------------------------------------ kernels
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
+// Persistent: one CTA per SM walks the tiles tile = blockIdx.x + i * gridDim.x
+// (row tiles fastest, so the CTAs running at one time share a vocabulary tile
+// and its weight is read from HBM once).  The TMA ring runs on across tiles;
+// two TMEM accumulators (columns 0-255 and 256-511) let the MMA thread fill
+// one while the epilogue warps drain the other.
 __global__ void __launch_bounds__(LIN_THREADS, 1)
 linear_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
               const LinArgs P) {
@@ -151,25 +161,28 @@ linear_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant_
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;              // 1024-byte aligned ring
   const uint32_t bars = base + LSTAGES * STAGE_BYTES;
-  const uint32_t full0 = bars, empty0 = bars + 8 * LSTAGES, tfull = bars + 16 * LSTAGES;
-  const uint32_t slot = tfull + 8;                            // TMEM address written by the allocation
+  const uint32_t full0 = bars, empty0 = bars + 8 * LSTAGES;
+  const uint32_t accf0 = bars + 16 * LSTAGES, acce0 = accf0 + 16;   // accumulator full / empty, x2
+  const uint32_t slot = acce0 + 16;                           // TMEM address written by the allocation
   uint32_t* slot_ptr = reinterpret_cast<uint32_t*>(smem_raw + (slot - raw));
   uint32_t* flag_ptr = slot_ptr + 1;                          // a wait gave up
-  const int m_tile = static_cast<int>(blockIdx.x % P.mt);
-  const int n_tile = static_cast<int>(blockIdx.x / P.mt);
+  const int ntiles = P.mt * NTILE;
 
   if (tid == 0) {
     for (int s = 0; s < LSTAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
-    mbar_init(tfull, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf0 + 8 * b, 1);
+      mbar_init(acce0 + 8 * b, 4);                            // one arrival per epilogue warp
+    }
     *flag_ptr = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 1) {
-    tmem_alloc(slot, 256);
+    tmem_alloc(slot, 512);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -178,78 +191,97 @@ linear_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant_
   const uint32_t tmem = *slot_ptr;
 
   if (warp == 0 && lane == 0) {
-    // ---- producer
-    for (int kb = 0; kb < P.nk; ++kb) {
-      const int s = kb % LSTAGES;
-      if (kb >= LSTAGES && !mbar_wait_parity_bounded(empty0 + 8 * s, ((kb / LSTAGES) - 1) & 1)) {
-        *flag_ptr = 1u;
-        break;
+    // ---- producer: every K stage of every tile of this CTA through the ring
+    uint32_t it = 0;
+    for (int tile = blockIdx.x; tile < ntiles && !*flag_ptr; tile += gridDim.x) {
+      const int m_tile = tile % P.mt, n_tile = tile / P.mt;
+      for (int kb = 0; kb < P.nk; ++kb, ++it) {
+        const uint32_t s = it % LSTAGES;
+        if (it >= LSTAGES && !mbar_wait_parity_bounded(empty0 + 8 * s, ((it / LSTAGES) - 1) & 1)) {
+          *flag_ptr = 1u;
+          break;
+        }
+        const uint32_t a = base + s * STAGE_BYTES, b = a + A_BYTES;
+        mbar_arrive_expect_tx(full0 + 8 * s, STAGE_BYTES);
+        tma_load_2d(a, &tmap_a, kb * LK, m_tile * LM, full0 + 8 * s);
+        tma_load_2d(b, &tmap_b, kb * LK, n_tile * LN, full0 + 8 * s);
       }
-      const uint32_t a = base + s * STAGE_BYTES, b = a + A_BYTES;
-      mbar_arrive_expect_tx(full0 + 8 * s, STAGE_BYTES);
-      tma_load_2d(a, &tmap_a, kb * LK, m_tile * LM, full0 + 8 * s);
-      tma_load_2d(b, &tmap_b, kb * LK, n_tile * LN, full0 + 8 * s);
     }
   } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer
-    for (int kb = 0; kb < P.nk; ++kb) {
-      const int s = kb % LSTAGES;
-      if (!mbar_wait_parity_bounded(full0 + 8 * s, (kb / LSTAGES) & 1)) {
-        *flag_ptr = 1u;
-        break;
-      }
+    // ---- MMA issuer: tile j accumulates in buffer j & 1
+    uint32_t it = 0, j = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+      const uint32_t buf = j & 1;
+      if (j >= 2 && !mbar_wait_parity_bounded(acce0 + 8 * buf, ((j >> 1) - 1) & 1)) *flag_ptr = 1u;
       tc_fence_after();
-      const uint32_t a = base + s * STAGE_BYTES, b = a + A_BYTES;
-      const uint64_t ad = sw128_desc(a), bd = sw128_desc(b);
+      const uint32_t d = tmem + buf * 256;
+      for (int kb = 0; kb < P.nk; ++kb, ++it) {
+        const uint32_t s = it % LSTAGES;
+        if (!*flag_ptr && !mbar_wait_parity_bounded(full0 + 8 * s, (it / LSTAGES) & 1)) *flag_ptr = 1u;
+        if (*flag_ptr) continue;                              // keep the phase count, issue nothing
+        tc_fence_after();
+        const uint32_t a = base + s * STAGE_BYTES, b = a + A_BYTES;
+        const uint64_t ad = sw128_desc(a), bd = sw128_desc(b);
 #pragma unroll
-      for (int k = 0; k < LK / 16; ++k)       // +32 bytes along K per step: +2 in the address field
-        umma_bf16(tmem, ad + 2 * k, bd + 2 * k, (kb | k) != 0 ? 1u : 0u);
-      umma_commit(empty0 + 8 * s);
+        for (int k = 0; k < LK / 16; ++k)                     // +32 bytes along K: +2 in the address field
+          umma_bf16(d, ad + 2 * k, bd + 2 * k, (kb | k) != 0 ? 1u : 0u);
+        umma_commit(empty0 + 8 * s);
+      }
+      umma_commit(accf0 + 8 * buf);
     }
-    umma_commit(tfull);
   } else if (warp >= 4) {
-    // ---- epilogue: thread = row of the tile
+    // ---- epilogue: thread = row of the tile (TMEM lane)
     const int ew = warp - 4;
-    const int64_t row = static_cast<int64_t>(m_tile) * LM + ew * 32 + lane;
-    const bool live = row < P.T;
-    const bool ok = mbar_wait_parity_bounded(tfull, 0);
-    tc_fence_after();
-    const float tau = live ? (P.tau_arr ? P.tau_arr[row] : P.tau_s) : 1.0f;
-    const float c = __fdiv_rn(LOG2E, tau);
-    const int tcol = live ? P.target[row] - n_tile * LN : -1;
-    float m = -INFINITY, l = 0.0f, xt = __int_as_float(0x7fc00000);
-    const uint32_t trow = tmem + (static_cast<uint32_t>(ew * 32) << 16);
+    uint32_t j = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+      const int m_tile = tile % P.mt, n_tile = tile / P.mt;
+      const uint32_t buf = j & 1;
+      const bool ok = mbar_wait_parity_bounded(accf0 + 8 * buf, (j >> 1) & 1);
+      tc_fence_after();
+      const int64_t row = static_cast<int64_t>(m_tile) * LM + ew * 32 + lane;
+      const bool live = row < P.T;
+      const float tau = live ? (P.tau_arr ? P.tau_arr[row] : P.tau_s) : 1.0f;
+      const float c = __fdiv_rn(LOG2E, tau);
+      const int tcol = live ? P.target[row] - n_tile * LN : -1;
+      float m = -INFINITY, l = 0.0f, xt = __int_as_float(0x7fc00000);
+      const uint32_t trow = tmem + buf * 256 + (static_cast<uint32_t>(ew * 32) << 16);
 #pragma unroll 1
-    for (int ch = 0; ch < LN / 32; ++ch) {
-      float v[32];
-      tmem_ld32(trow + ch * 32, v);            // warp-collective: every lane takes part
-      const int col0 = n_tile * LN + ch * 32;
-      float cmax = -INFINITY;
+      for (int ch = 0; ch < LN / 32; ++ch) {
+        float v[32];
+        tmem_ld32(trow + ch * 32, v);                         // warp-collective: every lane takes part
+        if (ch == LN / 32 - 1) {                              // the accumulator is read: hand it back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acce0 + 8 * buf);
+        }
+        const int col0 = n_tile * LN + ch * 32;
+        float cmax = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        if (col0 + j < VREAL) cmax = fmaxf(cmax, v[j]);
-        if (tcol == ch * 32 + j) xt = v[j];
-      }
-      if (cmax > m) {
-        l = l * ex2((m - cmax) * c);
-        m = cmax;
-      }
+        for (int jj = 0; jj < 32; ++jj) {
+          if (col0 + jj < VREAL) cmax = fmaxf(cmax, v[jj]);
+          if (tcol == ch * 32 + jj) xt = v[jj];
+        }
+        if (cmax > m) {
+          l = l * ex2((m - cmax) * c);
+          m = cmax;
+        }
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (col0 + j < VREAL) l += ex2((v[j] - m) * c);
-    }
-    if (live) {
-      const bool good = ok && *flag_ptr == 0u;
-      P.ws_ml[row * NTILE + n_tile] = good ? make_float2(m, l) : make_float2(__int_as_float(0x7fc00000), 0.0f);
-      if (tcol >= 0 && tcol < LN) P.ws_xt[row] = xt;
-      if (!good && P.err && n_tile == 0) atomicAdd(P.err, 1);
+        for (int jj = 0; jj < 32; ++jj)
+          if (col0 + jj < VREAL) l += ex2((v[jj] - m) * c);
+      }
+      if (live) {
+        const bool good = ok && *flag_ptr == 0u;
+        P.ws_ml[row * NTILE + n_tile] = good ? make_float2(m, l) : make_float2(__int_as_float(0x7fc00000), 0.0f);
+        if (tcol >= 0 && tcol < LN) P.ws_xt[row] = xt;
+        if (!good && P.err && n_tile == 0) atomicAdd(P.err, 1);
+      }
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -374,8 +406,13 @@ rlk_status rlk_linear_logp(const void* hidden, int64_t T, int64_t H, int64_t hid
     if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     configured[dev] = true;
   }
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+  const int64_t ntiles = static_cast<int64_t>(P.mt) * NTILE;
+  const unsigned grid = static_cast<unsigned>(ntiles < sms ? ntiles : sms);   // one CTA per SM
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  linear_kernel<<<static_cast<unsigned>(P.mt) * NTILE, LIN_THREADS, LIN_SMEM, st>>>(ta, tb, P);
+  linear_kernel<<<grid, LIN_THREADS, LIN_SMEM, st>>>(ta, tb, P);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(RLK_ECUDA, "kernel launch: %s", cudaGetErrorString(e));
   merge_lin_kernel<<<static_cast<unsigned>((T + 3) / 4), 128, 0, st>>>(P, out_full);
