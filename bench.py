@@ -1,8 +1,9 @@
 """Throughput of the strict token-logprob step on GB300.
 
-One step = the whole hot path over one batch: the policy pass (full-vocabulary
-and top-k-then-top-p restricted logprobs from 8 virtual-shard summaries) and
-the reference pass with the per-row KL term, on the T = 8192 workload
+One step = the whole hot path over one batch, one rlk_logp_kl call: the policy
+pass (full-vocabulary and top-k-then-top-p restricted logprobs from 8
+virtual-shard summaries) and the reference full pass, as alternating clusters
+of one launch, then the per-row KL term, on the T = 8192 workload
 (4N(0,1) logits + hot sets of 1..256 columns, tau 1.3, top-p 0.99,
 top-k 128, reference = policy + N(0, 0.05^2)).  Inputs are synthetic and
 resident in HBM (5.0 GB per step, far above the 129 MB L2, so no flush).
@@ -37,7 +38,7 @@ WORKLOAD = "c2_hot1-256_T8192_policy+ref_kl"
 # the fused kernel's sources: its own file and the device code it includes
 KERNEL_SRCS = [os.path.join(ROOT, "rollout_consistent_vocab_gb300", "csrc", f)
                for f in ("rlk_logp.cu", "rlk_device.cuh")]
-NCU_SUMMARY = os.path.join(ROOT, "profiles", "logp_pair_kernel_c2.md")
+NCU_SUMMARY = os.path.join(ROOT, "profiles", "logp_kl_step_c2.md")
 
 
 def parse():
@@ -107,8 +108,9 @@ def kernel_sha() -> str:
 
 
 def ncu_traffic():
-    """DRAM bytes per launch of the pair kernel from the committed ncu summary,
-    or None when the summary is missing or the kernel source changed since."""
+    """DRAM bytes per launch of the step's kernel (the interleaved policy +
+    reference launch) from the committed ncu summary, or None when the summary
+    is missing or the kernel source changed since."""
     try:
         text = open(NCU_SUMMARY).read()
     except OSError:
@@ -264,37 +266,48 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.current_stream()
 
     def step():
-        pkg.logp_pair(x, tg, TAU, TOP_P, TOP_K, out_full=full, out_restr=restr, out_support=sup,
-                      stream=stream)
-        pkg.logp_kl_ref(ref, tg, full, TAU, out_full_ref=full_ref, out_kl=kl, stream=stream)
+        # one call: the policy pair pass and the reference full pass as
+        # alternating clusters of one launch, then the KL difference
+        pkg.logp_kl(x, ref, tg, TAU, TOP_P, TOP_K, out_full=full, out_restr=restr, out_support=sup,
+                    out_full_ref=full_ref, out_kl=kl, stream=stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     smi_index = vis.split(",")[local] if vis else str(local)
     with ClockSampler(smi_index) as clk:
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
+        ev[0].record(stream)
         for i in range(K):
-            ev[i][0].record(stream)
-            pkg.logp_pair(x, tg, TAU, TOP_P, TOP_K, out_full=full, out_restr=restr,
-                          out_support=sup, stream=stream)
-            ev[i][1].record(stream)
-            pkg.logp_kl_ref(ref, tg, full, TAU, out_full_ref=full_ref, out_kl=kl, stream=stream)
-            ev[i][2].record(stream)
+            step()
+            ev[i + 1].record(stream)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
-    pair_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    ref_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    total_ms = ev[0].elapsed_time(ev[K])
     total_ms = max_over_ranks(total_ms, dev)
     value = throughput(world, T_ROWS, K, total_ms)
+
+    # ---- the policy pair pass alone (the full + restricted pass whose HBM
+    #      fraction is the roofline figure), and the reference pass alone
+    Kp = min(K, 300)
+    pev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * Kp + 1)]
+    pev[0].record(stream)
+    for i in range(Kp):
+        pkg.logp_pair(x, tg, TAU, TOP_P, TOP_K, out_full=full, out_restr=restr, out_support=sup,
+                      stream=stream)
+        pev[2 * i + 1].record(stream)
+        pkg.logp_kl_ref(ref, tg, full, TAU, out_full_ref=full_ref, out_kl=kl, stream=stream)
+        pev[2 * i + 2].record(stream)
+    torch.cuda.synchronize()
+    pair_ms = [pev[2 * i].elapsed_time(pev[2 * i + 1]) for i in range(Kp)]
+    ref_ms = [pev[2 * i + 1].elapsed_time(pev[2 * i + 2]) for i in range(Kp)]
 
     # ---- end to end through the public API from pinned host buffers
     e2e = None
@@ -510,23 +523,31 @@ def run_ours(args, rank, world, local):
     if rank == 0:
         peak, peak_kind = measured_peak()
         pair_avg = statistics.mean(pair_ms)
-        algo_bytes = T_ROWS * VPAD * 2
-        achieved = algo_bytes / (pair_avg / 1e3) / 1e9
+        algo_bytes = T_ROWS * VPAD * 2                 # one pass over the logits
+        step_ms = total_ms / K
+        step_bytes = 2 * algo_bytes                    # policy + reference logits
+        achieved = step_bytes / (step_ms / 1e3) / 1e9
         traffic = ncu_traffic()
         ref_avg = statistics.mean(ref_ms)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-            "warmup": max(args.warmup, 3), "ms_per_step": total_ms / K, "higher_is_better": True,
+            "warmup": max(args.warmup, 3), "ms_per_step": step_ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": workload_config(),
-            "roofline": {"bound": "hbm", "kernel": "logp_kernel<true> (policy pair pass)",
+            "roofline": {"bound": "hbm",
+                         "kernel": "logp_kernel<true> (rlk_logp_kl: policy pair and reference full "
+                                   "passes as alternating clusters of one launch; the step's 32 KB "
+                                   "kl_kernel is counted in its time)",
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
-                         "traffic": traffic, "algorithmic_bytes_per_launch": algo_bytes,
-                         "avg_launch_ms": pair_avg},
+                         "traffic": traffic, "algorithmic_bytes_per_launch": step_bytes,
+                         "avg_launch_ms": step_ms},
+            "pair_pass": {"kernel": "logp_kernel<true> (policy pair pass alone: full + restricted)",
+                          "avg_launch_ms": pair_avg,
+                          "achieved_gbs": algo_bytes / (pair_avg / 1e3) / 1e9,
+                          "frac": algo_bytes / (pair_avg / 1e3) / 1e9 / peak},
             "ref_pass": {"avg_launch_ms": ref_avg,
                          "achieved_gbs": algo_bytes / (ref_avg / 1e3) / 1e9},
-            "step_hbm_gbs": 2 * algo_bytes * K / (total_ms / 1e3) / 1e9,
             "gpu_launches": 2 * K,
             "clocks": clk.summary(),
             "e2e": e2e,

@@ -141,8 +141,12 @@ rlk_status rlk_logp_pair(const rlk_logp_args* args, float* out_full, float* out_
  * KL-reference paragraph).  ref_logits follows the same layout rules as
  * args->logits with its own ref_row_stride.  out_full, out_full_ref and
  * out_kl are required; out_restr and out_support may be NULL.  Two launches
- * on `stream`: the policy pass, then the reference pass, whose epilogue
- * forms the difference. */
+ * on `stream`: one cluster launch over 2T rows in which even clusters
+ * resolve policy row i (full and restricted) and odd clusters the same
+ * row's reference logits (full only), then a small kernel that forms the
+ * difference.  Each row's results are bit-identical to rlk_logp_pair
+ * followed by rlk_logp_kl_ref.  RLK_EINVAL when T >= 2^27 (the doubled
+ * cluster count must stay below 2^31 CTAs). */
 rlk_status rlk_logp_kl(const rlk_logp_args* policy, const void* ref_logits,
                        int64_t ref_row_stride, float* out_full, float* out_restr,
                        int32_t* out_support, float* out_full_ref, float* out_kl,

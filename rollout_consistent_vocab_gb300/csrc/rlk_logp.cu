@@ -129,6 +129,10 @@ struct KParams {
   int32_t* out_token;
   struct SampMsg* out_samp;     // resolution pass: per-row record for the draw
   const struct SampMsg* in_samp;
+  // rlk_logp_kl: the reference logits, interleaved with the policy rows
+  const uint16_t* ref_logits;
+  int64_t ref_stride;
+  float* out_full_ref;
 };
 
 enum { MODE_FWD = 0, MODE_BWD = 1, MODE_SAMPLE = 2 };
@@ -285,10 +289,20 @@ logp_kernel(const KParams P) {
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
   const uint32_t r = cluster_rank();
-  const int64_t row = blockIdx.x / NSHARD;
+  // rlk_logp_kl's single launch: clusters alternate between the policy pair
+  // pass of row i and the reference full pass of row i (a latency-bound and a
+  // bandwidth-bound workload sharing the SMs)
+  const int64_t cid = blockIdx.x / NSHARD;
+  const bool pair_kl = MODE == MODE_FWD && P.ref_logits != nullptr;
+  const bool is_ref = pair_kl && (cid & 1);
+  const int64_t row = pair_kl ? (cid >> 1) : cid;
+  float* const o_full = is_ref ? P.out_full_ref : P.out_full;
+  float* const o_restr = is_ref ? nullptr : P.out_restr;
+  int32_t* const o_support = is_ref ? nullptr : P.out_support;
+  int32_t* const o_err = is_ref ? nullptr : P.err;
 
   const int nchunks = (r == NSHARD - 1) ? LAST_CHUNKS : SHARD_CHUNKS;
-  const uint16_t* rowp = P.logits + row * P.stride;
+  const uint16_t* rowp = is_ref ? P.ref_logits + row * P.ref_stride : P.logits + row * P.stride;
   const uint32_t bar_load = smem_addr(&S.bar_load);
   const uint32_t bar_mid = smem_addr(&S.bar_mid);
   const uint32_t bar_sum = smem_addr(&S.bar_sum);
@@ -314,8 +328,8 @@ logp_kernel(const KParams P) {
 
   // ---- row parameters (every CTA of the cluster takes the same decisions)
   const float tau = P.tau_arr ? P.tau_arr[row] : P.tau_s;
-  const float p = RESTR ? (P.p_arr ? P.p_arr[row] : P.p_s) : 1.0f;
-  const int k = RESTR ? (P.k_arr ? P.k_arr[row] : P.k_s) : -1;
+  const float p = (RESTR && !is_ref) ? (P.p_arr ? P.p_arr[row] : P.p_s) : 1.0f;
+  const int k = (RESTR && !is_ref) ? (P.k_arr ? P.k_arr[row] : P.k_s) : -1;
   const int t = SAMPLE ? 0 : P.target[row];     // the sampler's pass has no target
   const bool valid = (tau >= 0.0f) && (tau <= 3.402823466e38f) && (p > 0.0f) && (p <= 1.0f) &&
                      (k == -1 || (k >= 1 && k <= VREAL)) && (t >= 0) && (t < VREAL);
@@ -324,16 +338,16 @@ logp_kernel(const KParams P) {
       // the copy writes this CTA's shared memory: let it land before leaving
       mbar_wait_bounded(bar_load);
       if (r == 0) {
-        if (P.out_full) P.out_full[row] = __int_as_float(0x7fc00000);
-        if (RESTR && P.out_restr) P.out_restr[row] = __int_as_float(0x7fc00000);
-        if (RESTR && P.out_support) P.out_support[row] = -1;
+        if (o_full) o_full[row] = __int_as_float(0x7fc00000);
+        if (RESTR && o_restr) o_restr[row] = __int_as_float(0x7fc00000);
+        if (RESTR && o_support) o_support[row] = -1;
         if (P.out_kl) P.out_kl[row] = __int_as_float(0x7fc00000);
         if (P.out_stats) P.out_stats[row] = nan_stats();
         if (SAMPLE) {
           P.out_token[row] = -1;
           P.out_samp[row] = SampMsg{};     // nothing to draw
         }
-        if (P.err) atomicAdd(P.err, 1);
+        if (o_err) atomicAdd(o_err, 1);
       }
     }
     if (BWD)
@@ -629,11 +643,11 @@ logp_kernel(const KParams P) {
   }
 
   if (tid == 0 && !SAMPLE) {
-    if (P.out_full) P.out_full[row] = full;
-    if (RESTR && P.out_restr) P.out_restr[row] = restr;
-    if (RESTR && P.out_support) P.out_support[row] = support;
+    if (o_full) o_full[row] = full;
+    if (RESTR && o_restr) o_restr[row] = restr;
+    if (RESTR && o_support) o_support[row] = support;
     if (P.out_kl) P.out_kl[row] = P.kl_policy_full[row] - full;
-    if (timed_out && P.err) atomicAdd(P.err, 1);
+    if (timed_out && o_err) atomicAdd(o_err, 1);
   }
 
   if (BWD || P.out_stats) {
@@ -724,6 +738,12 @@ sample_kernel(const KParams P) {
   if (!mbar_wait_bounded(bar_load)) mbar_wait_bounded(bar_load);
   cluster_wait();                             // every peer's barrier is ready for the masses
   sample_shard(S, P, row, r, S.shard, nchunks, m, tau, bar_zr);
+}
+
+// The KL term of each row: the policy's full logprob minus the reference's.
+__global__ void kl_kernel(const float* full, const float* full_ref, float* kl, int64_t T) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < T) kl[i] = full[i] - full_ref[i];
 }
 
 // ------------------------------------------------------------ host side
@@ -830,20 +850,22 @@ rlk_status rlk_logp_kl(const rlk_logp_args* policy, const void* ref_logits, int6
   if ((s = check_out(out_kl, "out_kl", true)) != RLK_OK) return s;
   if ((s = check_out(out_restr, "out_restr", false)) != RLK_OK) return s;
   if ((s = check_out(out_support, "out_support", false)) != RLK_OK) return s;
+  if (policy->T >= (int64_t(1) << 27))
+    return fail(RLK_EINVAL, "T = %lld: at most 2^27 - 1 rows per rlk_logp_kl call", (long long)policy->T);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   KParams P = make_params(policy);
   P.out_full = out_full;
   P.out_restr = out_restr;
   P.out_support = out_support;
-  if ((s = launch<true>(P, policy->T, st)) != RLK_OK) return s;
-  KParams R = make_params(policy);
-  R.logits = static_cast<const uint16_t*>(ref_logits);
-  R.stride = ref_row_stride;
-  R.out_full = out_full_ref;
-  R.kl_policy_full = out_full;
-  R.out_kl = out_kl;
-  R.err = nullptr;   // the policy pass already counted rejected rows
-  return launch<false>(R, policy->T, st);
+  P.ref_logits = static_cast<const uint16_t*>(ref_logits);
+  P.ref_stride = ref_row_stride;
+  P.out_full_ref = out_full_ref;
+  if ((s = launch<true>(P, 2 * policy->T, st)) != RLK_OK) return s;
+  kl_kernel<<<static_cast<unsigned>((policy->T + 255) / 256), 256, 0, st>>>(out_full, out_full_ref, out_kl,
+                                                                             policy->T);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(RLK_ECUDA, "kernel launch: %s", cudaGetErrorString(e));
+  return RLK_OK;
 }
 
 rlk_status rlk_logp_kl_ref(const rlk_logp_args* ref, const float* full_policy,
