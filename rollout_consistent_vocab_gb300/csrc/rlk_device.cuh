@@ -276,6 +276,50 @@ __device__ __forceinline__ int pass_max(const uint4* sh, int tid, int nchunks,
   return okey_of(fmaxf(__low2float(m2), __high2float(m2)));
 }
 
+// Two bf16 NaN tests on raw bits: a bf16 is NaN iff its magnitude bits
+// exceed 0x7F80, i.e. iff adding 0x7F to them carries into bit 15 (no carry
+// crosses into the other half).
+__device__ __forceinline__ uint32_t nan_bits2(uint32_t w) {
+  return ((w & 0x7FFF7FFFu) + 0x007F007Fu) & 0x80008000u;
+}
+
+// Greedy rows, and rows whose shard maximum is -inf, get no sum-exp, so a NaN
+// must be found by a scan: it tests the raw bits of this thread's chunks.
+// For greedy rows it also returns this thread's lowest column (in shard
+// coordinates) equal to the shard maximum xm, looking only inside the chunks
+// whose register maximum reaches xm (0x7fffffff: none).
+__device__ __forceinline__ int scan_nan_first(const uint4* sh, int tid, int nchunks,
+                                              const __nv_bfloat162 (&cm)[MAXCH], float xm,
+                                              bool want_first, bool& nan_seen) {
+  uint32_t hit = 0;               // chunks (by register slot) whose maximum reaches xm
+  if (want_first && xm > -INFINITY) {
+    const __nv_bfloat162 xm2 = __floats2bfloat162_rn(xm, xm);   // xm is a bf16 value
+#pragma unroll
+    for (int i = 0; i < MAXCH; ++i)
+      if (__hge2_mask(cm[i], xm2) != 0u) hit |= 1u << i;       // absent chunks hold -inf
+  }
+  uint32_t nb = 0;
+#pragma unroll 2
+  for (int ch = tid; ch < nchunks; ch += NTHR) {
+    const uint4 v = sh[ch];
+    nb |= nan_bits2(v.x) | nan_bits2(v.y) | nan_bits2(v.z) | nan_bits2(v.w);
+  }
+  nan_seen = nb != 0u;
+  int f = 0x7fffffff;
+  while (hit) {
+    const int ch = tid + (__ffs(hit) - 1) * NTHR;
+    hit &= hit - 1;
+    const uint4 v = sh[ch];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 7; j >= 0; --j) {
+      const float x = (j & 1) ? bf16_hi(w[j >> 1]) : bf16_lo(w[j >> 1]);
+      if (x == xm) f = min(f, ch * 8 + j);
+    }
+  }
+  return f;
+}
+
 // This thread's share of the shard sum-exp: exp(s_j - m) over its chunks in
 // chunk order, even and odd columns in the two lanes of a packed f32x2
 // accumulator; c = log2(e) / tau.  block_sum_fixed completes the tree.

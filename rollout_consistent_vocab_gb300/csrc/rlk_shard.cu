@@ -154,18 +154,8 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM) shard_summary_kernel(const 
   uint32_t first = 0x7fffffffu;
   if (rp.greedy || xm == -INFINITY) {
     // greedy: first column of this shard holding its maximum; both: NaN scan
-    bool nan_seen = false;
-    int f = 0x7fffffff;
-    for (int ch = tid; ch < nchunks; ch += NTHR) {
-      const uint4 v = sh[ch];
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int j = 7; j >= 0; --j) {
-        const float x = (j & 1) ? bf16_hi(w[j >> 1]) : bf16_lo(w[j >> 1]);
-        nan_seen |= (x != x);
-        if (x == xm) f = min(f, ch * 8 + j);
-      }
-    }
+    bool nan_seen;
+    int f = scan_nan_first(sh, tid, nchunks, cm, xm, rp.greedy, nan_seen);
     if (__syncthreads_or(nan_seen)) bad = true;
     if (rp.greedy) {
       f = block_min_int(f, S);
