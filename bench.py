@@ -58,6 +58,8 @@ def parse():
                     help="launches of the backward pass timed beside the forward (0: skip)")
     ap.add_argument("--sharded-steps", type=int, default=50,
                     help="steps of the vocabulary-sharded form timed beside the fused pass (0: skip)")
+    ap.add_argument("--norm-steps", type=int, default=20,
+                    help="calls of the deterministic gradient norm timed per size (0: skip)")
     ap.add_argument("--rows", type=int, default=T_ROWS,
                     help="rows per GPU (default: the 8192-row workload; smaller only for profiling)")
     return ap.parse_args()
@@ -509,6 +511,54 @@ def run_ours(args, rank, world, local):
                   "peak_kind": bf16_kind, "frac": flops / (l_ms / 1e3) / 1e12 / bf16_peak}
         del hid, wgt, lin_ws
 
+    # ---- the deterministic gradient norm (exact FP32 squares in integer
+    #      exponent bins): 10M BF16 elements (the size the pages time), with
+    #      L2 flushed before each call and without, and 2^31-element BF16 /
+    #      2^30-element FP32 gradients for the HBM roofline
+    gnorm = None
+    if args.norm_steps > 0:
+        gen = torch.Generator(device=dev).manual_seed(rank_seed(10, rank))
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        nbins = pkg.norm_bins(dev)
+        nout = torch.empty(2, dtype=torch.float64, device=dev)
+
+        def norm_ms(t, do_flush):
+            for _ in range(3):
+                pkg.grad_norm(t, bins=nbins, out=nout, stream=stream)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.norm_steps)]
+            for a, b in evs:
+                if do_flush:
+                    flush.fill_(1)             # a 256 MB write: L2 keeps none of t
+                a.record(stream)
+                pkg.grad_norm(t, bins=nbins, out=nout, stream=stream)
+                b.record(stream)
+            torch.cuda.synchronize()
+            return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+        g10 = (1e-2 * torch.randn(10_000_000, generator=gen, device=dev)).to(torch.bfloat16)
+        cold, warm = norm_ms(g10, True), norm_ms(g10, False)
+        del g10
+        gnorm = {"kernel": "sqnorm_kernel (128-bit fixed-point per thread, exact exponent bins) + finalize",
+                 "calls": "one grad_norm call = clear bins + accumulate + finalize, median of "
+                          f"{args.norm_steps}",
+                 "bf16_10m": {"ms_l2_flushed": cold, "ms_l2_warm": warm,
+                              "pages_h100_ms": 0.36,
+                              "note": "the pages' 10M-element BF16-derived FP32 norm on H100 (context)"}}
+        for name, n_el, dt in (("bf16_2e31", 1 << 31, torch.bfloat16), ("f32_2e30", 1 << 30, torch.float32)):
+            big = torch.empty(n_el, dtype=dt, device=dev)
+            for a0 in range(0, n_el, 1 << 28):
+                big[a0:a0 + (1 << 28)] = torch.randn(min(1 << 28, n_el - a0), generator=gen, device=dev)
+            ms = norm_ms(big, False)
+            nbytes = n_el * big.element_size()
+            peak_n, peak_kind_n = measured_peak()
+            gnorm[name] = {"ms": ms, "bytes": nbytes, "achieved_gbs": nbytes / (ms / 1e3) / 1e9,
+                           "bound": "hbm", "peak": peak_n, "peak_kind": peak_kind_n,
+                           "frac": nbytes / (ms / 1e3) / 1e9 / peak_n}
+            del big
+        del flush
+        torch.cuda.empty_cache()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample_rows = np.arange(0, T_ROWS, 7)
@@ -555,6 +605,7 @@ def run_ours(args, rank, world, local):
             "backward": backward,
             "sampler": sampler,
             "linear": linear,
+            "grad_norm": gnorm,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

@@ -65,7 +65,8 @@ class ShardArgs(ctypes.Structure):
 COMPUTE = ("rlk_logp_full", "rlk_logp_restricted", "rlk_logp_pair", "rlk_logp_kl", "rlk_logp_kl_ref",
            "rlk_logp_backward", "rlk_logp_pair_save", "rlk_logp_backward_saved", "rlk_sample",
            "rlk_sample_noalloc", "rlk_linear_logp",
-           "rlk_logp_shard_summary", "rlk_logp_shard_counts", "rlk_logp_merge")
+           "rlk_logp_shard_summary", "rlk_logp_shard_counts", "rlk_logp_merge",
+           "rlk_sqnorm_accumulate", "rlk_sqnorm_finalize", "rlk_grad_norm")
 RLK_GRAD_BF16, RLK_GRAD_F32 = 0, 1
 EXPORTS = COMPUTE + ("rlk_status_string", "rlk_last_error", "rlk_abi_version")
 
@@ -101,6 +102,9 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     f32, i32 = ctypes.c_float, ctypes.c_int32
     lib.rlk_logp_merge.argtypes = [VP, VP, VP, VP, ctypes.c_int64, VP, VP, f32, VP, f32, VP, i32,
                                    VP, i32, VP, VP, VP, VP]
+    lib.rlk_sqnorm_accumulate.argtypes = [VP, i64, i32, VP, VP]
+    lib.rlk_sqnorm_finalize.argtypes = [VP, VP, VP]
+    lib.rlk_grad_norm.argtypes = [VP, i64, i32, VP, VP, VP]
     for f in COMPUTE:
         getattr(lib, f).restype = ctypes.c_int
     lib.rlk_status_string.argtypes = [ctypes.c_int]
@@ -516,3 +520,71 @@ def linear_logp(hidden, weight, target, temperature=1.0, *, out=None, workspace=
                               weight.data_ptr(), weight.stride(0), _ptr(target), tp, ts, _ptr(out),
                               workspace.data_ptr(), _ptr(err_count), _stream(stream)))
     return out
+
+
+# ----------------------------------------------------------------- gradient norm
+
+NORM_BINS = 384
+RLK_DT_F32, RLK_DT_BF16, RLK_DT_F16 = 0, 1, 2
+
+
+def _norm_dtype(t) -> int:
+    torch = _torch()
+    codes = {torch.float32: RLK_DT_F32, torch.bfloat16: RLK_DT_BF16, torch.float16: RLK_DT_F16}
+    if t.dtype not in codes:
+        raise TypeError(f"gradient norm: dtype {t.dtype} is not float32, bfloat16 or float16")
+    return codes[t.dtype]
+
+
+def norm_bins(device=None):
+    """A cleared bin vector for sqnorm_accumulate: the 384 uint64 words in int64 storage."""
+    torch = _torch()
+    return torch.zeros(NORM_BINS, dtype=torch.int64, device=device)
+
+
+def sqnorm_accumulate(x, bins, stream=None):
+    """Add the FP32 squares of the elements of x (contiguous) into bins."""
+    lib = load_library()
+    if not x.is_contiguous():
+        raise ValueError("gradient norm: x must be contiguous")
+    if bins.dtype != _torch().int64 or bins.numel() != NORM_BINS:
+        raise ValueError("gradient norm: bins must be int64 [384] (see norm_bins)")
+    n = x.numel()
+    check(lib.rlk_sqnorm_accumulate(_ptr(x) if n else None, n, _norm_dtype(x), _ptr(bins),
+                                    _stream(stream)))
+    return bins
+
+
+def sqnorm_finalize(bins, out=None, stream=None):
+    """(sum of squares, norm) as a device float64 [2]."""
+    lib = load_library()
+    torch = _torch()
+    out = torch.empty(2, dtype=torch.float64, device=bins.device) if out is None else out
+    check(lib.rlk_sqnorm_finalize(_ptr(bins), _ptr(out), _stream(stream)))
+    return out
+
+
+def reduce_bins_(bins, group=None):
+    """The distributed reduction: every rank's bins summed elementwise (integer
+    adds, exact in any order), in place."""
+    import torch.distributed as dist
+    dist.all_reduce(bins, op=dist.ReduceOp.SUM, group=group)
+    return bins
+
+
+def grad_norm(tensors, *, distributed=False, group=None, bins=None, out=None, stream=None):
+    """L2 norm of a list of gradient tensors, identical whatever their order,
+    the launch shape, or (with ``distributed``) the split across the ranks
+    of ``group``.  Returns the device float64 [2] (sum of squares, norm)."""
+    torch = _torch()
+    if isinstance(tensors, torch.Tensor):
+        tensors = [tensors]
+    if bins is None:
+        bins = norm_bins(tensors[0].device)
+    else:
+        bins.zero_()
+    for t in tensors:
+        sqnorm_accumulate(t, bins, stream)
+    if distributed:
+        reduce_bins_(bins, group)
+    return sqnorm_finalize(bins, out, stream)

@@ -10,7 +10,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, f) for f in ("rlk_logp.cu", "rlk_shard.cu", "rlk_grad.cu", "rlk_noalloc.cu",
-                                          "rlk_linear.cu")]
+                                          "rlk_linear.cu", "rlk_norm.cu")]
 HEADERS = [os.path.join(CSRC, "rlk_device.cuh"), os.path.join(CSRC, "rlk_host.h")]
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "lib")
@@ -34,7 +34,7 @@ def needs_build() -> bool:
     if not os.path.exists(LIB):
         return True
     lib_t = os.path.getmtime(LIB)
-    deps = [*SOURCES, *HEADERS, os.path.join(INCLUDE, "rlk_logp.h")]
+    deps = [*SOURCES, *HEADERS, os.path.join(INCLUDE, "rlk_logp.h"), os.path.join(INCLUDE, "rlk_norm.h")]
     return any(os.path.getmtime(d) > lib_t for d in deps)
 
 

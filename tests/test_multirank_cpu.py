@@ -56,3 +56,40 @@ def test_reference_arm_other_ranks_exit_silently(capsys):
         steps, warmup, gpus = 1, 0, 2
     assert bench.run_reference(A, rank=1, world=2) is None
     assert capsys.readouterr().out == ""
+
+
+def _norm_worker(rank, world, port, q):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import oracle
+    import rollout_consistent_vocab_gb300 as pkg
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    x = np.random.default_rng(3).standard_normal(10001).astype(np.float32) * 1e-2
+    mine = np.array_split(x, world)[rank]
+    bins = torch.from_numpy(oracle.sqnorm_bins(mine, "f32").view(np.int64).copy())
+    pkg.reduce_bins_(bins)
+    q.put((rank, oracle.norm_finalize(bins.numpy().view(np.uint64))))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_norm_bins_distributed_reduction_gloo():
+    """The gradient norm's distributed reduction (an integer all-reduce of the
+    bins) over two ranks gives the single-rank result exactly."""
+    import numpy as np
+    import oracle
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_norm_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    x = np.random.default_rng(3).standard_normal(10001).astype(np.float32) * 1e-2
+    want = oracle.grad_norm(x, "f32")
+    assert [r[1] for r in res] == [want, want]
