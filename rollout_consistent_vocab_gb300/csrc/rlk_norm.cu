@@ -11,8 +11,9 @@
 // fixed-point accumulator whose unit is 2^(eb-150).  A square with
 // eb <= E <= eb + 32 adds M << (E - eb) (< 2^56) to a 64-bit batch sum,
 // folded into the 128-bit value after every batch of at most 32 squares.  A
-// square above that window moves the window up: the accumulator's low bits
-// that would fall out are first written to the bins in 24-bit pieces.  A
+// square above that window moves the window up, to 8 binades above it: the
+// accumulator's low bits that would fall out are first written to the bins
+// in 24-bit pieces.  A
 // square below it goes straight to its own bin.  At the end the thread writes
 // its accumulator to the bins in 24-bit pieces.  Every step is exact, so the
 // bins hold the exact sum of the squares; only how that value is split over
@@ -38,6 +39,7 @@ constexpr int NB = RLK_NORM_BINS;
 constexpr int NAN_BIN = 0;
 constexpr int INF_BIN = NB - 1;
 constexpr int WIN_BINADES = 32;    // window of a thread accumulator: M << 32 < 2^56
+constexpr int HEADROOM = 8;        // binades left above a new largest square when the window moves
 constexpr int PIECE = 24;          // bits per piece written to a bin (each increment < 2^24)
 constexpr int NORM_THREADS = 256;
 #ifndef NORM_MIN_BLOCKS
@@ -132,9 +134,12 @@ __device__ __forceinline__ void acc_add(Acc& a, uint32_t u, unsigned long long* 
       bin_add(sb, e, M);
       return;
     }
-    acc_fold(a);                   // a new largest square: move the window up
-    acc_spill(a, d - WIN_BINADES, sb);
-    d = WIN_BINADES;
+    // a new largest square: move the window up, leaving HEADROOM binades above
+    // it, but never past eb = 254 - 32, so that an exponent field of 255 (NaN,
+    // infinity) stays outside the window
+    acc_fold(a);
+    acc_spill(a, min(e - (WIN_BINADES - HEADROOM), 254 - WIN_BINADES) - a.eb, sb);
+    d = e - a.eb;
   }
   add128(a.lo, a.hi, static_cast<unsigned long long>(M) << d);
 }
@@ -179,6 +184,7 @@ __device__ __forceinline__ void acc_vec(Acc& a, const uint4& v, unsigned long lo
 #pragma unroll
   for (int j = 0; j < NQ; ++j) rest |= acc_fast(a, square_bits<DT>(vec_elem<DT>(v, j)));
   if (rest) {                      // rare: the squares acc_fast left, by its own test at eb0
+#pragma unroll 1
     for (int j = 0; j < NQ; ++j) {
       const uint32_t u = square_bits<DT>(vec_elem<DT>(v, j));
       if ((u >> 23) - static_cast<uint32_t>(eb0) > static_cast<uint32_t>(WIN_BINADES) && u != 0u)
