@@ -308,11 +308,11 @@ rlk_status rlk_linear_logp(const void* hidden, int64_t T, int64_t H, int64_t hid
  * topology reuses TP4/CP2": every shard yields a summary and the summaries
  * combine in one fixed vocabulary order).
  *
- * Round 1: rlk_logp_shard_summary on each shard (on whichever device holds
+ * Phase 1: rlk_logp_shard_summary on each shard (on whichever device holds
  * it); gather the [T] outputs of the 8 shards into shard-major [8][T] arrays
  * (the summary exchange of the tensor-parallel setting); rlk_logp_merge then
  * gives the full logprob, bit-identical to rlk_logp_full/pair on the whole
- * row.  Round 2 (restricted side): rlk_logp_shard_counts on each shard with
+ * row.  Phase 2 (restricted side): rlk_logp_shard_counts on each shard with
  * the gathered summaries, then rlk_logp_merge with the counts of all shards
  * gives the restricted logprob and support, bit-identical to rlk_logp_pair
  * for every row whose support lies within 1024 order keys of the row maximum
@@ -356,7 +356,7 @@ rlk_status rlk_logp_shard_summary(const rlk_shard_args* args, float* out_max, fl
 /* Per-row exact counts of this shard's tokens on the row's candidate window
  * (at most 1024 order keys below the row maximum, derived from the 8
  * summaries exactly as the fused kernel derives it).  maxes, sumexps, aux
- * are the gathered shard-major [8][T] round-1 outputs.  out_counts: device
+ * are the gathered shard-major [8][T] phase-1 outputs.  out_counts: device
  * uint32 [T][1024], 16-byte aligned; entry i counts the tokens whose bf16
  * order key is the row maximum's key minus i (zero beyond the window and for
  * rows without a top-k or top-p filter). */

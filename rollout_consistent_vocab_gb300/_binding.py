@@ -280,7 +280,7 @@ def make_shard_args(shard_logits, shard, target, temperature=1.0, top_p=1.0, top
 
 def shard_summary(shard_logits, shard, target, temperature=1.0, top_p=1.0, top_k=-1, *,
                   out_max, out_sumexp, out_aux, out_target_logit, err_count=None, stream=None):
-    """Round 1 on one shard: per-row (max, sum-exp, aux) into the given [T]
+    """Phase 1 on one shard: per-row (max, sum-exp, aux) into the given [T]
     views, and the target logit for rows whose target lies in this shard."""
     lib = load_library()
     a = make_shard_args(shard_logits, shard, target, temperature, top_p, top_k, err_count)
@@ -290,7 +290,7 @@ def shard_summary(shard_logits, shard, target, temperature=1.0, top_p=1.0, top_k
 
 def shard_counts(shard_logits, shard, target, maxes, sumexps, aux, temperature=1.0, top_p=1.0,
                  top_k=-1, *, out_counts, stream=None):
-    """Round 2 on one shard: exact per-key counts [T, 1024] on each row's window."""
+    """Phase 2 on one shard: exact per-key counts [T, 1024] on each row's window."""
     lib = load_library()
     a = make_shard_args(shard_logits, shard, target, temperature, top_p, top_k, None)
     check(lib.rlk_logp_shard_counts(ctypes.byref(a), _ptr(maxes), _ptr(sumexps), _ptr(aux),
@@ -320,7 +320,7 @@ def logp_merge(maxes, sumexps, aux, target_logit, target, temperature=1.0, top_p
 
 def logp_sharded(shards, target, temperature=1.0, top_p=1.0, top_k=-1, *, restricted=True,
                  err_count=None, stream=None):
-    """All rounds over 8 shard buffers (shard r holds vocabulary columns
+    """All phases over 8 shard buffers (shard r holds vocabulary columns
     [19072 r, 19072 (r+1))): summaries, then counts when restricted, then the
     merge.  Returns (full,) or (full, restricted, support)."""
     torch = _torch()

@@ -6,11 +6,11 @@
 // profile the Qwen3-8B TP4/CP2 experiment, "How non-default CUDA topology
 // reuses TP4/CP2"):
 //
-//   round 1  shard_summary_kernel, one CTA per row of one shard: the same
+//   phase 1  shard_summary_kernel, one CTA per row of one shard: the same
 //            max pass, top-k witness, greedy/NaN scan and fixed-tree sum-exp
 //            as a CTA of the fused kernel, so the (max, sum-exp) pair has the
 //            same bits;
-//   round 2  shard_counts_kernel: the row's candidate window from the 8
+//   phase 2  shard_counts_kernel: the row's candidate window from the 8
 //            gathered summaries (candidate_window, as in the fused kernel)
 //            and the exact per-key counts of this shard's tokens in it;
 //   merge    merge_kernel, one warp per row: the left fold over shard index
@@ -52,12 +52,12 @@ struct ShardParams {
   const int32_t* k_arr;
   float tau_s, p_s;
   int32_t k_s;
-  // round 1 outputs
+  // phase 1 outputs
   float* out_max;
   float* out_sumexp;
   int32_t* out_aux;
   float* out_xt;
-  // round 2: gathered summaries in, counts out
+  // phase 2: gathered summaries in, counts out
   const float* g_max;
   const float* g_sumexp;
   const int32_t* g_aux;
@@ -105,7 +105,7 @@ __device__ __forceinline__ void load_shard_row(ShardSmem& S, const uint16_t* row
   }
 }
 
-// ------------------------------------------------------------ round 1
+// ------------------------------------------------------------ phase 1
 
 __global__ void __launch_bounds__(NTHR, CTAS_PER_SM) shard_summary_kernel(const ShardParams P) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM) shard_summary_kernel(const 
   }
 }
 
-// ------------------------------------------------------------ round 2
+// ------------------------------------------------------------ phase 2
 
 // The row's candidate window from the gathered summaries: maximum and top-k
 // witness folded over the shards, and for top-p-only rows the total mass Z
