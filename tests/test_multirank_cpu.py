@@ -93,3 +93,17 @@ def test_norm_bins_distributed_reduction_gloo():
     x = np.random.default_rng(3).standard_normal(10001).astype(np.float32) * 1e-2
     want = oracle.grad_norm(x, "f32")
     assert [r[1] for r in res] == [want, want]
+
+
+def test_cpu_baseline_one_process_per_core():
+    """bench.py's all-core CPU baseline: every core's process reports rows."""
+    import numpy as np
+    import torch
+    import bench
+    from rollout_consistent_vocab_gb300 import workloads as W
+    wl = W.workload_c2(device="cpu", T=4)
+    bits = wl.logits.view(torch.int16).numpy().view(np.uint16)
+    rbits = wl.ref_logits.view(torch.int16).numpy().view(np.uint16)
+    tg = W.structural_targets(4, wl.hot, wl.hot_n, seed=2).numpy()
+    rate, rows, secs, ncores = bench.cpu_oracle_rate_all_cores(bits, rbits, tg, 1.0)
+    assert ncores >= 1 and rows >= ncores and secs >= 1.0 and rate == rows / secs
