@@ -471,7 +471,7 @@ def run_ours(args, rank, world, local):
         tok = torch.empty(T_ROWS, dtype=torch.int32, device=dev)
         s_restr, s_full = torch.empty(T_ROWS, **f32), torch.empty(T_ROWS, **f32)
         s_sup = torch.empty(T_ROWS, dtype=torch.int32, device=dev)
-        s_ws = torch.empty((T_ROWS, 4), dtype=torch.int32, device=dev)
+        s_ws = torch.empty(pkg._binding.sample_workspace_bytes(T_ROWS), dtype=torch.uint8, device=dev)
 
         def sample_step():
             pkg.sample(x, TAU, TOP_P, TOP_K, seed=1234, counter=ctr, out_token=tok, out_restr=s_restr,
@@ -490,7 +490,7 @@ def run_ours(args, rank, world, local):
         s_ms = statistics.mean(sev[i].elapsed_time(sev[i + 1]) for i in range(Ks))
         peak_s, _ = measured_peak()
         s_bytes = T_ROWS * VPAD * 2
-        sampler = {"kernel": "logp_kernel<true, sample> + sample_kernel (two launches)",
+        sampler = {"kernel": "logp_kernel<true, sample> (resolves rows, marks chunks) + sample_bits_kernel (draws rows from the marked chunks) + sample_kernel (draws the other rows: unfiltered or wide supports)",
                    "avg_launch_ms": s_ms,
                    "tokens_per_s": T_ROWS / (s_ms / 1e3),
                    "achieved_gbs": s_bytes / (s_ms / 1e3) / 1e9,

@@ -237,13 +237,19 @@ rlk_status rlk_logp_backward_saved(const rlk_logp_args* args, const rlk_row_stat
  *   out_support: optional int32[T], as in rlk_logp_pair.
  *   workspace: device scratch of RLK_SAMPLE_WORKSPACE_BYTES(T) bytes,
  *     16-byte aligned, owned by the caller: the pair pass leaves a 16-byte
- *     record per row there for the draw.  Its contents on entry do not
+ *     record per row there for the draw, then (from byte 16 T on) one bit per
+ *     16-byte chunk of the row marking the chunks that reach the row's
+ *     candidate window (2432 bytes per row).  Its contents on entry do not
  *     matter; calls that share a workspace must not overlap on the GPU.
  * A row whose support reaches below the 1024-key window is resolved exactly
- * (slower path), as in rlk_logp_pair.  Two launches on `stream`: the pair
- * pass that resolves every row (greedy and NaN rows finish there), then one
- * cluster per drawing row that re-reads the row and draws. */
-#define RLK_SAMPLE_WORKSPACE_BYTES(T) ((size_t)(T) * 16u)
+ * (slower path), as in rlk_logp_pair.  Three launches on `stream`: the pair
+ * pass that resolves every row (greedy and NaN rows finish there); one block
+ * per filtered row whose support lies in the candidate window, which reads
+ * only the marked chunks and draws; one cluster per other drawing row
+ * (unfiltered or wide supports), which re-reads the row and draws.  Both
+ * draws compute the same fixed-point masses in the same column order, so
+ * the results do not depend on which one a row takes. */
+#define RLK_SAMPLE_WORKSPACE_BYTES(T) ((size_t)(T) * (16u + 2432u))
 
 rlk_status rlk_sample(const rlk_logp_args* args, unsigned long long seed,
                       const unsigned long long* counter, const uint32_t* uniform,

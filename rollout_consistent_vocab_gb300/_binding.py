@@ -460,14 +460,19 @@ def logp_autograd(logits, target, temperature=1.0, top_p=1.0, top_k=-1):
 
 # ------------------------------------------------------------ sampler
 
+def sample_workspace_bytes(T: int) -> int:
+    """RLK_SAMPLE_WORKSPACE_BYTES(T): a 16-byte record and a 2432-byte chunk bitmap per row."""
+    return T * (16 + 2432)
+
+
 def sample(logits, temperature=1.0, top_p=1.0, top_k=-1, *, seed=0, counter=None, uniform=None,
            out_token=None, out_restr=None, out_full=None, out_support=None, workspace=None,
            err_count=None, stream=None):
     """Draw one token per row from the restricted distribution (inverse CDF in
     column order).  Random words: ``uniform`` (uint32 bits in an int32 [T]
     tensor) or Philox4x32-10 of ``seed`` over ``counter`` (int64 [T]).
-    ``workspace``: int32 [T, 4] scratch (allocated here if not given).
-    Returns (token, restricted logprob, full logprob, support)."""
+    ``workspace``: uint8 [sample_workspace_bytes(T)] scratch (allocated here
+    if not given).  Returns (token, restricted logprob, full logprob, support)."""
     lib = load_library()
     torch = _torch()
     a = make_args(logits, None, temperature, top_p, top_k, err_count)
@@ -482,9 +487,9 @@ def sample(logits, temperature=1.0, top_p=1.0, top_k=-1, *, seed=0, counter=None
     out_full = _empty(T, torch.float32, logits) if out_full is None else out_full
     out_support = _empty(T, torch.int32, logits) if out_support is None else out_support
     if workspace is None:
-        workspace = torch.empty((T, 4), dtype=torch.int32, device=logits.device)
-    if workspace.numel() * workspace.element_size() < 16 * T or not workspace.is_contiguous():
-        raise ValueError("workspace must be a contiguous tensor of at least 16 * T bytes")
+        workspace = torch.empty(sample_workspace_bytes(T), dtype=torch.uint8, device=logits.device)
+    if workspace.numel() * workspace.element_size() < sample_workspace_bytes(T) or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor of at least sample_workspace_bytes(T) bytes")
     check(lib.rlk_sample(ctypes.byref(a), int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(counter), _ptr(uniform),
                          _ptr(out_token), _ptr(out_restr), _ptr(out_full), _ptr(out_support),
                          workspace.data_ptr() if T else None, _stream(stream)))

@@ -36,7 +36,10 @@ constexpr int NTHR = RLK_NTHR;       // threads per CTA
 constexpr int NWARP = NTHR / 32;
 constexpr int ROW_WARPS = NSHARD * NWARP;
 constexpr int CTAS_PER_SM = 5;
-constexpr int MAXCH = (SHARD_CHUNKS + NTHR - 1) / NTHR;     // chunks per thread (9 or 10)
+constexpr int MAXCH = (SHARD_CHUNKS + NTHR - 1) / NTHR;     // chunks per thread (19)
+// sampler: one bit per chunk of a shard, word i * NWARP + w holding chunks
+// (i * NWARP + w) * 32 .. + 31 (76 words, 2432 >= 2384 bits)
+constexpr int SAMP_BITWORDS = MAXCH * NWARP;
 constexpr int WIN = 1024;            // candidate window, in bf16 order keys (8 binades)
 constexpr int TMA_PIECES = 4;
 constexpr int BUSY_HITS = 16;        // candidate chunks per warp above which it counts locally

@@ -102,4 +102,13 @@ inline rlk_status check_grad_args(const float* grad_full, const float* grad_rest
   return RLK_OK;
 }
 
+// The sampler behind rlk_sample and rlk_sample_noalloc: `workspace` holds
+// the 16-byte per-row records; `bits` (NULL: not kept) the per-row, per-shard
+// chunk bitmaps that let rows whose support lies in the first candidate
+// window be drawn from the marked chunks alone.
+rlk_status sample_impl(const rlk_logp_args* args, unsigned long long seed,
+                       const unsigned long long* counter, const uint32_t* uniform,
+                       int32_t* out_token, float* out_restr, float* out_full,
+                       int32_t* out_support, void* workspace, uint32_t* bits, void* stream);
+
 }  // namespace rlk

@@ -129,6 +129,8 @@ struct KParams {
   int32_t* out_token;
   struct SampMsg* out_samp;     // resolution pass: per-row record for the draw
   const struct SampMsg* in_samp;
+  uint32_t* samp_bits;          // resolution pass: per row and shard, the chunks reaching the
+                                // candidate window (SAMP_BITWORDS words); NULL: not kept
   // rlk_logp_kl: the reference logits, interleaved with the policy rows
   const uint16_t* ref_logits;
   int64_t ref_stride;
@@ -139,11 +141,12 @@ enum { MODE_FWD = 0, MODE_BWD = 1, MODE_SAMPLE = 2 };
 
 // Sampler: per-row record of the resolved row, written by the leader of the
 // pair pass and read by the draw kernel (16 bytes).
-enum : uint32_t { SAMP_DRAW = 1u, SAMP_SEL = 2u };
+enum : uint32_t { SAMP_DRAW = 1u, SAMP_SEL = 2u, SAMP_BITS = 4u };
 struct __align__(16) SampMsg {
   float M, Z;
   int32_t min_key;
-  uint32_t flags;                  // SAMP_DRAW: the row draws (not greedy / NaN); SAMP_SEL: filtered
+  uint32_t flags;                  // SAMP_DRAW: the row draws (not greedy / NaN); SAMP_SEL: filtered;
+                                   // SAMP_BITS: the support lies in the chunks the bitmap marks
 };
 
 // The 16-byte exchange message of this CTA (rank r) to CTA `to` (a local
@@ -481,10 +484,22 @@ logp_kernel(const KParams P) {
       const uint32_t dst = map_rank(smem_addr(S.merged), 0);
       const uint32_t rbar = map_rank(bar_hist, 0);
       // chunks whose maximum reaches the window, from the register chunk maxima
+      // (an absent last chunk holds -inf in cm: excluded explicitly, for a
+      // window whose bottom is -inf itself)
       uint32_t hitmask = 0;
 #pragma unroll
       for (int i = 0; i < MAXCH; ++i)
-        if (__hge2_mask(cm[i], vlo2) != 0u) hitmask |= 1u << i;
+        if ((i < MAXCH - 1 || tid + i * NTHR < nchunks) && __hge2_mask(cm[i], vlo2) != 0u)
+          hitmask |= 1u << i;
+      if (SAMPLE && P.samp_bits) {
+        // the draw reads only these chunks when the support lies in the window
+        uint32_t* wb = P.samp_bits + (row * NSHARD + r) * SAMP_BITWORDS;
+#pragma unroll
+        for (int i = 0; i < MAXCH; ++i) {
+          const uint32_t word = __ballot_sync(0xffffffffu, (hitmask >> i) & 1u);
+          if ((tid & 31) == 0) wb[i * NWARP + (tid >> 5)] = word;
+        }
+      }
       // warps with many candidate chunks count locally and push per key;
       // the others send one add per element
       const bool busy = (r != 0) && __reduce_add_sync(0xffffffffu, __popc(hitmask)) > BUSY_HITS;
@@ -523,6 +538,25 @@ logp_kernel(const KParams P) {
           if (hw & 0xFFFFu) { red_async_add(dst + 8u * iw, hw & 0xFFFFu, rbar); ++sent; }
           if (hw >> 16) { red_async_add(dst + 8u * iw + 4u, hw >> 16, rbar); ++sent; }
         }
+      }
+    } else {
+      if (tid == 0 && xm == -INFINITY && lo <= KEY_NEG_INF && lo <= hi) {
+        // every element of this shard is -inf (a NaN makes the row NaN) and
+        // the window reaches -inf: the whole shard counts at that key
+        const int idx = hi - KEY_NEG_INF;
+        const uint32_t cnt = static_cast<uint32_t>(nchunks) * 8u;
+        if (r == 0) {
+          red_shared_add(&S.merged[idx], cnt);
+        } else {
+          red_async_add(map_rank(smem_addr(S.merged), 0) + 4u * static_cast<uint32_t>(idx), cnt,
+                        map_rank(bar_hist, 0));
+          ++sent;
+        }
+      }
+      if (SAMPLE && P.samp_bits) {
+        // no element of this shard reaches the window with any mass
+        uint32_t* wb = P.samp_bits + (row * NSHARD + r) * SAMP_BITWORDS;
+        for (int i = tid; i < SAMP_BITWORDS; i += NTHR) wb[i] = 0u;
       }
     }
     // the leader learns how many adds each peer sent from its summary
@@ -674,7 +708,8 @@ logp_kernel(const KParams P) {
     m.M = M;
     m.Z = Z;
     m.min_key = sel ? sr.min_key : 0;
-    m.flags = (!bad && !greedy ? SAMP_DRAW : 0u) | (sel ? SAMP_SEL : 0u);
+    m.flags = (!bad && !greedy ? SAMP_DRAW : 0u) | (sel ? SAMP_SEL : 0u) |
+              (sel && !shard_reused && P.samp_bits ? SAMP_BITS : 0u);
     P.out_samp[row] = m;
     if (P.out_support) P.out_support[row] = support;
     if (bad) {
@@ -703,7 +738,8 @@ sample_kernel(const KParams P) {
   const uint32_t r = cluster_rank();
   const int64_t row = blockIdx.x / NSHARD;
   const SampMsg m = P.in_samp[row];
-  if (!(m.flags & SAMP_DRAW)) return;         // the same decision in every CTA of the cluster
+  // the same decision in every CTA of the cluster; SAMP_BITS rows are drawn by sample_bits_kernel
+  if (!(m.flags & SAMP_DRAW) || (m.flags & SAMP_BITS)) return;
   const int nchunks = (r == NSHARD - 1) ? LAST_CHUNKS : SHARD_CHUNKS;
   const uint32_t bar_load = smem_addr(&S.bar_load);
   const uint32_t bar_zr = smem_addr(&S.bar_zr);
@@ -728,6 +764,96 @@ sample_kernel(const KParams P) {
   if (!mbar_wait_bounded(bar_load)) mbar_wait_bounded(bar_load);
   cluster_wait();                             // every peer's barrier is ready for the masses
   sample_shard(S, P, row, r, S.shard, nchunks, m, tau, bar_zr);
+}
+
+// Rows whose support lies inside the first candidate window (SAMP_BITS): one
+// CTA per row reads only the chunks the pair pass marked as reaching the
+// window (every support element is in one of them) and draws with the same
+// fixed-point masses, the same column order and the same arithmetic as
+// sample_shard, so the token and its logprobs are bit-identical to the
+// cluster path's.  Each thread takes a run of consecutive bitmap words, so a
+// block scan of the threads' masses is a scan in column order.
+struct SampBitsSmem {
+  uint32_t bw[NSHARD * SAMP_BITWORDS];
+  uint32_t scan_c[NWARP];
+  unsigned long long scan_m[NWARP];
+};
+
+__global__ void __launch_bounds__(NTHR) sample_bits_kernel(const KParams P) {
+  __shared__ SampBitsSmem S;
+  constexpr int NW = NSHARD * SAMP_BITWORDS;
+  const int64_t row = blockIdx.x;
+  const SampMsg m = P.in_samp[row];
+  if (!(m.flags & SAMP_DRAW) || !(m.flags & SAMP_BITS)) return;   // uniform over the block
+  const int tid = threadIdx.x;
+  const uint32_t* src_bits = P.samp_bits + row * NW;
+  for (int i = tid; i < NW; i += NTHR) S.bw[i] = src_bits[i];
+  __syncthreads();
+  const float tau = P.tau_arr ? P.tau_arr[row] : P.tau_s;
+  const float c = __fdiv_rn(LOG2E, tau);
+  const float vmin_f = m.min_key <= KEY_NEG_INF ? -INFINITY : key_value(m.min_key);
+  const __nv_bfloat162 vmin2 = __floats2bfloat162_rn(vmin_f, vmin_f);
+  const uint4* rowp = reinterpret_cast<const uint4*>(P.logits + row * P.stride);
+  constexpr int PER = (NW + NTHR - 1) / NTHR;
+  const int w0 = min(NW, tid * PER), w1 = min(NW, w0 + PER);
+  // chunk g of shard q is 16-byte chunk q * SHARD_CHUNKS + g of the row
+  unsigned long long mine = 0;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t bits = S.bw[w];
+    const int q = w / SAMP_BITWORDS, g0 = (w % SAMP_BITWORDS) * 32;
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1;
+      mine += chunk_support_mass(__ldg(rowp + q * SHARD_CHUNKS + g0 + b), vmin2, m.M, c);
+    }
+  }
+  uint32_t ec, tc;
+  unsigned long long excl, zs;
+  block_excl_scan(0u, mine, ec, excl, tc, zs, S);
+  const uint32_t u = P.uniform ? P.uniform[row] : philox_word0(P.seed, P.counter[row]);
+  const unsigned long long draw = scale_draw(u, zs);
+  if (mine == 0 || draw < excl || draw - excl >= mine) return;   // another thread holds it
+  // this thread's run holds the draw: walk its chunks, then the columns, in order
+  unsigned long long left = draw - excl;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t bits = S.bw[w];
+    const int q = w / SAMP_BITWORDS, g0 = (w % SAMP_BITWORDS) * 32;
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1;
+      const uint4 v = __ldg(rowp + q * SHARD_CHUNKS + g0 + b);
+      const unsigned long long mc = chunk_support_mass(v, vmin2, m.M, c);
+      if (left >= mc) {
+        left -= mc;
+        continue;
+      }
+      const uint32_t sb = chunk_support_bits(v, vmin2);
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+      int jstar = -1;
+      uint32_t xb = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t e = (w4[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
+        if (jstar < 0 && ((sb >> ((j >> 1) + 16 * (j & 1))) & 1u)) {
+          const unsigned long long qm = qfx(__uint_as_float(e << 16), m.M, c);
+          if (left < qm) {
+            jstar = j;
+            xb = e;
+          } else {
+            left -= qm;
+          }
+        }
+      }
+      const float xa = __uint_as_float(xb << 16);
+      const float d = __fdiv_rn(xa - m.M, tau);
+      const float full = d - logf(m.Z);
+      const float restr = (m.flags & SAMP_SEL) ? d - logf(__ull2float_rn(zs) * (1.0f / FX_SCALE)) : full;
+      P.out_token[row] = q * SW + (g0 + b) * 8 + jstar;
+      if (P.out_full) P.out_full[row] = full;
+      if (P.out_restr) P.out_restr[row] = restr;
+      return;
+    }
+  }
 }
 
 // The KL term of each row: the policy's full logprob minus the reference's.
@@ -901,6 +1027,22 @@ rlk_status rlk_sample(const rlk_logp_args* args, unsigned long long seed,
                       const unsigned long long* counter, const uint32_t* uniform,
                       int32_t* out_token, float* out_restr, float* out_full,
                       int32_t* out_support, void* workspace, void* stream) {
+  // the records first, then the chunk bitmaps (T * 16 keeps them 16-byte aligned)
+  uint32_t* bits = (args && workspace && args->T > 0)
+                       ? reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + args->T * 16)
+                       : nullptr;
+  return sample_impl(args, seed, counter, uniform, out_token, out_restr, out_full, out_support,
+                     workspace, bits, stream);
+}
+
+}  // extern "C"
+
+namespace rlk {
+
+rlk_status sample_impl(const rlk_logp_args* args, unsigned long long seed,
+                       const unsigned long long* counter, const uint32_t* uniform,
+                       int32_t* out_token, float* out_restr, float* out_full,
+                       int32_t* out_support, void* workspace, uint32_t* bits, void* stream) {
   rlk_status s = check_args(args, true, false);
   if (s != RLK_OK || args->T == 0) return s;
   if (!counter && !uniform) return fail(RLK_EINVAL, "counter and uniform are both NULL");
@@ -923,8 +1065,14 @@ rlk_status rlk_sample(const rlk_logp_args* args, unsigned long long seed,
   P.seed = seed;
   P.out_samp = static_cast<SampMsg*>(workspace);
   P.in_samp = static_cast<const SampMsg*>(workspace);
+  P.samp_bits = bits;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if ((s = launch<true, MODE_SAMPLE>(P, args->T, st)) != RLK_OK) return s;
+  if (bits) {
+    sample_bits_kernel<<<static_cast<unsigned>(args->T), NTHR, 0, st>>>(P);
+    const cudaError_t eb = cudaGetLastError();
+    if (eb != cudaSuccess) return fail(RLK_ECUDA, "kernel launch: %s", cudaGetErrorString(eb));
+  }
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -942,6 +1090,10 @@ rlk_status rlk_sample(const rlk_logp_args* args, unsigned long long seed,
   if (e != cudaSuccess) return fail(RLK_ECUDA, "kernel launch: %s", cudaGetErrorString(e));
   return RLK_OK;
 }
+
+}  // namespace rlk
+
+extern "C" {
 
 const char* rlk_status_string(rlk_status status) {
   switch (status) {

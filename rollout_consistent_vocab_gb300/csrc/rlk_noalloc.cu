@@ -62,13 +62,14 @@ rlk_status rlk_sample_noalloc(const rlk_logp_args* args, unsigned long long seed
                 "split the batch or call rlk_sample with a workspace",
                 (long long)args->T, RLK_SAMPLE_NOALLOC_MAX_ROWS);
   if (!args || args->T <= 0)                  // validation and the empty batch, as rlk_sample
-    return rlk_sample(args, seed, counter, uniform, out_token, out_restr, out_full, out_support,
-                      nullptr, stream);
+    return sample_impl(args, seed, counter, uniform, out_token, out_restr, out_full, out_support,
+                       nullptr, nullptr, stream);
   void* scratch = nullptr;
   rlk_status s = scratch_on_current_device(&scratch);
   if (s != RLK_OK) return s;
-  return rlk_sample(args, seed, counter, uniform, out_token, out_restr, out_full, out_support,
-                    scratch, stream);
+  // the records only: every row is drawn by re-reading its shards (no chunk bitmaps)
+  return sample_impl(args, seed, counter, uniform, out_token, out_restr, out_full, out_support,
+                     scratch, nullptr, stream);
 }
 
 }  // extern "C"

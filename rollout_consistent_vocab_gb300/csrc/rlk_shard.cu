@@ -233,6 +233,9 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM) shard_counts_kernel(const S
       const __nv_bfloat162 vlo2 = __floats2bfloat162_rn(vlo_f, vlo_f);
 #pragma unroll
       for (int i = 0; i < MAXCH; ++i) {
+        // an absent last chunk holds -inf in cm: skip it even when the
+        // window's bottom is -inf itself
+        if (i == MAXCH - 1 && tid + i * NTHR >= nchunks) continue;
         if (__hge2_mask(cm[i], vlo2) == 0u) continue;
         const uint4 v = S.shard[tid + i * NTHR];
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -242,6 +245,12 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM) shard_counts_kernel(const S
           if (__uint_as_float(b << 16) >= vlo_f) red_shared_add(&S.hist[hi - okey(b)], 1u);
         }
       }
+    }
+    if (!count && xm == -INFINITY && lo <= KEY_NEG_INF && lo <= hi) {
+      // every element of this shard is -inf and the window reaches -inf: the
+      // whole shard counts at that key (as in the fused kernel)
+      __syncthreads();          // the histogram is zeroed
+      if (tid == 0) S.hist[hi - KEY_NEG_INF] = static_cast<uint32_t>(nchunks) * 8u;
     }
   }
   __syncthreads();

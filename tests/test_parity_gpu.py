@@ -334,3 +334,38 @@ def test_wide_support_fallback_path():
     st = Stats()
     check_rows(st, bits, tau, p, k, tg, f, r, s)
     print("fallback", st)
+
+
+def test_window_reaching_minus_infinity():
+    """Rows whose maximum lies within a few order keys of -inf and whose top-k
+    witness is -inf: the candidate window then reaches -inf itself, and only
+    the shard's real chunks may be counted (the support includes the -inf
+    tokens, at zero mass).  Also drawn, through both sampler paths."""
+    from _support import Stats, check_rows
+    rng = np.random.default_rng(91)
+    rows, first = [], []
+    for n_fin in (100, 3, 5000):
+        cols = rng.choice(VR, n_fin, replace=False)
+        vals = rng.choice([-1.75 * 2.0 ** 127, -1.5 * 2.0 ** 127, -1.25 * 2.0 ** 127], n_fin)
+        rows.append(_row(float("-inf"), {int(c): float(v) for c, v in zip(cols, vals)}, "garbage"))
+        first.append(int(cols[np.argmax(vals)]))
+    bits = np.stack(rows * 3)
+    x = rows_from_bits(bits)
+    T = bits.shape[0]
+    taus = np.array([1.0] * T, np.float32)
+    ps = np.array([1.0, 1.0, 1.0, 0.9, 0.9, 0.9, 0.9, 0.9, 0.9], np.float32)
+    ks = np.array([1000, 1000, 1000, 1000, 1000, 1000, -1, -1, -1], np.int32)
+    ts = np.array(first * 3, np.int32)
+    ts[1] = 5                                   # a -inf column
+    f, r, s = run_pair(x, _t(ts, torch.int32), _t(taus, torch.float32), _t(ps, torch.float32),
+                       _t(ks, torch.int32))
+    st = Stats()
+    check_rows(st, bits, taus, ps, ks, ts, f, r, s)
+    u = torch.as_tensor(rng.integers(0, 2 ** 32, T, dtype=np.uint64).astype(np.uint32).view(np.int32),
+                        device=DEV)
+    tok, rs, fs, ss = pkg.sample(x, _t(taus, torch.float32), _t(ps, torch.float32), _t(ks, torch.int32),
+                                 uniform=u)
+    torch.cuda.synchronize()
+    for i in range(T):
+        o = oracle.logp_row(bits[i], float(taus[i]), float(ps[i]), int(ks[i]), int(tok[i]))
+        assert math.isfinite(o.restr) and int(ss[i]) == o.support, i

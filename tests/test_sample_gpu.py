@@ -162,3 +162,41 @@ def test_full_size_draws_are_in_support():
     assert (sup <= 128 + 64).all()
     del wl
     torch.cuda.empty_cache()
+
+
+def _sample_noalloc(x, tau, p, k, u):
+    """The cluster draw for every row (rlk_sample_noalloc keeps no chunk bitmaps)."""
+    import ctypes
+    from rollout_consistent_vocab_gb300 import _binding as b
+    lib = pkg.load_library()
+    T = x.shape[0]
+    a = b.make_args(x, None, tau, p, k)
+    outs = (torch.empty(T, dtype=torch.int32, device=DEV), torch.empty(T, device=DEV),
+            torch.empty(T, device=DEV), torch.empty(T, dtype=torch.int32, device=DEV))
+    st = lib.rlk_sample_noalloc(ctypes.byref(a), 0, None, u.data_ptr(), outs[0].data_ptr(),
+                                outs[1].data_ptr(), outs[2].data_ptr(), outs[3].data_ptr(),
+                                torch.cuda.current_stream().cuda_stream)
+    assert st == b.RLK_OK, lib.rlk_last_error()
+    return outs
+
+
+@pytest.mark.parametrize("case", ["bench_workload", "mixed"])
+def test_bitmap_draw_equals_cluster_draw(case):
+    """Rows whose support lies in the candidate window are drawn from the
+    marked chunks alone; the result must equal the cluster draw's, which
+    re-reads every shard, bit for bit (tokens, logprobs, supports)."""
+    if case == "bench_workload":
+        wl = W.workload_c2(device=DEV, with_ref=False)
+        x, T = wl.logits, wl.T
+        tau, p, k = _t([1.3] * T, torch.float32), _t([0.99] * T, torch.float32), _t([128] * T, torch.int32)
+    else:
+        x, tau_n, p_n, k_n, _ = mixed(2000, 71)
+        T = x.shape[0]
+        tau, p, k = _t(tau_n, torch.float32), _t(p_n, torch.float32), _t(k_n, torch.int32)
+    rng = np.random.default_rng(72)
+    u = _u32_tensor(rng.integers(0, 2 ** 32, T, dtype=np.uint64).astype(np.uint32))
+    got = pkg.sample(x, tau, p, k, uniform=u)
+    want = _sample_noalloc(x, tau, p, k, u)
+    torch.cuda.synchronize()
+    for g, w in zip(got, want):
+        assert torch.equal(g.view(torch.int32), w.view(torch.int32))
