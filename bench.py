@@ -488,13 +488,29 @@ def run_ours(args, rank, world, local):
             sev[i + 1].record(stream)
         torch.cuda.synchronize()
         s_ms = statistics.mean(sev[i].elapsed_time(sev[i + 1]) for i in range(Ks))
+
+        def sample_unfiltered():        # temperature only: the support is every token
+            pkg.sample(x, 1.0, 1.0, -1, seed=1234, counter=ctr, out_token=tok, out_restr=s_restr,
+                       out_full=s_full, out_support=s_sup, workspace=s_ws, stream=stream)
+
+        for _ in range(3):
+            sample_unfiltered()
+        torch.cuda.synchronize()
+        sev[0].record(stream)
+        for i in range(Ks):
+            sample_unfiltered()
+            sev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        u_ms = statistics.mean(sev[i].elapsed_time(sev[i + 1]) for i in range(Ks))
         peak_s, _ = measured_peak()
         s_bytes = T_ROWS * VPAD * 2
-        sampler = {"kernel": "logp_kernel<true, sample> (resolves rows, marks chunks) + sample_bits_kernel (draws rows from the marked chunks) + sample_kernel (draws the other rows: unfiltered or wide supports)",
+        sampler = {"kernel": "logp_kernel<true, sample> (resolves rows, marks chunks) + sample_row_kernel (one block per row draws from the marked chunks)",
                    "avg_launch_ms": s_ms,
                    "tokens_per_s": T_ROWS / (s_ms / 1e3),
                    "achieved_gbs": s_bytes / (s_ms / 1e3) / 1e9,
-                   "frac": s_bytes / (s_ms / 1e3) / 1e9 / peak_s}
+                   "frac": s_bytes / (s_ms / 1e3) / 1e9 / peak_s,
+                   "unfiltered_ms": u_ms,
+                   "unfiltered_note": "tau 1, top-p 1, top-k off on the same logits: every chunk is read twice"}
 
     # ---- the LM head fused with the full logprob (tensor cores): hidden
     #      [T, 4096] (the Qwen3-8B hidden size) and a random padded head

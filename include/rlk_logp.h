@@ -242,13 +242,13 @@ rlk_status rlk_logp_backward_saved(const rlk_logp_args* args, const rlk_row_stat
  *     candidate window (2432 bytes per row).  Its contents on entry do not
  *     matter; calls that share a workspace must not overlap on the GPU.
  * A row whose support reaches below the 1024-key window is resolved exactly
- * (slower path), as in rlk_logp_pair.  Three launches on `stream`: the pair
- * pass that resolves every row (greedy and NaN rows finish there); one block
- * per filtered row whose support lies in the candidate window, which reads
- * only the marked chunks and draws; one cluster per other drawing row
- * (unfiltered or wide supports), which re-reads the row and draws.  Both
- * draws compute the same fixed-point masses in the same column order, so
- * the results do not depend on which one a row takes. */
+ * (slower path), as in rlk_logp_pair.  Two launches on `stream`: the pair
+ * pass that resolves every row (greedy and NaN rows finish there), then one
+ * block per drawing row, which reads the marked chunks when the row's
+ * support lies inside its candidate window and every real chunk otherwise
+ * (unfiltered rows, wider supports); both cases compute the same
+ * fixed-point masses in the same column order, so the result does not
+ * depend on which chunks are read. */
 #define RLK_SAMPLE_WORKSPACE_BYTES(T) ((size_t)(T) * (16u + 2432u))
 
 rlk_status rlk_sample(const rlk_logp_args* args, unsigned long long seed,

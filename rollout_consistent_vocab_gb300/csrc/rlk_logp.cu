@@ -87,16 +87,6 @@ struct __align__(128) Smem {
   unsigned long long bar_load, bar_mid, bar_sum, bar_hist, bar_lead;
 };
 
-// Shared memory of the draw kernel.
-struct __align__(128) SampSmem {
-  uint4 shard[SHARD_CHUNKS];
-  uint32_t hist[WIN / 2];           // per-warp partial masses of the draw (u64 pairs)
-  uint4 zr[NSHARD];                 // every shard's fixed-point support mass
-  unsigned long long samp_res;      // residual draw inside the owning row of chunks
-  int32_t samp_i;
-  unsigned long long bar_load, bar_zr;
-};
-static_assert(sizeof(SampSmem) + 1024 <= 233472 / CTAS_PER_SM, "shared memory budget of 5 CTAs per SM");
 // five CTAs per SM: 5 * (sizeof + 1 KB reserved) <= 228 KB
 static_assert(sizeof(Smem) + 1024 <= 233472 / CTAS_PER_SM, "shared memory budget of 5 CTAs per SM");
 
@@ -162,126 +152,6 @@ __device__ __forceinline__ void send_mid(Smem& S, uint32_t r, int to, float xm, 
 }
 
 // ------------------------------------------------------------ the kernel
-
-// The draw once the row is resolved: every shard sums the fixed-point mass
-// of its support tokens (each thread keeps its chunks' masses in registers)
-// and sends it to the 7 others; the shard holding the drawn mass finds the
-// row of chunks, the chunk and the column, in column order, and writes the
-// token and its logprobs.
-template <class SM>
-__device__ __forceinline__ void sample_shard(SM& S, const KParams& P, int64_t row, uint32_t r,
-                                             const uint4* src, int nchunks, const SampMsg& m,
-                                             float tau, uint32_t bar_zr) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float c = __fdiv_rn(LOG2E, tau);
-  // keys at or below -inf's are the whole vocabulary (min_key 0 when unfiltered;
-  // key_value of keys below -inf's would be a NaN pattern)
-  const float vmin_f = m.min_key <= KEY_NEG_INF ? -INFINITY : key_value(m.min_key);
-  const __nv_bfloat162 vmin2 = __floats2bfloat162_rn(vmin_f, vmin_f);
-  unsigned long long* wsum = reinterpret_cast<unsigned long long*>(S.hist);
-  // ---- this shard's support mass
-  unsigned long long mi[MAXCH];
-  unsigned long long acc = 0;
-#pragma unroll
-  for (int i = 0; i < MAXCH; ++i) {
-    const int ch = tid + i * NTHR;
-    mi[i] = (i < MAXCH - 1 || ch < nchunks) ? chunk_support_mass(src[ch], vmin2, m.M, c) : 0ull;
-    acc += mi[i];
-  }
-  acc = warp_sum_u64(acc);
-  if (lane == 0) wsum[warp] = acc;
-  __syncthreads();
-  if (tid == 0) {
-    unsigned long long zr = 0;
-    for (int w = 0; w < NWARP; ++w) zr += wsum[w];
-    const uint4 v = make_uint4(static_cast<uint32_t>(zr), static_cast<uint32_t>(zr >> 32), 0u, 0u);
-    S.zr[r] = v;
-    for (int q = 0; q < NSHARD; ++q)
-      if (q != static_cast<int>(r)) st_async_v4(map_rank(smem_addr(&S.zr[r]), q), v, map_rank(bar_zr, q));
-    // one thread waits for the 7 peers' masses; the block barrier publishes them
-    S.samp_i = mbar_wait_bounded(bar_zr) ? 1 : 0;
-  }
-  __syncthreads();
-  // ---- the drawn mass, and the shard that holds it
-  const bool ok = S.samp_i != 0;
-  unsigned long long zs = 0, before = 0, mine = 0;
-  for (int q = 0; q < NSHARD; ++q) {
-    const unsigned long long zq = (static_cast<unsigned long long>(S.zr[q].y) << 32) | S.zr[q].x;
-    if (q < static_cast<int>(r)) before += zq;
-    if (q == static_cast<int>(r)) mine = zq;
-    zs += zq;
-  }
-  if (!ok) {
-    if (tid == 0) {
-      P.out_token[row] = -1;
-      if (P.err) atomicAdd(P.err, 1);
-    }
-    return;
-  }
-  const uint32_t u = P.uniform ? P.uniform[row] : philox_word0(P.seed, P.counter[row]);
-  const unsigned long long draw = scale_draw(u, zs);
-  if (draw < before || draw - before >= mine) return;      // another shard holds it
-  const unsigned long long rr = draw - before;
-  // ---- per row of chunks (chunk index = i * NTHR + tid), then within the row
-  __syncthreads();                  // every thread has read S.samp_i
-#pragma unroll
-  for (int i = 0; i < MAXCH; ++i) {
-    const unsigned long long w = warp_sum_u64(mi[i]);
-    if (lane == 0) wsum[NWARP + i * NWARP + warp] = w;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    unsigned long long cum = 0;
-    int istar = MAXCH - 1;
-    unsigned long long res = 0;
-    for (int i = 0; i < MAXCH; ++i) {
-      unsigned long long tot = 0;
-      for (int w = 0; w < NWARP; ++w) tot += wsum[NWARP + i * NWARP + w];
-      if (rr - cum < tot) { istar = i; res = rr - cum; break; }
-      cum += tot;
-    }
-    S.samp_i = istar;
-    S.samp_res = res;
-  }
-  __syncthreads();
-  const int istar = S.samp_i;
-  const unsigned long long res = S.samp_res;
-  unsigned long long mt = 0;
-#pragma unroll
-  for (int i = 0; i < MAXCH; ++i)
-    if (i == istar) mt = mi[i];
-  unsigned long long excl = warp_incl_scan_u64(mt) - mt;
-  for (int w = 0; w < warp; ++w) excl += wsum[NWARP + istar * NWARP + w];
-  if (mt == 0 || res < excl || res - excl >= mt) return;
-  // this thread's chunk holds the draw: walk its support columns in order
-  const int ch = tid + istar * NTHR;
-  const uint4 v = src[ch];
-  const uint32_t sb = chunk_support_bits(v, vmin2);
-  unsigned long long left = res - excl;
-  const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-  int jstar = -1;
-  uint32_t bits = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t b = (w4[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
-    if (jstar < 0 && ((sb >> ((j >> 1) + 16 * (j & 1))) & 1u)) {
-      const unsigned long long q = qfx(__uint_as_float(b << 16), m.M, c);
-      if (left < q) {
-        jstar = j;
-        bits = b;
-      } else {
-        left -= q;
-      }
-    }
-  }
-  const float xa = __uint_as_float(bits << 16);
-  const float d = __fdiv_rn(xa - m.M, tau);
-  const float full = d - logf(m.Z);
-  const float restr = (m.flags & SAMP_SEL) ? d - logf(__ull2float_rn(zs) * (1.0f / FX_SCALE)) : full;
-  P.out_token[row] = static_cast<int32_t>(r) * SW + ch * 8 + jstar;
-  if (P.out_full) P.out_full[row] = full;
-  if (P.out_restr) P.out_restr[row] = restr;
-}
 
 template <bool RESTR, int MODE>
 __global__ void __cluster_dims__(NSHARD, 1, 1) __launch_bounds__(NTHR, CTAS_PER_SM)
@@ -727,133 +597,137 @@ logp_kernel(const KParams P) {
 
 // ------------------------------------------------------------ the draw
 
-// One cluster of 8 CTAs per row, after the pair pass resolved every row:
-// each CTA streams its shard into shared memory and takes part in the draw
-// (sample_shard).  Rows without a draw (greedy, NaN, rejected) exit at once.
-__global__ void __cluster_dims__(NSHARD, 1, 1) __launch_bounds__(NTHR, CTAS_PER_SM)
-sample_kernel(const KParams P) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  SampSmem& S = *reinterpret_cast<SampSmem*>(smem_raw);
-  const int tid = threadIdx.x;
-  const uint32_t r = cluster_rank();
-  const int64_t row = blockIdx.x / NSHARD;
-  const SampMsg m = P.in_samp[row];
-  // the same decision in every CTA of the cluster; SAMP_BITS rows are drawn by sample_bits_kernel
-  if (!(m.flags & SAMP_DRAW) || (m.flags & SAMP_BITS)) return;
-  const int nchunks = (r == NSHARD - 1) ? LAST_CHUNKS : SHARD_CHUNKS;
-  const uint32_t bar_load = smem_addr(&S.bar_load);
-  const uint32_t bar_zr = smem_addr(&S.bar_zr);
-  if (tid == 0) {
-    mbar_init(bar_load, 1);
-    mbar_init(bar_zr, 1);
-    mbar_arrive_expect_tx(bar_zr, (NSHARD - 1) * 16);
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    const uint32_t bytes = static_cast<uint32_t>(nchunks) * 16u;
-    mbar_arrive_expect_tx(bar_load, bytes);
-    const uint64_t pol = evict_first_policy();
-    const uint32_t piece = bytes / TMA_PIECES;
-    const char* src = reinterpret_cast<const char*>(P.logits + row * P.stride + static_cast<int64_t>(r) * SW);
-    const uint32_t dst = smem_addr(S.shard);
-#pragma unroll
-    for (int i = 0; i < TMA_PIECES; ++i) bulk_load(dst + i * piece, src + i * piece, piece, bar_load, pol);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  const float tau = P.tau_arr ? P.tau_arr[row] : P.tau_s;
-  __syncthreads();
-  cluster_arrive_relaxed();
-  if (!mbar_wait_bounded(bar_load)) mbar_wait_bounded(bar_load);
-  cluster_wait();                             // every peer's barrier is ready for the masses
-  sample_shard(S, P, row, r, S.shard, nchunks, m, tau, bar_zr);
-}
-
-// Rows whose support lies inside the first candidate window (SAMP_BITS): one
-// CTA per row reads only the chunks the pair pass marked as reaching the
-// window (every support element is in one of them) and draws with the same
-// fixed-point masses, the same column order and the same arithmetic as
-// sample_shard, so the token and its logprobs are bit-identical to the
-// cluster path's.  Each thread takes a run of consecutive bitmap words, so a
-// block scan of the threads' masses is a scan in column order.
-struct SampBitsSmem {
-  uint32_t bw[NSHARD * SAMP_BITWORDS];
+// One block per row, after the pair pass resolved every row (greedy, NaN
+// and rejected rows were finished there and exit at once).  The support mass
+// of a 16-byte chunk is the sum of its support elements' fixed-point masses
+// (the selection's per-key values, 2^-44 units); the drawn mass
+// floor(u Z_S / 2^32) is located in column order.  The chunks read are the
+// ones the pair pass marked as reaching the candidate window when the
+// support lies inside it (SAMP_BITS: about 150 of a row's 19,000 on the
+// 8192-row workload), otherwise every real chunk of the row.  Each thread
+// takes a run of consecutive bitmap words (32 chunks each), so a block scan
+// of the threads' masses is a scan in column order; the thread holding the
+// draw finds the word from the per-word masses kept in shared memory, and
+// warp 0 finds the chunk (one chunk per lane, a warp scan) and the column.
+struct SampRowSmem {
+  uint32_t bw[NSHARD * SAMP_BITWORDS];               // the chunks to read
+  unsigned long long wm[NSHARD * SAMP_BITWORDS];     // support mass per bitmap word
   uint32_t scan_c[NWARP];
   unsigned long long scan_m[NWARP];
+  int32_t own_w;                                     // the word holding the draw
+  unsigned long long own_res;                        // the draw's offset inside that word
 };
 
-__global__ void __launch_bounds__(NTHR) sample_bits_kernel(const KParams P) {
-  __shared__ SampBitsSmem S;
+__global__ void __launch_bounds__(NTHR) sample_row_kernel(const KParams P) {
+  __shared__ SampRowSmem S;
   constexpr int NW = NSHARD * SAMP_BITWORDS;
   const int64_t row = blockIdx.x;
   const SampMsg m = P.in_samp[row];
-  if (!(m.flags & SAMP_DRAW) || !(m.flags & SAMP_BITS)) return;   // uniform over the block
-  const int tid = threadIdx.x;
-  const uint32_t* src_bits = P.samp_bits + row * NW;
-  for (int i = tid; i < NW; i += NTHR) S.bw[i] = src_bits[i];
+  if (!(m.flags & SAMP_DRAW)) return;                 // uniform over the block
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (m.flags & SAMP_BITS) {
+    const uint32_t* src_bits = P.samp_bits + row * NW;
+    for (int i = tid; i < NW; i += NTHR) S.bw[i] = src_bits[i];
+  } else {
+    for (int i = tid; i < NW; i += NTHR) {         // every real chunk
+      const int q = i / SAMP_BITWORDS, g0 = (i % SAMP_BITWORDS) * 32;
+      const int n = (q == NSHARD - 1 ? LAST_CHUNKS : SHARD_CHUNKS) - g0;
+      S.bw[i] = n >= 32 ? 0xffffffffu : (n > 0 ? (1u << n) - 1u : 0u);
+    }
+  }
+  if (tid == 0) S.own_w = -1;
   __syncthreads();
   const float tau = P.tau_arr ? P.tau_arr[row] : P.tau_s;
   const float c = __fdiv_rn(LOG2E, tau);
+  // keys at or below -inf's are the whole vocabulary (min_key 0 when
+  // unfiltered; key_value of keys below -inf's would be a NaN pattern)
   const float vmin_f = m.min_key <= KEY_NEG_INF ? -INFINITY : key_value(m.min_key);
   const __nv_bfloat162 vmin2 = __floats2bfloat162_rn(vmin_f, vmin_f);
   const uint4* rowp = reinterpret_cast<const uint4*>(P.logits + row * P.stride);
   constexpr int PER = (NW + NTHR - 1) / NTHR;
   const int w0 = min(NW, tid * PER), w1 = min(NW, w0 + PER);
-  // chunk g of shard q is 16-byte chunk q * SHARD_CHUNKS + g of the row
+  // ---- support mass per word, four chunk loads in flight at a time
   unsigned long long mine = 0;
   for (int w = w0; w < w1; ++w) {
     uint32_t bits = S.bw[w];
-    const int q = w / SAMP_BITWORDS, g0 = (w % SAMP_BITWORDS) * 32;
+    const uint4* base = rowp + (w / SAMP_BITWORDS) * SHARD_CHUNKS + (w % SAMP_BITWORDS) * 32;
+    unsigned long long ws = 0;
     while (bits) {
-      const int b = __ffs(bits) - 1;
-      bits &= bits - 1;
-      mine += chunk_support_mass(__ldg(rowp + q * SHARD_CHUNKS + g0 + b), vmin2, m.M, c);
+      int b[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        b[t] = bits ? __ffs(bits) - 1 : -1;
+        bits &= bits - 1;
+      }
+      uint4 v[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        if (b[t] >= 0) v[t] = __ldg(base + b[t]);
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        if (b[t] >= 0) ws += chunk_support_mass(v[t], vmin2, m.M, c);
     }
+    S.wm[w] = ws;
+    mine += ws;
   }
   uint32_t ec, tc;
   unsigned long long excl, zs;
-  block_excl_scan(0u, mine, ec, excl, tc, zs, S);
+  block_excl_scan(0u, mine, ec, excl, tc, zs, S);    // ends with a block barrier
   const uint32_t u = P.uniform ? P.uniform[row] : philox_word0(P.seed, P.counter[row]);
   const unsigned long long draw = scale_draw(u, zs);
-  if (mine == 0 || draw < excl || draw - excl >= mine) return;   // another thread holds it
-  // this thread's run holds the draw: walk its chunks, then the columns, in order
-  unsigned long long left = draw - excl;
-  for (int w = w0; w < w1; ++w) {
-    uint32_t bits = S.bw[w];
-    const int q = w / SAMP_BITWORDS, g0 = (w % SAMP_BITWORDS) * 32;
-    while (bits) {
-      const int b = __ffs(bits) - 1;
-      bits &= bits - 1;
-      const uint4 v = __ldg(rowp + q * SHARD_CHUNKS + g0 + b);
-      const unsigned long long mc = chunk_support_mass(v, vmin2, m.M, c);
-      if (left >= mc) {
-        left -= mc;
-        continue;
+  if (mine != 0 && draw >= excl && draw - excl < mine) {
+    // this thread's run holds the draw: the word, from the kept word masses
+    unsigned long long left = draw - excl;
+    for (int w = w0; w < w1; ++w) {
+      if (left < S.wm[w]) {
+        S.own_w = w;
+        S.own_res = left;
+        break;
       }
-      const uint32_t sb = chunk_support_bits(v, vmin2);
-      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-      int jstar = -1;
-      uint32_t xb = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t e = (w4[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
-        if (jstar < 0 && ((sb >> ((j >> 1) + 16 * (j & 1))) & 1u)) {
-          const unsigned long long qm = qfx(__uint_as_float(e << 16), m.M, c);
-          if (left < qm) {
-            jstar = j;
-            xb = e;
-          } else {
-            left -= qm;
-          }
-        }
-      }
-      const float xa = __uint_as_float(xb << 16);
-      const float d = __fdiv_rn(xa - m.M, tau);
-      const float full = d - logf(m.Z);
-      const float restr = (m.flags & SAMP_SEL) ? d - logf(__ull2float_rn(zs) * (1.0f / FX_SCALE)) : full;
-      P.out_token[row] = q * SW + (g0 + b) * 8 + jstar;
-      if (P.out_full) P.out_full[row] = full;
-      if (P.out_restr) P.out_restr[row] = restr;
-      return;
+      left -= S.wm[w];
     }
   }
+  __syncthreads();
+  const int w = S.own_w;
+  if (tid >= 32 || w < 0) return;
+  // ---- warp 0: the chunk (lane j takes chunk j of the word), then the column
+  const uint32_t bits = S.bw[w];
+  const int q = w / SAMP_BITWORDS, g0 = (w % SAMP_BITWORDS) * 32;
+  const bool marked = (bits >> lane) & 1u;
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  unsigned long long mc = 0;
+  if (marked) {
+    v = __ldg(rowp + q * SHARD_CHUNKS + g0 + lane);
+    mc = chunk_support_mass(v, vmin2, m.M, c);
+  }
+  const unsigned long long ex = warp_incl_scan_u64(mc) - mc;
+  const unsigned long long res = S.own_res;
+  if (mc == 0 || res < ex || res - ex >= mc) return;
+  unsigned long long left = res - ex;
+  const uint32_t sb = chunk_support_bits(v, vmin2);
+  const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+  int jstar = -1;
+  uint32_t xb = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t e = (w4[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
+    if (jstar < 0 && ((sb >> ((j >> 1) + 16 * (j & 1))) & 1u)) {
+      const unsigned long long qm = qfx(__uint_as_float(e << 16), m.M, c);
+      if (left < qm) {
+        jstar = j;
+        xb = e;
+      } else {
+        left -= qm;
+      }
+    }
+  }
+  const float xa = __uint_as_float(xb << 16);
+  const float d = __fdiv_rn(xa - m.M, tau);
+  const float full = d - logf(m.Z);
+  const float restr = (m.flags & SAMP_SEL) ? d - logf(__ull2float_rn(zs) * (1.0f / FX_SCALE)) : full;
+  P.out_token[row] = q * SW + (g0 + lane) * 8 + jstar;
+  if (P.out_full) P.out_full[row] = full;
+  if (P.out_restr) P.out_restr[row] = restr;
 }
 
 // The KL term of each row: the policy's full logprob minus the reference's.
@@ -1068,25 +942,8 @@ rlk_status sample_impl(const rlk_logp_args* args, unsigned long long seed,
   P.samp_bits = bits;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if ((s = launch<true, MODE_SAMPLE>(P, args->T, st)) != RLK_OK) return s;
-  if (bits) {
-    sample_bits_kernel<<<static_cast<unsigned>(args->T), NTHR, 0, st>>>(P);
-    const cudaError_t eb = cudaGetLastError();
-    if (eb != cudaSuccess) return fail(RLK_ECUDA, "kernel launch: %s", cudaGetErrorString(eb));
-  }
-  static bool configured[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(sizeof(SampSmem)));
-    if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    configured[dev] = true;
-  }
-  sample_kernel<<<static_cast<unsigned>(args->T * NSHARD), NTHR, sizeof(SampSmem), st>>>(P);
-  e = cudaGetLastError();
+  sample_row_kernel<<<static_cast<unsigned>(args->T), NTHR, 0, st>>>(P);
+  const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(RLK_ECUDA, "kernel launch: %s", cudaGetErrorString(e));
   return RLK_OK;
 }
