@@ -375,7 +375,8 @@ def run_ours(args, rank, world, local):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     # ---- the vocabulary-sharded form of the policy pair pass (8 shard buffers):
-    #      8 summary launches, 8 count launches, one merge
+    #      8 summary launches (which also keep each 16-byte chunk's maximum), 8
+    #      count launches (reading only the chunks that reach the window), one merge
     sharded = None
     if args.sharded_steps > 0:
         SW = pkg.SHARD_WIDTH
@@ -385,6 +386,7 @@ def run_ours(args, rank, world, local):
         aux = torch.empty((8, T_ROWS), dtype=torch.int32, device=dev)
         xt = torch.empty(T_ROWS, **f32)
         counts = torch.empty((8, T_ROWS, 1024), dtype=torch.int32, device=dev)
+        cmax = torch.empty((8, T_ROWS, pkg._binding.SHARD_CHUNKS), dtype=torch.int16, device=dev)
         s_full, s_restr = torch.empty(T_ROWS, **f32), torch.empty(T_ROWS, **f32)
         s_sup = torch.empty(T_ROWS, dtype=torch.int32, device=dev)
 
@@ -393,11 +395,11 @@ def run_ours(args, rank, world, local):
             for r in range(8):
                 pkg.shard_summary(shards[r], r, tg, TAU, TOP_P, TOP_K, out_max=maxes[r],
                                   out_sumexp=sumexps[r], out_aux=aux[r], out_target_logit=xt,
-                                  stream=stream)
+                                  out_chunk_max=cmax[r], stream=stream)
             if evs: evs[1].record(stream)
             for r in range(8):
                 pkg.shard_counts(shards[r], r, tg, maxes, sumexps, aux, TAU, TOP_P, TOP_K,
-                                 out_counts=counts[r], stream=stream)
+                                 out_counts=counts[r], chunk_max=cmax[r], stream=stream)
             if evs: evs[2].record(stream)
             pkg.logp_merge(maxes, sumexps, aux, xt, tg, TAU, TOP_P, TOP_K, counts=counts,
                            out_full=s_full, out_restr=s_restr, out_support=s_sup, stream=stream)
@@ -421,7 +423,7 @@ def run_ours(args, rank, world, local):
                    "summary_gbs": T_ROWS * VPAD * 2 / (phase[0] / 1e3) / 1e9,
                    "rows_outside_window": int((s_sup == -2).sum().item()),
                    "bitwise_equal_to_fused": same, "gpu_launches_per_step": 17}
-        del shards, counts
+        del shards, counts, cmax
 
     # ---- the backward pass (gradient of g_full * full + g_restr * restr, bf16
     #      [T, 152576] written): the streaming pass from the record saved by the

@@ -75,7 +75,7 @@ extern "C" {
 #define RLK_VOCAB_REAL 151936
 #define RLK_NUM_SHARDS 8
 #define RLK_SHARD_WIDTH 19072
-#define RLK_ABI_VERSION 1
+#define RLK_ABI_VERSION 2
 
 typedef enum {
   RLK_OK = 0,
@@ -355,20 +355,30 @@ typedef struct rlk_shard_args {
  *               maximum; rows with 1 <= k <= 1024: the shard's top-k witness
  *               (an order key); otherwise 0;
  *   out_target_logit  the target's logit, written only for rows whose target
- *               lies in this shard (other entries are left untouched). */
+ *               lies in this shard (other entries are left untouched);
+ *   out_chunk_max  optional (NULL: not written), device uint16 [T][2384],
+ *               16-byte aligned: the maximum (bf16 bits) of each 16-byte chunk
+ *               (8 columns) of the shard, for rlk_logp_shard_counts; shard 7
+ *               writes its 2304 real chunks. */
+#define RLK_SHARD_CHUNKS 2384
+
 rlk_status rlk_logp_shard_summary(const rlk_shard_args* args, float* out_max, float* out_sumexp,
-                                  int32_t* out_aux, float* out_target_logit, void* stream);
+                                  int32_t* out_aux, float* out_target_logit, uint16_t* out_chunk_max,
+                                  void* stream);
 
 /* Per-row exact counts of this shard's tokens on the row's candidate window
  * (at most 1024 order keys below the row maximum, derived from the 8
  * summaries exactly as the fused kernel derives it).  maxes, sumexps, aux
- * are the gathered shard-major [8][T] phase-1 outputs.  out_counts: device
+ * are the gathered shard-major [8][T] phase-1 outputs.  chunk_max: optional,
+ * this shard's out_chunk_max from phase 1; given, only the chunks whose
+ * maximum reaches the window are read (a few percent of the shard on typical
+ * rows) instead of the whole shard, with the same counts.  out_counts: device
  * uint32 [T][1024], 16-byte aligned; entry i counts the tokens whose bf16
  * order key is the row maximum's key minus i (zero beyond the window and for
  * rows without a top-k or top-p filter). */
 rlk_status rlk_logp_shard_counts(const rlk_shard_args* args, const float* maxes,
-                                 const float* sumexps, const int32_t* aux, uint32_t* out_counts,
-                                 void* stream);
+                                 const float* sumexps, const int32_t* aux,
+                                 const uint16_t* chunk_max, uint32_t* out_counts, void* stream);
 
 /* Merge of the 8 summaries of every row in fixed shard order.
  *   maxes, sumexps, aux: shard-major [8][T]; target_logit: [T] (from the

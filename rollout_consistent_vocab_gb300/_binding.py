@@ -97,8 +97,8 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     lib.rlk_linear_logp.argtypes = [VP, i64, i64, i64, VP, i64, VP, VP, ctypes.c_float, VP, VP, VP, VP]
     lib.rlk_logp_backward_saved.argtypes = [A, VP, VP, VP, VP, ctypes.c_int64, ctypes.c_int32, VP]
     SA = P(ShardArgs)
-    lib.rlk_logp_shard_summary.argtypes = [SA, VP, VP, VP, VP, VP]
-    lib.rlk_logp_shard_counts.argtypes = [SA, VP, VP, VP, VP, VP]
+    lib.rlk_logp_shard_summary.argtypes = [SA, VP, VP, VP, VP, VP, VP]
+    lib.rlk_logp_shard_counts.argtypes = [SA, VP, VP, VP, VP, VP, VP]
     f32, i32 = ctypes.c_float, ctypes.c_int32
     lib.rlk_logp_merge.argtypes = [VP, VP, VP, VP, ctypes.c_int64, VP, VP, f32, VP, f32, VP, i32,
                                    VP, i32, VP, VP, VP, VP]
@@ -113,7 +113,7 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     lib.rlk_last_error.restype = ctypes.c_char_p
     lib.rlk_abi_version.argtypes = []
     lib.rlk_abi_version.restype = ctypes.c_int
-    if lib.rlk_abi_version() != 1:
+    if lib.rlk_abi_version() != 2:
         raise ImportError("librlk_logp.so ABI version mismatch")
     _lib = lib
     return lib
@@ -278,23 +278,29 @@ def make_shard_args(shard_logits, shard, target, temperature=1.0, top_p=1.0, top
     return a
 
 
+SHARD_CHUNKS = 2384
+
+
 def shard_summary(shard_logits, shard, target, temperature=1.0, top_p=1.0, top_k=-1, *,
-                  out_max, out_sumexp, out_aux, out_target_logit, err_count=None, stream=None):
+                  out_max, out_sumexp, out_aux, out_target_logit, out_chunk_max=None, err_count=None,
+                  stream=None):
     """Phase 1 on one shard: per-row (max, sum-exp, aux) into the given [T]
-    views, and the target logit for rows whose target lies in this shard."""
+    views, the target logit for rows whose target lies in this shard, and
+    optionally each 16-byte chunk's maximum (int16 [T, 2384], bf16 bits)."""
     lib = load_library()
     a = make_shard_args(shard_logits, shard, target, temperature, top_p, top_k, err_count)
     check(lib.rlk_logp_shard_summary(ctypes.byref(a), _ptr(out_max), _ptr(out_sumexp), _ptr(out_aux),
-                                     _ptr(out_target_logit), _stream(stream)))
+                                     _ptr(out_target_logit), _ptr(out_chunk_max), _stream(stream)))
 
 
 def shard_counts(shard_logits, shard, target, maxes, sumexps, aux, temperature=1.0, top_p=1.0,
-                 top_k=-1, *, out_counts, stream=None):
-    """Phase 2 on one shard: exact per-key counts [T, 1024] on each row's window."""
+                 top_k=-1, *, out_counts, chunk_max=None, stream=None):
+    """Phase 2 on one shard: exact per-key counts [T, 1024] on each row's
+    window; with phase 1's chunk maxima only the chunks reaching it are read."""
     lib = load_library()
     a = make_shard_args(shard_logits, shard, target, temperature, top_p, top_k, None)
     check(lib.rlk_logp_shard_counts(ctypes.byref(a), _ptr(maxes), _ptr(sumexps), _ptr(aux),
-                                    _ptr(out_counts), _stream(stream)))
+                                    _ptr(chunk_max), _ptr(out_counts), _stream(stream)))
 
 
 def logp_merge(maxes, sumexps, aux, target_logit, target, temperature=1.0, top_p=1.0, top_k=-1, *,
@@ -319,10 +325,12 @@ def logp_merge(maxes, sumexps, aux, target_logit, target, temperature=1.0, top_p
 
 
 def logp_sharded(shards, target, temperature=1.0, top_p=1.0, top_k=-1, *, restricted=True,
-                 err_count=None, stream=None):
+                 chunk_maxima=True, err_count=None, stream=None):
     """All phases over 8 shard buffers (shard r holds vocabulary columns
-    [19072 r, 19072 (r+1))): summaries, then counts when restricted, then the
-    merge.  Returns (full,) or (full, restricted, support)."""
+    [19072 r, 19072 (r+1))): summaries, then counts when restricted (reading
+    only the chunks whose phase-1 maximum reaches the window, unless
+    ``chunk_maxima`` is False), then the merge.  Returns (full,) or
+    (full, restricted, support)."""
     torch = _torch()
     if len(shards) != NUM_SHARDS:
         raise ValueError(f"expected {NUM_SHARDS} shard tensors")
@@ -333,15 +341,20 @@ def logp_sharded(shards, target, temperature=1.0, top_p=1.0, top_k=-1, *, restri
     aux = torch.empty((NUM_SHARDS, T), dtype=torch.int32, device=dev)
     xt = torch.empty((T,), dtype=torch.float32, device=dev)
     pk = (top_p, top_k) if restricted else (1.0, -1)
+    cmax = (torch.empty((NUM_SHARDS, T, SHARD_CHUNKS), dtype=torch.int16, device=dev)
+            if restricted and chunk_maxima else None)
     for r, sh in enumerate(shards):
         shard_summary(sh, r, target, temperature, *pk, out_max=maxes[r], out_sumexp=sumexps[r],
-                      out_aux=aux[r], out_target_logit=xt, err_count=err_count, stream=stream)
+                      out_aux=aux[r], out_target_logit=xt,
+                      out_chunk_max=None if cmax is None else cmax[r], err_count=err_count,
+                      stream=stream)
     counts = None
     if restricted:
         counts = torch.empty((NUM_SHARDS, T, 1024), dtype=torch.int32, device=dev)
         for r, sh in enumerate(shards):
             shard_counts(sh, r, target, maxes, sumexps, aux, temperature, top_p, top_k,
-                         out_counts=counts[r], stream=stream)
+                         out_counts=counts[r], chunk_max=None if cmax is None else cmax[r],
+                         stream=stream)
     return logp_merge(maxes, sumexps, aux, xt, target, temperature, *pk, counts=counts,
                       stream=stream)
 

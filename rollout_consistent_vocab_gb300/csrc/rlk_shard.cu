@@ -22,6 +22,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <stddef.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -31,14 +32,17 @@
 
 namespace rlk {
 
+// The shard's copy comes last: the counts kernel, given phase 1's chunk
+// maxima, reads its few chunks from global memory and is launched without it.
 struct __align__(128) ShardSmem {
-  uint4 shard[SHARD_CHUNKS];
   uint32_t hist[WIN];              // counts kernel: per-key counts of this shard
   uint32_t red_u[NWARP];
   int32_t red_i[NWARP];
   float red_f[NWARP];
   unsigned long long bar_load;
+  alignas(128) uint4 shard[SHARD_CHUNKS];
 };
+constexpr size_t SHARD_SMEM_NO_COPY = offsetof(ShardSmem, shard);
 static_assert(sizeof(ShardSmem) + 1024 <= 233472 / CTAS_PER_SM, "shared memory budget of 5 CTAs per SM");
 
 struct ShardParams {
@@ -57,7 +61,10 @@ struct ShardParams {
   float* out_sumexp;
   int32_t* out_aux;
   float* out_xt;
+  uint16_t* out_cmax;           // optional: per 16-byte chunk, its maximum (bf16 bits), [T][SHARD_CHUNKS]
   // phase 2: gathered summaries in, counts out
+  const uint16_t* in_cmax;      // optional: phase 1's chunk maxima (only the chunks reaching
+                                // the window are then read)
   const float* g_max;
   const float* g_sumexp;
   const int32_t* g_aux;
@@ -139,6 +146,16 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM) shard_summary_kernel(const 
   const uint4* sh = S.shard;
   __nv_bfloat162 cm[MAXCH];
   const int tkey = pass_max(sh, tid, nchunks, cm);
+  if (P.out_cmax) {
+    // each chunk's maximum, for phase 2 to read only the chunks reaching the window
+    uint16_t* dst = P.out_cmax + row * SHARD_CHUNKS;
+#pragma unroll
+    for (int i = 0; i < MAXCH; ++i) {
+      const int ch = tid + i * NTHR;
+      if (ch < nchunks)
+        dst[ch] = __bfloat16_as_ushort(__hmax(__low2bfloat16(cm[i]), __high2bfloat16(cm[i])));
+    }
+  }
   const int kw = (rp.k + ROW_WARPS - 1) / ROW_WARPS;
   const bool k_bound = !rp.greedy && rp.k_on && kw <= 32;
   stage_max_bound(tkey, k_bound ? kw : 0, S);
@@ -204,7 +221,11 @@ __device__ __forceinline__ void gathered_window(const float* g_max, const float*
   candidate_window(M, L, Z, rp.tau, rp.p, rp.k_on, hi, lo);
 }
 
-__global__ void __launch_bounds__(NTHR, CTAS_PER_SM) shard_counts_kernel(const ShardParams P) {
+// CMAX: phase 1's chunk maxima are given; the kernel then reads only the
+// chunks that reach the window, from global memory, holds no shard copy and
+// runs more blocks per SM to cover the load latency.
+template <bool CMAX>
+__global__ void __launch_bounds__(NTHR, CMAX ? 16 : CTAS_PER_SM) shard_counts_kernel(const ShardParams P) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   ShardSmem& S = *reinterpret_cast<ShardSmem*>(smem_raw);
   const int tid = threadIdx.x;
@@ -222,7 +243,33 @@ __global__ void __launch_bounds__(NTHR, CTAS_PER_SM) shard_counts_kernel(const S
     // reaches the window
     const float xm = P.g_max[static_cast<int64_t>(r) * P.T + row];
     const bool count = (xm > -INFINITY) && (xm < INFINITY) && lo <= hi && okey_of(xm) >= lo;
-    if (count) {
+    if (CMAX && count) {
+      // phase 1's chunk maxima pick the chunks to read, straight from global memory
+      __syncthreads();          // histogram zeroed
+      const float vlo_f = key_value(lo);
+      const uint16_t* cmax = P.in_cmax + row * SHARD_CHUNKS;
+      const uint4* rowv = reinterpret_cast<const uint4*>(P.logits + row * P.stride);
+      // all of this thread's chunk maxima first (independent loads), then the
+      // few chunks that reach the window
+      uint32_t hit = 0;
+#pragma unroll
+      for (int i = 0; i < MAXCH; ++i) {
+        const int ch = tid + i * NTHR;
+        if (ch < nchunks && __uint_as_float(static_cast<uint32_t>(__ldg(cmax + ch)) << 16) >= vlo_f)
+          hit |= 1u << i;
+      }
+      while (hit) {
+        const int i = __ffs(hit) - 1;
+        hit &= hit - 1;
+        const uint4 v = __ldg(rowv + tid + i * NTHR);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t b = (w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
+          if (__uint_as_float(b << 16) >= vlo_f) red_shared_add(&S.hist[hi - okey(b)], 1u);
+        }
+      }
+    } else if (!CMAX && count) {
       const uint32_t bar = smem_addr(&S.bar_load);
       load_shard_row(S, P.logits + row * P.stride, nchunks);
       __syncthreads();          // barrier initialised and histogram zeroed
@@ -403,7 +450,8 @@ ShardParams make_shard_params(const rlk_shard_args* a) {
 
 template <int WHICH>
 rlk_status launch_shard(void (*kernel)(ShardParams), const ShardParams& P, cudaStream_t stream) {
-  static bool configured[64] = {};
+  static bool configured_by_kind[2][64] = {};
+  bool* configured = configured_by_kind[(WHICH == 1 && P.in_cmax) ? 1 : 0];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
@@ -415,7 +463,9 @@ rlk_status launch_shard(void (*kernel)(ShardParams), const ShardParams& P, cudaS
     if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     configured[dev] = true;
   }
-  kernel<<<static_cast<unsigned>(P.T), NTHR, sizeof(ShardSmem), stream>>>(P);
+  // the counts kernel with chunk maxima never touches the shard copy
+  const size_t smem = (WHICH == 1 && P.in_cmax) ? SHARD_SMEM_NO_COPY : sizeof(ShardSmem);
+  kernel<<<static_cast<unsigned>(P.T), NTHR, smem, stream>>>(P);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(RLK_ECUDA, "kernel launch: %s", cudaGetErrorString(e));
   return RLK_OK;
@@ -428,7 +478,8 @@ using namespace rlk;
 extern "C" {
 
 rlk_status rlk_logp_shard_summary(const rlk_shard_args* args, float* out_max, float* out_sumexp,
-                                  int32_t* out_aux, float* out_target_logit, void* stream) {
+                                  int32_t* out_aux, float* out_target_logit, uint16_t* out_chunk_max,
+                                  void* stream) {
   rlk_status s = check_shard_args(args);
   if (s != RLK_OK || args->T == 0) return s;
   if ((s = check_out(out_max, "out_max", true)) != RLK_OK) return s;
@@ -440,12 +491,15 @@ rlk_status rlk_logp_shard_summary(const rlk_shard_args* args, float* out_max, fl
   P.out_sumexp = out_sumexp;
   P.out_aux = out_aux;
   P.out_xt = out_target_logit;
+  if (out_chunk_max && !aligned(out_chunk_max, 16))
+    return fail(RLK_EALIGN, "out_chunk_max is not 16-byte aligned");
+  P.out_cmax = out_chunk_max;
   return launch_shard<0>(shard_summary_kernel, P, static_cast<cudaStream_t>(stream));
 }
 
 rlk_status rlk_logp_shard_counts(const rlk_shard_args* args, const float* maxes,
-                                 const float* sumexps, const int32_t* aux, uint32_t* out_counts,
-                                 void* stream) {
+                                 const float* sumexps, const int32_t* aux,
+                                 const uint16_t* chunk_max, uint32_t* out_counts, void* stream) {
   rlk_status s = check_shard_args(args);
   if (s != RLK_OK || args->T == 0) return s;
   if ((s = check_out(maxes, "maxes", true)) != RLK_OK) return s;
@@ -458,7 +512,10 @@ rlk_status rlk_logp_shard_counts(const rlk_shard_args* args, const float* maxes,
   P.g_sumexp = sumexps;
   P.g_aux = aux;
   P.out_counts = out_counts;
-  return launch_shard<1>(shard_counts_kernel, P, static_cast<cudaStream_t>(stream));
+  if (chunk_max && !aligned(chunk_max, 16)) return fail(RLK_EALIGN, "chunk_max is not 16-byte aligned");
+  P.in_cmax = chunk_max;
+  return chunk_max ? launch_shard<1>(shard_counts_kernel<true>, P, static_cast<cudaStream_t>(stream))
+                   : launch_shard<1>(shard_counts_kernel<false>, P, static_cast<cudaStream_t>(stream));
 }
 
 rlk_status rlk_logp_merge(const float* maxes, const float* sumexps, const int32_t* aux,

@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.rlk_abi_version() == 1
+    assert lib.rlk_abi_version() == 2
     assert lib.rlk_status_string(0) == b"ok"
     assert lib.rlk_status_string(2) == b"misaligned pointer or stride"
 
@@ -167,22 +167,24 @@ def _sargs(**kw):
 ])
 def test_shard_entry_points_reject_bad_arguments_on_host(lib, kw, status):
     a = _sargs(**kw)
-    assert lib.rlk_logp_shard_summary(ctypes.byref(a), OUT, OUT, OUT, OUT, None) == status
-    assert lib.rlk_logp_shard_counts(ctypes.byref(a), OUT, OUT, OUT, OUT, None) == status
+    assert lib.rlk_logp_shard_summary(ctypes.byref(a), OUT, OUT, OUT, OUT, None, None) == status
+    assert lib.rlk_logp_shard_counts(ctypes.byref(a), OUT, OUT, OUT, None, OUT, None) == status
     assert lib.rlk_last_error()
 
 
 def test_shard_outputs_checked(lib):
     a = _sargs()
-    assert lib.rlk_logp_shard_summary(ctypes.byref(a), None, OUT, OUT, OUT, None) == b.RLK_EINVAL
-    assert lib.rlk_logp_shard_summary(ctypes.byref(a), OUT, OUT, OUT, OUT + 2, None) == b.RLK_EALIGN
-    assert lib.rlk_logp_shard_counts(ctypes.byref(a), OUT, OUT, OUT, None, None) == b.RLK_EINVAL
+    assert lib.rlk_logp_shard_summary(ctypes.byref(a), None, OUT, OUT, OUT, None, None) == b.RLK_EINVAL
+    assert lib.rlk_logp_shard_summary(ctypes.byref(a), OUT, OUT, OUT, OUT + 2, None, None) == b.RLK_EALIGN
+    assert lib.rlk_logp_shard_summary(ctypes.byref(a), OUT, OUT, OUT, OUT, OUT + 2, None) == b.RLK_EALIGN
+    assert lib.rlk_logp_shard_counts(ctypes.byref(a), OUT, OUT, OUT, None, None, None) == b.RLK_EINVAL
     # the count rows are copied out as 16-byte vectors
-    assert lib.rlk_logp_shard_counts(ctypes.byref(a), OUT, OUT, OUT, OUT + 4, None) == b.RLK_EALIGN
-    assert lib.rlk_logp_shard_counts(ctypes.byref(a), None, OUT, OUT, OUT, None) == b.RLK_EINVAL
+    assert lib.rlk_logp_shard_counts(ctypes.byref(a), OUT, OUT, OUT, None, OUT + 4, None) == b.RLK_EALIGN
+    assert lib.rlk_logp_shard_counts(ctypes.byref(a), OUT, OUT, OUT, OUT + 2, OUT, None) == b.RLK_EALIGN
+    assert lib.rlk_logp_shard_counts(ctypes.byref(a), None, OUT, OUT, None, OUT, None) == b.RLK_EINVAL
     z = _sargs(T=0, logits=None, target=None)
-    assert lib.rlk_logp_shard_summary(ctypes.byref(z), None, None, None, None, None) == b.RLK_OK
-    assert lib.rlk_logp_shard_counts(ctypes.byref(z), None, None, None, None, None) == b.RLK_OK
+    assert lib.rlk_logp_shard_summary(ctypes.byref(z), None, None, None, None, None, None) == b.RLK_OK
+    assert lib.rlk_logp_shard_counts(ctypes.byref(z), None, None, None, None, None, None) == b.RLK_OK
 
 
 def _merge(lib, T=4, tau=0.7, p=0.95, k=-1, counts=OUT, nc=8, full=OUT, restr=OUT, sup=OUT,

@@ -60,7 +60,11 @@ def mixed_rows(T: int, seed: int):
 def compare(x, t, tau, p, k, err=None, err_sharded=None):
     f0, r0, s0 = pkg.logp_pair(x, t, tau, p, k, err_count=err)
     f1, r1, s1 = pkg.logp_sharded(split(x), t, tau, p, k, err_count=err_sharded)
+    # phase 2 reading whole shards instead of the chunks phase 1 marked: the same bits
+    f2, r2, s2 = pkg.logp_sharded(split(x), t, tau, p, k, chunk_maxima=False)
     torch.cuda.synchronize()
+    for u, v in ((f1, f2), (r1, r2), (s1, s2)):
+        assert torch.equal(u.view(torch.int32), v.view(torch.int32))
     f0b, f1b = bits32(f0), bits32(f1)
     assert (f0b == f1b).all(), np.nonzero(f0b != f1b)[0][:10]
     s0n, s1n = s0.cpu().numpy(), s1.cpu().numpy()
