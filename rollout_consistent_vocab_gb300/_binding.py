@@ -597,7 +597,10 @@ def grad_norm(tensors, *, distributed=False, group=None, bins=None, out=None, st
     torch = _torch()
     if isinstance(tensors, torch.Tensor):
         tensors = [tensors]
+    tensors = list(tensors)
     if bins is None:
+        if not tensors:
+            raise ValueError("grad_norm: no tensors (pass bins to take the device from them)")
         bins = norm_bins(tensors[0].device)
     else:
         bins.zero_()
