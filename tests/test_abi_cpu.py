@@ -283,3 +283,25 @@ def test_linear_logp_validation(lib):
     assert L(ws=None) == b.RLK_EINVAL
     assert L(ws=0xB0004) == b.RLK_EALIGN
     assert L(out=None) == b.RLK_EINVAL
+
+
+def _declared_param_counts():
+    """Parameter count of every rlk_* function declared in include/*.h."""
+    counts = {}
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", fn)).read(), flags=re.S)
+        for m in re.finditer(r"(?:rlk_status|const char\*|int)\s+(rlk_\w+)\s*\(([^)]*)\)\s*;", text):
+            params = m.group(2).strip()
+            counts[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return counts
+
+
+def test_binding_argument_counts_match_the_headers(lib):
+    """The ctypes binding passes as many arguments as each C declaration takes."""
+    counts = _declared_param_counts()
+    assert set(counts) == set(b.EXPORTS)
+    for name, n in counts.items():
+        argtypes = getattr(lib, name).argtypes
+        assert argtypes is not None and len(argtypes) == n, (name, n, argtypes)
