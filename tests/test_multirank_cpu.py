@@ -107,3 +107,21 @@ def test_cpu_baseline_one_process_per_core():
     tg = W.structural_targets(4, wl.hot, wl.hot_n, seed=2).numpy()
     rate, rows, secs, ncores = bench.cpu_oracle_rate_all_cores(bits, rbits, tg, 1.0)
     assert ncores >= 1 and rows >= ncores and secs >= 1.0 and rate == rows / secs
+
+
+def test_reference_arm_prints_one_complete_line(capsys):
+    """bench.py --impl reference on rank 0: one JSON line with the contract's keys."""
+    import json
+    import bench
+
+    class A:
+        steps, warmup, gpus = 1, 0, 1
+    bench.run_reference(A, rank=0, world=1)
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
