@@ -305,3 +305,24 @@ def test_binding_argument_counts_match_the_headers(lib):
     for name, n in counts.items():
         argtypes = getattr(lib, name).argtypes
         assert argtypes is not None and len(argtypes) == n, (name, n, argtypes)
+
+
+def test_binding_sizes_match_the_header_macros():
+    """The binding's workspace sizes and constants follow the C header's macros."""
+    text = open(os.path.join(ROOT, "include", "rlk_logp.h")).read()
+    norm = open(os.path.join(ROOT, "include", "rlk_norm.h")).read()
+
+    def macro(src, name):
+        m = re.search(r"#define\s+" + name + r"(\([A-Za-z]+\))?\s+(.+)", src)
+        assert m, name
+        return m.group(2).strip()
+
+    for T in (1, 7, 8192):
+        ws = eval(re.sub(r"\(size_t\)|u\b", "", macro(text, "RLK_SAMPLE_WORKSPACE_BYTES")).replace("(T)", f"({T})"))
+        assert b.sample_workspace_bytes(T) == ws
+        lw = eval(re.sub(r"\(size_t\)|u\b", "", macro(text, "RLK_LINEAR_WORKSPACE_BYTES")).replace("(T)", f"({T})"))
+        assert b.linear_workspace_bytes(T) == lw
+    assert int(macro(text, "RLK_SHARD_CHUNKS")) == b.SHARD_CHUNKS
+    assert int(macro(norm, "RLK_NORM_BINS")) == b.NORM_BINS
+    assert int(macro(text, "RLK_VOCAB_PADDED")) == b.VOCAB_PADDED
+    assert int(macro(text, "RLK_VOCAB_REAL")) == b.VOCAB_REAL
