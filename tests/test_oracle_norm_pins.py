@@ -173,3 +173,25 @@ def test_planted_norm_mistake_is_caught(mutant):
         except (AssertionError, ValueError, OverflowError):
             failed.append(pin.__name__)
     assert failed, f"{mutant.__name__} passed every pin"
+
+
+def test_norm_equals_fsum_on_random_float32_arrays():
+    """Property: for any FP32 array (any exponents, subnormals, zeros), the
+    oracle's sum of squares is math.fsum of the FP32 squares."""
+    hypothesis = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+
+    @hypothesis.settings(max_examples=200, deadline=None)
+    @hypothesis.given(st.lists(st.floats(width=32, allow_nan=False, allow_infinity=False),
+                               min_size=0, max_size=64))
+    def check(vals):
+        x = np.array(vals, dtype=np.float32)
+        with np.errstate(over="ignore", under="ignore"):
+            q = (x * x).astype(np.float64)
+        if not np.all(np.isfinite(q)):
+            assert oracle.grad_norm(x, "f32") == (math.inf, math.inf)
+            return
+        want = math.fsum(q.tolist())
+        assert oracle.grad_norm(x, "f32") == (want, math.sqrt(want))
+
+    check()
