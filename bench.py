@@ -62,6 +62,8 @@ def parse():
                     help="calls of the deterministic gradient norm timed per size (0: skip)")
     ap.add_argument("--norm-small-only", action="store_true",
                     help="time the gradient norm on the 10M-element case only (for profiling)")
+    ap.add_argument("--configs-steps", type=int, default=20,
+                    help="launches of the pair pass timed on each of the other workloads (0: skip)")
     ap.add_argument("--rows", type=int, default=T_ROWS,
                     help="rows per GPU (default: the 8192-row workload; smaller only for profiling)")
     return ap.parse_args()
@@ -183,19 +185,65 @@ class ClockSampler:
 # ------------------------------------------------------------------ CPU oracle
 
 def cpu_oracle_rate(bits, ref_bits, targets, seconds: float):
-    """Rows per second of the oracle over a bounded sample (policy pair + ref full + KL)."""
+    """Rows per second of the oracle over a bounded sample (policy pair + ref full + KL).
+    Also returns each resolved row's oracle results, which the parity object
+    compares with the GPU's outputs for the same rows."""
     import oracle
     t0 = time.perf_counter()
     n = 0
+    results = []
     while n < bits.shape[0]:
         t = int(targets[n])
-        oracle.logp_row(bits[n], TAU, TOP_P, TOP_K, t)
-        oracle.logp_row(ref_bits[n], TAU, 1.0, -1, t)
+        r = oracle.logp_row(bits[n], TAU, TOP_P, TOP_K, t, want_margins=True)
+        rr = oracle.logp_row(ref_bits[n], TAU, 1.0, -1, t)
+        results.append((r, rr.full))
         n += 1
         if time.perf_counter() - t0 > seconds:
             break
     dt = time.perf_counter() - t0
-    return n / dt, n, dt
+    return n / dt, n, dt, results
+
+
+def parity_summary(results, full, restr, sup, full_ref, kl, tol=2e-5, margin=1e-6):
+    """GPU outputs of the sampled rows against the oracle results of the CPU
+    leg: rows compared, worst deviations, support differences (each allowed
+    only at a tie class within `margin` of the nucleus threshold), and rows
+    with such a near-threshold class."""
+    import numpy as np
+    worst_f = worst_r = worst_kl = 0.0
+    differs = differs_far = near_rows = near_tokens = over_tol = 0
+    for i, (r, ref_full) in enumerate(results):
+        df = abs(float(full[i]) - r.full)
+        dk = abs(float(kl[i]) - (r.full - ref_full))
+        worst_f = max(worst_f, df, abs(float(full_ref[i]) - ref_full))
+        worst_kl = max(worst_kl, dk)
+        if r.g_desc is not None:
+            near = np.abs(r.g_desc - TOP_P) / TOP_P <= margin
+            if near.any():
+                near_rows += 1
+                near_tokens += int(np.sum(r.counts_desc[near]))
+        if int(sup[i]) != r.support:
+            differs += 1
+            cum = np.cumsum(r.counts_desc) if r.counts_desc is not None else np.array([])
+            ok = int(sup[i]) in cum
+            if ok:
+                j_g = int(np.nonzero(cum == int(sup[i]))[0][0])
+                j_o = int(np.nonzero(cum == r.support)[0][0])
+                ok = all(abs(r.g_desc[j] - TOP_P) / TOP_P <= margin
+                         for j in range(min(j_g, j_o) + 1, max(j_g, j_o) + 1))
+            differs_far += 0 if ok else 1
+        elif math.isfinite(r.restr):
+            worst_r = max(worst_r, abs(float(restr[i]) - r.restr))
+        elif float(restr[i]) != r.restr:
+            over_tol += 1
+        if df > tol or dk > 2 * tol:
+            over_tol += 1
+    return {"rows": len(results), "max_abs_dfull": worst_f, "max_abs_drestr": worst_r,
+            "max_abs_dkl": worst_kl, "tol": tol, "rows_over_tol": over_tol,
+            "support_differs": differs, "support_differs_beyond_margin": differs_far,
+            "near_threshold_rows": near_rows, "near_threshold_tokens": near_tokens,
+            "margin": margin,
+            "pass": over_tol == 0 and differs_far == 0}
 
 
 def cpu_oracle_rate_all_cores(bits, ref_bits, targets, seconds: float):
@@ -220,21 +268,40 @@ def cpu_oracle_rate_all_cores(bits, ref_bits, targets, seconds: float):
 
 
 def run_reference(args, rank, world):
-    """The oracle as the reference arm: each step is a bounded sample of the workload."""
+    """The oracle as the reference arm: each step is a bounded sample of the workload.
+
+    The sample is rows of the very workload the other arm times (generated
+    on the GPU with the same seeds when one is present, then copied to the
+    host), every 97th row, policy pair + reference full logprob per row."""
     if rank != 0:
         return
     import numpy as np
     import torch
     from rollout_consistent_vocab_gb300 import workloads as W
     rows = max(1, min(8, 200 // max(1, args.steps)))
-    wl = W.workload_c2(device="cpu", T=64)
-    bits = wl.logits.view(torch.int16).numpy().view(np.uint16)
-    rbits = wl.ref_logits.view(torch.int16).numpy().view(np.uint16)
-    tg = W.structural_targets(64, wl.hot, wl.hot_n, seed=2).numpy()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    if dev == "cuda":
+        x, hot, n = W.hot_logits(T_ROWS, 1, 256, seed=rank_seed(2, 0), device=dev)
+        ref = W.perturbed_copy(x, 0.05, seed=rank_seed(102, 0))
+        tg_all = W.structural_targets(T_ROWS, hot, n, seed=rank_seed(2, 0), device=dev)
+        pick = torch.arange(0, T_ROWS, 97, device=dev)
+        bits = x[pick].view(torch.int16).cpu().numpy().view(np.uint16)
+        rbits = ref[pick].view(torch.int16).cpu().numpy().view(np.uint16)
+        tg = tg_all[pick].cpu().numpy()
+        del x, ref, hot, n, tg_all
+        torch.cuda.empty_cache()
+        where = f"every 97th row ({bits.shape[0]} rows) of this T={T_ROWS} workload"
+    else:
+        wl = W.workload_c2(device="cpu", T=64)
+        bits = wl.logits.view(torch.int16).numpy().view(np.uint16)
+        rbits = wl.ref_logits.view(torch.int16).numpy().view(np.uint16)
+        tg = W.structural_targets(64, wl.hot, wl.hot_n, seed=2).numpy()
+        where = "a 64-row instance of this workload's distribution generated on the CPU (no GPU here)"
+    nsamp = bits.shape[0]
     import oracle
     def step(i):
         for j in range(rows):
-            r = (i * rows + j) % 64
+            r = (i * rows + j) % nsamp
             oracle.logp_row(bits[r], TAU, TOP_P, TOP_K, int(tg[r]))
             oracle.logp_row(rbits[r], TAU, 1.0, -1, int(tg[r]))
     for i in range(args.warmup):
@@ -250,7 +317,8 @@ def run_reference(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{rows} rows of the T=8192 workload per step (policy pair + ref full)"},
+                         "sample": f"{rows} rows per step cycling through {where} "
+                                   f"(policy pair + reference full per row), one host core"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -318,6 +386,8 @@ def run_ours(args, rank, world, local):
     total_ms = ev[0].elapsed_time(ev[K])
     total_ms = max_over_ranks(total_ms, dev)
     value = throughput(world, T_ROWS, K, total_ms)
+    # the step's outputs, kept for the parity sample of the CPU leg
+    step_out = [t.clone() for t in (full, restr, sup, full_ref, kl)]
 
     # ---- the policy pair pass alone (the full + restricted pass whose HBM
     #      fraction is the roofline figure), and the reference pass alone
@@ -333,6 +403,51 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     pair_ms = [pev[2 * i].elapsed_time(pev[2 * i + 1]) for i in range(Kp)]
     ref_ms = [pev[2 * i + 1].elapsed_time(pev[2 * i + 2]) for i in range(Kp)]
+
+    # ---- the pair pass on the other workloads (full + restricted, per-row
+    #      parameters for the mixed one); the small ones flush L2 between launches
+    configs = None
+    if args.configs_steps > 0:
+        configs = {}
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        for name, make in (("c0", W.workload_c0), ("c1", W.workload_c1), ("c4", W.workload_c4)):
+            wl = make(device=dev)
+            tgc = W.structural_targets(wl.T, wl.hot, wl.hot_n, seed=rank_seed(5, rank), device=dev)
+            fo, ro = torch.empty(wl.T, **f32), torch.empty(wl.T, **f32)
+            so = torch.empty(wl.T, dtype=torch.int32, device=dev)
+            nbytes = wl.T * VPAD * 2
+            do_flush = nbytes < 4 * (129 << 20)
+
+            def cstep():
+                pkg.logp_pair(wl.logits, tgc, wl.temperature, wl.top_p, wl.top_k, out_full=fo,
+                              out_restr=ro, out_support=so, stream=stream)
+
+            for _ in range(3):
+                cstep()
+            torch.cuda.synchronize()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.configs_steps)]
+            for a, b in evs:
+                if do_flush:
+                    flush.fill_(1)
+                a.record(stream)
+                cstep()
+                b.record(stream)
+            torch.cuda.synchronize()
+            ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+            peak_c, peak_kind_c = measured_peak()
+            configs[name] = {"workload": wl.name, "rows": wl.T,
+                             "temperature": wl.temperature if isinstance(wl.temperature, float) else "per row",
+                             "top_p": wl.top_p if isinstance(wl.top_p, float) else "per row",
+                             "top_k": wl.top_k if isinstance(wl.top_k, int) else "per row",
+                             "ms": ms, "tokens_per_s": wl.T / (ms / 1e3),
+                             "achieved_gbs": nbytes / (ms / 1e3) / 1e9,
+                             "frac": nbytes / (ms / 1e3) / 1e9 / peak_c, "peak_kind": peak_kind_c,
+                             "l2": "256 MB write before each launch" if do_flush else "inputs larger than L2",
+                             "launches_timed": args.configs_steps}
+            del wl, tgc, fo, ro, so
+            torch.cuda.empty_cache()
+        del flush
 
     # ---- end to end through the public API from pinned host buffers
     e2e = None
@@ -603,13 +718,18 @@ def run_ours(args, rank, world, local):
         torch.cuda.empty_cache()
 
     cpu = None
+    parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample_rows = np.arange(0, T_ROWS, 7)
         ridx = torch.as_tensor(sample_rows, device=dev)
         bits = x[ridx].view(torch.int16).cpu().numpy().view(np.uint16)
         rbits = ref[ridx].view(torch.int16).cpu().numpy().view(np.uint16)
         tgs = tg[ridx].cpu().numpy()
-        rate1, nrows1, secs1 = cpu_oracle_rate(bits, rbits, tgs, args.cpu_seconds / 2)
+        rate1, nrows1, secs1, o_res = cpu_oracle_rate(bits, rbits, tgs, args.cpu_seconds / 2)
+        picked = torch.as_tensor(sample_rows[:nrows1], device=dev)
+        parity = parity_summary(o_res, *(t[picked].cpu().numpy() for t in step_out))
+        parity["sample"] = (f"rows 0, 7, 14, ... of the bench workload ({nrows1} rows, the ones the "
+                            f"single-core oracle leg resolved), the step's outputs")
         sub = slice(0, None, 9)          # every 63rd row of the workload for the all-core leg
         rate, nrows, secs, ncores = cpu_oracle_rate_all_cores(bits[sub], rbits[sub], tgs[sub],
                                                               args.cpu_seconds / 2)
@@ -649,6 +769,8 @@ def run_ours(args, rank, world, local):
             "ref_pass": {"avg_launch_ms": ref_avg,
                          "achieved_gbs": algo_bytes / (ref_avg / 1e3) / 1e9},
             "gpu_launches": 2 * K,
+            "parity": parity,
+            "configs": configs,
             "clocks": clk.summary(),
             "e2e": e2e,
             "sharded": sharded,

@@ -266,9 +266,10 @@ rlk_status rlk_sample(const rlk_logp_args* args, unsigned long long seed,
  *     16 bytes (1 MiB) of device memory on every GPU that loads the library,
  *     held until the process exits.  T above RLK_SAMPLE_NOALLOC_MAX_ROWS is
  *     rejected with RLK_EINVAL (split the batch, or use rlk_sample).
- *   Set-up: the first call on each device (with that device current) looks
- *     up the array's device address; make that first call before any stream
- *     capture.  Nothing is allocated by this or any later call.
+ *   Set-up: every call looks up the array's device address on the current
+ *     device (cudaGetSymbolAddress, no stream work).  The first call on a
+ *     device also loads the library's device code there: make that first
+ *     call before any stream capture.  Nothing is allocated by any call.
  *   Sharing: every call on a device uses the same array.  Each call writes
  *     every record it reads, so leftovers from an earlier call never matter,
  *     but calls that overlap on the GPU (different streams, or host threads

@@ -136,6 +136,27 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar) {
   }
   return true;
 }
+// Wait on phase 0 of a barrier until a wall-clock deadline (globaltimer ns).
+// Used after a bounded wait gave up on a peer's messages: the CTA stays
+// resident, so that a late message never lands in the shared memory of a
+// CTA that has exited.  Deadlines are staged from each CTA's start (the
+// CTAs of a cluster start together), every stage's senders finishing their
+// own bounded waits before the stage's receivers stop draining:
+//   DRAIN_MID:  exchange messages, sent once the sender's shard copy landed
+//               (at most 2 TIMEOUT_NS after its start);
+//   DRAIN_SUM:  summaries and histogram adds, sent after the sender's
+//               exchange wait (at most DRAIN_MID);
+//   DRAIN_LEAD: the backward's row record, sent after the leader's summary
+//               wait (at most DRAIN_SUM) and its selection.
+constexpr unsigned long long DRAIN_MID = 4 * TIMEOUT_NS;
+constexpr unsigned long long DRAIN_SUM = 6 * TIMEOUT_NS;
+constexpr unsigned long long DRAIN_LEAD = 8 * TIMEOUT_NS;
+__device__ __forceinline__ bool mbar_wait_until(uint32_t bar, unsigned long long deadline) {
+  while (!mbar_try(bar, 0)) {
+    if (global_timer() > deadline) return false;
+  }
+  return true;
+}
 
 // packed f32x2 arithmetic (sm_100+ FP32x2 instructions)
 __device__ __forceinline__ uint64_t pack2(float lo, float hi) {

@@ -186,6 +186,9 @@ logp_kernel(const KParams P) {
                            : nullptr;
 
   // ---- 1. the bulk copy of the shard into shared memory goes out first
+  // (thread 0 also notes the start time, from which the drain deadlines of
+  // a timed-out wait are measured)
+  const unsigned long long t_start = (tid == 0) ? global_timer() : 0ull;
   if (tid == 0) {
     mbar_init(bar_load, 1);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -209,7 +212,7 @@ logp_kernel(const KParams P) {
   if (!valid) {
     if (tid == 0) {
       // the copy writes this CTA's shared memory: let it land before leaving
-      mbar_wait_bounded(bar_load);
+      if (!mbar_wait_bounded(bar_load)) mbar_wait_bounded(bar_load);
       if (r == 0) {
         if (o_full) o_full[row] = __int_as_float(0x7fc00000);
         if (RESTR && o_restr) o_restr[row] = __int_as_float(0x7fc00000);
@@ -322,7 +325,10 @@ logp_kernel(const KParams P) {
   if (sel) {
     if (tid == 0) {
       // the window of candidate keys, the same in every CTA of the cluster
-      if (!mbar_wait_bounded(bar_mid)) flags |= FLAG_TIMEOUT;
+      if (!mbar_wait_bounded(bar_mid)) {
+        flags |= FLAG_TIMEOUT;
+        mbar_wait_until(bar_mid, t_start + DRAIN_MID);   // stay resident for late messages
+      }
       int L = 0x7fffffff;
       float M = -INFINITY;
 #pragma unroll
@@ -443,8 +449,15 @@ logp_kernel(const KParams P) {
   }
   if (r != 0) {                // messages carry everything the leader needs
     if (BWD) {
-      // the leader's resolution of the row, then this shard's gradient
-      const bool ok = mbar_wait_bounded(bar_lead);
+      // the leader's resolution of the row (one thread waits; after a timeout
+      // it stays resident for a late record), then this shard's gradient
+      if (tid == 0) {
+        const bool got = mbar_wait_bounded(bar_lead);
+        if (!got) mbar_wait_until(bar_lead, t_start + DRAIN_LEAD);
+        S.win[3] = got ? 1 : 0;
+      }
+      __syncthreads();
+      const bool ok = S.win[3] != 0;
       const GradCoeffs m = ok ? grad_coeffs(*reinterpret_cast<const rlk_row_stats*>(&S.lead), tau,
                                             P.g_full ? P.g_full[row] : 0.0f,
                                             (RESTR && P.g_restr) ? P.g_restr[row] : 0.0f)
@@ -459,12 +472,19 @@ logp_kernel(const KParams P) {
   // whole block joins only for the general (wide-support) selection.
   if (tid == 0) {
     bool timed_out = !mbar_wait_bounded(bar_sum);
-    uint32_t pushed = 0;
+    // after a timeout, stay resident until every peer is past its own
+    // bounded waits (its summary and adds are then in); the adds can only be
+    // awaited once every summary has announced their number
+    const bool sums_in = !timed_out || mbar_wait_until(bar_sum, t_start + DRAIN_SUM);
+    if (sel && sums_in) {
+      uint32_t pushed = 0;
 #pragma unroll
-    for (int q = 1; q < NSHARD; ++q) pushed += S.slot[q].aux;
-    if (sel) {
+      for (int q = 1; q < NSHARD; ++q) pushed += S.slot[q].aux;
       mbar_arrive_expect_tx(bar_hist, 4u * pushed);
-      if (!mbar_wait_bounded(bar_hist)) timed_out = true;
+      if (!mbar_wait_bounded(bar_hist)) {
+        timed_out = true;
+        mbar_wait_until(bar_hist, t_start + DRAIN_SUM);
+      }
     }
     S.win[3] = timed_out ? 1 : 0;
   }

@@ -12,7 +12,6 @@
 // is allocated per call.
 
 #include <cuda_runtime.h>
-#include <mutex>
 #include <stdint.h>
 
 #include "rlk_logp.h"
@@ -25,25 +24,15 @@ namespace rlk {
 // from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_sample_scratch[RLK_SAMPLE_NOALLOC_MAX_ROWS * 16];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// The scratch array's device address on the current device, looked up on the
-// first call made with that device current.
+// The scratch array's device address on the current device.  It is looked
+// up on every call rather than cached: the lookup is a host-side table read
+// (no stream work), and a cached address would go stale if the device's
+// primary context were reset and the library's module loaded again.
 rlk_status scratch_on_current_device(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices) return fail(RLK_EINVAL, "device %d: at most %d devices", dev, kMaxDevices);
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_sample_scratch);
-    if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_sample_scratch);
+  if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+  *out = p;
   return RLK_OK;
 }
 

@@ -125,3 +125,28 @@ def test_reference_arm_prints_one_complete_line(capsys):
         assert key in d, key
     assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_bench_parity_object_from_the_cpu_leg():
+    """bench.py's parity object: the single-core oracle leg's results against
+    outputs for the same rows; exact outputs pass, a planted deviation counts."""
+    import numpy as np
+    import torch
+    import bench
+    from rollout_consistent_vocab_gb300 import workloads as W
+    wl = W.workload_c2(device="cpu", T=3)
+    bits = wl.logits.view(torch.int16).numpy().view(np.uint16)
+    rbits = wl.ref_logits.view(torch.int16).numpy().view(np.uint16)
+    tg = W.structural_targets(3, wl.hot, wl.hot_n, seed=2).numpy()
+    rate, n, secs, res = bench.cpu_oracle_rate(bits, rbits, tg, 60.0)
+    assert n == 3 and len(res) == 3
+    full = np.array([r.full for r, _ in res], np.float32)
+    restr = np.array([r.restr for r, _ in res], np.float32)
+    sup = np.array([r.support for r, _ in res], np.int32)
+    fref = np.array([f for _, f in res], np.float32)
+    kl = full - fref
+    d = bench.parity_summary(res, full, restr, sup, fref, kl)
+    assert d["pass"] and d["rows"] == 3 and d["rows_over_tol"] == 0 and d["support_differs"] == 0
+    full[1] += 1e-3
+    d = bench.parity_summary(res, full, restr, sup, fref, kl)
+    assert not d["pass"] and d["rows_over_tol"] >= 1

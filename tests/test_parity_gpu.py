@@ -18,7 +18,8 @@ import oracle
 import rollout_consistent_vocab_gb300 as pkg
 from rollout_consistent_vocab_gb300 import workloads as W
 
-from _support import TOL, Stats, bits_of, check_row, check_rows, oracle_targets
+from _support import (TOL, Stats, bits_of, check_row, check_rows, check_rows_parallel,
+                      oracle_targets, oracle_targets_parallel, record)
 
 pytestmark = pytest.mark.gpu
 VR, VP = oracle.VREAL, oracle.VPAD
@@ -178,78 +179,78 @@ def test_c0_spread_all_rows():
     st = Stats()
     check_rows(st, bits, 0.7 * ones, 0.95 * ones, -ones, targets, f, r, s)
     assert sum(r[i] == -math.inf for i in forced) == 4
-    print("c0", st)
+    record("c0 T=64 N(0,9) tau0.7 p0.95", st)
 
 
-def test_c1_microbatch_sampled_rows():
-    """T = 1024 rows on the GPU; 96 sampled rows checked (oracle targets, 5% forced out)."""
+def test_c1_microbatch_all_rows():
+    """T = 1024 rows, every row checked: targets drawn from each row's restricted
+    distribution by the oracle, 5% of the rows forced outside the support."""
     wl = W.workload_c1(device=DEV)
+    T = wl.T
+    bits = bits_of(wl.logits)
     rng = np.random.default_rng(1)
-    rows = np.sort(rng.choice(wl.T, 96, replace=False))
-    bits = bits_of(wl.logits[torch.as_tensor(rows, device=DEV)])
-    targets = W.structural_targets(wl.T, wl.hot, wl.hot_n, seed=1, device=DEV)
-    forced = set(rng.choice(len(rows), 5, replace=False).tolist())
-    ones = np.ones(len(rows))
-    tsel = oracle_targets(bits, 0.7 * ones, 0.95 * ones, -ones.astype(int), rng, forced)
-    targets[torch.as_tensor(rows, device=DEV)] = _t(tsel, torch.int32)
-    f, r, s = run_pair(wl.logits, targets, 0.7, 0.95, -1)
+    forced = np.zeros(T, bool)
+    forced[rng.choice(T, T // 20, replace=False)] = True
+    tg = oracle_targets_parallel(bits, 0.7, 0.95, -1, forced, seed=1)
+    f, r, s = run_pair(wl.logits, _t(tg, torch.int32), 0.7, 0.95, -1)
     st = Stats()
-    check_rows(st, bits, 0.7 * ones, 0.95 * ones, -ones, tsel, f[rows], r[rows], s[rows])
-    print("c1", st)
+    check_rows_parallel(st, bits, 0.7, 0.95, -1, tg, f, r, s)
+    assert st.rows == T
+    assert np.all(r[forced] == -np.inf)
+    record("c1 T=1024 hot32 tau0.7 p0.95", st, forced_out=int(forced.sum()))
 
 
-def test_c2_pair_and_kl_sampled_rows():
-    """T = 8192, tau 1.3, p 0.99, k 128, plus the KL term against perturbed reference logits."""
+def test_c2_pair_and_kl_all_rows():
+    """T = 8192, tau 1.3, p 0.99, k 128, plus the KL term against perturbed
+    reference logits; every row's pair, reference full logprob and KL term
+    checked (targets from the oracle's restricted distribution, 5% forced out)."""
     wl = W.workload_c2(device=DEV)
     T = wl.T
-    targets = W.structural_targets(T, wl.hot, wl.hot_n, seed=2, device=DEV)
+    bits = bits_of(wl.logits)
+    rbits = bits_of(wl.ref_logits)
+    rng = np.random.default_rng(2)
+    forced = np.zeros(T, bool)
+    forced[rng.choice(T, T // 20, replace=False)] = True
+    tg_np = oracle_targets_parallel(bits, 1.3, 0.99, 128, forced, seed=2)
+    targets = _t(tg_np, torch.int32)
     full, restr, sup, full_ref, kl = pkg.logp_kl(wl.logits, wl.ref_logits, targets, 1.3, 0.99, 128)
     f2, r2, s2 = pkg.logp_pair(wl.logits, targets, 1.3, 0.99, 128)
     torch.cuda.synchronize()
     assert torch.equal(full, f2) and torch.equal(restr.nan_to_num(), r2.nan_to_num()) and torch.equal(sup, s2)
     assert torch.equal(kl, full - full_ref)
-    rng = np.random.default_rng(2)
-    rows = np.sort(rng.choice(T, 40, replace=False))
-    ridx = torch.as_tensor(rows, device=DEV)
-    bits = bits_of(wl.logits[ridx])
-    rbits = bits_of(wl.ref_logits[ridx])
-    ts = targets[ridx].cpu().numpy()
-    f, r, s = full[ridx].cpu().numpy(), restr[ridx].cpu().numpy(), sup[ridx].cpu().numpy()
-    fr, klv = full_ref[ridx].cpu().numpy(), kl[ridx].cpu().numpy()
+    f, r, s = full.cpu().numpy(), restr.cpu().numpy(), sup.cpu().numpy()
     st = Stats()
-    ones = np.ones(len(rows))
-    check_rows(st, bits, 1.3 * ones, 0.99 * ones, 128 * ones, ts, f, r, s)
-    for n in range(len(rows)):
-        o_ref = oracle.logp_row(rbits[n], 1.3, 1.0, -1, int(ts[n]))
-        o_pol = oracle.logp_row(bits[n], 1.3, 1.0, -1, int(ts[n]))
-        assert abs(fr[n] - o_ref.full) <= TOL
-        assert abs(klv[n] - (o_pol.full - o_ref.full)) <= 2 * TOL
-    assert (s[s >= 0] >= 1).all() and (s <= 128 + 64).all()
-    print("c2", st)
+    check_rows_parallel(st, bits, 1.3, 0.99, 128, tg_np, f, r, s, ref_bits=rbits,
+                        full_ref=full_ref.cpu().numpy(), kl=kl.cpu().numpy())
+    assert st.rows == T
+    assert (s >= 1).all() and (s <= 128 + 64).all()
+    assert np.all(r[forced] == -np.inf)
+    record("c2 T=8192 hot1-256 tau1.3 p0.99 k128 (+ref, kl)", st, forced_out=int(forced.sum()))
 
 
-def test_c4_mixed_parameters_sampled_rows():
-    """T = 55296 (16.9 GB of logits) with per-row tau/p/k; rows sampled per parameter combo."""
+def test_c4_mixed_parameters_all_rows():
+    """T = 55296 (16.9 GB of logits) with per-row tau/p/k: every row checked,
+    in blocks of 4096 rows copied to the host."""
     wl = W.workload_c4(device=DEV)
     T = wl.T
     targets = W.structural_targets(T, wl.hot, wl.hot_n, seed=4, device=DEV)
     full, restr, sup = pkg.logp_pair(wl.logits, targets, wl.temperature, wl.top_p, wl.top_k)
     torch.cuda.synchronize()
     tau, p, k = wl.temperature.cpu().numpy(), wl.top_p.cpu().numpy(), wl.top_k.cpu().numpy()
-    rng = np.random.default_rng(4)
-    rows = []
+    f, r, s, tg = full.cpu().numpy(), restr.cpu().numpy(), sup.cpu().numpy(), targets.cpu().numpy()
+    st = Stats()
+    for a in range(0, T, 4096):
+        b = min(T, a + 4096)
+        bits = bits_of(wl.logits[a:b])
+        check_rows_parallel(st, bits, tau[a:b], p[a:b], k[a:b], tg[a:b], f[a:b], r[a:b], s[a:b],
+                            rows=np.arange(a, b))
+    assert st.rows == T
+    kinds = {}
     for tv in np.unique(tau):
         for pv in np.unique(p):
             for kv in np.unique(k):
-                idx = np.nonzero((tau == tv) & (p == pv) & (k == kv))[0]
-                rows += rng.choice(idx, 3, replace=False).tolist()
-    rows = np.sort(np.asarray(rows))
-    ridx = torch.as_tensor(rows, device=DEV)
-    bits = bits_of(wl.logits[ridx])
-    st = Stats()
-    check_rows(st, bits, tau[rows], p[rows], k[rows], targets[ridx].cpu().numpy(),
-               full[ridx].cpu().numpy(), restr[ridx].cpu().numpy(), sup[ridx].cpu().numpy())
-    print("c4", st)
+                kinds[f"{tv:g}/{pv:g}/{kv}"] = int(np.sum((tau == tv) & (p == pv) & (k == kv)))
+    record("c4 T=55296 mixed tau/p/k", st, rows_per_kind=kinds)
     del wl, full, restr, sup
     torch.cuda.empty_cache()
 
@@ -268,7 +269,7 @@ def test_ragged_batches_random_parameters(T):
                        _t(k, torch.int32))
     st = Stats()
     check_rows(st, bits, tau, p, k, tg, f, r, s)
-    print(T, st)
+    record(f"ragged T={T} random tau/p/k", st)
 
 
 def test_entry_points_agree_bitwise():
@@ -311,7 +312,7 @@ def test_top_p_only_deep_nucleus():
                        _t(k, torch.int32))
     st = Stats()
     check_rows(st, bits, tau, p, k, tg, f, r, s)
-    print("deep nucleus", st)
+    record("deep nucleus top-p only", st)
 
 
 def test_wide_support_fallback_path():
@@ -333,7 +334,7 @@ def test_wide_support_fallback_path():
                        _t(p, torch.float32), _t(k, torch.int32))
     st = Stats()
     check_rows(st, bits, tau, p, k, tg, f, r, s)
-    print("fallback", st)
+    record("wide support (global-memory windows)", st)
 
 
 def test_window_reaching_minus_infinity():
@@ -341,7 +342,6 @@ def test_window_reaching_minus_infinity():
     witness is -inf: the candidate window then reaches -inf itself, and only
     the shard's real chunks may be counted (the support includes the -inf
     tokens, at zero mass).  Also drawn, through both sampler paths."""
-    from _support import Stats, check_rows
     rng = np.random.default_rng(91)
     rows, first = [], []
     for n_fin in (100, 3, 5000):
