@@ -54,14 +54,20 @@ struct __align__(16) MidSlot {
   float xm;        // shard maximum (a bf16 value or -inf / +inf)
   int32_t lkey;    // order key reached by ceil(k/W) lane maxima of every warp of the shard
   uint32_t flags;
-  float l;         // top-p-only rows: the shard's sum-exp (0 otherwise)
+  float l;         // unused (0)
+};
+// Top-p-only rows' second exchange, once the row maximum is known.
+struct __align__(16) Mid2Slot {
+  float l;         // the shard's sum-exp
+  uint32_t codes_lo, codes_hi;   // level codes 0..3 and 4..5 (0: none)
+  uint32_t flags;
 };
 
 // Sent by every CTA to the leader at the end.
 struct __align__(16) Summary {
   float xm;        // shard maximum
   float l;         // sum over the shard of exp(s_j - m_r) (NaN if the shard holds a NaN)
-  uint32_t aux;    // greedy: first column holding the maximum; otherwise candidate messages sent
+  uint32_t aux;    // greedy: first column holding the maximum; otherwise histogram-add bytes / 4 sent
   uint32_t flags;
 };
 
@@ -70,10 +76,12 @@ struct __align__(128) Smem {
   uint32_t merged[WIN];            // leader: per-key candidate counts of the whole row
   uint32_t hist[WIN / 2];          // busy warps' per-key counts (u16 pairs), pushed once
   MidSlot mid[NSHARD];
+  Mid2Slot mid2[NSHARD];
   Summary slot[NSHARD];
   uint32_t red_u[NWARP];
   int32_t red_i[NWARP];
   float red_f[NWARP];
+  float red_lev[NWARP][NLEV];
   uint32_t scan_c[NWARP];
   unsigned long long scan_m[NWARP];
   int32_t found_i;
@@ -84,7 +92,7 @@ struct __align__(128) Smem {
   float bc_f[4];
   int32_t sel_done;
   alignas(16) uint4 lead;          // backward: the leader's resolution of the row
-  unsigned long long bar_load, bar_mid, bar_sum, bar_hist, bar_lead;
+  unsigned long long bar_load, bar_mid, bar_mid2, bar_sum, bar_hist, bar_lead;
 };
 
 // five CTAs per SM: 5 * (sizeof + 1 KB reserved) <= 228 KB
@@ -178,6 +186,7 @@ logp_kernel(const KParams P) {
   const uint16_t* rowp = is_ref ? P.ref_logits + row * P.ref_stride : P.logits + row * P.stride;
   const uint32_t bar_load = smem_addr(&S.bar_load);
   const uint32_t bar_mid = smem_addr(&S.bar_mid);
+  const uint32_t bar_mid2 = smem_addr(&S.bar_mid2);
   const uint32_t bar_sum = smem_addr(&S.bar_sum);
   const uint32_t bar_hist = smem_addr(&S.bar_hist);
   const uint32_t bar_lead = smem_addr(&S.bar_lead);
@@ -238,10 +247,12 @@ logp_kernel(const KParams P) {
   // ---- barriers that peers signal, and the leader's histogram
   if (tid == 0) {
     mbar_init(bar_mid, 1);
+    mbar_init(bar_mid2, 1);
     mbar_init(bar_sum, 1);
     mbar_init(bar_hist, 1);
     // messages from the 7 peers: 16 bytes each
     if (sel) mbar_arrive_expect_tx(bar_mid, (NSHARD - 1) * 16);
+    if (sel && !k_on) mbar_arrive_expect_tx(bar_mid2, (NSHARD - 1) * 16);
     if (r == 0) mbar_arrive_expect_tx(bar_sum, (NSHARD - 1) * 16);
     if (BWD && r != 0) {
       mbar_init(bar_lead, 1);
@@ -308,16 +319,43 @@ logp_kernel(const KParams P) {
   }
 
   cluster_wait();              // S0 complete: peers' barriers and histogram are ready
-  // Rows with top-k send their maximum and bound now and overlap the exchange
-  // with the sum-exp pass; top-p-only rows also send their sum-exp, which
-  // tightens the candidate window, so they send after that pass.
+  // Restricted rows send their maximum and bound now and overlap the
+  // exchange with the sum-exp pass; top-p-only rows then exchange their
+  // sum-exp (which sets the candidate window) and level codes in a second round.
   const bool late_mid = sel && !k_on;
-  if (sel && !late_mid && tid < NSHARD) send_mid(S, r, tid, xm, lkey, flags, 0.0f, bar_mid);
+  if (sel && tid < NSHARD) send_mid(S, r, tid, xm, lkey, flags, 0.0f, bar_mid);
 
   // ---- 3. shard sum-exp, fixed tree (while the peers' messages travel)
   float l = 0.0f;
-  if (!greedy && xm_finite) l = block_sum_fixed(pass_sumexp(sh, tid, nchunks, xm, __fdiv_rn(LOG2E, tau)), S);
-  if (late_mid && tid < NSHARD) send_mid(S, r, tid, xm, lkey, flags, l, bar_mid);
+  const float cexp = __fdiv_rn(LOG2E, tau);
+  if (!greedy && xm_finite) l = block_sum_fixed(pass_sumexp(sh, tid, nchunks, xm, cexp), S);
+  if (late_mid) {
+    // every thread acquires the first exchange and forms the row maximum
+    if (!mbar_wait_bounded(bar_mid)) {
+      flags |= FLAG_TIMEOUT;
+      if (tid == 0) mbar_wait_until(bar_mid, t_start + DRAIN_MID);   // stay resident for late messages
+    }
+    float Mr = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < NSHARD; ++q) Mr = fmaxf(Mr, S.mid[q].xm);
+    unsigned long long codes = 0;
+    if (xm_finite && Mr < INFINITY && p <= LEV_MAX_P) {
+      // many chunks inside the nucleus's a-priori depth below M: level codes pay
+      const float depth = nucleus_depth(tau, p);
+      const float lb = key_value(okey_floor(__fsub_rn(Mr, depth)));   // a bf16 value <= M - depth
+      const int inside = count_chunks_reaching(cm, tid, nchunks, __floats2bfloat162_rn(lb, lb));
+      if (__syncthreads_count(inside >= LEV_GATE_CHUNKS) >= LEV_GATE_THREADS)
+        codes = shard_level_codes(sh, tid, nchunks, Mr, cexp, depth, shard_mass(l, xm, Mr, cexp), S);
+    }
+    if (tid < NSHARD) {
+      const uint4 msg = make_uint4(__float_as_uint(l), static_cast<uint32_t>(codes),
+                                   static_cast<uint32_t>(codes >> 32), flags);
+      if (tid == static_cast<int>(r))
+        *reinterpret_cast<uint4*>(&S.mid2[r]) = msg;
+      else
+        st_async_v4(map_rank(smem_addr(&S.mid2[r]), tid), msg, map_rank(bar_mid2, tid));
+    }
+  }
 
   // ---- 4. candidate pass: every element of the window is counted straight
   //           into the leader's histogram (one shared-memory add per element)
@@ -325,9 +363,10 @@ logp_kernel(const KParams P) {
   if (sel) {
     if (tid == 0) {
       // the window of candidate keys, the same in every CTA of the cluster
-      if (!mbar_wait_bounded(bar_mid)) {
+      const uint32_t bar_w = late_mid ? bar_mid2 : bar_mid;
+      if (!mbar_wait_bounded(bar_w)) {
         flags |= FLAG_TIMEOUT;
-        mbar_wait_until(bar_mid, t_start + DRAIN_MID);   // stay resident for late messages
+        mbar_wait_until(bar_w, t_start + (late_mid ? DRAIN_MID2 : DRAIN_MID));   // resident for late messages
       }
       int L = 0x7fffffff;
       float M = -INFINITY;
@@ -336,15 +375,25 @@ logp_kernel(const KParams P) {
         M = fmaxf(M, S.mid[q].xm);
         L = min(L, S.mid[q].lkey);
       }
-      float Z = 0.0f;
-      if (!k_on) {
-        const float cz = __fdiv_rn(LOG2E, tau);
-#pragma unroll
-        for (int q = 0; q < NSHARD; ++q)
-          if (S.mid[q].xm > -INFINITY) Z = fmaf(S.mid[q].l, ex2((S.mid[q].xm - M) * cz), Z);
-      }
       int whi, wlo;
-      candidate_window(M, L, Z, tau, p, k_on, whi, wlo);
+      if (!k_on) {
+        // total mass from the second exchange, then the certified level, if any
+        float Z = 0.0f, T_q[NSHARD];
+        unsigned long long codes_q[NSHARD];
+        bool levels = false;
+#pragma unroll
+        for (int q = 0; q < NSHARD; ++q) {
+          const float xq = S.mid[q].xm;
+          T_q[q] = xq > -INFINITY ? shard_mass(S.mid2[q].l, xq, M, cexp) : 0.0f;
+          if (xq > -INFINITY) Z = fmaf(S.mid2[q].l, ex2((xq - M) * cexp), Z);
+          codes_q[q] = S.mid2[q].codes_lo | (static_cast<unsigned long long>(S.mid2[q].codes_hi) << 32);
+          levels |= codes_q[q] != 0ull;
+        }
+        candidate_window(M, L, Z, tau, p, false, whi, wlo);
+        if (levels && wlo <= whi) wlo = max(wlo, min(certified_bottom(codes_q, T_q, M, Z, tau, p), whi));
+      } else {
+        candidate_window(M, L, 0.0f, tau, p, true, whi, wlo);
+      }
       S.win[0] = whi;
       S.win[1] = wlo;
       S.win[2] = static_cast<int>(flags);
@@ -411,8 +460,12 @@ logp_kernel(const KParams P) {
         const int nwords = (hi - lo + 2) >> 1;
         for (int iw = tid; iw < nwords; iw += NTHR) {
           const uint32_t hw = S.hist[iw];
-          if (hw & 0xFFFFu) { red_async_add(dst + 8u * iw, hw & 0xFFFFu, rbar); ++sent; }
-          if (hw >> 16) { red_async_add(dst + 8u * iw + 4u, hw >> 16, rbar); ++sent; }
+          if (hw) {
+            // both keys of the word in one 8-byte add (neither 32-bit count can carry)
+            red_async_add_u64(dst + 8u * iw,
+                              (static_cast<unsigned long long>(hw >> 16) << 32) | (hw & 0xFFFFu), rbar);
+            sent += 2;
+          }
         }
       }
     } else {
@@ -435,7 +488,7 @@ logp_kernel(const KParams P) {
         for (int i = tid; i < SAMP_BITWORDS; i += NTHR) wb[i] = 0u;
       }
     }
-    // the leader learns how many adds each peer sent from its summary
+    // the leader learns how many add bytes (in 4-byte units) each peer sent from its summary
     sent = __reduce_add_sync(0xffffffffu, sent);
     if ((tid & 31) == 0 && sent) atomicAdd(&S.npush, sent);
     __syncthreads();

@@ -369,3 +369,26 @@ def test_window_reaching_minus_infinity():
     for i in range(T):
         o = oracle.logp_row(bits[i], float(taus[i]), float(ps[i]), int(ks[i]), int(tok[i]))
         assert math.isfinite(o.restr) and int(ss[i]) == o.support, i
+
+
+def test_top_p_only_high_temperature_rows_all_checked():
+    """Top-p-only rows at temperatures 1.0 and 1.3 (p 0.9 .. 0.99, k off) on
+    hot-set logits: the rows whose candidate window the shards' level codes
+    narrow.  Every row against the oracle (targets from the oracle's
+    restricted distribution, a tenth forced outside the support)."""
+    T = 384
+    rng = np.random.default_rng(21)
+    x, hot, n = W.hot_logits(T, 1, 512, seed=21, device=DEV)
+    tau = rng.choice([1.0, 1.3], T).astype(np.float32)
+    p = rng.choice([0.9, 0.95, 0.97, 0.99], T).astype(np.float32)
+    k = np.full(T, -1, np.int32)
+    bits = bits_of(x)
+    forced = np.zeros(T, bool)
+    forced[rng.choice(T, T // 10, replace=False)] = True
+    tg = oracle_targets_parallel(bits, tau, p, k, forced, seed=21)
+    f, r, s = run_pair(x, _t(tg, torch.int32), _t(tau, torch.float32), _t(p, torch.float32),
+                       _t(k, torch.int32))
+    st = Stats()
+    check_rows_parallel(st, bits, tau, p, k, tg, f, r, s)
+    assert st.rows == T
+    record("top-p only tau1.0/1.3 p0.9-0.99 hot1-512", st)
