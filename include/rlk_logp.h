@@ -75,7 +75,7 @@ extern "C" {
 #define RLK_VOCAB_REAL 151936
 #define RLK_NUM_SHARDS 8
 #define RLK_SHARD_WIDTH 19072
-#define RLK_ABI_VERSION 2
+#define RLK_ABI_VERSION 3
 
 typedef enum {
   RLK_OK = 0,
@@ -399,6 +399,59 @@ rlk_status rlk_logp_merge(const float* maxes, const float* sumexps, const int32_
                           const uint32_t* counts, int32_t count_shards,
                           float* out_full, float* out_restr, int32_t* out_support,
                           void* stream);
+
+/* Rows whose support reaches below the first window.  rlk_logp_merge cannot
+ * resolve a row whose top-k or top-p threshold lies more than 1024 order keys
+ * below the row maximum (support -2): the fused kernel re-reads such a row,
+ * a shard holder cannot.  The resumable pair below continues such rows over
+ * successive lower windows of 1024 keys, the caller counting each window on
+ * every shard in between, exactly as the fused kernel's fallback walks them
+ * (top-k first, from the top; then the nucleus, from the top again), so the
+ * results are bit-identical to rlk_logp_pair.  Same sources as the merge:
+ * each shard yields a summary and the summaries combine in a fixed order of
+ * vocabulary position ("Reproduce and profile the Qwen3-8B TP4/CP2
+ * experiment", "How non-default CUDA topology reuses TP4/CP2").
+ *
+ * Per-row state, device [T], caller-owned, zeroed by the caller before the
+ * first merge call (stage 0 = the first window). */
+typedef struct rlk_merge_state {
+  int32_t stage;      /* 0 first window; 1 toward the k-th largest value; 2 toward the nucleus
+                         threshold; 3 resolved (the row's outputs are final) */
+  int32_t hi, lo;     /* stages 1, 2: the window (order keys, inclusive) the next counts cover */
+  int32_t vk_key;     /* stage 2: lowest order key of the top-k set (-1: top-k off) */
+  uint32_t carry_c;   /* tokens above the window, in the current stage */
+  uint32_t pad;
+  uint64_t carry_m;   /* their mass, exp((x - M) / tau) in 2^-44 fixed point */
+  uint64_t zk;        /* stage 2: mass of the top-k set in the same units */
+} rlk_merge_state;
+
+/* rlk_logp_merge for restricted rows with a resolution state.  counts must
+ * hold, per row, the counts of the window its state names: for stage-0 rows
+ * rlk_logp_shard_counts' first window, for stage-1/2 rows
+ * rlk_logp_shard_counts_window's.  Rows in stage 3 are skipped (outputs and
+ * state untouched).  A row resolved by this call gets its outputs and stage
+ * 3; a row that needs a lower window gets restricted NaN, support -2 and the
+ * window in its state, and counts one in out_pending (optional device
+ * int32, added to: zero it before the call).  Repeat counts + merge until no
+ * row is pending (at most 2 * 64 rounds; one or two in practice).  Other
+ * arguments and errors as rlk_logp_merge (counts required). */
+rlk_status rlk_logp_merge_resumable(const float* maxes, const float* sumexps, const int32_t* aux,
+                                    const float* target_logit, int64_t T, const int32_t* target,
+                                    const float* temperature, float temperature_scalar,
+                                    const float* top_p, float top_p_scalar,
+                                    const int32_t* top_k, int32_t top_k_scalar,
+                                    const uint32_t* counts, int32_t count_shards,
+                                    rlk_merge_state* state, float* out_full, float* out_restr,
+                                    int32_t* out_support, int32_t* out_pending, void* stream);
+
+/* Per-row exact counts of this shard's real tokens on the window that each
+ * row's state names (stages 1 and 2: order keys state.lo .. state.hi, entry i
+ * counting key state.hi - i); rows in stages 0 and 3 get zeros.  chunk_max as
+ * in rlk_logp_shard_counts (optional; given, only chunks whose maximum
+ * reaches state.lo are read).  out_counts: device uint32 [T][1024], 16-byte
+ * aligned. */
+rlk_status rlk_logp_shard_counts_window(const rlk_shard_args* args, const rlk_merge_state* state,
+                                        const uint16_t* chunk_max, uint32_t* out_counts, void* stream);
 
 /* Static message for a status code. */
 const char* rlk_status_string(rlk_status status);

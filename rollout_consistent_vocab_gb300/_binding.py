@@ -66,6 +66,7 @@ COMPUTE = ("rlk_logp_full", "rlk_logp_restricted", "rlk_logp_pair", "rlk_logp_kl
            "rlk_logp_backward", "rlk_logp_pair_save", "rlk_logp_backward_saved", "rlk_sample",
            "rlk_sample_noalloc", "rlk_linear_logp",
            "rlk_logp_shard_summary", "rlk_logp_shard_counts", "rlk_logp_merge",
+           "rlk_logp_merge_resumable", "rlk_logp_shard_counts_window",
            "rlk_sqnorm_accumulate", "rlk_sqnorm_finalize", "rlk_grad_norm")
 RLK_GRAD_BF16, RLK_GRAD_F32 = 0, 1
 EXPORTS = COMPUTE + ("rlk_status_string", "rlk_last_error", "rlk_abi_version")
@@ -102,6 +103,9 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     f32, i32 = ctypes.c_float, ctypes.c_int32
     lib.rlk_logp_merge.argtypes = [VP, VP, VP, VP, ctypes.c_int64, VP, VP, f32, VP, f32, VP, i32,
                                    VP, i32, VP, VP, VP, VP]
+    lib.rlk_logp_merge_resumable.argtypes = [VP, VP, VP, VP, ctypes.c_int64, VP, VP, f32, VP, f32, VP,
+                                             i32, VP, i32, VP, VP, VP, VP, VP, VP]
+    lib.rlk_logp_shard_counts_window.argtypes = [SA, VP, VP, VP, VP]
     lib.rlk_sqnorm_accumulate.argtypes = [VP, i64, i32, VP, VP]
     lib.rlk_sqnorm_finalize.argtypes = [VP, VP, VP]
     lib.rlk_grad_norm.argtypes = [VP, i64, i32, VP, VP, VP]
@@ -113,7 +117,7 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     lib.rlk_last_error.restype = ctypes.c_char_p
     lib.rlk_abi_version.argtypes = []
     lib.rlk_abi_version.restype = ctypes.c_int
-    if lib.rlk_abi_version() != 2:
+    if lib.rlk_abi_version() != 3:
         raise ImportError("librlk_logp.so ABI version mismatch")
     _lib = lib
     return lib
@@ -324,12 +328,52 @@ def logp_merge(maxes, sumexps, aux, target_logit, target, temperature=1.0, top_p
     return (out_full,) if counts is None else (out_full, out_restr, out_support)
 
 
+MERGE_STATE_WORDS = 5        # rlk_merge_state: 40 bytes per row, as int64 words
+MAX_RESUME_ROUNDS = 2 * 64 + 2
+
+
+def merge_state(T, device):
+    """A zeroed per-row resolution state (rlk_merge_state [T]) for the resumable merge."""
+    return _torch().zeros((T, MERGE_STATE_WORDS), dtype=_torch().int64, device=device)
+
+
+def shard_counts_window(shard_logits, shard, target, state, *, out_counts, chunk_max=None,
+                        stream=None):
+    """Counts [T, 1024] of one shard's tokens on each pending row's next window
+    (the window its state names; zeros for rows that are not pending)."""
+    lib = load_library()
+    a = make_shard_args(shard_logits, shard, target, 1.0, 1.0, -1, None)
+    check(lib.rlk_logp_shard_counts_window(ctypes.byref(a), _ptr(state), _ptr(chunk_max),
+                                           _ptr(out_counts), _stream(stream)))
+
+
+def logp_merge_resumable(maxes, sumexps, aux, target_logit, target, temperature=1.0, top_p=1.0,
+                         top_k=-1, *, counts, state, out_full, out_restr, out_support,
+                         out_pending=None, stream=None):
+    """One round of the resumable merge: resolves what the given counts allow
+    and records the next window of the rows that stay pending."""
+    lib = load_library()
+    torch = _torch()
+    T = target.shape[0]
+    tp, ts = _param(temperature, T, torch.float32, "temperature")
+    pp, ps = _param(top_p, T, torch.float32, "top_p")
+    kp, ks = _param(top_k, T, torch.int32, "top_k")
+    check(lib.rlk_logp_merge_resumable(_ptr(maxes), _ptr(sumexps), _ptr(aux), _ptr(target_logit), T,
+                                       _ptr(target), tp, ts, pp, ps, kp, ks, _ptr(counts),
+                                       counts.shape[0], _ptr(state), _ptr(out_full), _ptr(out_restr),
+                                       _ptr(out_support), _ptr(out_pending), _stream(stream)))
+
+
 def logp_sharded(shards, target, temperature=1.0, top_p=1.0, top_k=-1, *, restricted=True,
-                 chunk_maxima=True, err_count=None, stream=None):
+                 chunk_maxima=True, resolve=True, err_count=None, stream=None):
     """All phases over 8 shard buffers (shard r holds vocabulary columns
     [19072 r, 19072 (r+1))): summaries, then counts when restricted (reading
     only the chunks whose phase-1 maximum reaches the window, unless
-    ``chunk_maxima`` is False), then the merge.  Returns (full,) or
+    ``chunk_maxima`` is False), then the merge.  With ``resolve`` (the
+    default) rows whose support reaches below the first window are carried
+    through lower windows (counts + resumable merge rounds, each round
+    reading the number of pending rows on the host) until every row is
+    resolved; without it such rows keep support -2.  Returns (full,) or
     (full, restricted, support)."""
     torch = _torch()
     if len(shards) != NUM_SHARDS:
@@ -355,8 +399,30 @@ def logp_sharded(shards, target, temperature=1.0, top_p=1.0, top_k=-1, *, restri
             shard_counts(sh, r, target, maxes, sumexps, aux, temperature, top_p, top_k,
                          out_counts=counts[r], chunk_max=None if cmax is None else cmax[r],
                          stream=stream)
-    return logp_merge(maxes, sumexps, aux, xt, target, temperature, *pk, counts=counts,
-                      stream=stream)
+    if not (restricted and resolve and T > 0):
+        return logp_merge(maxes, sumexps, aux, xt, target, temperature, *pk, counts=counts,
+                          stream=stream)
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    state = merge_state(T, dev)
+    pending = torch.zeros(1, dtype=torch.int32, device=dev)
+    full = torch.empty(T, dtype=torch.float32, device=dev)
+    restr = torch.empty(T, dtype=torch.float32, device=dev)
+    support = torch.empty(T, dtype=torch.int32, device=dev)
+    for rnd in range(MAX_RESUME_ROUNDS + 1):
+        if rnd > 0:
+            for r, sh in enumerate(shards):
+                shard_counts_window(sh, r, target, state, out_counts=counts[r],
+                                    chunk_max=None if cmax is None else cmax[r], stream=stream)
+        with torch.cuda.stream(st):
+            pending.zero_()
+        logp_merge_resumable(maxes, sumexps, aux, xt, target, temperature, top_p, top_k,
+                             counts=counts, state=state, out_full=full, out_restr=restr,
+                             out_support=support, out_pending=pending, stream=stream)
+        with torch.cuda.stream(st):
+            left = int(pending.item())
+        if left == 0:
+            return full, restr, support
+    raise RlkError(f"{left} rows still pending after {MAX_RESUME_ROUNDS} windows")
 
 
 # ------------------------------------------------------------ backward

@@ -18,7 +18,18 @@
 //            the summed counts.
 //
 // The fused kernel resolves a support that reaches below the window by
-// re-reading the row; a shard cannot, so such rows are reported (support -2).
+// re-reading the row; a shard cannot, so rlk_logp_merge reports such rows
+// (support -2).  The resumable pair continues them instead:
+//
+//   merge_kernel<true, true>  the merge with a per-row state: a row whose
+//            threshold lies below the window records the next window (and
+//            the exact integer carries above it) and stays pending;
+//   window_counts_kernel      exact per-key counts of this shard's tokens on
+//            each pending row's next window;
+//
+// repeated by the caller until no row is pending.  The windows and carries
+// are those of the fused kernel's fallback (select_support), so the
+// results are the same bits.
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -306,6 +317,43 @@ __global__ void __launch_bounds__(NTHR, CMAX ? 16 : CTAS_PER_SM) shard_counts_ke
   for (int i = tid; i < WIN / 4; i += NTHR) dst[i] = src[i];
 }
 
+// ------------------------------------------------------------ lower windows
+
+// Counts of this shard's real tokens on each pending row's next window
+// (order keys state.lo .. state.hi, entry i = key state.hi - i), read from
+// global memory: every real chunk, or with phase 1's chunk maxima only the
+// chunks whose maximum reaches state.lo.  Rows that are not pending get zeros.
+template <bool CMAX>
+__global__ void __launch_bounds__(NTHR) window_counts_kernel(const ShardParams P,
+                                                             const rlk_merge_state* state) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  ShardSmem& S = *reinterpret_cast<ShardSmem*>(smem_raw);
+  const int tid = threadIdx.x;
+  const int64_t row = blockIdx.x;
+  const int nchunks = (P.shard == NSHARD - 1) ? LAST_CHUNKS : SHARD_CHUNKS;
+  const rlk_merge_state st = state[row];
+  for (int i = tid; i < WIN; i += NTHR) S.hist[i] = 0u;
+  __syncthreads();
+  if ((st.stage == 1 || st.stage == 2) && st.lo <= st.hi && st.hi - st.lo < WIN) {
+    const uint4* rowv = reinterpret_cast<const uint4*>(P.logits + row * P.stride);
+    const uint16_t* cmax = CMAX ? P.in_cmax + row * SHARD_CHUNKS : nullptr;
+    for (int ch = tid; ch < nchunks; ch += NTHR) {
+      if (CMAX && okey(__ldg(cmax + ch)) < st.lo) continue;
+      const uint4 v = __ldg(rowv + ch);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int K = okey((w[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
+        if (K >= st.lo && K <= st.hi) red_shared_add(&S.hist[st.hi - K], 1u);
+      }
+    }
+  }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(P.out_counts + row * WIN);
+  const uint4* src = reinterpret_cast<const uint4*>(S.hist);
+  for (int i = tid; i < WIN / 4; i += NTHR) dst[i] = src[i];
+}
+
 // ------------------------------------------------------------ merge
 
 struct MergeParams {
@@ -325,16 +373,141 @@ struct MergeParams {
   float* out_full;
   float* out_restr;
   int32_t* out_support;
+  rlk_merge_state* state;       // resumable merge: per-row state
+  int32_t* out_pending;
 };
 
 constexpr int MERGE_ROWS = NTHR / 32;   // one warp per row
 
-template <bool RESTR>
+// One window of the resumable selection, on one warp: keys hi, hi - 1, ...
+// with per-key counts cnt[i] and masses count * qfx(key).  Finds the first
+// index i < nlim whose condition holds, given the counts and masses (rc, rm)
+// of the keys before it plus the carry:
+//   topk:  rc < k and (rc + c_i >= k, or i is the row's last key (last));
+//   else:  rm < T and (rm + m_i >= T, or i == nlim - 1 and last).
+// Returns i with (rc + c_i, rm + m_i) in fc, fm; or -1, after adding the
+// totals of keys 0 .. nlim - 1 to the carry.
+__device__ __forceinline__ int window_find(const uint32_t* cnt, int nlim, int hi, float M, float c,
+                                           bool topk, uint32_t k, unsigned long long T, bool last,
+                                           uint32_t& carry_c, unsigned long long& carry_m,
+                                           uint32_t& fc, unsigned long long& fm) {
+  constexpr int KPL = 4, BLK = 32 * KPL;
+  const int lane = threadIdx.x & 31;
+  for (int b0 = 0; b0 < nlim; b0 += BLK) {
+    uint32_t cj[KPL], lc = 0;
+    unsigned long long mj[KPL], lm = 0;
+#pragma unroll
+    for (int j = 0; j < KPL; ++j) {
+      const int i = b0 + KPL * lane + j;
+      cj[j] = (i < nlim) ? cnt[i] : 0u;
+      mj[j] = cj[j] ? cj[j] * qfx(key_value(hi - i), M, c) : 0ull;
+      lc += cj[j];
+      lm += mj[j];
+    }
+    const uint32_t ic = warp_incl_scan_u32(lc);
+    const unsigned long long im = warp_incl_scan_u64(lm);
+    uint32_t rc = carry_c + ic - lc;
+    unsigned long long rm = carry_m + im - lm;
+    int f = -1;
+    uint32_t f_c = 0;
+    unsigned long long f_m = 0;
+#pragma unroll
+    for (int j = 0; j < KPL; ++j) {
+      const int i = b0 + KPL * lane + j;
+      const bool at_last = last && i == nlim - 1;
+      const bool hit = topk ? (rc < k && (rc + cj[j] >= k || at_last))
+                            : (rm < T && (rm + mj[j] >= T || at_last));
+      if (f < 0 && i < nlim && hit) {
+        f = i;
+        f_c = rc + cj[j];
+        f_m = rm + mj[j];
+      }
+      rc += cj[j];
+      rm += mj[j];
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, f >= 0);
+    if (bal) {
+      const int src = __ffs(bal) - 1;
+      fc = __shfl_sync(0xffffffffu, f_c, src);
+      fm = __shfl_sync(0xffffffffu, f_m, src);
+      return __shfl_sync(0xffffffffu, f, src);
+    }
+    carry_c += __shfl_sync(0xffffffffu, ic, 31);
+    carry_m += __shfl_sync(0xffffffffu, im, 31);
+  }
+  return -1;
+}
+
+// One step of the fallback selection over lower windows (the fused kernel's
+// select_support, one window per call): top-k from the top window down to
+// the k-th largest value, then the nucleus from the top window down to its
+// threshold.  cnt holds the counts of the window st names; (hi0, lo0) is the
+// row's first window.  Returns true with the result when the row is
+// resolved, else advances st to the window to count next.
+__device__ __forceinline__ bool resume_select(const uint32_t* cnt, rlk_merge_state& st, int hi0,
+                                              int lo0, float M, float c, float p, int k, bool p_on,
+                                              SelResult& out) {
+  const int n = st.hi - st.lo + 1;
+  uint32_t fc = 0;
+  unsigned long long fm = 0;
+  unsigned long long carry_m = st.carry_m;
+  if (st.stage == 1) {
+    const int f = window_find(cnt, n, st.hi, M, c, true, static_cast<uint32_t>(k), 0ull, st.lo == 0,
+                              st.carry_c, carry_m, fc, fm);
+    st.carry_m = carry_m;
+    if (f >= 0) {
+      if (!p_on) {
+        out = SelResult{fc, fm, st.hi - f};
+        return true;
+      }
+      // the nucleus inside the top-k set, from the top window again
+      st.vk_key = st.hi - f;
+      st.zk = fm;
+      st.stage = 2;
+      st.hi = hi0;
+      st.lo = lo0;
+      st.carry_c = 0;
+      st.carry_m = 0;
+      return false;
+    }
+    if (st.lo == 0) {                       // not reached: the last key always resolves
+      out = SelResult{st.carry_c, st.carry_m, 0};
+      return true;
+    }
+  } else {
+    const unsigned long long T = nucleus_bound(p, st.zk);
+    const bool k_in = st.vk_key >= st.lo;
+    const int nlim = k_in ? st.hi - st.vk_key + 1 : n;
+    const bool bounded = k_in || st.lo == 0;
+    const int f = window_find(cnt, nlim, st.hi, M, c, false, 0u, T, bounded, st.carry_c, carry_m,
+                              fc, fm);
+    st.carry_m = carry_m;
+    if (f >= 0) {
+      out = SelResult{fc, fm, st.hi - f};
+      return true;
+    }
+    if (bounded) {                          // not reached: the bound always resolves
+      out = SelResult{st.carry_c, st.carry_m, st.lo};
+      return true;
+    }
+  }
+  st.hi = st.lo - 1;
+  st.lo = max(0, st.hi - (WIN - 1));
+  return false;
+}
+
+template <bool RESTR, bool RESUME = false>
 __global__ void __launch_bounds__(NTHR) merge_kernel(const MergeParams P) {
   __shared__ uint32_t cnt[MERGE_ROWS][WIN];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * MERGE_ROWS + warp;
   if (row >= P.T) return;
+  rlk_merge_state st{};
+  if (RESUME) {
+    st = P.state[row];
+    if (st.stage == 3) return;              // resolved by an earlier call
+  }
+  bool pending = false;
   const int64_t T = P.T;
   const RowParams rp = row_params(P.tau_arr, P.tau_s, P.p_arr, P.p_s, P.k_arr, P.k_s, P.target, row);
   const float qnan = __int_as_float(0x7fc00000);
@@ -381,7 +554,10 @@ __global__ void __launch_bounds__(NTHR) merge_kernel(const MergeParams P) {
       float Mw;
       int hi, lo;
       gathered_window(P.g_max, P.g_sumexp, P.g_aux, T, row, rp, Mw, hi, lo);
-      const int n = hi - lo + 1;
+      // the window these counts cover: the first one, or the one the state names
+      const bool first = !RESUME || st.stage == 0;
+      const int whi = first ? hi : st.hi, wlo = first ? lo : st.lo;
+      const int n = whi - wlo + 1;
       for (int i = lane; i < n; i += 32) {
         uint32_t sum = 0;
         for (int q = 0; q < P.count_shards; ++q) sum += P.counts[(q * T + row) * WIN + i];
@@ -389,16 +565,36 @@ __global__ void __launch_bounds__(NTHR) merge_kernel(const MergeParams P) {
       }
       __syncwarp();
       SelResult sr{0u, 0ull, 0};
-      if (n > 0 && select_warp(cnt[warp], hi, lo, M, c, Z, rp.p, rp.k, rp.k_on, rp.p_on, sr)) {
+      bool done = first && n > 0 && select_warp(cnt[warp], hi, lo, M, c, Z, rp.p, rp.k, rp.k_on, rp.p_on, sr);
+      if (RESUME && !done && n > 0) {
+        if (first) {
+          // as the fused kernel's fallback: top-k (or the nucleus) from the top window
+          st.stage = rp.k_on ? 1 : 2;
+          st.hi = hi;
+          st.lo = lo;
+          st.vk_key = -1;
+          st.carry_c = 0;
+          st.carry_m = 0;
+          st.zk = rp.k_on ? 0ull : __float2ull_rn(Z * FX_SCALE);
+        }
+        done = resume_select(cnt[warp], st, hi, lo, M, c, rp.p, rp.k, rp.p_on, sr);
+        pending = !done;
+      }
+      if (done) {
         const bool in_s = okey_of(xt) >= sr.min_key;
         const float zs = __ull2float_rn(sr.zs) * (1.0f / FX_SCALE);
         restr = in_s ? d - logf(zs) : -INFINITY;
         support = static_cast<int>(sr.support);
       } else {
-        restr = qnan;           // the support reaches below the exchanged window
+        restr = qnan;           // the support reaches below this window
         support = -2;
       }
     }
+  }
+  if (RESUME && lane == 0) {
+    if (!pending) st.stage = 3;
+    P.state[row] = st;
+    if (pending && P.out_pending) atomicAdd(P.out_pending, 1);
   }
   if (lane == 0) {
     P.out_full[row] = full;
@@ -570,6 +766,87 @@ rlk_status rlk_logp_merge(const float* maxes, const float* sumexps, const int32_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (restr) merge_kernel<true><<<grid, NTHR, 0, st>>>(P);
   else merge_kernel<false><<<grid, NTHR, 0, st>>>(P);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(RLK_ECUDA, "kernel launch: %s", cudaGetErrorString(e));
+  return RLK_OK;
+}
+
+rlk_status rlk_logp_merge_resumable(const float* maxes, const float* sumexps, const int32_t* aux,
+                                    const float* target_logit, int64_t T, const int32_t* target,
+                                    const float* temperature, float temperature_scalar,
+                                    const float* top_p, float top_p_scalar,
+                                    const int32_t* top_k, int32_t top_k_scalar,
+                                    const uint32_t* counts, int32_t count_shards,
+                                    rlk_merge_state* state, float* out_full, float* out_restr,
+                                    int32_t* out_support, int32_t* out_pending, void* stream) {
+  if (T < 0 || T >= (int64_t(1) << 31)) return fail(RLK_EINVAL, "T = %lld out of range [0, 2^31)", (long long)T);
+  if (T == 0) return RLK_OK;
+  rlk_status s;
+  if (!counts) return fail(RLK_EINVAL, "counts is NULL");
+  if (!state) return fail(RLK_EINVAL, "state is NULL");
+  if (!aligned(state, 8)) return fail(RLK_EALIGN, "state is not 8-byte aligned");
+  if ((s = check_out(out_pending, "out_pending", false)) != RLK_OK) return s;
+  if ((s = check_out(maxes, "maxes", true)) != RLK_OK) return s;
+  if ((s = check_out(sumexps, "sumexps", true)) != RLK_OK) return s;
+  if ((s = check_out(aux, "aux", true)) != RLK_OK) return s;
+  if ((s = check_out(target_logit, "target_logit", true)) != RLK_OK) return s;
+  if ((s = check_out(target, "target", true)) != RLK_OK) return s;
+  if ((s = check_out(out_full, "out_full", true)) != RLK_OK) return s;
+  if ((s = check_tau(temperature, temperature_scalar)) != RLK_OK) return s;
+  if (count_shards != 1 && count_shards != NSHARD)
+    return fail(RLK_EINVAL, "count_shards %d must be 1 or %d", count_shards, NSHARD);
+  if (!aligned(counts, 4)) return fail(RLK_EALIGN, "counts is not 4-byte aligned");
+  if ((s = check_top_p(top_p, top_p_scalar)) != RLK_OK) return s;
+  if ((s = check_top_k(top_k, top_k_scalar)) != RLK_OK) return s;
+  if (!out_restr && !out_support) return fail(RLK_EINVAL, "out_restr and out_support are both NULL");
+  if ((s = check_out(out_restr, "out_restr", false)) != RLK_OK) return s;
+  if ((s = check_out(out_support, "out_support", false)) != RLK_OK) return s;
+  MergeParams P;
+  memset(&P, 0, sizeof(P));
+  P.g_max = maxes;
+  P.g_sumexp = sumexps;
+  P.g_aux = aux;
+  P.xt = target_logit;
+  P.T = T;
+  P.target = target;
+  P.tau_arr = temperature;
+  P.tau_s = temperature_scalar;
+  P.p_arr = top_p;
+  P.p_s = top_p_scalar;
+  P.k_arr = top_k;
+  P.k_s = top_k_scalar;
+  P.counts = counts;
+  P.count_shards = count_shards;
+  P.out_full = out_full;
+  P.out_restr = out_restr;
+  P.out_support = out_support;
+  P.state = state;
+  P.out_pending = out_pending;
+  const unsigned grid = static_cast<unsigned>((T + MERGE_ROWS - 1) / MERGE_ROWS);
+  merge_kernel<true, true><<<grid, NTHR, 0, static_cast<cudaStream_t>(stream)>>>(P);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(RLK_ECUDA, "kernel launch: %s", cudaGetErrorString(e));
+  return RLK_OK;
+}
+
+rlk_status rlk_logp_shard_counts_window(const rlk_shard_args* args, const rlk_merge_state* state,
+                                        const uint16_t* chunk_max, uint32_t* out_counts, void* stream) {
+  rlk_status s = check_shard_args(args);
+  if (s != RLK_OK || args->T == 0) return s;
+  if (!state) return fail(RLK_EINVAL, "state is NULL");
+  if (!aligned(state, 8)) return fail(RLK_EALIGN, "state is not 8-byte aligned");
+  if (!out_counts) return fail(RLK_EINVAL, "out_counts is NULL");
+  if (!aligned(out_counts, 16)) return fail(RLK_EALIGN, "out_counts is not 16-byte aligned");
+  if (chunk_max && !aligned(chunk_max, 16)) return fail(RLK_EALIGN, "chunk_max is not 16-byte aligned");
+  ShardParams P = make_shard_params(args);
+  P.out_counts = out_counts;
+  P.in_cmax = chunk_max;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const unsigned grid = static_cast<unsigned>(args->T);
+  if (chunk_max)
+    window_counts_kernel<true><<<grid, NTHR, SHARD_SMEM_NO_COPY, st>>>(P, state);
+  else
+    window_counts_kernel<false><<<grid, NTHR, SHARD_SMEM_NO_COPY, st>>>(P, state);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(RLK_ECUDA, "kernel launch: %s", cudaGetErrorString(e));
   return RLK_OK;

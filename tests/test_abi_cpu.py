@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.rlk_abi_version() == 2
+    assert lib.rlk_abi_version() == 3
     assert lib.rlk_status_string(0) == b"ok"
     assert lib.rlk_status_string(2) == b"misaligned pointer or stride"
 
@@ -207,6 +207,44 @@ def test_merge_validation(lib):
     assert _merge(lib, restr=None, sup=None) == b.RLK_EINVAL
     assert _merge(lib, counts=OUT + 2) == b.RLK_EALIGN
     assert _merge(lib, restr=OUT + 1) == b.RLK_EALIGN
+
+
+def _merge_res(lib, T=4, counts=OUT, nc=8, state=OUT, pending=None, full=OUT, restr=OUT, sup=OUT,
+               p=0.95, k=-1):
+    return lib.rlk_logp_merge_resumable(OUT, OUT, OUT, OUT, T, OUT, None, 0.7, None, p, None, k, counts,
+                                        nc, state, full, restr, sup, pending, None)
+
+
+def test_resumable_merge_and_window_counts_validation(lib):
+    assert _merge_res(lib, T=0, state=None, counts=None) == b.RLK_OK
+    assert _merge_res(lib, state=None) == b.RLK_EINVAL
+    assert _merge_res(lib, state=OUT + 4) == b.RLK_EALIGN
+    assert _merge_res(lib, counts=None) == b.RLK_EINVAL
+    assert _merge_res(lib, pending=OUT + 2) == b.RLK_EALIGN
+    assert _merge_res(lib, nc=3) == b.RLK_EINVAL
+    assert _merge_res(lib, restr=None, sup=None) == b.RLK_EINVAL
+    assert _merge_res(lib, p=0.0) == b.RLK_EINVAL
+    a = _sargs()
+    assert lib.rlk_logp_shard_counts_window(ctypes.byref(a), None, None, OUT, None) == b.RLK_EINVAL
+    assert lib.rlk_logp_shard_counts_window(ctypes.byref(a), OUT + 4, None, OUT, None) == b.RLK_EALIGN
+    assert lib.rlk_logp_shard_counts_window(ctypes.byref(a), OUT, None, None, None) == b.RLK_EINVAL
+    assert lib.rlk_logp_shard_counts_window(ctypes.byref(a), OUT, None, OUT + 4, None) == b.RLK_EALIGN
+    assert lib.rlk_logp_shard_counts_window(ctypes.byref(a), OUT, OUT + 2, OUT, None) == b.RLK_EALIGN
+    bad = _sargs(shard=9)
+    assert lib.rlk_logp_shard_counts_window(ctypes.byref(bad), OUT, None, OUT, None) == b.RLK_EINVAL
+    z = _sargs(T=0, logits=None, target=None)
+    assert lib.rlk_logp_shard_counts_window(ctypes.byref(z), None, None, None, None) == b.RLK_OK
+
+
+def test_merge_state_layout():
+    """rlk_merge_state is 40 bytes: five int64 words in the binding's state tensor."""
+    import re
+    hdr = open(os.path.join(os.path.dirname(__file__), "..", "include", "rlk_logp.h")).read()
+    body = re.search(r"typedef struct rlk_merge_state \{(.*?)\} rlk_merge_state;", hdr, re.S).group(1)
+    sizes = {"int32_t": 4, "uint32_t": 4, "uint64_t": 8}
+    fields = re.findall(r"^\s*(int32_t|uint32_t|uint64_t)\s+([\w, ]+);", body, re.M)
+    total = sum(sizes[t] * len(names.split(",")) for t, names in fields)
+    assert total == 8 * b.MERGE_STATE_WORDS == 40
 
 
 # ------------------------------------------------------------ backward

@@ -3,9 +3,10 @@ candidate counts, merge) against the fused kernel and the oracle.
 
 The fused kernel and the sharded form run the same per-shard passes and the
 same fixed-order merge, so full logprobs must agree bit for bit, and so must
-the restricted logprob and support of every row whose support lies within
-the 1024-key window (other rows are reported with support -2).  The shard
-summaries themselves are checked against the oracle's fp64 summaries.
+the restricted logprob and support of every row: rows whose support reaches
+below the first 1024-key window are carried through lower windows by the
+resumable merge (one merge round alone reports them with support -2).  The
+shard summaries themselves are checked against the oracle's fp64 summaries.
 """
 
 import math
@@ -58,25 +59,32 @@ def mixed_rows(T: int, seed: int):
 
 
 def compare(x, t, tau, p, k, err=None, err_sharded=None):
+    """Fused pass against the sharded form: bit for bit on every row (rows
+    beyond the first window resolved over lower windows).  Also returns the
+    supports of a single merge round, where such rows report -2."""
     f0, r0, s0 = pkg.logp_pair(x, t, tau, p, k, err_count=err)
     f1, r1, s1 = pkg.logp_sharded(split(x), t, tau, p, k, err_count=err_sharded)
     # phase 2 reading whole shards instead of the chunks phase 1 marked: the same bits
     f2, r2, s2 = pkg.logp_sharded(split(x), t, tau, p, k, chunk_maxima=False)
+    # one merge round: rows outside the first window stay at support -2
+    f3, r3, s3 = pkg.logp_sharded(split(x), t, tau, p, k, resolve=False)
     torch.cuda.synchronize()
     for u, v in ((f1, f2), (r1, r2), (s1, s2)):
         assert torch.equal(u.view(torch.int32), v.view(torch.int32))
-    f0b, f1b = bits32(f0), bits32(f1)
-    assert (f0b == f1b).all(), np.nonzero(f0b != f1b)[0][:10]
-    s0n, s1n = s0.cpu().numpy(), s1.cpu().numpy()
-    ok = s1n != -2
-    r0b, r1b = bits32(r0), bits32(r1)
-    bad = np.nonzero(ok & ((r0b != r1b) | (s0n != s1n)))[0]
+    for fx in (f1, f3):
+        f0b, fxb = bits32(f0), bits32(fx)
+        assert (f0b == fxb).all(), np.nonzero(f0b != fxb)[0][:10]
+    s0n, s1n, s3n = s0.cpu().numpy(), s1.cpu().numpy(), s3.cpu().numpy()
+    r0b, r1b, r3b = bits32(r0), bits32(r1), bits32(r3)
+    bad = np.nonzero((r0b != r1b) | (s0n != s1n))[0]
     assert len(bad) == 0, (bad[:10], s0n[bad[:10]], s1n[bad[:10]])
-    # rows outside the window: NaN restricted, a real support in the fused kernel
+    ok = s3n != -2
+    assert ((r3b == r0b) | ~ok).all() and ((s3n == s0n) | ~ok).all()
+    # rows outside the first window: NaN restricted after one round, a real support in the fused kernel
     wide = np.nonzero(~ok)[0]
-    assert np.isnan(r1.cpu().numpy()[wide]).all()
+    assert np.isnan(r3.cpu().numpy()[wide]).all()
     assert (s0n[wide] > 0).all()
-    return s0n, s1n
+    return s0n, s3n
 
 
 def test_sharded_matches_fused_mixed_parameters():
@@ -128,7 +136,10 @@ def test_sharded_nonfinite_and_invalid_rows():
 def test_sharded_spread_rows_and_wide_supports():
     """Spread rows (N(0,3^2), tau 0.7, p 0.95) keep their nucleus inside the
     window; rows centred on 0 with a small spread, whose nucleus crosses zero
-    (many binades below the maximum), are reported with support -2."""
+    (many binades below the maximum), need lower windows: one merge round
+    reports them with support -2, the resumable rounds resolve them to the
+    fused kernel's bits (top-p alone, top-k alone, and top-k reaching below
+    the window followed by top-p from the top window again)."""
     wl = W.workload_c0(device=DEV, T=32)
     t = W.structural_targets(32, None, None, seed=24, device=DEV)
     s0, s1 = compare(wl.logits, t, 0.7, 0.95, -1)
@@ -194,3 +205,25 @@ def test_shard_summaries_match_the_oracle():
             assert float(np.float32(m[r, i]) / np.float32(taus[i])) == om[r]
             assert abs(l[r, i] - ol[r]) <= 2e-5 * ol[r], (i, r, l[r, i], ol[r])
         assert xt[i].item() == float(oracle.bf16_bits_to_f32(bits[i][t[i].item():t[i].item() + 1])[0])
+
+
+def test_sharded_resolves_every_row_of_deep_top_p_workloads():
+    """Top-p-only rows at temperature 1.3 and p 0.99 (supports of thousands of
+    tokens), the fused kernel's wide-support rows, and k beyond 1024 with top-p:
+    through the sharded entry points every row resolves, bit for bit equal to
+    the fused pass, and no row keeps support -2."""
+    x, hot, n = W.hot_logits(48, 1, 512, seed=27, device=DEV)
+    t = W.structural_targets(48, hot, n, seed=27, device=DEV)
+    s0, s3 = compare(x, t, 1.3, 0.99, -1)
+    assert (s0 > 1000).sum() >= 10
+    rng = np.random.default_rng(28)
+    xw = (0.02 * rng.standard_normal((8, VP))).astype(np.float32)
+    xw[:, 5] = 3.0
+    xw = torch.as_tensor(xw, device=DEV).to(torch.bfloat16)
+    xw[:, VR:] = float("-inf")
+    tw = _t([5, 9, 5, 77, 5, 1000, 5, 151935], torch.int32)
+    tau = _t([1.0, 1.0, 0.5, 1.0, 2.0, 1.0, 1.0, 1.0], torch.float32)
+    p = _t([0.9, 0.5, 0.99, 1.0, 0.7, 0.99, 0.3, 0.999], torch.float32)
+    k = _t([-1, -1, -1, 100000, 70000, 3000, 120000, 20000], torch.int32)
+    s0, s3 = compare(xw, tw, tau, p, k)
+    assert (s3 == -2).sum() >= 5
