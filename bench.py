@@ -64,6 +64,12 @@ def parse():
                     help="time the gradient norm on the 10M-element case only (for profiling)")
     ap.add_argument("--configs-steps", type=int, default=20,
                     help="launches of the pair pass timed on each of the other workloads (0: skip)")
+    ap.add_argument("--kinds-steps", type=int, default=10,
+                    help="launches of the pair pass timed per row kind (tau/p/k) on one 8192-row "
+                         "hot-set tensor (0: skip)")
+    ap.add_argument("--kind", default=None,
+                    help="profiling: time only the pair pass on --rows rows of one kind TAU/P/K "
+                         "(hot sets of 1..512 columns) and exit")
     ap.add_argument("--rows", type=int, default=T_ROWS,
                     help="rows per GPU (default: the 8192-row workload; smaller only for profiling)")
     return ap.parse_args()
@@ -324,6 +330,35 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# (tau, top-p, top-k) of the row-kind timings: unfiltered, greedy, the 8192-row
+# workload's filter, top-k only, and top-p only at three temperatures
+ROW_KINDS = [(1.0, 1.0, -1), (0.0, 1.0, -1), (1.3, 0.99, 128), (1.3, 1.0, 50), (0.7, 0.95, -1),
+             (0.7, 0.9, -1), (1.0, 0.9, -1), (1.0, 0.95, -1), (1.3, 0.9, -1), (1.3, 0.95, -1),
+             (1.3, 0.99, -1)]
+
+
+def run_kind(args, dev):
+    """Profiling aid: only the pair pass, on --rows rows of one row kind."""
+    import torch
+    import rollout_consistent_vocab_gb300 as pkg
+    from rollout_consistent_vocab_gb300 import workloads as W
+    tau_k, p_k, k_k = args.kind.split("/")
+    tau_k, p_k, k_k = float(tau_k), float(p_k), int(k_k)
+    T = args.rows
+    x, h, n = W.hot_logits(T, 1, 512, seed=77, device=dev)
+    t = W.structural_targets(T, h, n, seed=77, device=dev)
+    for _ in range(max(args.warmup, 3)):
+        pkg.logp_pair(x, t, tau_k, p_k, k_k)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        pkg.logp_pair(x, t, tau_k, p_k, k_k)
+    e1.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"kind": args.kind, "rows": T, "ms_per_launch": e0.elapsed_time(e1) / args.steps}))
+
+
 def workload_config():
     return {"workload": WORKLOAD, "rows_per_gpu": T_ROWS, "vocab_padded": VPAD,
             "vocab_real": VREAL, "temperature": TAU, "top_p": TOP_P, "top_k": TOP_K,
@@ -345,6 +380,9 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pkg.load_library()
+    if args.kind is not None:
+        run_kind(args, dev)
+        return
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
@@ -448,6 +486,35 @@ def run_ours(args, rank, world, local):
             del wl, tgc, fo, ro, so
             torch.cuda.empty_cache()
         del flush
+
+    # ---- the pair pass per row kind (one parameter set per launch) on one
+    #      8192-row tensor of hot-set logits (1..512 hot columns per row)
+    kinds = None
+    if args.kinds_steps > 0:
+        kinds = {}
+        xk, hk, nk = W.hot_logits(8192, 1, 512, seed=rank_seed(77, rank), device=dev)
+        tk = W.structural_targets(8192, hk, nk, seed=rank_seed(77, rank), device=dev)
+        fo, ro = torch.empty(8192, **f32), torch.empty(8192, **f32)
+        so = torch.empty(8192, dtype=torch.int32, device=dev)
+        peak_k, _ = measured_peak()
+        for tau_k, p_k, k_k in ROW_KINDS:
+            for _ in range(3):
+                pkg.logp_pair(xk, tk, tau_k, p_k, k_k, out_full=fo, out_restr=ro, out_support=so,
+                              stream=stream)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.kinds_steps)]
+            for a, b in evs:
+                a.record(stream)
+                pkg.logp_pair(xk, tk, tau_k, p_k, k_k, out_full=fo, out_restr=ro, out_support=so,
+                              stream=stream)
+                b.record(stream)
+            torch.cuda.synchronize()
+            ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+            kinds[f"{tau_k}/{p_k}/{k_k}"] = {
+                "ms": ms, "frac": 8192 * VPAD * 2 / (ms / 1e3) / 1e9 / peak_k,
+                "mean_support": float(so.float().mean().item())}
+        del xk, hk, nk, tk
+        torch.cuda.empty_cache()
 
     # ---- end to end through the public API from pinned host buffers
     e2e = None
@@ -771,6 +838,7 @@ def run_ours(args, rank, world, local):
             "gpu_launches": 2 * K,
             "parity": parity,
             "configs": configs,
+            "row_kinds": kinds,
             "clocks": clk.summary(),
             "e2e": e2e,
             "sharded": sharded,
