@@ -351,6 +351,40 @@ def linear_logp_rows(h_bits: np.ndarray, w_bits: np.ndarray, tau, targets, vreal
     return out
 
 
+def linear_logp_pair_row(h_bits: np.ndarray, w_bits: np.ndarray, tau: float, top_p: float,
+                         top_k: int, target: int, vreal: int = VREAL) -> RowResult:
+    """Full and restricted logprob of ``target`` when the logits are the LM
+    head's output x = h . W^T, formed exactly (fp64 products of bf16 values,
+    fp64 sums), as in ``linear_logp_row``.
+
+    The policy side keeps its own sampling support while the reference side is
+    scaled over the whole vocabulary ("Configurable H100 consistency runs",
+    KL-reference paragraph); the support is the same top-k-then-top-p set as
+    for stored logits (``logp_row``), here over the full-precision logits:
+    s = x / tau; S_k = {j : x_j >= k-th largest x} (ties kept); S = the tokens
+    of S_k whose renormalised mass strictly above them is < p.  tau > 0.
+    """
+    if not (math.isfinite(tau) and tau > 0.0):
+        raise InvalidArgument(f"temperature must be finite and > 0, got {tau}")
+    validate(tau, top_p, top_k, target, vreal)
+    h = bf16_bits_to_f32(np.asarray(h_bits, dtype=np.uint16)).astype(np.float64)
+    w = bf16_bits_to_f32(np.asarray(w_bits, dtype=np.uint16)[:vreal]).astype(np.float64)
+    x = w @ h
+    s = x / float(np.float32(tau))
+    m = float(np.max(s))
+    with np.errstate(under="ignore"):
+        e = np.exp(s - m)
+    full = (float(s[target]) - m) - math.log(math.fsum(e))
+    k_on = not (top_k == -1 or top_k >= vreal)
+    p_on = top_p < 1.0
+    if not k_on and not p_on:
+        return RowResult(full=full, restr=full, support=vreal, top_p=top_p)
+    sk = top_k_mask(s, top_k)
+    S = top_p_mask(s, sk, top_p)[0] if p_on else sk
+    restr = (float(s[target]) - m) - math.log(math.fsum(e[S])) if S[target] else -math.inf
+    return RowResult(full=full, restr=restr, support=int(np.count_nonzero(S)), top_p=top_p)
+
+
 # ----------------------------------------------------------------- sampling
 
 _PHILOX_M = (0xD2511F53, 0xCD9E8D57)   # round multipliers
