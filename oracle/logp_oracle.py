@@ -364,11 +364,15 @@ def linear_logp_pair_row(h_bits: np.ndarray, w_bits: np.ndarray, tau: float, top
     s = x / tau; S_k = {j : x_j >= k-th largest x} (ties kept); S = the tokens
     of S_k whose renormalised mass strictly above them is < p.  tau > 0.
     """
+    w = bf16_bits_to_f32(np.asarray(w_bits, dtype=np.uint16)[:vreal]).astype(np.float64)
+    return _linear_pair(h_bits, w, tau, top_p, top_k, target, vreal)
+
+
+def _linear_pair(h_bits, w, tau, top_p, top_k, target, vreal):
     if not (math.isfinite(tau) and tau > 0.0):
         raise InvalidArgument(f"temperature must be finite and > 0, got {tau}")
     validate(tau, top_p, top_k, target, vreal)
     h = bf16_bits_to_f32(np.asarray(h_bits, dtype=np.uint16)).astype(np.float64)
-    w = bf16_bits_to_f32(np.asarray(w_bits, dtype=np.uint16)[:vreal]).astype(np.float64)
     x = w @ h
     s = x / float(np.float32(tau))
     m = float(np.max(s))
@@ -383,6 +387,25 @@ def linear_logp_pair_row(h_bits: np.ndarray, w_bits: np.ndarray, tau: float, top
     S = top_p_mask(s, sk, top_p)[0] if p_on else sk
     restr = (float(s[target]) - m) - math.log(math.fsum(e[S])) if S[target] else -math.inf
     return RowResult(full=full, restr=restr, support=int(np.count_nonzero(S)), top_p=top_p)
+
+
+def linear_logp_pair_rows(h_bits: np.ndarray, w_bits: np.ndarray, tau, top_p, top_k, targets,
+                          vreal: int = VREAL):
+    """linear_logp_pair_row for several rows (h_bits [n, H]; scalar or per-row
+    tau, top_p, top_k) with the weight widened once: the same definition, row
+    by row.  Returns (full[n], restr[n], support[n])."""
+    w = bf16_bits_to_f32(np.asarray(w_bits, dtype=np.uint16)[:vreal]).astype(np.float64)
+    n = h_bits.shape[0]
+    full, restr, sup = np.empty(n), np.empty(n), np.empty(n, dtype=np.int64)
+
+    def at(v, i):
+        return v[i] if np.ndim(v) else v
+
+    for i in range(n):
+        r = _linear_pair(h_bits[i], w, float(at(tau, i)), float(at(top_p, i)), int(at(top_k, i)),
+                         int(targets[i]), vreal)
+        full[i], restr[i], sup[i] = r.full, r.restr, r.support
+    return full, restr, sup
 
 
 # ----------------------------------------------------------------- sampling

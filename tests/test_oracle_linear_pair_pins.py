@@ -163,3 +163,49 @@ def test_planted_linear_pair_mistake_is_caught(mutant):
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, f"{mutant.__name__} passed every pin"
+
+
+# ------------------------------------------------------ linear_logp_pair_rows
+
+def pin_rows_equal_the_row_definition(rows_impl):
+    """The batch form, with scalar and with per-row tau, top_p, top_k, equals
+    linear_logp_pair_row (itself pinned above) row by row."""
+    rng = np.random.default_rng(44)
+    wb = _bits(0.5 * rng.standard_normal((VPAD, H)).astype(np.float32))
+    hb = _bits(rng.standard_normal((5, H)) * 2)
+    taus = np.array([0.7, 1.0, 1.3, 2.0, 0.5], np.float32)
+    ps = np.array([0.9, 0.95, 1.0, 0.5, 0.99], np.float32)
+    ks = np.array([-1, 50, 128, -1, 7])
+    tg = np.array([3, 77, 1000, 151935, 42])
+    for tau, p, k in ((taus, ps, ks), (1.3, 0.99, 128)):
+        full, restr, sup = rows_impl(hb, wb, tau, p, k, tg)
+        for i in range(5):
+            at = (lambda v: v[i] if np.ndim(v) else v)
+            r = oracle.linear_logp_pair_row(hb[i], wb, float(at(tau)), float(at(p)), int(at(k)), int(tg[i]))
+            assert full[i] == r.full and sup[i] == r.support, (i, tau)
+            assert restr[i] == r.restr, (i, tau)
+
+
+def test_linear_pair_rows_pin():
+    pin_rows_equal_the_row_definition(oracle.linear_logp_pair_rows)
+
+
+def _mut_rows_tau_shift(h, w, tau, p, k, targets):
+    t = np.roll(tau, 1) if np.ndim(tau) else tau
+    return oracle.linear_logp_pair_rows(h, w, t, p, k, targets)
+
+
+def _mut_rows_first_params(h, w, tau, p, k, targets):
+    first = (lambda v: v[0] if np.ndim(v) else v)
+    return oracle.linear_logp_pair_rows(h, w, first(tau), first(p), first(k), targets)
+
+
+def _mut_rows_target_roll(h, w, tau, p, k, targets):
+    return oracle.linear_logp_pair_rows(h, w, tau, p, k, np.roll(np.asarray(targets), 1))
+
+
+@pytest.mark.parametrize("mutant", [_mut_rows_tau_shift, _mut_rows_first_params, _mut_rows_target_roll],
+                         ids=lambda f: f.__name__)
+def test_planted_pair_rows_mistake_is_caught(mutant):
+    with pytest.raises(AssertionError):
+        pin_rows_equal_the_row_definition(mutant)
