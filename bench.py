@@ -732,7 +732,37 @@ def run_ours(args, rank, world, local):
                   "hidden": H, "avg_ms": l_ms, "tokens_per_s": T_ROWS / (l_ms / 1e3),
                   "tflops": flops / (l_ms / 1e3) / 1e12, "bound": "tensor", "peak_tflops": bf16_peak,
                   "peak_kind": bf16_kind, "frac": flops / (l_ms / 1e3) / 1e12 / bf16_peak}
-        del hid, wgt, lin_ws
+        del lin_ws
+
+        # the restricted side from the LM head: the summary GEMM, then window
+        # rounds that recompute the GEMM for row tiles with unresolved rows
+        pair_ws = torch.empty(pkg._binding.linear_pair_workspace_bytes(T_ROWS), dtype=torch.uint8, device=dev)
+        p_full, p_restr = torch.empty(T_ROWS, **f32), torch.empty(T_ROWS, **f32)
+        p_sup = torch.empty(T_ROWS, dtype=torch.int32, device=dev)
+        pair_kinds = {}
+        for label, (ptau, pp, pk) in (("tau1.3_p0.99_k128", (TAU, TOP_P, TOP_K)),
+                                      ("tau1.3_p0.99_k-1", (TAU, TOP_P, -1))):
+            def pair_step():
+                pkg.linear_logp_pair(hid, wgt, tg, ptau, pp, pk, out_full=p_full, out_restr=p_restr,
+                                     out_support=p_sup, workspace=pair_ws, stream=stream)
+            for _ in range(3):
+                pair_step()
+            torch.cuda.synchronize()
+            Kp = max(2, Kl // 2)
+            pev = [torch.cuda.Event(enable_timing=True) for _ in range(Kp + 1)]
+            pev[0].record(stream)
+            for i in range(Kp):
+                pair_step()
+                pev[i + 1].record(stream)
+            torch.cuda.synchronize()
+            p_ms = statistics.mean(pev[i].elapsed_time(pev[i + 1]) for i in range(Kp))
+            pair_kinds[label] = {"avg_ms": p_ms, "tokens_per_s": T_ROWS / (p_ms / 1e3),
+                                 "gemm_passes_equivalent": p_ms / l_ms,
+                                 "support_median": float(p_sup.float().median().item()),
+                                 "restr_finite_frac": float(torch.isfinite(p_restr).float().mean().item())}
+        linear["pair"] = {"kernels": "linear_kernel<summary> + prep + 12 x (compact + linear_kernel<window> "
+                                     "+ round) + final", "kinds": pair_kinds}
+        del hid, wgt, pair_ws
 
     # ---- the deterministic gradient norm (exact FP32 squares in integer
     #      exponent bins): 10M BF16 elements (the size the pages time), with

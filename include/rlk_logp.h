@@ -75,7 +75,7 @@ extern "C" {
 #define RLK_VOCAB_REAL 151936
 #define RLK_NUM_SHARDS 8
 #define RLK_SHARD_WIDTH 19072
-#define RLK_ABI_VERSION 3
+#define RLK_ABI_VERSION 4
 
 typedef enum {
   RLK_OK = 0,
@@ -307,6 +307,45 @@ rlk_status rlk_linear_logp(const void* hidden, int64_t T, int64_t H, int64_t hid
                            const void* weight, int64_t weight_stride, const int32_t* target,
                            const float* temperature, float temperature_scalar, float* out_full,
                            void* workspace, int32_t* err_count, void* stream);
+
+/* Full and restricted logprob straight from the LM head, without storing the
+ * logits: the policy side keeps its top-k-then-top-p support while the
+ * reference side is scaled over the whole vocabulary ("Configurable H100
+ * consistency runs", KL-reference and sampling-flags paragraphs).  The
+ * logits are the fp32 x = h . W^T of rlk_linear_logp, s = x / tau, and
+ * full, restr and support follow the definitions at the top of this file on
+ * those fp32 values (order keys of fp32; -0 ties with +0); the nucleus uses
+ * the fixed-point masses of rlk_logp_pair (exp(s_j - s_max) in units of
+ * 2^-44, Z_k their exact sum; without top-k, Z_k is the float normaliser of
+ * the full side scaled to those units).  out_full is bit-identical to
+ * rlk_linear_logp.
+ *   hidden, weight, H, strides, target, temperature: as rlk_linear_logp
+ *     (tau > 0: no greedy rows).
+ *   top_p / top_k: per-row device arrays [T] or NULL for the scalars, domains
+ *     as in rlk_logp_args.
+ *   out_restr: float [T], required; out_full: float [T] or NULL; out_support:
+ *     int32 [T] or NULL.
+ *   workspace: RLK_LINEAR_PAIR_WORKSPACE_BYTES(T) bytes of device scratch,
+ *     256-byte aligned (tile summaries, per-row search state, bucket counts
+ *     and listed keys).
+ * The support is found by exact selection over the fp32 order keys: each
+ * round recomputes the GEMM for the row tiles that still hold an unresolved
+ * row, histogramming and listing the keys of each row's current window; most
+ * rows resolve in the first round (top-k windows hold about k keys), at most
+ * five rounds per stage.  3 + 3 x 12 launches on `stream`; rounds with no
+ * unresolved row do no GEMM work.  A rejected row gets NaN outputs, support
+ * -1 and counts in err_count; a row with a NaN or infinite logit gets NaN
+ * restr and support -1; a wait that gives up leaves NaN and counts in
+ * err_count; a row still unresolved after the last round (not expected) gets
+ * NaN and support -2. */
+#define RLK_LINEAR_PAIR_WORKSPACE_BYTES(T) ((size_t)(T) * 33600u + 4096u)
+
+rlk_status rlk_linear_logp_pair(const void* hidden, int64_t T, int64_t H, int64_t hidden_stride,
+                                const void* weight, int64_t weight_stride, const int32_t* target,
+                                const float* temperature, float temperature_scalar, const float* top_p,
+                                float top_p_scalar, const int32_t* top_k, int32_t top_k_scalar,
+                                float* out_full, float* out_restr, int32_t* out_support, void* workspace,
+                                int32_t* err_count, void* stream);
 
 /* ---------------------------------------------------------------------
  * Vocabulary-sharded form: the fixed virtual TP8 partition with each shard

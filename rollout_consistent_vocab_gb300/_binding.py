@@ -64,7 +64,7 @@ class ShardArgs(ctypes.Structure):
 
 COMPUTE = ("rlk_logp_full", "rlk_logp_restricted", "rlk_logp_pair", "rlk_logp_kl", "rlk_logp_kl_ref",
            "rlk_logp_backward", "rlk_logp_pair_save", "rlk_logp_backward_saved", "rlk_sample",
-           "rlk_sample_noalloc", "rlk_linear_logp",
+           "rlk_sample_noalloc", "rlk_linear_logp", "rlk_linear_logp_pair",
            "rlk_logp_shard_summary", "rlk_logp_shard_counts", "rlk_logp_merge",
            "rlk_logp_merge_resumable", "rlk_logp_shard_counts_window",
            "rlk_sqnorm_accumulate", "rlk_sqnorm_finalize", "rlk_grad_norm")
@@ -96,6 +96,8 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     lib.rlk_sample_noalloc.argtypes = [A, ctypes.c_uint64, VP, VP, VP, VP, VP, VP, VP]
     i64 = ctypes.c_int64
     lib.rlk_linear_logp.argtypes = [VP, i64, i64, i64, VP, i64, VP, VP, ctypes.c_float, VP, VP, VP, VP]
+    lib.rlk_linear_logp_pair.argtypes = [VP, i64, i64, i64, VP, i64, VP, VP, ctypes.c_float, VP,
+                                         ctypes.c_float, VP, ctypes.c_int32, VP, VP, VP, VP, VP, VP]
     lib.rlk_logp_backward_saved.argtypes = [A, VP, VP, VP, VP, ctypes.c_int64, ctypes.c_int32, VP]
     SA = P(ShardArgs)
     lib.rlk_logp_shard_summary.argtypes = [SA, VP, VP, VP, VP, VP, VP]
@@ -117,7 +119,7 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     lib.rlk_last_error.restype = ctypes.c_char_p
     lib.rlk_abi_version.argtypes = []
     lib.rlk_abi_version.restype = ctypes.c_int
-    if lib.rlk_abi_version() != 3:
+    if lib.rlk_abi_version() != 4:
         raise ImportError("librlk_logp.so ABI version mismatch")
     _lib = lib
     return lib
@@ -604,6 +606,44 @@ def linear_logp(hidden, weight, target, temperature=1.0, *, out=None, workspace=
                               weight.data_ptr(), weight.stride(0), _ptr(target), tp, ts, _ptr(out),
                               workspace.data_ptr(), _ptr(err_count), _stream(stream)))
     return out
+
+
+def linear_pair_workspace_bytes(T: int) -> int:
+    return T * 33600 + 4096
+
+
+def linear_logp_pair(hidden, weight, target, temperature=1.0, top_p=1.0, top_k=-1, *, out_full=None,
+                     out_restr=None, out_support=None, workspace=None, err_count=None, stream=None):
+    """Full and restricted logprob of each row's target, and the support size,
+    with logits = hidden . weight^T formed on the tensor cores and never
+    stored; the support is selected exactly over the fp32 logits.  Returns
+    (full, restr, support)."""
+    lib = load_library()
+    torch = _torch()
+    T, H = hidden.shape
+    for t, name in ((hidden, "hidden"), (weight, "weight")):
+        if t.dtype != torch.bfloat16 or t.dim() != 2 or t.stride(1) != 1 or not t.is_cuda:
+            raise ValueError(f"{name} must be a bf16 CUDA matrix with unit column stride")
+    if weight.shape[0] != VOCAB_PADDED or weight.shape[1] != H:
+        raise ValueError(f"weight must be [{VOCAB_PADDED}, {H}]")
+    if target.dtype != torch.int32 or target.shape != (T,) or not target.is_contiguous():
+        raise ValueError("target must be a contiguous int32 tensor of shape [T]")
+    tp, ts = _param(temperature, T, torch.float32, "temperature")
+    pp, ps = _param(top_p, T, torch.float32, "top_p")
+    kp, ks = _param(top_k, T, torch.int32, "top_k")
+    out_full = _empty(T, torch.float32, hidden) if out_full is None else out_full
+    out_restr = _empty(T, torch.float32, hidden) if out_restr is None else out_restr
+    out_support = _empty(T, torch.int32, hidden) if out_support is None else out_support
+    if workspace is None:
+        workspace = torch.empty(max(1, linear_pair_workspace_bytes(T)), dtype=torch.uint8,
+                                device=hidden.device)
+    elif workspace.numel() * workspace.element_size() < linear_pair_workspace_bytes(T):
+        raise ValueError("workspace must hold at least linear_pair_workspace_bytes(T) bytes")
+    check(lib.rlk_linear_logp_pair(hidden.data_ptr() if T else None, T, H, hidden.stride(0) if T else H,
+                                   weight.data_ptr(), weight.stride(0), _ptr(target), tp, ts, pp, ps, kp,
+                                   ks, _ptr(out_full), _ptr(out_restr), _ptr(out_support),
+                                   workspace.data_ptr(), _ptr(err_count), _stream(stream)))
+    return out_full, out_restr, out_support
 
 
 # ----------------------------------------------------------------- gradient norm

@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.rlk_abi_version() == 3
+    assert lib.rlk_abi_version() == 4
     assert lib.rlk_status_string(0) == b"ok"
     assert lib.rlk_status_string(2) == b"misaligned pointer or stride"
 
@@ -323,6 +323,37 @@ def test_linear_logp_validation(lib):
     assert L(out=None) == b.RLK_EINVAL
 
 
+def test_linear_logp_pair_validation(lib):
+    f32 = ctypes.c_float
+
+    def L(T=4, H=256, hs=256, w=0xA0000, ws_=256, tg=OUT, tau=1.0, pp=None, p=0.9, kp=None, k=50,
+          full=None, restr=OUT, sup=None, ws=0xB0000, h=0xC0000, err=None):
+        return lib.rlk_linear_logp_pair(h, T, H, hs, w, ws_, tg, None, f32(tau), pp, f32(p), kp, k, full,
+                                        restr, sup, ws, err, None)
+    assert L(T=-1) == b.RLK_EINVAL
+    assert L(T=1 << 24) == b.RLK_EINVAL
+    assert L(T=0, h=None, w=None, tg=None, restr=None, ws=None) == b.RLK_OK
+    assert L(restr=None) == b.RLK_EINVAL        # the restricted output is required
+    assert L(restr=OUT + 2) == b.RLK_EALIGN
+    assert L(full=OUT + 2) == b.RLK_EALIGN
+    assert L(sup=OUT + 6) == b.RLK_EALIGN
+    assert L(p=0.0) == b.RLK_EINVAL
+    assert L(p=1.5) == b.RLK_EINVAL
+    assert L(k=0) == b.RLK_EINVAL
+    assert L(k=-2) == b.RLK_EINVAL
+    assert L(k=b.VOCAB_REAL + 1) == b.RLK_EINVAL
+    assert L(pp=OUT + 2) == b.RLK_EALIGN
+    assert L(kp=OUT + 2) == b.RLK_EALIGN
+    assert L(ws=None) == b.RLK_EINVAL
+    assert L(ws=0xB0010) == b.RLK_EALIGN        # the pair's workspace is 256-byte aligned
+    assert L(H=100) == b.RLK_EINVAL
+    assert L(hs=260) == b.RLK_EALIGN
+    assert L(h=0xC0008) == b.RLK_EALIGN
+    assert L(tau=0.0) == b.RLK_EINVAL
+    assert L(tg=None) == b.RLK_EINVAL
+    assert L(err=OUT + 2) == b.RLK_EALIGN
+
+
 def _declared_param_counts():
     """Parameter count of every rlk_* function declared in include/*.h."""
     counts = {}
@@ -360,6 +391,8 @@ def test_binding_sizes_match_the_header_macros():
         assert b.sample_workspace_bytes(T) == ws
         lw = eval(re.sub(r"\(size_t\)|u\b", "", macro(text, "RLK_LINEAR_WORKSPACE_BYTES")).replace("(T)", f"({T})"))
         assert b.linear_workspace_bytes(T) == lw
+        lp = eval(re.sub(r"\(size_t\)|u\b", "", macro(text, "RLK_LINEAR_PAIR_WORKSPACE_BYTES")).replace("(T)", f"({T})"))
+        assert b.linear_pair_workspace_bytes(T) == lp
     assert int(macro(text, "RLK_SHARD_CHUNKS")) == b.SHARD_CHUNKS
     assert int(macro(norm, "RLK_NORM_BINS")) == b.NORM_BINS
     assert int(macro(text, "RLK_VOCAB_PADDED")) == b.VOCAB_PADDED
