@@ -326,19 +326,21 @@ rlk_status rlk_linear_logp(const void* hidden, int64_t T, int64_t H, int64_t hid
  *   out_restr: float [T], required; out_full: float [T] or NULL; out_support:
  *     int32 [T] or NULL.
  *   workspace: RLK_LINEAR_PAIR_WORKSPACE_BYTES(T) bytes of device scratch,
- *     256-byte aligned (tile summaries, per-row search state, bucket counts
- *     and listed keys).
- * The support is found by exact selection over the fp32 order keys: each
- * round recomputes the GEMM for the row tiles that still hold an unresolved
- * row, histogramming and listing the keys of each row's current window; most
- * rows resolve in the first round (top-k windows hold about k keys), at most
- * five rounds per stage.  3 + 3 x 12 launches on `stream`; rounds with no
+ *     256-byte aligned (tile summaries, the 8 largest logits of every
+ *     256-column tile, per-row search state, bucket counts and listed keys).
+ * The support is found by exact selection over the fp32 order keys.  The
+ * first GEMM pass keeps each tile's 8 largest logits; a row whose first
+ * window (top-k: at or above the k-th largest kept logit; top-p alone: the
+ * a-priori mass bound) they provably contain is resolved from them.  Other
+ * rows go through rounds that recompute the GEMM for the row tiles holding
+ * them, histogramming and listing the keys of each row's current window (at
+ * most five rounds per stage).  3 + 3 x 12 launches on `stream`; rounds with no
  * unresolved row do no GEMM work.  A rejected row gets NaN outputs, support
  * -1 and counts in err_count; a row with a NaN or infinite logit gets NaN
  * restr and support -1; a wait that gives up leaves NaN and counts in
  * err_count; a row still unresolved after the last round (not expected) gets
  * NaN and support -2. */
-#define RLK_LINEAR_PAIR_WORKSPACE_BYTES(T) ((size_t)(T) * 33600u + 4096u)
+#define RLK_LINEAR_PAIR_WORKSPACE_BYTES(T) ((size_t)(T) * 52640u + 4096u)
 
 rlk_status rlk_linear_logp_pair(const void* hidden, int64_t T, int64_t H, int64_t hidden_stride,
                                 const void* weight, int64_t weight_stride, const int32_t* target,

@@ -609,7 +609,7 @@ def linear_logp(hidden, weight, target, temperature=1.0, *, out=None, workspace=
 
 
 def linear_pair_workspace_bytes(T: int) -> int:
-    return T * 33600 + 4096
+    return T * 52640 + 4096
 
 
 def linear_logp_pair(hidden, weight, target, temperature=1.0, top_p=1.0, top_k=-1, *, out_full=None,

@@ -19,7 +19,8 @@
 //   warps 4-7            epilogue: each thread owns one row (TMEM lane), reads
 //                        its 256 fp32 logits 32 columns at a time and
 //                        EPI_SUMMARY: keeps an online (max, sum-exp) over the
-//                          real columns;
+//                          real columns (EPI_SUMMARY_TOP8: and the 8 largest
+//                          logits of the tile, for the restricted side);
 //                        EPI_WINDOW: histograms and lists the logits whose
 //                          order key lies in its row's current window (the
 //                          restricted side below).
@@ -66,7 +67,8 @@ constexpr uint32_t LIN_IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
                                (static_cast<uint32_t>(LN >> 3) << 17) |
                                (static_cast<uint32_t>(LM >> 4) << 24);
 
-enum : int { EPI_SUMMARY = 0, EPI_WINDOW = 1 };
+enum : int { EPI_SUMMARY = 0, EPI_WINDOW = 1, EPI_SUMMARY_TOP8 = 2 };
+constexpr int TOPR = 8;                     // largest logits kept per (row, vocabulary tile)
 
 // ---- restricted side: exact selection over fp32 order keys
 constexpr int NB = 1024;                    // histogram buckets of a window
@@ -74,6 +76,9 @@ constexpr int LIST_CAP = 4096;              // keys listed per row and round
 constexpr int PAIR_ROUNDS = 12;             // window rounds launched per call
 constexpr uint32_t KEY_BOTTOM = 0x007FFFFFu;   // order key of -inf; smaller keys are NaN patterns
 enum : uint32_t { WIN_IDLE = 0, WIN_KEY = 1, WIN_VALUE = 2 };
+// mode bit: every logit of the window is already listed (from the first
+// pass's per-tile top logits), so the next round needs no GEMM for the row
+constexpr uint32_t WIN_LISTED = 0x100u;
 constexpr uint32_t LIST_FAILED = 0x80000000u;   // listn bit: a histogram round lost a tile
 
 // Order key of an fp32 value: unsigned order equals numeric order for
@@ -123,6 +128,7 @@ struct LinArgs {
   float2* ws_ml;                            // [T][NTILE] (max, sum-exp) of each tile
   float* ws_xt;                             // [T] the target's logit
   int32_t* err;
+  float* ws_top;                            // [T][NTILE][TOPR] EPI_SUMMARY_TOP8: descending
   // EPI_WINDOW rounds
   const uint32_t* np;                       // number of listed row tiles
   const int32_t* mlist;                     // row tiles with an unresolved row
@@ -226,7 +232,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant_
               const LinArgs P) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nm = EPI == EPI_SUMMARY ? P.mt : static_cast<int>(*P.np);
+  const int nm = EPI != EPI_WINDOW ? P.mt : static_cast<int>(*P.np);
   if (nm == 0) return;                                        // uniform: nothing allocated yet
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;              // 1024-byte aligned ring
@@ -237,7 +243,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant_
   uint32_t* slot_ptr = reinterpret_cast<uint32_t*>(smem_raw + (slot - raw));
   uint32_t* flag_ptr = slot_ptr + 1;                          // a wait gave up
   const int ntiles = nm * NTILE;
-  auto row_tile = [&](int tile) { return EPI == EPI_SUMMARY ? tile % nm : P.mlist[tile % nm]; };
+  auto row_tile = [&](int tile) { return EPI != EPI_WINDOW ? tile % nm : P.mlist[tile % nm]; };
 
   if (tid == 0) {
     for (int s = 0; s < LSTAGES; ++s) {
@@ -312,11 +318,14 @@ linear_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant_
       const int64_t row = static_cast<int64_t>(m_tile) * LM + ew * 32 + lane;
       const bool live = row < P.T;
       const uint32_t trow = tmem + buf * 256 + (static_cast<uint32_t>(ew * 32) << 16);
-      if constexpr (EPI == EPI_SUMMARY) {
+      if constexpr (EPI != EPI_WINDOW) {
         const float tau = live ? (P.tau_arr ? P.tau_arr[row] : P.tau_s) : 1.0f;
         const float c = __fdiv_rn(LOG2E, tau);
         const int tcol = live ? P.target[row] - n_tile * LN : -1;
         float m = -INFINITY, l = 0.0f, xt = __int_as_float(0x7fc00000);
+        float top[TOPR];                                      // descending; NaN never enters
+#pragma unroll
+        for (int q = 0; q < TOPR; ++q) top[q] = -INFINITY;
 #pragma unroll 1
         for (int ch = 0; ch < LN / 32; ++ch) {
           float v[32];
@@ -340,12 +349,31 @@ linear_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant_
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj)
             if (col0 + jj < VREAL) l += ex2((v[jj] - m) * c);
+          if constexpr (EPI == EPI_SUMMARY_TOP8) {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              if (col0 + jj < VREAL && v[jj] > top[TOPR - 1]) {
+                top[TOPR - 1] = v[jj];
+#pragma unroll
+                for (int q = TOPR - 1; q > 0; --q) {        // one bubble step keeps the order
+                  const float hi = fmaxf(top[q - 1], top[q]), lo = fminf(top[q - 1], top[q]);
+                  top[q - 1] = hi;
+                  top[q] = lo;
+                }
+              }
+            }
+          }
         }
         if (live) {
           const bool good = ok && *flag_ptr == 0u;
           P.ws_ml[row * NTILE + n_tile] = good ? make_float2(m, l) : make_float2(__int_as_float(0x7fc00000), 0.0f);
           if (tcol >= 0 && tcol < LN) P.ws_xt[row] = xt;
           if (!good && P.err && n_tile == 0) atomicAdd(P.err, 1);
+          if constexpr (EPI == EPI_SUMMARY_TOP8) {
+            float4* dst = reinterpret_cast<float4*>(P.ws_top + (row * NTILE + n_tile) * TOPR);
+            dst[0] = make_float4(top[0], top[1], top[2], top[3]);
+            dst[1] = make_float4(top[4], top[5], top[6], top[7]);
+          }
         }
       } else {
         // histogram and list the logits of the row's window (exact integer
@@ -353,7 +381,8 @@ linear_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant_
         LinWin w;
         w.mode = WIN_IDLE;
         if (live) w = P.win[row];
-        const bool act = w.mode != WIN_IDLE && ok && *flag_ptr == 0u;
+        const bool want = w.mode != WIN_IDLE && !(w.mode & WIN_LISTED);
+        const bool act = want && ok && *flag_ptr == 0u;
         uint32_t* cnt = P.hcnt + row * NB;
         unsigned long long* mass = P.hmass + row * NB;
         uint32_t* lst = P.list + row * LIST_CAP;
@@ -388,7 +417,7 @@ linear_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant_
           }
         }
         // a wait gave up: the row's counts are incomplete; the selection fails it
-        if (live && w.mode != WIN_IDLE && !act) atomicOr(P.listn + row, LIST_FAILED);
+        if (live && want && !act) atomicOr(P.listn + row, LIST_FAILED);
       }
     }
   }
@@ -460,9 +489,12 @@ __global__ void __launch_bounds__(128) merge_lin_kernel(const LinArgs P, float* 
 // the row from the list (every in-window key listed: sorted, exact) or moves
 // the window to the bucket where the count or mass target is crossed,
 // carrying the counts and masses above it.  The first window of a search is
-// bounded a priori: for top-k by the k-th largest of the 596 tile maxima (k
-// distinct tokens reach it), for top-p alone by the mass bound (a token of
-// mass <= (1 - p) Z / V leaves at least p Z above it), halved for margin.
+// bounded a priori: for top-k by the k-th largest of the logits the first
+// pass kept (the 8 largest of every 256-column tile: k distinct tokens reach
+// it), for top-p alone by the mass bound (a token of mass <= (1 - p) Z / V
+// leaves at least p Z above it), halved for margin.  When every tile's 8th
+// kept logit lies below that window, the kept logits hold the whole window:
+// the row is listed from them and its first round needs no GEMM.
 
 // Per-row selection state.
 struct LinSel {
@@ -580,27 +612,21 @@ __global__ void __launch_bounds__(128) pair_prep_kernel(const LinArgs P, const P
   s.top_key = key32(M);
   s.p = p_on ? p : 1.0f;
   s.k = k_on ? k : 0;
+  const float* tp = P.ws_top + row * NTILE * TOPR;             // each tile's 8 largest, descending
   if (finite && k_on) {
-    // the k-th largest tile maximum: k distinct real tokens are >= it
-    const float2* ml = P.ws_ml + row * NTILE;
-    uint32_t tk[(NTILE + 31) / 32];
-#pragma unroll
-    for (int i = 0; i < (NTILE + 31) / 32; ++i) {
-      const int q = lane + 32 * i;
-      tk[i] = q < NTILE ? key32(ml[q].x) : 0u;
-    }
+    // the k-th largest stored logit, to its top 16 key bits: k distinct
+    // real tokens are >= it
     uint32_t pre = 0u;
-    for (int bit = 31; bit >= 0; --bit) {
-      const uint32_t cand = pre | (1u << bit);
+    for (int bit = 15; bit >= 0; --bit) {
+      const uint32_t cand = (pre | (1u << bit)) << 16;
       int n = 0;
-#pragma unroll
-      for (int i = 0; i < (NTILE + 31) / 32; ++i) n += tk[i] >= cand;
+      for (int i = lane; i < NTILE * TOPR; i += 32) n += key32(tp[i]) >= cand;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
-      if (n >= k) pre = cand;
+      if (n >= k) pre |= 1u << bit;
     }
     s.stage = 0u;
-    open_window(w, (k <= NTILE && pre > KEY_BOTTOM) ? pre : KEY_BOTTOM, s.top_key);
+    open_window(w, (k <= NTILE * TOPR && (pre << 16) > KEY_BOTTOM) ? (pre << 16) : KEY_BOTTOM, s.top_key);
   } else if (finite && p_on) {
     s.T = nucleus_bound(p, __float2ull_rn(z * FX_SCALE));
     s.stage = 1u;
@@ -613,6 +639,36 @@ __global__ void __launch_bounds__(128) pair_prep_kernel(const LinArgs P, const P
     }
     open_window(w, lo, s.top_key);
   }
+  uint32_t listed = 0u;
+  if (w.mode != WIN_IDLE) {
+    // the first pass kept each tile's 8 largest logits: when every tile's 8th
+    // lies below the window, the window's logits are all among them
+    bool covered = true;
+    for (int q = lane; q < NTILE; q += 32) covered = covered && key32(tp[q * TOPR + TOPR - 1]) < w.wlo;
+    if (__all_sync(0xffffffffu, covered)) {
+      uint32_t mine = 0u;
+      const int per = (NTILE * TOPR + 31) / 32;                // a contiguous run per lane
+      const int i0 = lane * per, i1 = min(NTILE * TOPR, i0 + per);
+      for (int i = i0; i < i1; ++i) mine += key32(tp[i]) >= w.wlo;
+      uint32_t before = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, before, o);
+        if (lane >= o) before += t;
+      }
+      const uint32_t total = __shfl_sync(0xffffffffu, before, 31);
+      before -= mine;
+      if (total <= static_cast<uint32_t>(LIST_CAP)) {
+        uint32_t* dst = A.list + row * LIST_CAP;
+        for (int i = i0; i < i1; ++i) {
+          const uint32_t K = key32(tp[i]);
+          if (K >= w.wlo) dst[before++] = K;
+        }
+        w.mode |= WIN_LISTED;
+        listed = total;
+      }
+    }
+  }
   if (lane == 0) {
     if (A.out_full) A.out_full[row] = full;
     if (!finite) {
@@ -622,17 +678,19 @@ __global__ void __launch_bounds__(128) pair_prep_kernel(const LinArgs P, const P
       A.out_restr[row] = full;
       if (A.out_support) A.out_support[row] = VREAL;
     }
-    A.listn[row] = 0u;
+    A.listn[row] = listed;
     A.win[row] = w;
     A.sel[row] = s;
   }
 }
 
-// One block per row tile: list the unresolved rows and row tiles of a round.
+// One block per row tile: list the unresolved rows of a round, and the row
+// tiles where one of them needs the GEMM.
 __global__ void __launch_bounds__(128) pair_compact_kernel(const PairArgs A, int round) {
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 128 + threadIdx.x;
-  const bool act = row < A.T && A.win[row].mode != WIN_IDLE;
+  const uint32_t mode = row < A.T ? A.win[row].mode : WIN_IDLE;
+  const bool act = mode != WIN_IDLE;
   uint32_t* cnt = A.counters + 2 * round;
   const unsigned m = __ballot_sync(0xffffffffu, act);
   if (m) {
@@ -641,7 +699,8 @@ __global__ void __launch_bounds__(128) pair_compact_kernel(const PairArgs A, int
     at = __shfl_sync(0xffffffffu, at, 0);
     if (act) A.rowlist[at + __popc(m & ((1u << lane) - 1u))] = static_cast<int32_t>(row);
   }
-  if (__syncthreads_or(act) && threadIdx.x == 0) A.mlist[atomicAdd(cnt + 1, 1u)] = static_cast<int32_t>(blockIdx.x);
+  if (__syncthreads_or(act && !(mode & WIN_LISTED)) && threadIdx.x == 0)
+    A.mlist[atomicAdd(cnt + 1, 1u)] = static_cast<int32_t>(blockIdx.x);
 }
 
 // Inclusive prefix sums, in place, of n masses (and counts, if cc) in
@@ -1002,6 +1061,9 @@ rlk_status lin_setup(LinLaunch& L, const void* hidden, int64_t T, int64_t H, int
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(linear_kernel<EPI_WINDOW>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(LIN_SMEM));
     if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(linear_kernel<EPI_SUMMARY_TOP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(LIN_SMEM));
+    if (e == cudaSuccess)
       e = cudaFuncSetAttribute(pair_round_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ROUND_SMEM));
     if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     configured[dev] = true;
@@ -1020,7 +1082,7 @@ inline rlk_status launched() {
 
 // Workspace of the pair entry point, regions 256-byte aligned.
 struct PairLayout {
-  size_t hmass, ml, sel, win, hcnt, list, xt, listn, rowlist, mlist, counters, total;
+  size_t hmass, ml, top, sel, win, hcnt, list, xt, listn, rowlist, mlist, counters, total;
 };
 inline PairLayout pair_layout(int64_t T) {
   auto up = [](size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); };
@@ -1029,6 +1091,7 @@ inline PairLayout pair_layout(int64_t T) {
   size_t o = 0;
   L.hmass = o;    o = up(o + t * NB * 8);
   L.ml = o;       o = up(o + t * NTILE * 8);
+  L.top = o;      o = up(o + t * NTILE * TOPR * 4);
   L.sel = o;      o = up(o + t * sizeof(LinSel));
   L.win = o;      o = up(o + t * sizeof(LinWin));
   L.hcnt = o;     o = up(o + t * NB * 4);
@@ -1098,6 +1161,7 @@ rlk_status rlk_linear_logp_pair(const void* hidden, int64_t T, int64_t H, int64_
   LinArgs& P = L.P;
   P.ws_ml = reinterpret_cast<float2*>(ws + W.ml);
   P.ws_xt = reinterpret_cast<float*>(ws + W.xt);
+  P.ws_top = reinterpret_cast<float*>(ws + W.top);
   PairArgs A;
   memset(&A, 0, sizeof(A));
   A.T = T;
@@ -1126,7 +1190,7 @@ rlk_status rlk_linear_logp_pair(const void* hidden, int64_t T, int64_t H, int64_
   P.listn = A.listn;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  linear_kernel<EPI_SUMMARY><<<L.grid, LIN_THREADS, LIN_SMEM, st>>>(L.ta, L.tb, P);
+  linear_kernel<EPI_SUMMARY_TOP8><<<L.grid, LIN_THREADS, LIN_SMEM, st>>>(L.ta, L.tb, P);
   if ((s = launched()) != RLK_OK) return s;
   pair_prep_kernel<<<static_cast<unsigned>((T + 3) / 4), 128, 0, st>>>(P, A);
   if ((s = launched()) != RLK_OK) return s;
