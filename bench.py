@@ -760,7 +760,7 @@ def run_ours(args, rank, world, local):
                                  "gemm_passes_equivalent": p_ms / l_ms,
                                  "support_median": float(p_sup.float().median().item()),
                                  "restr_finite_frac": float(torch.isfinite(p_restr).float().mean().item())}
-        linear["pair"] = {"kernels": "linear_kernel<summary> + prep + 12 x (compact + linear_kernel<window> "
+        linear["pair"] = {"kernels": "linear_kernel<summary+top8> + prep + 12 x (linear_kernel<window> "
                                      "+ round) + final", "kinds": pair_kinds}
         del hid, wgt, pair_ws
 

@@ -330,11 +330,12 @@ rlk_status rlk_linear_logp(const void* hidden, int64_t T, int64_t H, int64_t hid
  *     256-column tile, per-row search state, bucket counts and listed keys).
  * The support is found by exact selection over the fp32 order keys.  The
  * first GEMM pass keeps each tile's 8 largest logits; a row whose first
- * window (top-k: at or above the k-th largest kept logit; top-p alone: the
- * a-priori mass bound) they provably contain is resolved from them.  Other
- * rows go through rounds that recompute the GEMM for the row tiles holding
- * them, histogramming and listing the keys of each row's current window (at
- * most five rounds per stage).  3 + 3 x 12 launches on `stream`; rounds with no
+ * window (top-k: at or above the k-th largest tile maximum, else the k-th
+ * largest kept logit; top-p alone: the a-priori mass bound) they provably
+ * contain is resolved from them.  Other rows go through rounds that
+ * recompute the GEMM for the row tiles holding them, histogramming and
+ * listing the keys of each row's current window (at most five rounds per
+ * stage).  One memset and 3 + 2 x 12 launches on `stream`; rounds with no
  * unresolved row do no GEMM work.  A rejected row gets NaN outputs, support
  * -1 and counts in err_count; a row with a NaN or infinite logit gets NaN
  * restr and support -1; a wait that gives up leaves NaN and counts in

@@ -528,9 +528,11 @@ struct PairArgs {
   unsigned long long* hmass;                // [T][NB]
   uint32_t* list;                           // [T][LIST_CAP]
   uint32_t* listn;                          // [T]
-  int32_t* rowlist;                         // [T] rows of the current round
-  int32_t* mlist;                           // [row tiles] row tiles of the current round
+  int32_t* rowlist;                         // [2][T] rows of a round (round parity)
+  int32_t* mlist;                           // [2][row tiles] row tiles of a round needing the GEMM
+  uint32_t* mflag;                          // [PAIR_ROUNDS][row tiles] a tile is listed for the round
   uint32_t* counters;                       // [PAIR_ROUNDS][2]: rows, row tiles listed per round
+  int mt;
 };
 
 constexpr int RT = 256;                     // threads of pair_round_kernel
@@ -563,13 +565,23 @@ __device__ __forceinline__ void open_window(LinWin& w, uint32_t lo, uint32_t top
   }
 }
 
+// Put an unresolved row on round r's list, and its row tile on the round's
+// GEMM list unless the row's window is already listed (counters and flags
+// are cleared before the first pass).
+__device__ __forceinline__ void enqueue_row(const PairArgs& A, int r, int64_t row, bool gemm) {
+  if (r >= PAIR_ROUNDS) return;
+  A.rowlist[(r & 1) * A.T + atomicAdd(A.counters + 2 * r, 1u)] = static_cast<int32_t>(row);
+  const int m = static_cast<int>(row / LM);
+  if (gemm && atomicExch(A.mflag + r * A.mt + m, 1u) == 0u)
+    A.mlist[(r & 1) * A.mt + atomicAdd(A.counters + 2 * r + 1, 1u)] = m;
+}
+
 // One warp per row: validate, merge the tile summaries (the full logprob,
 // bit-identical to rlk_linear_logp), finish the rows with nothing to select
 // and open the first window of the others; clear the row's round buffers.
 __global__ void __launch_bounds__(128) pair_prep_kernel(const LinArgs P, const PairArgs A) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + warp;
-  if (blockIdx.x == 0 && threadIdx.x < 2 * PAIR_ROUNDS) A.counters[threadIdx.x] = 0u;
   if (row >= P.T) return;
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   uint4* hc = reinterpret_cast<uint4*>(A.hcnt + row * NB);
@@ -613,20 +625,67 @@ __global__ void __launch_bounds__(128) pair_prep_kernel(const LinArgs P, const P
   s.p = p_on ? p : 1.0f;
   s.k = k_on ? k : 0;
   const float* tp = P.ws_top + row * NTILE * TOPR;             // each tile's 8 largest, descending
+  uint32_t listed = 0u;
+  // When every tile's 8th kept logit lies below the window, the window's
+  // logits are all among the kept ones: list them (no GEMM round needed).
+  auto try_list = [&]() -> bool {
+    bool covered = true;
+    for (int q = lane; q < NTILE; q += 32) covered = covered && key32(tp[q * TOPR + TOPR - 1]) < w.wlo;
+    if (!__all_sync(0xffffffffu, covered)) return false;
+    // lane-strided (coalesced) pass; ballots keep the list order fixed
+    uint32_t* dst = A.list + row * LIST_CAP;
+    uint32_t total = 0u;
+    for (int i0 = 0; i0 < NTILE * TOPR; i0 += 32) {
+      const int i = i0 + lane;
+      const uint32_t K = i < NTILE * TOPR ? key32(tp[i]) : 0u;
+      const bool in = K >= w.wlo;
+      const unsigned m = __ballot_sync(0xffffffffu, in);
+      const uint32_t at = total + __popc(m & ((1u << lane) - 1u));
+      if (in && at < static_cast<uint32_t>(LIST_CAP)) dst[at] = K;
+      total += __popc(m);
+    }
+    if (total > static_cast<uint32_t>(LIST_CAP)) return false;
+    w.mode |= WIN_LISTED;
+    listed = total;
+    return true;
+  };
   if (finite && k_on) {
-    // the k-th largest stored logit, to its top 16 key bits: k distinct
-    // real tokens are >= it
+    // first bound: the k-th largest tile maximum (k distinct real tokens reach it)
+    const float2* ml = P.ws_ml + row * NTILE;
+    uint32_t tk[(NTILE + 31) / 32];
+#pragma unroll
+    for (int i = 0; i < (NTILE + 31) / 32; ++i) {
+      const int q = lane + 32 * i;
+      tk[i] = q < NTILE ? key32(ml[q].x) : 0u;
+    }
     uint32_t pre = 0u;
-    for (int bit = 15; bit >= 0; --bit) {
-      const uint32_t cand = (pre | (1u << bit)) << 16;
+    for (int bit = 31; bit >= 0; --bit) {
+      const uint32_t cand = pre | (1u << bit);
       int n = 0;
-      for (int i = lane; i < NTILE * TOPR; i += 32) n += key32(tp[i]) >= cand;
+#pragma unroll
+      for (int i = 0; i < (NTILE + 31) / 32; ++i) n += tk[i] >= cand;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
-      if (n >= k) pre |= 1u << bit;
+      if (n >= k) pre = cand;
     }
     s.stage = 0u;
-    open_window(w, (k <= NTILE * TOPR && (pre << 16) > KEY_BOTTOM) ? (pre << 16) : KEY_BOTTOM, s.top_key);
+    open_window(w, (k <= NTILE && pre > KEY_BOTTOM) ? pre : KEY_BOTTOM, s.top_key);
+    if (!try_list() && k <= NTILE * TOPR) {
+      // tighter: the k-th largest kept logit, to its top 16 key bits
+      uint32_t p16 = 0u;
+      for (int bit = 15; bit >= 0; --bit) {
+        const uint32_t cand = (p16 | (1u << bit)) << 16;
+        int n = 0;
+        for (int i = lane; i < NTILE * TOPR; i += 32) n += key32(tp[i]) >= cand;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+        if (n >= k) p16 |= 1u << bit;
+      }
+      if ((p16 << 16) > w.wlo) {
+        open_window(w, p16 << 16, s.top_key);
+        try_list();
+      }
+    }
   } else if (finite && p_on) {
     s.T = nucleus_bound(p, __float2ull_rn(z * FX_SCALE));
     s.stage = 1u;
@@ -638,36 +697,7 @@ __global__ void __launch_bounds__(128) pair_prep_kernel(const LinArgs P, const P
       if (B > -INFINITY && B < M) lo = key32(B);
     }
     open_window(w, lo, s.top_key);
-  }
-  uint32_t listed = 0u;
-  if (w.mode != WIN_IDLE) {
-    // the first pass kept each tile's 8 largest logits: when every tile's 8th
-    // lies below the window, the window's logits are all among them
-    bool covered = true;
-    for (int q = lane; q < NTILE; q += 32) covered = covered && key32(tp[q * TOPR + TOPR - 1]) < w.wlo;
-    if (__all_sync(0xffffffffu, covered)) {
-      uint32_t mine = 0u;
-      const int per = (NTILE * TOPR + 31) / 32;                // a contiguous run per lane
-      const int i0 = lane * per, i1 = min(NTILE * TOPR, i0 + per);
-      for (int i = i0; i < i1; ++i) mine += key32(tp[i]) >= w.wlo;
-      uint32_t before = mine;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xffffffffu, before, o);
-        if (lane >= o) before += t;
-      }
-      const uint32_t total = __shfl_sync(0xffffffffu, before, 31);
-      before -= mine;
-      if (total <= static_cast<uint32_t>(LIST_CAP)) {
-        uint32_t* dst = A.list + row * LIST_CAP;
-        for (int i = i0; i < i1; ++i) {
-          const uint32_t K = key32(tp[i]);
-          if (K >= w.wlo) dst[before++] = K;
-        }
-        w.mode |= WIN_LISTED;
-        listed = total;
-      }
-    }
+    try_list();
   }
   if (lane == 0) {
     if (A.out_full) A.out_full[row] = full;
@@ -681,26 +711,8 @@ __global__ void __launch_bounds__(128) pair_prep_kernel(const LinArgs P, const P
     A.listn[row] = listed;
     A.win[row] = w;
     A.sel[row] = s;
+    if (w.mode != WIN_IDLE) enqueue_row(A, 0, row, !(w.mode & WIN_LISTED));
   }
-}
-
-// One block per row tile: list the unresolved rows of a round, and the row
-// tiles where one of them needs the GEMM.
-__global__ void __launch_bounds__(128) pair_compact_kernel(const PairArgs A, int round) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * 128 + threadIdx.x;
-  const uint32_t mode = row < A.T ? A.win[row].mode : WIN_IDLE;
-  const bool act = mode != WIN_IDLE;
-  uint32_t* cnt = A.counters + 2 * round;
-  const unsigned m = __ballot_sync(0xffffffffu, act);
-  if (m) {
-    uint32_t at = 0u;
-    if (lane == 0) at = atomicAdd(cnt, static_cast<uint32_t>(__popc(m)));
-    at = __shfl_sync(0xffffffffu, at, 0);
-    if (act) A.rowlist[at + __popc(m & ((1u << lane) - 1u))] = static_cast<int32_t>(row);
-  }
-  if (__syncthreads_or(act && !(mode & WIN_LISTED)) && threadIdx.x == 0)
-    A.mlist[atomicAdd(cnt + 1, 1u)] = static_cast<int32_t>(blockIdx.x);
 }
 
 // Inclusive prefix sums, in place, of n masses (and counts, if cc) in
@@ -920,7 +932,7 @@ __global__ void __launch_bounds__(RT) pair_round_kernel(const PairArgs A, int ro
   const int tid = threadIdx.x;
   const uint32_t nrows = A.counters[2 * round];
   for (uint32_t idx = blockIdx.x; idx < nrows; idx += gridDim.x) {
-    const int64_t row = A.rowlist[idx];
+    const int64_t row = A.rowlist[(round & 1) * A.T + idx];
     const uint32_t ln = A.listn[row];
     if (tid == 0) {
       sw = A.win[row];
@@ -964,6 +976,7 @@ __global__ void __launch_bounds__(RT) pair_round_kernel(const PairArgs A, int ro
     if (tid == 0) {
       A.win[row] = sw;
       A.sel[row] = ss;
+      if (sw.mode != WIN_IDLE) enqueue_row(A, round + 1, row, true);
     }
     __syncthreads();
   }
@@ -1082,7 +1095,7 @@ inline rlk_status launched() {
 
 // Workspace of the pair entry point, regions 256-byte aligned.
 struct PairLayout {
-  size_t hmass, ml, top, sel, win, hcnt, list, xt, listn, rowlist, mlist, counters, total;
+  size_t hmass, ml, top, sel, win, hcnt, list, xt, listn, rowlist, mlist, counters, mflag, total;
 };
 inline PairLayout pair_layout(int64_t T) {
   auto up = [](size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); };
@@ -1098,9 +1111,10 @@ inline PairLayout pair_layout(int64_t T) {
   L.list = o;     o = up(o + t * LIST_CAP * 4);
   L.xt = o;       o = up(o + t * 4);
   L.listn = o;    o = up(o + t * 4);
-  L.rowlist = o;  o = up(o + t * 4);
-  L.mlist = o;    o = up(o + mt * 4);
-  L.counters = o; o = up(o + 2 * PAIR_ROUNDS * 4);
+  L.rowlist = o;  o = up(o + 2 * t * 4);
+  L.mlist = o;    o = up(o + 2 * mt * 4);
+  L.counters = o; o = up(o + 2 * PAIR_ROUNDS * 4);       // counters and flags are contiguous:
+  L.mflag = o;    o = up(o + PAIR_ROUNDS * mt * 4);      // one memset clears both
   L.total = o;
   return L;
 }
@@ -1182,7 +1196,8 @@ rlk_status rlk_linear_logp_pair(const void* hidden, int64_t T, int64_t H, int64_
   A.rowlist = reinterpret_cast<int32_t*>(ws + W.rowlist);
   A.mlist = reinterpret_cast<int32_t*>(ws + W.mlist);
   A.counters = reinterpret_cast<uint32_t*>(ws + W.counters);
-  P.mlist = A.mlist;
+  A.mflag = reinterpret_cast<uint32_t*>(ws + W.mflag);
+  A.mt = P.mt;
   P.win = A.win;
   P.hcnt = A.hcnt;
   P.hmass = A.hmass;
@@ -1190,15 +1205,16 @@ rlk_status rlk_linear_logp_pair(const void* hidden, int64_t T, int64_t H, int64_
   P.listn = A.listn;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const cudaError_t me = cudaMemsetAsync(ws + W.counters, 0, W.total - W.counters, st);
+  if (me != cudaSuccess) return fail(RLK_ECUDA, "cudaMemsetAsync: %s", cudaGetErrorString(me));
   linear_kernel<EPI_SUMMARY_TOP8><<<L.grid, LIN_THREADS, LIN_SMEM, st>>>(L.ta, L.tb, P);
   if ((s = launched()) != RLK_OK) return s;
   pair_prep_kernel<<<static_cast<unsigned>((T + 3) / 4), 128, 0, st>>>(P, A);
   if ((s = launched()) != RLK_OK) return s;
   const unsigned rgrid = static_cast<unsigned>(T < 4 * L.sms ? T : 4 * L.sms);
   for (int r = 0; r < PAIR_ROUNDS; ++r) {
-    pair_compact_kernel<<<static_cast<unsigned>(P.mt), 128, 0, st>>>(A, r);
-    if ((s = launched()) != RLK_OK) return s;
     P.np = A.counters + 2 * r + 1;
+    P.mlist = A.mlist + (r & 1) * P.mt;
     linear_kernel<EPI_WINDOW><<<static_cast<unsigned>(L.sms), LIN_THREADS, LIN_SMEM, st>>>(L.ta, L.tb, P);
     if ((s = launched()) != RLK_OK) return s;
     pair_round_kernel<<<rgrid, RT, ROUND_SMEM, st>>>(A, r);
