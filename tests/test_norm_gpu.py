@@ -150,3 +150,23 @@ def test_norm_large_f32():
     _check(x)
     del x
     torch.cuda.empty_cache()
+
+
+def test_norm_every_bf16_pattern():
+    """All 65536 BF16 bit patterns (both zeros, subnormals, the exponents at the
+    edges of the BF16 integer path, infinities, NaNs) in shuffled order, then
+    the finite ones alone and mixed with ordinary values: bin for bin against
+    the oracle."""
+    g = torch.Generator(device=DEV).manual_seed(15)
+    pats = torch.arange(65536, dtype=torch.int32, device=DEV).to(torch.int16).view(torch.bfloat16)
+    x = pats[torch.randperm(65536, generator=g, device=DEV)]
+    assert torch.isnan(x.float()).any()
+    _check(x)
+    finite = x[torch.isfinite(x.float())]
+    _check(finite)
+    mixed = torch.cat([finite, (1e-3 * torch.randn(200000, generator=g, device=DEV)).to(torch.bfloat16)])
+    _check(mixed[torch.randperm(mixed.numel(), generator=g, device=DEV)])
+    # exponents just inside and outside the integer path, with a window that moves
+    e = torch.tensor([58, 59, 60, 61, 120, 184, 185, 186, 190, 191, 200], device=DEV, dtype=torch.float32)
+    edge = torch.exp2(e.repeat(5000) - 127.0) * (1.0 + torch.rand(55000, generator=g, device=DEV))
+    _check(edge.to(torch.bfloat16)[torch.randperm(55000, generator=g, device=DEV)])
