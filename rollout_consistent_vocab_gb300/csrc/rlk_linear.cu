@@ -576,144 +576,6 @@ __device__ __forceinline__ void enqueue_row(const PairArgs& A, int r, int64_t ro
     A.mlist[(r & 1) * A.mt + atomicAdd(A.counters + 2 * r + 1, 1u)] = m;
 }
 
-// One warp per row: validate, merge the tile summaries (the full logprob,
-// bit-identical to rlk_linear_logp), finish the rows with nothing to select
-// and open the first window of the others; clear the row's round buffers.
-__global__ void __launch_bounds__(128) pair_prep_kernel(const LinArgs P, const PairArgs A) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + warp;
-  if (row >= P.T) return;
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  uint4* hc = reinterpret_cast<uint4*>(A.hcnt + row * NB);
-  for (int i = lane; i < NB / 4; i += 32) hc[i] = zero;
-  uint4* hm = reinterpret_cast<uint4*>(A.hmass + row * NB);
-  for (int i = lane; i < NB / 2; i += 32) hm[i] = zero;
-
-  const float tau = P.tau_arr ? P.tau_arr[row] : P.tau_s;
-  const int t = P.target[row];
-  const float p = A.top_p ? A.top_p[row] : A.top_p_s;
-  const int k = A.top_k ? A.top_k[row] : A.top_k_s;
-  LinWin w;
-  memset(&w, 0, sizeof(w));
-  LinSel s;
-  memset(&s, 0, sizeof(s));
-  const float qnan = __int_as_float(0x7fc00000);
-  if (!tau_ok(tau) || t < 0 || t >= VREAL || !(p > 0.0f && p <= 1.0f) || !(k == -1 || (k >= 1 && k <= VREAL))) {
-    if (lane == 0) {
-      if (A.out_full) A.out_full[row] = qnan;
-      A.out_restr[row] = qnan;
-      if (A.out_support) A.out_support[row] = -1;
-      if (A.err) atomicAdd(A.err, 1);
-      A.listn[row] = 0u;
-      A.win[row] = w;
-    }
-    return;
-  }
-  const float c = __fdiv_rn(LOG2E, tau);
-  float M, z;
-  lin_merge(P, row, lane, c, M, z);
-  const float xt = P.ws_xt[row];
-  const float d = __fdiv_rn(xt - M, tau);
-  const float full = d - logf(z);
-  const bool k_on = !(k == -1 || k >= VREAL), p_on = p < 1.0f;
-  const bool finite = M > -INFINITY && M < INFINITY && z > 0.0f && z < INFINITY;
-  w.M = M;
-  w.c = c;
-  s.kt = key32(xt);
-  s.d = d;
-  s.top_key = key32(M);
-  s.p = p_on ? p : 1.0f;
-  s.k = k_on ? k : 0;
-  const float* tp = P.ws_top + row * NTILE * TOPR;             // each tile's 8 largest, descending
-  uint32_t listed = 0u;
-  // When every tile's 8th kept logit lies below the window, the window's
-  // logits are all among the kept ones: list them (no GEMM round needed).
-  auto try_list = [&]() -> bool {
-    bool covered = true;
-    for (int q = lane; q < NTILE; q += 32) covered = covered && key32(tp[q * TOPR + TOPR - 1]) < w.wlo;
-    if (!__all_sync(0xffffffffu, covered)) return false;
-    // lane-strided (coalesced) pass; ballots keep the list order fixed
-    uint32_t* dst = A.list + row * LIST_CAP;
-    uint32_t total = 0u;
-    for (int i0 = 0; i0 < NTILE * TOPR; i0 += 32) {
-      const int i = i0 + lane;
-      const uint32_t K = i < NTILE * TOPR ? key32(tp[i]) : 0u;
-      const bool in = K >= w.wlo;
-      const unsigned m = __ballot_sync(0xffffffffu, in);
-      const uint32_t at = total + __popc(m & ((1u << lane) - 1u));
-      if (in && at < static_cast<uint32_t>(LIST_CAP)) dst[at] = K;
-      total += __popc(m);
-    }
-    if (total > static_cast<uint32_t>(LIST_CAP)) return false;
-    w.mode |= WIN_LISTED;
-    listed = total;
-    return true;
-  };
-  if (finite && k_on) {
-    // first bound: the k-th largest tile maximum (k distinct real tokens reach it)
-    const float2* ml = P.ws_ml + row * NTILE;
-    uint32_t tk[(NTILE + 31) / 32];
-#pragma unroll
-    for (int i = 0; i < (NTILE + 31) / 32; ++i) {
-      const int q = lane + 32 * i;
-      tk[i] = q < NTILE ? key32(ml[q].x) : 0u;
-    }
-    uint32_t pre = 0u;
-    for (int bit = 31; bit >= 0; --bit) {
-      const uint32_t cand = pre | (1u << bit);
-      int n = 0;
-#pragma unroll
-      for (int i = 0; i < (NTILE + 31) / 32; ++i) n += tk[i] >= cand;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
-      if (n >= k) pre = cand;
-    }
-    s.stage = 0u;
-    open_window(w, (k <= NTILE && pre > KEY_BOTTOM) ? pre : KEY_BOTTOM, s.top_key);
-    if (!try_list() && k <= NTILE * TOPR) {
-      // tighter: the k-th largest kept logit, to its top 16 key bits
-      uint32_t p16 = 0u;
-      for (int bit = 15; bit >= 0; --bit) {
-        const uint32_t cand = (p16 | (1u << bit)) << 16;
-        int n = 0;
-        for (int i = lane; i < NTILE * TOPR; i += 32) n += key32(tp[i]) >= cand;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
-        if (n >= k) p16 |= 1u << bit;
-      }
-      if ((p16 << 16) > w.wlo) {
-        open_window(w, p16 << 16, s.top_key);
-        try_list();
-      }
-    }
-  } else if (finite && p_on) {
-    s.T = nucleus_bound(p, __float2ull_rn(z * FX_SCALE));
-    s.stage = 1u;
-    s.floor_key = KEY_BOTTOM;
-    uint32_t lo = KEY_BOTTOM;
-    if (1.0f - p >= 1e-4f) {
-      const float L = log2f((1.0f - p) * z / (2.0f * static_cast<float>(VREAL)));
-      const float B = M + L / c;
-      if (B > -INFINITY && B < M) lo = key32(B);
-    }
-    open_window(w, lo, s.top_key);
-    try_list();
-  }
-  if (lane == 0) {
-    if (A.out_full) A.out_full[row] = full;
-    if (!finite) {
-      A.out_restr[row] = qnan;
-      if (A.out_support) A.out_support[row] = -1;
-    } else if (!k_on && !p_on) {
-      A.out_restr[row] = full;
-      if (A.out_support) A.out_support[row] = VREAL;
-    }
-    A.listn[row] = listed;
-    A.win[row] = w;
-    A.sel[row] = s;
-    if (w.mode != WIN_IDLE) enqueue_row(A, 0, row, !(w.mode & WIN_LISTED));
-  }
-}
 
 // Inclusive prefix sums, in place, of n masses (and counts, if cc) in
 // shared memory: each thread sums a contiguous run, then a block scan.
@@ -919,6 +781,225 @@ __device__ void decide(const Items& it, LinWin& w, LinSel& s, int64_t row, const
   }
 }
 
+// Listed windows of at most WARP_LIST keys are resolved by the prep warp.
+constexpr int WARP_LIST = 512;
+
+// Bitonic sort of n <= WARP_LIST keys into descending order by one warp.
+__device__ void warp_sort_desc(uint32_t* keys, int n, int lane) {
+  int p2 = 32;
+  while (p2 < n) p2 <<= 1;
+  for (int i = n + lane; i < p2; i += 32) keys[i] = 0u;
+  __syncwarp();
+  for (int k = 2; k <= p2; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = lane; i < p2; i += 32) {
+        const int ix = i ^ j;
+        if (ix > i) {
+          const uint32_t a = keys[i], b = keys[ix];
+          if (((i & k) == 0) ? a < b : a > b) {
+            keys[i] = b;
+            keys[ix] = a;
+          }
+        }
+      }
+      __syncwarp();
+    }
+}
+
+// Inclusive prefix sums, in place, of n masses by one warp.
+__device__ void warp_prefix(unsigned long long* cm, int n, int lane) {
+  const int per = (n + 31) / 32;
+  const int i0 = min(n, lane * per), i1 = min(n, i0 + per);
+  unsigned long long sum = 0ull;
+  for (int i = i0; i < i1; ++i) sum += cm[i];
+  unsigned long long inc = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += t;
+  }
+  unsigned long long run = inc - sum;
+  for (int i = i0; i < i1; ++i) {
+    run += cm[i];
+    cm[i] = run;
+  }
+  __syncwarp();
+}
+
+// One warp per row: validate, merge the tile summaries (the full logprob,
+// bit-identical to rlk_linear_logp), finish the rows with nothing to select
+// and open the first window of the others; clear the row's round buffers.
+__global__ void __launch_bounds__(128) pair_prep_kernel(const LinArgs P, const PairArgs A) {
+  __shared__ uint32_t wkeys[4][WARP_LIST];
+  __shared__ unsigned long long wcm[4][WARP_LIST];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + warp;
+  if (row >= P.T) return;
+  const float tau = P.tau_arr ? P.tau_arr[row] : P.tau_s;
+  const int t = P.target[row];
+  const float p = A.top_p ? A.top_p[row] : A.top_p_s;
+  const int k = A.top_k ? A.top_k[row] : A.top_k_s;
+  LinWin w;
+  memset(&w, 0, sizeof(w));
+  LinSel s;
+  memset(&s, 0, sizeof(s));
+  const float qnan = __int_as_float(0x7fc00000);
+  if (!tau_ok(tau) || t < 0 || t >= VREAL || !(p > 0.0f && p <= 1.0f) || !(k == -1 || (k >= 1 && k <= VREAL))) {
+    if (lane == 0) {
+      if (A.out_full) A.out_full[row] = qnan;
+      A.out_restr[row] = qnan;
+      if (A.out_support) A.out_support[row] = -1;
+      if (A.err) atomicAdd(A.err, 1);
+      A.listn[row] = 0u;
+      A.win[row] = w;
+    }
+    return;
+  }
+  const float c = __fdiv_rn(LOG2E, tau);
+  float M, z;
+  lin_merge(P, row, lane, c, M, z);
+  const float xt = P.ws_xt[row];
+  const float d = __fdiv_rn(xt - M, tau);
+  const float full = d - logf(z);
+  const bool k_on = !(k == -1 || k >= VREAL), p_on = p < 1.0f;
+  const bool finite = M > -INFINITY && M < INFINITY && z > 0.0f && z < INFINITY;
+  w.M = M;
+  w.c = c;
+  s.kt = key32(xt);
+  s.d = d;
+  s.top_key = key32(M);
+  s.p = p_on ? p : 1.0f;
+  s.k = k_on ? k : 0;
+  const float* tp = P.ws_top + row * NTILE * TOPR;             // each tile's 8 largest, descending
+  uint32_t listed = 0u;
+  // When every tile's 8th kept logit lies below the window, the window's
+  // logits are all among the kept ones: list them (no GEMM round needed).
+  auto try_list = [&]() -> bool {
+    bool covered = true;
+#pragma unroll
+    for (int q0 = 0; q0 < NTILE; q0 += 32) {                   // independent loads, no short circuit
+      const int q = q0 + lane;
+      if (q < NTILE) covered &= key32(__ldg(tp + q * TOPR + TOPR - 1)) < w.wlo;
+    }
+    if (!__all_sync(0xffffffffu, covered)) return false;
+    // lane-strided (coalesced) pass, eight loads in flight; ballots keep the
+    // list order fixed; the first WARP_LIST keys also go to the warp's slice
+    uint32_t* dst = A.list + row * LIST_CAP;
+    uint32_t total = 0u;
+    constexpr int NV = NTILE * TOPR;
+    for (int i0 = 0; i0 < NV; i0 += 256) {
+      float v8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + 32 * u + lane;
+        v8[u] = i < NV ? __ldg(tp + i) : -INFINITY;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t K = key32(v8[u]);
+        const bool in = K >= w.wlo && i0 + 32 * u + lane < NV;
+        const unsigned m = __ballot_sync(0xffffffffu, in);
+        const uint32_t at = total + __popc(m & ((1u << lane) - 1u));
+        if (in && at < static_cast<uint32_t>(LIST_CAP)) dst[at] = K;
+        if (in && at < static_cast<uint32_t>(WARP_LIST)) wkeys[warp][at] = K;
+        total += __popc(m);
+      }
+    }
+    if (total > static_cast<uint32_t>(LIST_CAP)) return false;
+    w.mode |= WIN_LISTED;
+    listed = total;
+    return true;
+  };
+  if (finite && k_on) {
+    // first bound: the k-th largest tile maximum (k distinct real tokens reach it)
+    const float2* ml = P.ws_ml + row * NTILE;
+    uint32_t tk[(NTILE + 31) / 32];
+#pragma unroll
+    for (int i = 0; i < (NTILE + 31) / 32; ++i) {
+      const int q = lane + 32 * i;
+      tk[i] = q < NTILE ? key32(ml[q].x) : 0u;
+    }
+    uint32_t pre = 0u;
+    for (int bit = 31; bit >= 0; --bit) {
+      const uint32_t cand = pre | (1u << bit);
+      int n = 0;
+#pragma unroll
+      for (int i = 0; i < (NTILE + 31) / 32; ++i) n += tk[i] >= cand;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+      if (n >= k) pre = cand;
+    }
+    s.stage = 0u;
+    open_window(w, (k <= NTILE && pre > KEY_BOTTOM) ? pre : KEY_BOTTOM, s.top_key);
+    if (!try_list() && k <= NTILE * TOPR) {
+      // tighter: the k-th largest kept logit, to its top 16 key bits
+      uint32_t p16 = 0u;
+      for (int bit = 15; bit >= 0; --bit) {
+        const uint32_t cand = (p16 | (1u << bit)) << 16;
+        int n = 0;
+        for (int i = lane; i < NTILE * TOPR; i += 32) n += key32(tp[i]) >= cand;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+        if (n >= k) p16 |= 1u << bit;
+      }
+      if ((p16 << 16) > w.wlo) {
+        open_window(w, p16 << 16, s.top_key);
+        try_list();
+      }
+    }
+  } else if (finite && p_on) {
+    s.T = nucleus_bound(p, __float2ull_rn(z * FX_SCALE));
+    s.stage = 1u;
+    s.floor_key = KEY_BOTTOM;
+    uint32_t lo = KEY_BOTTOM;
+    if (1.0f - p >= 1e-4f) {
+      const float L = log2f((1.0f - p) * z / (2.0f * static_cast<float>(VREAL)));
+      const float B = M + L / c;
+      if (B > -INFINITY && B < M) lo = key32(B);
+    }
+    open_window(w, lo, s.top_key);
+    try_list();
+  }
+  if ((w.mode & WIN_LISTED) && listed <= static_cast<uint32_t>(WARP_LIST)) {
+    // resolve here: sort the listed keys, prefix their masses, one decision
+    const int n = static_cast<int>(listed);
+    uint32_t* kk = wkeys[warp];
+    unsigned long long* cmw = wcm[warp];
+    __syncwarp();
+    warp_sort_desc(kk, n, lane);
+    for (int i = lane; i < n; i += 32) cmw[i] = lmass(key32_value(kk[i]), w.M, w.c);
+    __syncwarp();
+    warp_prefix(cmw, n, lane);
+    if (lane == 0) {
+      decide(Items{true, n, kk, nullptr, cmw}, w, s, row, A);   // lane 0's state is kept below
+      if (w.mode != WIN_IDLE) listed = 0u;                      // a new window: GEMM rounds
+    }
+  }
+  if (lane == 0) {
+    if (A.out_full) A.out_full[row] = full;
+    if (!finite) {
+      A.out_restr[row] = qnan;
+      if (A.out_support) A.out_support[row] = -1;
+    } else if (!k_on && !p_on) {
+      A.out_restr[row] = full;
+      if (A.out_support) A.out_support[row] = VREAL;
+    }
+    A.listn[row] = (w.mode & WIN_LISTED) ? listed : 0u;
+    A.win[row] = w;
+    A.sel[row] = s;
+    if (w.mode != WIN_IDLE) enqueue_row(A, 0, row, !(w.mode & WIN_LISTED));
+  }
+  // a row going through GEMM rounds starts from clear bucket counts
+  const uint32_t mode = __shfl_sync(0xffffffffu, w.mode, 0);
+  if (mode != WIN_IDLE && !(mode & WIN_LISTED)) {
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    uint4* hc = reinterpret_cast<uint4*>(A.hcnt + row * NB);
+    for (int i = lane; i < NB / 4; i += 32) hc[i] = zero;
+    uint4* hm = reinterpret_cast<uint4*>(A.hmass + row * NB);
+    for (int i = lane; i < NB / 2; i += 32) hm[i] = zero;
+  }
+}
+
 // Rows of the round, one block at a time: resolve from the list or narrow
 // the window; clear the row's counts for the next round.
 __global__ void __launch_bounds__(RT) pair_round_kernel(const PairArgs A, int round) {
@@ -1078,6 +1159,18 @@ rlk_status lin_setup(LinLaunch& L, const void* hidden, int64_t T, int64_t H, int
                                static_cast<int>(LIN_SMEM));
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(pair_round_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ROUND_SMEM));
+    // one shared-memory carveout for every kernel of a call, so that the SMs
+    // are not reconfigured between the GEMM rounds and the small kernels
+    const void* kernels[] = {reinterpret_cast<const void*>(linear_kernel<EPI_SUMMARY>),
+                             reinterpret_cast<const void*>(linear_kernel<EPI_WINDOW>),
+                             reinterpret_cast<const void*>(linear_kernel<EPI_SUMMARY_TOP8>),
+                             reinterpret_cast<const void*>(merge_lin_kernel),
+                             reinterpret_cast<const void*>(pair_prep_kernel),
+                             reinterpret_cast<const void*>(pair_round_kernel),
+                             reinterpret_cast<const void*>(pair_final_kernel)};
+    for (const void* kf : kernels)
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kf, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     configured[dev] = true;
   }
