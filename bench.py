@@ -694,7 +694,8 @@ def run_ours(args, rank, world, local):
                    "achieved_gbs": s_bytes / (s_ms / 1e3) / 1e9,
                    "frac": s_bytes / (s_ms / 1e3) / 1e9 / peak_s,
                    "unfiltered_ms": u_ms,
-                   "unfiltered_note": "tau 1, top-p 1, top-k off on the same logits: every chunk is read twice"}
+                   "unfiltered_note": "tau 1, top-p 1, top-k off on the same logits: the pass writes float "
+                                      "masses per 32-chunk word, the draw reads one word per row"}
 
     # ---- the LM head fused with the full logprob (tensor cores): hidden
     #      [T, 4096] (the Qwen3-8B hidden size) and a random padded head

@@ -219,9 +219,13 @@ rlk_status rlk_logp_backward_saved(const rlk_logp_args* args, const rlk_row_stat
  * training side later recomputes.  The draw is inverse-CDF sampling with the
  * support in ascending column order: with U = u / 2^32 for a 32-bit random
  * word u, the token is the smallest column a in S whose cumulative
- * renormalised mass exceeds U (the masses are the exact fixed-point integers
- * of the support selection, so the draw is a function of the row and u
- * alone).  Greedy rows give the argmax (lowest column on ties).
+ * renormalised mass exceeds U.  Rows with top-k or top-p use the exact
+ * fixed-point integers of the support selection as masses; rows without
+ * either (S = every real token) use float masses exp((x - M) / tau) summed in
+ * a fixed order (per 16-byte chunk, per 32-chunk word relative to the shard
+ * maximum, then a scan over the words) with U = (u >> 8) / 2^24.  Either way
+ * the draw is a function of the row and u alone.  Greedy rows give the argmax
+ * (lowest column on ties).
  *   args: logits and per-row temperature / top_p / top_k as for
  *     rlk_logp_pair; args->target is not read (may be NULL).
  *   u per row: uniform[i] if uniform is not NULL, else word 0 of
@@ -237,18 +241,21 @@ rlk_status rlk_logp_backward_saved(const rlk_logp_args* args, const rlk_row_stat
  *   out_support: optional int32[T], as in rlk_logp_pair.
  *   workspace: device scratch of RLK_SAMPLE_WORKSPACE_BYTES(T) bytes,
  *     16-byte aligned, owned by the caller: the pair pass leaves a 16-byte
- *     record per row there for the draw, then (from byte 16 T on) one bit per
- *     16-byte chunk of the row marking the chunks that reach the row's
- *     candidate window (2432 bytes per row).  Its contents on entry do not
- *     matter; calls that share a workspace must not overlap on the GPU.
+ *     record per row there for the draw, then (from byte 16 T on, 2432 bytes
+ *     per row) for a filtered row one bit per 16-byte chunk marking the
+ *     chunks that reach the row's candidate window, for an unfiltered row
+ *     the float mass of every 32-chunk word and the shard maxima.  Its
+ *     contents on entry do not matter; calls that share a workspace must not
+ *     overlap on the GPU.
  * A row whose support reaches below the 1024-key window is resolved exactly
  * (slower path), as in rlk_logp_pair.  Two launches on `stream`: the pair
  * pass that resolves every row (greedy and NaN rows finish there), then one
- * block per drawing row, which reads the marked chunks when the row's
- * support lies inside its candidate window and every real chunk otherwise
- * (unfiltered rows, wider supports); both cases compute the same
- * fixed-point masses in the same column order, so the result does not
- * depend on which chunks are read. */
+ * block per drawing row, which reads the marked chunks when a filtered
+ * row's support lies inside its candidate window, every real chunk for a
+ * wider support, and for an unfiltered row the word masses and then the one
+ * word the draw lands in; each case computes the same masses in the same
+ * order as a read of every chunk would, so the result does not depend on
+ * which chunks are read. */
 #define RLK_SAMPLE_WORKSPACE_BYTES(T) ((size_t)(T) * (16u + 2432u))
 
 rlk_status rlk_sample(const rlk_logp_args* args, unsigned long long seed,

@@ -399,6 +399,47 @@ __device__ __forceinline__ float pass_sumexp(const uint4* sh, int tid, int nchun
   return e0 + e1;
 }
 
+// pass_sumexp for a drawing row without top-k/top-p: the same sum (same
+// operations, same order), and besides it the mass of every word of 32
+// consecutive chunks relative to the shard maximum xm: a chunk's mass is the
+// fixed tree ((e0+e1)+(e2+e3))+((e4+e5)+(e6+e7)) of its elements'
+// exponentials, a word's a fixed shuffle-down tree over its chunks, written
+// by lane 0 to dst[i * NWARP + warp] (word i * NWARP + warp covers chunks
+// 32 (i * NWARP + warp) .. + 31).
+__device__ __forceinline__ float pass_sumexp_words(const uint4* sh, int tid, int nchunks, float xm,
+                                                   float c, uint32_t* dst) {
+  const uint64_t nxm2 = pack2(-xm, -xm);
+  const uint64_t c2 = pack2(c, c);
+  uint64_t acc = pack2(0.0f, 0.0f);
+#pragma unroll
+  for (int i = 0; i < MAXCH; ++i) {
+    const int ch = tid + i * NTHR;
+    float cmass = 0.0f;
+    if (i < MAXCH - 1 || ch < nchunks) {
+      const uint4 v = sh[ch];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      float e[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint64_t a = mul2(add2(pack2(bf16_lo(w[j]), bf16_hi(w[j])), nxm2), c2);
+        float a0, a1;
+        unpack2(a, a0, a1);
+        e[2 * j] = ex2(a0);
+        e[2 * j + 1] = ex2(a1);
+        acc = add2(acc, pack2(e[2 * j], e[2 * j + 1]));
+      }
+      cmass = __fadd_rn(__fadd_rn(__fadd_rn(e[0], e[1]), __fadd_rn(e[2], e[3])),
+                        __fadd_rn(__fadd_rn(e[4], e[5]), __fadd_rn(e[6], e[7])));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cmass = __fadd_rn(cmass, __shfl_down_sync(0xffffffffu, cmass, o));
+    if ((tid & 31) == 0) dst[i * NWARP + (tid >> 5)] = __float_as_uint(cmass);
+  }
+  float e0, e1;
+  unpack2(acc, e0, e1);
+  return e0 + e1;
+}
+
 // Per warp: the maximum key and, when kw > 0, the kw-th largest lane key (the
 // pooled top-k witness), staged in red_u / red_i for a block fold.  Warp w
 // certifies kw lane maxima at or above its witness, so the W warps of a row

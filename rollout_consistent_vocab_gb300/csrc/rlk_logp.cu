@@ -139,13 +139,42 @@ enum { MODE_FWD = 0, MODE_BWD = 1, MODE_SAMPLE = 2 };
 
 // Sampler: per-row record of the resolved row, written by the leader of the
 // pair pass and read by the draw kernel (16 bytes).
-enum : uint32_t { SAMP_DRAW = 1u, SAMP_SEL = 2u, SAMP_BITS = 4u };
+enum : uint32_t { SAMP_DRAW = 1u, SAMP_SEL = 2u, SAMP_BITS = 4u, SAMP_WORDS = 8u };
 struct __align__(16) SampMsg {
   float M, Z;
   int32_t min_key;
   uint32_t flags;                  // SAMP_DRAW: the row draws (not greedy / NaN); SAMP_SEL: filtered;
-                                   // SAMP_BITS: the support lies in the chunks the bitmap marks
+                                   // SAMP_BITS: the support lies in the chunks the bitmap marks;
+                                   // SAMP_WORDS: an unfiltered row's word masses are in the workspace
 };
+
+// Unfiltered rows (every real token in the support) are drawn on float
+// masses: relative to its shard's maximum xm_q, an element's mass is
+// ex2((x - xm_q) c), a chunk's the fixed tree ((e0+e1)+(e2+e3))+((e4+e5)+
+// (e6+e7)), a word's (32 consecutive chunks) a fixed shuffle-down tree over
+// its chunks read in lane 0 (as pass_sumexp_words forms them), and each is
+// brought to the row maximum M by one product with s_q = ex2((xm_q - M) c).
+// The pair pass writes the word masses and xm_q (in the shard's 76th word,
+// past its last chunk); the draw recomputes only the chunks of the word it
+// lands in, with the same arithmetic.
+constexpr int SAMP_XM_WORD = SAMP_BITWORDS - 1;
+static_assert(SAMP_XM_WORD * 32 >= SHARD_CHUNKS, "the last word of a shard holds no chunk");
+__device__ __forceinline__ float chunk_mass_f(const uint4 v, float M, float c) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float e[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    e[2 * j] = ex2(__fmul_rn(__fsub_rn(bf16_lo(w[j]), M), c));
+    e[2 * j + 1] = ex2(__fmul_rn(__fsub_rn(bf16_hi(w[j]), M), c));
+  }
+  return __fadd_rn(__fadd_rn(__fadd_rn(e[0], e[1]), __fadd_rn(e[2], e[3])),
+                   __fadd_rn(__fadd_rn(e[4], e[5]), __fadd_rn(e[6], e[7])));
+}
+__device__ __forceinline__ float word_sum_lane0(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_down_sync(0xffffffffu, v, o));
+  return v;
+}
 
 // The 16-byte exchange message of this CTA (rank r) to CTA `to` (a local
 // store when `to` is this CTA).
@@ -244,6 +273,9 @@ logp_kernel(const KParams P) {
   const bool k_on = (k != -1) && (k < VREAL);
   const bool p_on = (p < 1.0f);
   const bool sel = RESTR && !greedy && (k_on || p_on);
+  // sampler, unfiltered drawing rows: each CTA writes the float mass of every
+  // word (32 chunks) of its shard, relative to its own maximum, and that maximum
+  const bool wmass = SAMPLE && P.samp_bits != nullptr && !greedy && !sel;
   // ---- barriers that peers signal, and the leader's histogram
   if (tid == 0) {
     mbar_init(bar_mid, 1);
@@ -328,7 +360,17 @@ logp_kernel(const KParams P) {
   // ---- 3. shard sum-exp, fixed tree (while the peers' messages travel)
   float l = 0.0f;
   const float cexp = __fdiv_rn(LOG2E, tau);
-  if (!greedy && xm_finite) l = block_sum_fixed(pass_sumexp(sh, tid, nchunks, xm, cexp), S);
+  if (wmass) {
+    uint32_t* dst = P.samp_bits + (row * NSHARD + r) * SAMP_BITWORDS;
+    if (xm_finite) {
+      l = block_sum_fixed(pass_sumexp_words(sh, tid, nchunks, xm, cexp, dst), S);
+    } else {
+      for (int i = tid; i < SAMP_XM_WORD; i += NTHR) dst[i] = 0u;    // -inf shard: no mass
+    }
+    if (tid == 0) dst[SAMP_XM_WORD] = __float_as_uint(xm);
+  } else if (!greedy && xm_finite) {
+    l = block_sum_fixed(pass_sumexp(sh, tid, nchunks, xm, cexp), S);
+  }
   if (late_mid) {
     // every thread acquires the first exchange and forms the row maximum
     if (!mbar_wait_bounded(bar_mid)) {
@@ -652,7 +694,7 @@ logp_kernel(const KParams P) {
     m.Z = Z;
     m.min_key = sel ? sr.min_key : 0;
     m.flags = (!bad && !greedy ? SAMP_DRAW : 0u) | (sel ? SAMP_SEL : 0u) |
-              (sel && !shard_reused && P.samp_bits ? SAMP_BITS : 0u);
+              (sel && !shard_reused && P.samp_bits ? SAMP_BITS : 0u) | (wmass ? SAMP_WORDS : 0u);
     P.out_samp[row] = m;
     if (P.out_support) P.out_support[row] = support;
     if (bad) {
@@ -683,6 +725,8 @@ logp_kernel(const KParams P) {
 // draw finds the word from the per-word masses kept in shared memory, and
 // warp 0 finds the chunk (one chunk per lane, a warp scan) and the column.
 struct SampRowSmem {
+  float wf[NSHARD * SAMP_BITWORDS];                  // unfiltered rows: float mass per word
+  float xm[NSHARD], sq[NSHARD];                      // unfiltered rows: shard maxima, their factors
   uint32_t bw[NSHARD * SAMP_BITWORDS];               // the chunks to read
   unsigned long long wm[NSHARD * SAMP_BITWORDS];     // support mass per bitmap word
   uint32_t scan_c[NWARP];
@@ -691,12 +735,147 @@ struct SampRowSmem {
   unsigned long long own_res;                        // the draw's offset inside that word
 };
 
+// An unfiltered row: the word holding the draw from the float word masses
+// (written by the pair pass, or computed here from every chunk), then the
+// chunk and the column inside it.  With P(w) the running sum of the scaled
+// word masses in column order (each lane of warp 0 sums a run of
+// consecutive words from the lanes' exclusive scan), Z the scan's total and
+// t = U Z for U = (u >> 8) / 2^24, the word is the first whose running sum
+// exceeds t, the chunk the first whose running sum inside the word exceeds
+// what is left of t, and likewise the column; where rounding leaves nothing
+// to exceed, the last one with a nonzero mass is taken.
+__device__ void draw_unfiltered(const KParams& P, SampRowSmem& S, int64_t row, const SampMsg& m) {
+  constexpr int NW = NSHARD * SAMP_BITWORDS;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float tau = P.tau_arr ? P.tau_arr[row] : P.tau_s;
+  const float c = __fdiv_rn(LOG2E, tau);
+  const uint4* rowp = reinterpret_cast<const uint4*>(P.logits + row * P.stride);
+  auto nch = [](int q) { return q == NSHARD - 1 ? LAST_CHUNKS : SHARD_CHUNKS; };
+  if (m.flags & SAMP_WORDS) {
+    const uint32_t* src = P.samp_bits + row * NW;
+    for (int i = tid; i < NW; i += NTHR) {
+      const bool xmw = (i % SAMP_BITWORDS) == SAMP_XM_WORD;
+      if (xmw) S.xm[i / SAMP_BITWORDS] = __uint_as_float(src[i]);
+      S.wf[i] = xmw ? 0.0f : __uint_as_float(src[i]);
+    }
+  } else {
+    // the shard maxima (as the pair pass's bf16 maximum), then the word masses
+    for (int q = warp; q < NSHARD; q += NWARP) {
+      float mx = -INFINITY;
+      for (int g = lane; g < nch(q); g += 32) {
+        const uint4 v = __ldg(rowp + q * SHARD_CHUNKS + g);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fmaxf(bf16_lo(w4[j]), bf16_hi(w4[j])));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if (lane == 0) S.xm[q] = mx;
+    }
+    __syncthreads();
+    for (int wd = warp; wd < NW; wd += NWARP) {
+      const int q = wd / SAMP_BITWORDS, g = (wd % SAMP_BITWORDS) * 32 + lane;
+      const float cm = g < nch(q) ? chunk_mass_f(__ldg(rowp + q * SHARD_CHUNKS + g), S.xm[q], c) : 0.0f;
+      const float ws = word_sum_lane0(cm);
+      if (lane == 0) S.wf[wd] = ws;
+    }
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  // each shard's factor to the row maximum, and the scaled word masses
+  const float sq = lane < NSHARD && S.xm[lane] > -INFINITY
+                       ? ex2(__fmul_rn(__fsub_rn(S.xm[lane], m.M), c)) : 0.0f;
+  if (lane < NSHARD) S.sq[lane] = sq;
+  __syncwarp();
+  constexpr int PER = (NW + 31) / 32;
+  const int w0 = min(NW, lane * PER), w1 = min(NW, w0 + PER);
+  for (int w = w0; w < w1; ++w) S.wf[w] = __fmul_rn(S.wf[w], S.sq[w / SAMP_BITWORDS]);
+  float run = 0.0f;
+  for (int w = w0; w < w1; ++w) run = __fadd_rn(run, S.wf[w]);
+  float incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl = __fadd_rn(incl, t);
+  }
+  const float Zd = __shfl_sync(0xffffffffu, incl, 31);
+  float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) excl = 0.0f;
+  const uint32_t u = P.uniform ? P.uniform[row] : philox_word0(P.seed, P.counter[row]);
+  const float tdraw = __fmul_rn(static_cast<float>(u >> 8) * 5.9604644775390625e-8f, Zd);
+  // the first word whose running sum exceeds t; else the last nonzero word
+  int wfound = -1, wlast = -1;
+  float before = 0.0f, before_last = 0.0f, acc = excl;
+  for (int w = w0; w < w1; ++w) {
+    const float ww = S.wf[w];
+    const float nxt = __fadd_rn(acc, ww);
+    if (wfound < 0 && nxt > tdraw) { wfound = w; before = acc; }
+    if (ww > 0.0f) { wlast = w; before_last = acc; }
+    acc = nxt;
+  }
+  const unsigned hit = __ballot_sync(0xffffffffu, wfound >= 0);
+  int ws;
+  float wbefore;
+  if (hit) {
+    const int src = __ffs(hit) - 1;
+    ws = __shfl_sync(0xffffffffu, wfound, src);
+    wbefore = __shfl_sync(0xffffffffu, before, src);
+  } else {
+    const unsigned has = __ballot_sync(0xffffffffu, wlast >= 0);
+    const int src = has ? 31 - __clz(has) : 0;
+    ws = __shfl_sync(0xffffffffu, wlast, src);
+    wbefore = __shfl_sync(0xffffffffu, before_last, src);
+  }
+  if (ws < 0) return;                                  // no mass at all (not a drawing row)
+  // the chunk: lane j takes chunk j of the word
+  const int q = ws / SAMP_BITWORDS, g = (ws % SAMP_BITWORDS) * 32 + lane;
+  const float xq = S.xm[q], sqq = S.sq[q];
+  const bool real = g < nch(q);
+  const uint4 v = real ? __ldg(rowp + q * SHARD_CHUNKS + g) : make_uint4(0u, 0u, 0u, 0u);
+  const float cm = real ? __fmul_rn(chunk_mass_f(v, xq, c), sqq) : 0.0f;
+  const float left = __fsub_rn(tdraw, wbefore);
+  float cin = cm;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(0xffffffffu, cin, o);
+    if (lane >= o) cin = __fadd_rn(cin, t);
+  }
+  const unsigned chit = __ballot_sync(0xffffffffu, cin > left);
+  const unsigned cnz = __ballot_sync(0xffffffffu, cm > 0.0f);
+  const int cl = chit ? __ffs(chit) - 1 : 31 - __clz(cnz);
+  if (lane != cl) return;
+  float rest = __fsub_rn(left, __fsub_rn(cin, cm));
+  const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+  int jstar = -1, jlast = -1;
+  uint32_t xb = 0, xlast = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t e16 = (w4[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
+    const float e = __fmul_rn(ex2(__fmul_rn(__fsub_rn(__uint_as_float(e16 << 16), xq), c)), sqq);
+    if (e > 0.0f) { jlast = j; xlast = e16; }
+    if (jstar < 0) {
+      if (rest < e) { jstar = j; xb = e16; } else { rest = __fsub_rn(rest, e); }
+    }
+  }
+  if (jstar < 0) { jstar = jlast; xb = xlast; }
+  const float xa = __uint_as_float(xb << 16);
+  const float d = __fdiv_rn(xa - m.M, tau);
+  const float full = d - logf(m.Z);
+  P.out_token[row] = q * SW + g * 8 + jstar;
+  if (P.out_full) P.out_full[row] = full;
+  if (P.out_restr) P.out_restr[row] = full;
+}
+
 __global__ void __launch_bounds__(NTHR) sample_row_kernel(const KParams P) {
   __shared__ SampRowSmem S;
   constexpr int NW = NSHARD * SAMP_BITWORDS;
   const int64_t row = blockIdx.x;
   const SampMsg m = P.in_samp[row];
   if (!(m.flags & SAMP_DRAW)) return;                 // uniform over the block
+  if (!(m.flags & SAMP_SEL)) {
+    draw_unfiltered(P, S, row, m);
+    return;
+  }
   const int tid = threadIdx.x, lane = tid & 31;
   if (m.flags & SAMP_BITS) {
     const uint32_t* src_bits = P.samp_bits + row * NW;

@@ -1,11 +1,12 @@
 """GPU: the sampler against the oracle's inverse-CDF draw.
 
-The GPU draws on exact fixed-point masses (2^-44 units of exp((x - M)/tau),
-float32 exponent arguments and ex2.approx), the oracle on fp64 masses, so the
-two can pick neighbouring tokens only when the draw U lies within 2e-6 of an
-edge of the oracle's CDF; such rows are counted, everything else must match
-exactly.  The sampled token's logprobs equal rlk_logp_pair's for that target
-bit for bit.
+The GPU draws filtered rows on exact fixed-point masses (2^-44 units of
+exp((x - M)/tau), float32 exponent arguments and ex2.approx) and unfiltered
+rows on float masses summed in a fixed order (chunks, 32-chunk words, a scan
+over the words); the oracle draws on fp64 masses, so the two can pick
+neighbouring tokens only when the draw U lies within 2e-6 of an edge of the
+oracle's CDF; such rows are counted, everything else must match exactly.  The
+sampled token's logprobs equal rlk_logp_pair's for that target bit for bit.
 """
 
 import math
@@ -147,6 +148,40 @@ def test_stratified_frequencies():
     _, restr, S = oracle.row_logprobs_all(bits_of(x)[0], 1.0, 0.95, 64)
     assert counts[~S].sum() == 0
     assert np.all(np.abs(counts[S] - n * np.exp(restr[S])) <= 2.0)
+
+
+def test_stratified_frequencies_unfiltered():
+    """The same on an unfiltered row (top-p 1, top-k off: every real token in
+    the support, drawn from the pair pass's word masses): each token drawn
+    2048 q_j times, up to two."""
+    x, _, _ = W.hot_logits(1, 40, 40, seed=46, device=DEV)
+    n = 2048
+    xs = x.expand(n, VP).contiguous()
+    u = ((np.arange(n) + 0.5) * 2 ** 32 / n).astype(np.uint64).astype(np.uint32)
+    tok, restr, full, sup = pkg.sample(xs, 1.0, 1.0, -1, uniform=_u32_tensor(u))
+    torch.cuda.synchronize()
+    assert (sup == VR).all() and torch.equal(restr.view(torch.int32), full.view(torch.int32))
+    counts = np.bincount(tok.cpu().numpy(), minlength=VR)
+    full_all, _, _ = oracle.row_logprobs_all(bits_of(x)[0], 1.0, 1.0, -1)
+    assert counts.sum() == n
+    assert np.all(np.abs(counts - n * np.exp(full_all)) <= 2.0)
+
+
+def test_unfiltered_rows_match_the_oracle():
+    """Unfiltered rows at several temperatures, drawn from the word masses:
+    tokens against the oracle (edge rows counted), logprobs bit for bit."""
+    x, _, _ = W.hot_logits(64, 1, 300, seed=47, device=DEV)
+    rng = np.random.default_rng(47)
+    tau = rng.choice([0.5, 0.7, 1.0, 1.3, 2.0], 64).astype(np.float32)
+    p = np.ones(64, np.float32)
+    k = np.full(64, -1, np.int32)
+    u = rng.integers(0, 2 ** 32, 64, dtype=np.uint64).astype(np.uint32)
+    tok, restr, full, sup = pkg.sample(x, _t(tau, torch.float32), 1.0, -1, uniform=_u32_tensor(u))
+    torch.cuda.synchronize()
+    near = check_draws(bits_of(x), tau, p, k, u, tok.cpu().numpy(), restr.cpu().numpy(),
+                       full.cpu().numpy(), sup.cpu().numpy())
+    print("unfiltered rows near a CDF edge:", near)
+    assert near <= 1
 
 
 def test_full_size_draws_are_in_support():
