@@ -316,22 +316,24 @@ def test_linear_pair_rejected_and_nonfinite_rows():
 
 
 def test_linear_pair_full_size_sampled_rows():
-    """T = 8192, H = 4096 with the policy-step parameters (tau 1.3, top-p 0.99,
-    top-k 128), the bench's case: every output finite, sampled rows against
-    the oracle."""
+    """T = 8192, H = 4096 (the bench's case): the policy-step parameters (tau
+    1.3, top-p 0.99, top-k 128; rows listed from the kept logits) and top-p
+    alone at tau 1.0, p 0.95 (GEMM window rounds); every output finite, sampled
+    rows against the oracle."""
     T, H = 8192, 4096
     h, w = _case(T, H, 14)
     g = torch.Generator(device=DEV).manual_seed(15)
     tg = torch.randint(0, VR, (T,), generator=g, device=DEV, dtype=torch.int32)
-    err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    full, restr, sup = pkg.linear_logp_pair(h, w, tg, 1.3, 0.99, 128, err_count=err)
-    torch.cuda.synchronize()
-    assert err.item() == 0 and torch.isfinite(full).all() and (sup >= 1).all()
     rows = np.array([0, 1, 127, 128, 4095, 4096, 8190, 8191])
     ri = torch.as_tensor(rows, device=DEV)
     hb, wb = _bits(h[ri]), _bits(w)
     x, S = _exact_logits(hb, wb)
-    check_pair("linear_pair_full_size_sampled", hb, wb, x, S, H, 1.3, 0.99, 128, tg.cpu().numpy()[rows],
-               full.cpu().numpy()[rows], restr.cpu().numpy()[rows], sup.cpu().numpy()[rows])
+    for name, (tau, p, k) in (("policy_step", (1.3, 0.99, 128)), ("top_p_only", (1.0, 0.95, -1))):
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        full, restr, sup = pkg.linear_logp_pair(h, w, tg, tau, p, k, err_count=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0 and torch.isfinite(full).all() and (sup >= 1).all(), name
+        check_pair("linear_pair_full_size_" + name, hb, wb, x, S, H, tau, p, k, tg.cpu().numpy()[rows],
+                   full.cpu().numpy()[rows], restr.cpu().numpy()[rows], sup.cpu().numpy()[rows])
     del h, w
     torch.cuda.empty_cache()
