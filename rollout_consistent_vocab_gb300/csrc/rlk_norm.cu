@@ -20,6 +20,10 @@
 // the entries depends on the order.  A block's bins live in shared memory and
 // reach the caller's bins with one global atomic add per nonzero entry.
 //
+// BF16 and FP16 inputs take a shorter route (sqnorm16_kernel): a block counts
+// the 32768 possible magnitudes and converts the counts into bin
+// contributions at the end.
+//
 // The finalize kernel forms the exact sum as a multi-word integer, rounds it
 // once to float64 (nearest even) and takes the correctly rounded square root.
 
@@ -262,6 +266,89 @@ __global__ void __launch_bounds__(NORM_THREADS, NORM_MIN_BLOCKS) sqnorm_kernel(c
   }
 }
 
+// ---------------------------------------------------------------- 16-bit types
+//
+// A BF16 or FP16 square depends only on the element's 15 magnitude bits, so
+// a block counts each of the 32768 magnitudes in shared memory (one add per
+// element; zeros add nothing) and at the end adds, for every magnitude
+// present, count x its FP32 square's significand to the square's bin (NaN
+// and infinite squares to their counters): the same exact sum, with no
+// per-element arithmetic beyond the add.
+
+constexpr int H16_THREADS = 1024;
+constexpr int NPAT = 32768;
+constexpr uint32_t H16_SMEM = NPAT * 4u;
+
+template <int DT>
+__global__ void __launch_bounds__(H16_THREADS, 1) sqnorm16_kernel(const char* x, int64_t head,
+                                                                  int64_t nvec, int64_t n,
+                                                                  unsigned long long* bins) {
+  extern __shared__ __align__(16) uint32_t cnt[];   // [NPAT] counts per magnitude
+  __shared__ unsigned long long sb[NB];
+  const int tid = threadIdx.x;
+  for (int i = tid; i < NPAT / 4; i += H16_THREADS) reinterpret_cast<uint4*>(cnt)[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = tid; i < NB; i += H16_THREADS) sb[i] = 0ull;
+  __syncthreads();
+  auto add2 = [&](uint32_t w) {                      // the two elements of a 32-bit word
+    const uint32_t lo = w & 0x7FFFu, hi = (w >> 16) & 0x7FFFu;
+    if (lo) atomicAdd(&cnt[lo], 1u);
+    if (hi) atomicAdd(&cnt[hi], 1u);
+  };
+  const uint4* vx = reinterpret_cast<const uint4*>(x + head * 2);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * H16_THREADS;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * H16_THREADS + tid;
+  for (; i + 3 * stride < nvec; i += 4 * stride) {  // four vectors in flight
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldg(vx + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      add2(v[u].x);
+      add2(v[u].y);
+      add2(v[u].z);
+      add2(v[u].w);
+    }
+  }
+  for (; i < nvec; i += stride) {
+    const uint4 v = __ldg(vx + i);
+    add2(v.x);
+    add2(v.y);
+    add2(v.z);
+    add2(v.w);
+  }
+  if (blockIdx.x == 0) {
+    const int64_t tail0 = head + nvec * 8;
+    const int64_t nrest = head + (n - tail0);
+    for (int64_t j = tid; j < nrest; j += H16_THREADS) {
+      const uint32_t m = load_elem<DT>(x, j < head ? j : tail0 + (j - head)) & 0x7FFFu;
+      if (m) atomicAdd(&cnt[m], 1u);
+    }
+  }
+  __syncthreads();
+  unsigned long long nan_c = 0ull, inf_c = 0ull;
+  for (int m = tid; m < NPAT; m += H16_THREADS) {
+    const uint32_t c = cnt[m];
+    if (!c) continue;
+    const uint32_t u = square_bits<DT>(static_cast<uint32_t>(m));
+    const int E = static_cast<int>((u >> 23) & 0xFFu);
+    const uint32_t f = u & 0x7FFFFFu;
+    if (E == 0xFF) {
+      if (f) nan_c += c;
+      else inf_c += c;
+      continue;
+    }
+    const uint32_t M = E ? (f | 0x800000u) : f;    // a subnormal square: unit 2^-149, as E = 1
+    if (M) atomicAdd(&sb[max(E, 1)], static_cast<unsigned long long>(c) * M);
+  }
+  if (nan_c) atomicAdd(&sb[NAN_BIN], nan_c);
+  if (inf_c) atomicAdd(&sb[INF_BIN], inf_c);
+  __syncthreads();
+  for (int e = tid; e < NB; e += H16_THREADS) {
+    const unsigned long long v = sb[e];
+    if (v) atomicAdd(&bins[e], v);
+  }
+}
+
 // ---------------------------------------------------------------- finalize
 
 constexpr int ND = 16;             // 32-bit digits: 512 bits > 381 + 64
@@ -385,9 +472,29 @@ extern "C" rlk_status rlk_sqnorm_accumulate(const void* x, int64_t n, int32_t dt
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const char* xc = static_cast<const char*>(x);
   unsigned long long* b = reinterpret_cast<unsigned long long*>(bins);
-  if (dtype == RLK_DT_F32) sqnorm_kernel<RLK_DT_F32><<<grid, NORM_THREADS, 0, st>>>(xc, head, nvec, n, b);
-  else if (dtype == RLK_DT_BF16) sqnorm_kernel<RLK_DT_BF16><<<grid, NORM_THREADS, 0, st>>>(xc, head, nvec, n, b);
-  else sqnorm_kernel<RLK_DT_F16><<<grid, NORM_THREADS, 0, st>>>(xc, head, nvec, n, b);
+  if (dtype == RLK_DT_F32) {
+    sqnorm_kernel<RLK_DT_F32><<<grid, NORM_THREADS, 0, st>>>(xc, head, nvec, n, b);
+  } else {
+    // one block per SM (128 KB of counts each), fewer for small inputs
+    static bool configured[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    if (!configured[dev & 63]) {
+      cudaError_t e = cudaFuncSetAttribute(sqnorm16_kernel<RLK_DT_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(H16_SMEM));
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(sqnorm16_kernel<RLK_DT_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(H16_SMEM));
+      if (e != cudaSuccess) return fail(RLK_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+      configured[dev & 63] = true;
+    }
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t want = (nvec + H16_THREADS * 16 - 1) / (H16_THREADS * 16);
+    const unsigned g16 = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(want, std::max(1, sms))));
+    if (dtype == RLK_DT_BF16) sqnorm16_kernel<RLK_DT_BF16><<<g16, H16_THREADS, H16_SMEM, st>>>(xc, head, nvec, n, b);
+    else sqnorm16_kernel<RLK_DT_F16><<<g16, H16_THREADS, H16_SMEM, st>>>(xc, head, nvec, n, b);
+  }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(RLK_ECUDA, "kernel launch: %s", cudaGetErrorString(e));
   return RLK_OK;
