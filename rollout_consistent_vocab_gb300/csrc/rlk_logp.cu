@@ -469,9 +469,33 @@ logp_kernel(const KParams P) {
       }
       // warps with many candidate chunks count locally and push per key;
       // the others send one add per element
-      const bool busy = (r != 0) && __reduce_add_sync(0xffffffffu, __popc(hitmask)) > BUSY_HITS;
+      const int warp_hits = __reduce_add_sync(0xffffffffu, __popc(hitmask));
+      const bool busy = (r != 0) && warp_hits > BUSY_HITS;
       // with a positive window every candidate is positive: its key is b | 0x8000
       const bool pos_window = vlo_f > 0.0f;
+      if ((r == 0 || busy) && warp_hits > DENSE_HITS) {
+        // a dense window (most elements candidates): every element of a hit
+        // chunk at fixed positions, the adds predicated, instead of a
+        // per-candidate search whose lanes diverge
+        while (hitmask) {
+          const int i = __ffs(hitmask) - 1;
+          hitmask &= hitmask - 1;
+          const uint4 v = sh[tid + i * NTHR];
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t m2 = __hge2_mask(as_bf2(w[j]), vlo2);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (!((m2 >> (16 * h)) & 1u)) continue;
+              const uint32_t b = h ? (w[j] >> 16) : (w[j] & 0xFFFFu);
+              const int idx = hi - (pos_window ? static_cast<int>(b | 0x8000u) : okey(b));
+              if (r == 0) red_shared_add(&S.merged[idx], 1u);
+              else red_shared_add(&S.hist[idx >> 1], 1u << ((idx & 1) * 16));
+            }
+          }
+        }
+      }
       while (hitmask) {
         const int i = __ffs(hitmask) - 1;
         hitmask &= hitmask - 1;
