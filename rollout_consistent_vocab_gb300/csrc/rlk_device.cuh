@@ -43,7 +43,7 @@ constexpr int SAMP_BITWORDS = MAXCH * NWARP;
 constexpr int WIN = 1024;            // candidate window, in bf16 order keys (8 binades)
 constexpr int TMA_PIECES = 4;
 constexpr int BUSY_HITS = 16;        // candidate chunks per warp above which it counts locally
-constexpr int DENSE_HITS = 256;      // ... and above which it counts every element of a hit chunk
+constexpr int DENSE_HITS = 128;      // ... and above which it counts every element of a hit chunk
 constexpr float LOG2E = 1.4426950408889634f;   // log2(e)
 constexpr float FX_SCALE = 17592186044416.0f;  // 2^44: fixed-point scale of masses
 constexpr unsigned long long TIMEOUT_NS = 200000000ull;   // 0.2 s bound on every wait
@@ -95,6 +95,12 @@ __device__ __forceinline__ void red_async_add_u64(uint32_t addr, unsigned long l
 // shared-memory add without a return value (nothing waits for it)
 __device__ __forceinline__ void red_shared_add(uint32_t* p, uint32_t v) {
   asm volatile("red.shared.add.u32 [%0], %1;" :: "r"(smem_addr(p)), "r"(v) : "memory");
+}
+// the same add, issued only where pred != 0 (a predicated instruction, no branch);
+// addr need not be valid where pred == 0
+__device__ __forceinline__ void red_shared_add_if(uint32_t addr, uint32_t v, uint32_t pred) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q red.shared.add.u32 [%0], %1;\n\t}"
+               :: "r"(addr), "r"(v), "r"(pred) : "memory");
 }
 __device__ __forceinline__ unsigned long long global_timer() {
   unsigned long long t;
@@ -150,8 +156,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar) {
 // own bounded waits before the stage's receivers stop draining:
 //   DRAIN_MID:  exchange messages, sent once the sender's shard copy landed
 //               (at most 2 TIMEOUT_NS after its start);
-//   DRAIN_MID2: top-p-only rows' second exchange (sum-exp and level codes),
-//               sent after the sender's first exchange wait (at most DRAIN_MID);
+//   DRAIN_MID2: top-p-only rows' second exchange (the shard's sum-exp),
+//               sent after the sender's sum-exp pass (its shard copy landed
+//               at most 2 TIMEOUT_NS after its start);
 //   DRAIN_SUM:  summaries and histogram adds, sent after the sender's
 //               exchange waits (at most DRAIN_MID2);
 //   DRAIN_LEAD: the backward's row record, sent after the leader's summary
@@ -451,131 +458,6 @@ __device__ __forceinline__ void stage_max_bound(int tkey, int kw, SM& S) {
   const int lw = kw > 0 ? warp_kth_largest(tkey, kw) : 0;
   const unsigned wmax = __reduce_max_sync(0xffffffffu, static_cast<unsigned>(tkey));
   if (lane == 0) { S.red_u[warp] = wmax; S.red_i[warp] = lw; }
-}
-
-// ------------------------------------------------------------ nucleus levels
-//
-// Top-p-only rows: the window's a-priori bottom (candidate_window) assumes the
-// worst case, all V tokens at the bottom, and can admit far more candidates
-// than the nucleus holds.  Once the row maximum M is known, a shard with many
-// chunks inside that depth therefore also reports, for NLEV levels lambda_j
-// = M - (0.2 + 0.1 j) tau ln(V / (1 - p)), a lower bound on its mass at or
-// above lambda_j: the mass of its chunk-maximum pairs (the largest even and
-// the largest odd column of every 16-byte chunk, two distinct real tokens)
-// that reach lambda_j.  If the shards' certified masses at lambda_j add up
-// to p Z (with a margin over the float error), the mass strictly above any
-// token below lambda_j is at least p Z, so no such token is in the nucleus
-// and the window can start at lambda_j.  The levels are the same for every
-// shard; a shard with few chunks inside the depth reports zero (a valid
-// lower bound), its candidates being cheap to count anyway.  Above
-// LEV_MAX_P the nucleus holds so much of the mass that the chunk-maximum
-// pairs (a quarter of the tokens) almost never certify it, and levels are
-// not computed.
-constexpr int NLEV = 6;
-constexpr float LEV_MAX_P = 0.975f;
-constexpr int LEV_GATE_CHUNKS = 6;   // a thread's chunks inside the depth ...
-constexpr int LEV_GATE_THREADS = 64; // ... in this many threads of a shard: levels pay
-
-// tau ln(V / (1 - p)): the a-priori depth of the nucleus below the maximum, in logit units
-__device__ __forceinline__ float nucleus_depth(float tau, float p) {
-  return __fmul_rn(tau, logf(__fdiv_rn(static_cast<float>(VREAL), __fsub_rn(1.0f, p))));
-}
-// level j: (0.2 + 0.1 j) of the a-priori depth below the row maximum M
-__device__ __forceinline__ float level_value(float M, float depth, int j) {
-  const float f = __fadd_rn(0.2f, __fmul_rn(0.1f, static_cast<float>(j)));
-  return __fsub_rn(M, __fmul_rn(depth, f));
-}
-
-// Chunks among this thread's register chunk maxima reaching v2 = (v, v).
-__device__ __forceinline__ int count_chunks_reaching(const __nv_bfloat162 (&cm)[MAXCH], int tid,
-                                                     int nchunks, __nv_bfloat162 v2) {
-  int n = 0;
-#pragma unroll
-  for (int i = 0; i < MAXCH; ++i)
-    n += ((i < MAXCH - 1 || tid + i * NTHR < nchunks) && __hge2_mask(cm[i], v2) != 0u) ? 1 : 0;
-  return n;
-}
-
-// Packed maximum of a 16-byte chunk: (largest even column, largest odd column).
-__device__ __forceinline__ __nv_bfloat162 chunk_max2(uint4 v) {
-  return __hmax2(__hmax2(as_bf2(v.x), as_bf2(v.y)), __hmax2(as_bf2(v.z), as_bf2(v.w)));
-}
-
-// The shard's level masses as six 8-bit codes, byte j = floor(255 m_j / T),
-// m_j = sum of exp(s_v - s_M) over the chunk-maximum pair elements v at or
-// above level j, and T (>= every m_j) the shard's whole mass relative to
-// exp(s_M); a code decodes to a lower bound of m_j.  Called by every thread
-// of the block (it reduces in a fixed tree through red_lev); kept out of
-// line, so that its registers do not weigh on the rest of the kernel.  The
-// pair elements come from the shard in shared memory; chunks below the
-// deepest level are skipped.
-template <class SM>
-__device__ __noinline__ unsigned long long shard_level_codes(const uint4* sh, int tid, int nchunks,
-                                                             float M, float c, float depth, float T,
-                                                             SM& S) {
-  float lam[NLEV], acc[NLEV];
-#pragma unroll
-  for (int j = 0; j < NLEV; ++j) {
-    lam[j] = level_value(M, depth, j);
-    acc[j] = 0.0f;
-  }
-  const float deep = key_value(okey_floor(lam[NLEV - 1]));   // a bf16 value <= the deepest level
-  const __nv_bfloat162 deep2 = __floats2bfloat162_rn(deep, deep);
-  for (int ch = tid; ch < nchunks; ch += NTHR) {              // chunk order, per thread
-    const __nv_bfloat162 cmx = chunk_max2(sh[ch]);
-    if (__hge2_mask(cmx, deep2) == 0u) continue;
-    const float v0 = __low2float(cmx), v1 = __high2float(cmx);
-    const float e0 = ex2(__fmul_rn(__fsub_rn(v0, M), c));
-    const float e1 = ex2(__fmul_rn(__fsub_rn(v1, M), c));
-#pragma unroll
-    for (int j = 0; j < NLEV; ++j) {
-      if (v0 >= lam[j]) acc[j] += e0;
-      if (v1 >= lam[j]) acc[j] += e1;
-    }
-  }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int j = 0; j < NLEV; ++j) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc[j] = acc[j] + __shfl_xor_sync(0xffffffffu, acc[j], o);
-    if (lane == 0) S.red_lev[warp][j] = acc[j];
-  }
-  __syncthreads();
-  unsigned long long codes = 0;
-#pragma unroll
-  for (int j = 0; j < NLEV; ++j) {
-    float m = S.red_lev[0][j];
-#pragma unroll
-    for (int w = 1; w < NWARP; ++w) m = m + S.red_lev[w][j];
-    const float q = floorf(__fmul_rn(__fdiv_rn(m, T), 255.0f));
-    const uint32_t code = (q >= 1.0f) ? static_cast<uint32_t>(fminf(q, 255.0f)) : 0u;   // NaN: 0
-    codes |= static_cast<unsigned long long>(code) << (8 * j);
-  }
-  __syncthreads();
-  return codes;
-}
-
-// A shard's whole mass relative to exp(s_M): l exp(s_xm - s_M).
-__device__ __forceinline__ float shard_mass(float l, float xm, float M, float c) {
-  return __fmul_rn(l, ex2(__fmul_rn(__fsub_rn(xm, M), c)));
-}
-
-// Order key of the highest level whose decoded, certified mass reaches p Z
-// (0 if none); codes_q / T_q: each shard's level codes and whole mass
-// relative to exp(s_M), in shard order.  One thread.
-__device__ __forceinline__ int certified_bottom(const unsigned long long (&codes_q)[NSHARD],
-                                                const float (&T_q)[NSHARD], float M, float Z,
-                                                float tau, float p) {
-  const float need = p * Z * 1.002f;   // the margin covers the float error of both sides (~1e-6)
-#pragma unroll
-  for (int j = 0; j < NLEV; ++j) {
-    float cert = 0.0f;
-#pragma unroll
-    for (int q = 0; q < NSHARD; ++q)
-      cert = fmaf(static_cast<float>((codes_q[q] >> (8 * j)) & 0xFFu) * (1.0f / 255.0f), T_q[q], cert);
-    if (cert >= need) return okey_floor(level_value(M, nucleus_depth(tau, p), j));
-  }
-  return 0;
 }
 
 // The candidate window [wlo, whi] of order keys of a restricted row, from the

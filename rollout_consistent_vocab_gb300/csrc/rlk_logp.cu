@@ -19,8 +19,8 @@
 //      witness (and, for top-p-only rows, its sum-exp) over DSMEM, derives
 //      the same candidate window of at most 1024 bf16 order keys below the
 //      row maximum, and counts its elements in the window into the leader's
-//      per-key histogram (remote shared-memory adds, or a local u16
-//      histogram pushed once by warps with many candidates);
+//      per-key histogram (remote shared-memory adds, or counts in the CTA's
+//      own array pushed once by warps with many candidates);
 //   5. the CTA stores its summary (m_r, l_r, aux, flags) into the leader
 //      CTA's shared memory.
 //
@@ -59,7 +59,7 @@ struct __align__(16) MidSlot {
 // Top-p-only rows' second exchange, once the row maximum is known.
 struct __align__(16) Mid2Slot {
   float l;         // the shard's sum-exp
-  uint32_t codes_lo, codes_hi;   // level codes 0..3 and 4..5 (0: none)
+  uint32_t unused0, unused1;
   uint32_t flags;
 };
 
@@ -73,15 +73,14 @@ struct __align__(16) Summary {
 
 struct __align__(128) Smem {
   uint4 shard[SHARD_CHUNKS];       // 38144 B; the leader reuses it as scratch at the end
-  uint32_t merged[WIN];            // leader: per-key candidate counts of the whole row
-  uint32_t hist[WIN / 2];          // busy warps' per-key counts (u16 pairs), pushed once
+  uint32_t merged[WIN];            // leader: per-key candidate counts of the whole row;
+                                   // peer: its busy warps' per-key counts, pushed once
   MidSlot mid[NSHARD];
   Mid2Slot mid2[NSHARD];
   Summary slot[NSHARD];
   uint32_t red_u[NWARP];
   int32_t red_i[NWARP];
   float red_f[NWARP];
-  float red_lev[NWARP][NLEV];
   uint32_t scan_c[NWARP];
   unsigned long long scan_m[NWARP];
   int32_t found_i;
@@ -292,12 +291,8 @@ logp_kernel(const KParams P) {
     }
     S.npush = 0u;
   }
-  if (sel) {
-    if (r == 0)
-      for (int i = tid; i < WIN; i += NTHR) S.merged[i] = 0u;
-    else
-      for (int i = tid; i < WIN / 2; i += NTHR) S.hist[i] = 0u;
-  }
+  if (sel)
+    for (int i = tid; i < WIN; i += NTHR) S.merged[i] = 0u;
   __syncthreads();
   // S0: barriers initialised and the leader's histogram zeroed.  One thread
   // publishes all of it to the cluster (the block barrier above orders the
@@ -353,7 +348,7 @@ logp_kernel(const KParams P) {
   cluster_wait();              // S0 complete: peers' barriers and histogram are ready
   // Restricted rows send their maximum and bound now and overlap the
   // exchange with the sum-exp pass; top-p-only rows then exchange their
-  // sum-exp (which sets the candidate window) and level codes in a second round.
+  // sum-exp (which sets the candidate window) in a second round.
   const bool late_mid = sel && !k_on;
   if (sel && tid < NSHARD) send_mid(S, r, tid, xm, lkey, flags, 0.0f, bar_mid);
 
@@ -371,32 +366,13 @@ logp_kernel(const KParams P) {
   } else if (!greedy && xm_finite) {
     l = block_sum_fixed(pass_sumexp(sh, tid, nchunks, xm, cexp), S);
   }
-  if (late_mid) {
-    // every thread acquires the first exchange and forms the row maximum
-    if (!mbar_wait_bounded(bar_mid)) {
-      flags |= FLAG_TIMEOUT;
-      if (tid == 0) mbar_wait_until(bar_mid, t_start + DRAIN_MID);   // stay resident for late messages
-    }
-    float Mr = -INFINITY;
-#pragma unroll
-    for (int q = 0; q < NSHARD; ++q) Mr = fmaxf(Mr, S.mid[q].xm);
-    unsigned long long codes = 0;
-    if (xm_finite && Mr < INFINITY && p <= LEV_MAX_P) {
-      // many chunks inside the nucleus's a-priori depth below M: level codes pay
-      const float depth = nucleus_depth(tau, p);
-      const float lb = key_value(okey_floor(__fsub_rn(Mr, depth)));   // a bf16 value <= M - depth
-      const int inside = count_chunks_reaching(cm, tid, nchunks, __floats2bfloat162_rn(lb, lb));
-      if (__syncthreads_count(inside >= LEV_GATE_CHUNKS) >= LEV_GATE_THREADS)
-        codes = shard_level_codes(sh, tid, nchunks, Mr, cexp, depth, shard_mass(l, xm, Mr, cexp), S);
-    }
-    if (tid < NSHARD) {
-      const uint4 msg = make_uint4(__float_as_uint(l), static_cast<uint32_t>(codes),
-                                   static_cast<uint32_t>(codes >> 32), flags);
-      if (tid == static_cast<int>(r))
-        *reinterpret_cast<uint4*>(&S.mid2[r]) = msg;
-      else
-        st_async_v4(map_rank(smem_addr(&S.mid2[r]), tid), msg, map_rank(bar_mid2, tid));
-    }
+  if (late_mid && tid < NSHARD) {
+    // the shard's sum-exp to every CTA: the window needs the row's total mass
+    const uint4 msg = make_uint4(__float_as_uint(l), 0u, 0u, flags);
+    if (tid == static_cast<int>(r))
+      *reinterpret_cast<uint4*>(&S.mid2[r]) = msg;
+    else
+      st_async_v4(map_rank(smem_addr(&S.mid2[r]), tid), msg, map_rank(bar_mid2, tid));
   }
 
   // ---- 4. candidate pass: every element of the window is counted straight
@@ -405,6 +381,11 @@ logp_kernel(const KParams P) {
   if (sel) {
     if (tid == 0) {
       // the window of candidate keys, the same in every CTA of the cluster
+      // (top-p-only rows: both exchanges in)
+      if (late_mid && !mbar_wait_bounded(bar_mid)) {
+        flags |= FLAG_TIMEOUT;
+        mbar_wait_until(bar_mid, t_start + DRAIN_MID);   // resident for late messages
+      }
       const uint32_t bar_w = late_mid ? bar_mid2 : bar_mid;
       if (!mbar_wait_bounded(bar_w)) {
         flags |= FLAG_TIMEOUT;
@@ -419,20 +400,14 @@ logp_kernel(const KParams P) {
       }
       int whi, wlo;
       if (!k_on) {
-        // total mass from the second exchange, then the certified level, if any
-        float Z = 0.0f, T_q[NSHARD];
-        unsigned long long codes_q[NSHARD];
-        bool levels = false;
+        // total mass from the second exchange
+        float Z = 0.0f;
 #pragma unroll
         for (int q = 0; q < NSHARD; ++q) {
           const float xq = S.mid[q].xm;
-          T_q[q] = xq > -INFINITY ? shard_mass(S.mid2[q].l, xq, M, cexp) : 0.0f;
           if (xq > -INFINITY) Z = fmaf(S.mid2[q].l, ex2((xq - M) * cexp), Z);
-          codes_q[q] = S.mid2[q].codes_lo | (static_cast<unsigned long long>(S.mid2[q].codes_hi) << 32);
-          levels |= codes_q[q] != 0ull;
         }
         candidate_window(M, L, Z, tau, p, false, whi, wlo);
-        if (levels && wlo <= whi) wlo = max(wlo, min(certified_bottom(codes_q, T_q, M, Z, tau, p), whi));
       } else {
         candidate_window(M, L, 0.0f, tau, p, true, whi, wlo);
       }
@@ -475,8 +450,10 @@ logp_kernel(const KParams P) {
       const bool pos_window = vlo_f > 0.0f;
       if ((r == 0 || busy) && warp_hits > DENSE_HITS) {
         // a dense window (most elements candidates): every element of a hit
-        // chunk at fixed positions, the adds predicated, instead of a
+        // chunk at fixed positions, each add a predicated instruction (the
+        // address of a non-candidate is never used), instead of a
         // per-candidate search whose lanes diverge
+        const uint32_t mbase = smem_addr(S.merged);
         while (hitmask) {
           const int i = __ffs(hitmask) - 1;
           hitmask &= hitmask - 1;
@@ -485,14 +462,11 @@ logp_kernel(const KParams P) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint32_t m2 = __hge2_mask(as_bf2(w[j]), vlo2);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              if (!((m2 >> (16 * h)) & 1u)) continue;
-              const uint32_t b = h ? (w[j] >> 16) : (w[j] & 0xFFFFu);
-              const int idx = hi - (pos_window ? static_cast<int>(b | 0x8000u) : okey(b));
-              if (r == 0) red_shared_add(&S.merged[idx], 1u);
-              else red_shared_add(&S.hist[idx >> 1], 1u << ((idx & 1) * 16));
-            }
+            const uint32_t b0 = w[j] & 0xFFFFu, b1 = w[j] >> 16;
+            const int i0 = hi - (pos_window ? static_cast<int>(b0 | 0x8000u) : okey(b0));
+            const int i1 = hi - (pos_window ? static_cast<int>(b1 | 0x8000u) : okey(b1));
+            red_shared_add_if(mbase + 4u * static_cast<uint32_t>(i0), 1u, m2 & 1u);
+            red_shared_add_if(mbase + 4u * static_cast<uint32_t>(i1), 1u, m2 & 0x10000u);
           }
         }
       }
@@ -511,10 +485,8 @@ logp_kernel(const KParams P) {
           const uint32_t wj = (j == 0) ? w[0] : (j == 1) ? w[1] : (j == 2) ? w[2] : w[3];
           const uint32_t b = (pos & 16) ? (wj >> 16) : (wj & 0xFFFFu);
           const int idx = hi - (pos_window ? static_cast<int>(b | 0x8000u) : okey(b));
-          if (r == 0) {
+          if (r == 0 || busy) {
             red_shared_add(&S.merged[idx], 1u);
-          } else if (busy) {
-            red_shared_add(&S.hist[idx >> 1], 1u << ((idx & 1) * 16));
           } else {
             red_async_add(dst + 4u * static_cast<uint32_t>(idx), 1u, rbar);
             ++sent;
@@ -522,14 +494,13 @@ logp_kernel(const KParams P) {
         }
       }
       if (__syncthreads_or(busy)) {
-        // push the busy warps' counts, one add per nonzero key
-        const int nwords = (hi - lo + 2) >> 1;
-        for (int iw = tid; iw < nwords; iw += NTHR) {
-          const uint32_t hw = S.hist[iw];
-          if (hw) {
-            // both keys of the word in one 8-byte add (neither 32-bit count can carry)
-            red_async_add_u64(dst + 8u * iw,
-                              (static_cast<unsigned long long>(hw >> 16) << 32) | (hw & 0xFFFFu), rbar);
+        // push the busy warps' counts, two keys per 8-byte add (neither
+        // 32-bit count can carry: a row has fewer than 2^32 tokens)
+        const int npairs = (hi - lo + 2) >> 1;
+        for (int iw = tid; iw < npairs; iw += NTHR) {
+          const uint2 cw = *reinterpret_cast<const uint2*>(&S.merged[2 * iw]);
+          if (cw.x | cw.y) {
+            red_async_add_u64(dst + 8u * iw, (static_cast<unsigned long long>(cw.y) << 32) | cw.x, rbar);
             sent += 2;
           }
         }

@@ -373,8 +373,8 @@ def test_window_reaching_minus_infinity():
 
 def test_top_p_only_high_temperature_rows_all_checked():
     """Top-p-only rows at temperatures 1.0 and 1.3 (p 0.9 .. 0.99, k off) on
-    hot-set logits: the rows whose candidate window the shards' level codes
-    narrow.  Every row against the oracle (targets from the oracle's
+    hot-set logits: the rows with the widest candidate windows (tens of
+    thousands of candidates each).  Every row against the oracle (targets from the oracle's
     restricted distribution, a tenth forced outside the support)."""
     T = 384
     rng = np.random.default_rng(21)
