@@ -102,6 +102,27 @@ __device__ __forceinline__ void red_shared_add_if(uint32_t addr, uint32_t v, uin
   asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q red.shared.add.u32 [%0], %1;\n\t}"
                :: "r"(addr), "r"(v), "r"(pred) : "memory");
 }
+// Dense count over a window of positive values: each bf16 half b of w at or
+// above vlo (a positive bf16 value) adds one at byte address A - 4 b, where A
+// is the address key 0x8000 (value +0) would have: a positive value's order
+// key is 0x8000 + b.  Both comparisons are on the halves unpacked by name
+// (lower, upper), each add a predicated instruction.
+__device__ __forceinline__ void count_pair_pos(uint32_t w, unsigned short vlo, uint32_t A) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b16 h0, h1;\n\t.reg .b32 t0, t1;\n\t"
+      "mov.b32 {h0, h1}, %0;\n\t"
+      "setp.ge.bf16 p0, h0, %1;\n\t"
+      "setp.ge.bf16 p1, h1, %1;\n\t"
+      "and.b32 t0, %0, 65535;\n\t"
+      "shl.b32 t0, t0, 2;\n\t"
+      "sub.u32 t0, %2, t0;\n\t"
+      "shr.b32 t1, %0, 16;\n\t"
+      "shl.b32 t1, t1, 2;\n\t"
+      "sub.u32 t1, %2, t1;\n\t"
+      "@p0 red.shared.add.u32 [t0], 1;\n\t"
+      "@p1 red.shared.add.u32 [t1], 1;\n\t}"
+      :: "r"(w), "h"(vlo), "r"(A) : "memory");
+}
 __device__ __forceinline__ unsigned long long global_timer() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -454,19 +454,32 @@ logp_kernel(const KParams P) {
         // address of a non-candidate is never used), instead of a
         // per-candidate search whose lanes diverge
         const uint32_t mbase = smem_addr(S.merged);
-        while (hitmask) {
-          const int i = __ffs(hitmask) - 1;
-          hitmask &= hitmask - 1;
-          const uint4 v = sh[tid + i * NTHR];
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        if (pos_window) {
+          // key 0x8000 + b: the add lands at A - 4 b
+          const uint32_t A = mbase + 4u * static_cast<uint32_t>(hi - 0x8000);
+          const unsigned short vlo16 = static_cast<unsigned short>(__float_as_uint(vlo_f) >> 16);
+          while (hitmask) {
+            const int i = __ffs(hitmask) - 1;
+            hitmask &= hitmask - 1;
+            const uint4 v = sh[tid + i * NTHR];
+            count_pair_pos(v.x, vlo16, A);
+            count_pair_pos(v.y, vlo16, A);
+            count_pair_pos(v.z, vlo16, A);
+            count_pair_pos(v.w, vlo16, A);
+          }
+        } else {
+          while (hitmask) {
+            const int i = __ffs(hitmask) - 1;
+            hitmask &= hitmask - 1;
+            const uint4 v = sh[tid + i * NTHR];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t m2 = __hge2_mask(as_bf2(w[j]), vlo2);
-            const uint32_t b0 = w[j] & 0xFFFFu, b1 = w[j] >> 16;
-            const int i0 = hi - (pos_window ? static_cast<int>(b0 | 0x8000u) : okey(b0));
-            const int i1 = hi - (pos_window ? static_cast<int>(b1 | 0x8000u) : okey(b1));
-            red_shared_add_if(mbase + 4u * static_cast<uint32_t>(i0), 1u, m2 & 1u);
-            red_shared_add_if(mbase + 4u * static_cast<uint32_t>(i1), 1u, m2 & 0x10000u);
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t m2 = __hge2_mask(as_bf2(w[j]), vlo2);
+              const int i0 = hi - okey(w[j] & 0xFFFFu), i1 = hi - okey(w[j] >> 16);
+              red_shared_add_if(mbase + 4u * static_cast<uint32_t>(i0), 1u, m2 & 1u);
+              red_shared_add_if(mbase + 4u * static_cast<uint32_t>(i1), 1u, m2 & 0x10000u);
+            }
           }
         }
       }
