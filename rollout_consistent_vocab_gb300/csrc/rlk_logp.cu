@@ -458,14 +458,29 @@ logp_kernel(const KParams P) {
           // key 0x8000 + b: the add lands at A - 4 b
           const uint32_t A = mbase + 4u * static_cast<uint32_t>(hi - 0x8000);
           const unsigned short vlo16 = static_cast<unsigned short>(__float_as_uint(vlo_f) >> 16);
-          while (hitmask) {
-            const int i = __ffs(hitmask) - 1;
-            hitmask &= hitmask - 1;
-            const uint4 v = sh[tid + i * NTHR];
-            count_pair_pos(v.x, vlo16, A);
-            count_pair_pos(v.y, vlo16, A);
-            count_pair_pos(v.z, vlo16, A);
-            count_pair_pos(v.w, vlo16, A);
+          if (warp_hits <= FULL_HITS) {
+            while (hitmask) {
+              const int i = __ffs(hitmask) - 1;
+              hitmask &= hitmask - 1;
+              const uint4 v = sh[tid + i * NTHR];
+              count_pair_pos(v.x, vlo16, A);
+              count_pair_pos(v.y, vlo16, A);
+              count_pair_pos(v.z, vlo16, A);
+              count_pair_pos(v.w, vlo16, A);
+            }
+          } else {
+            // nearly every chunk hit: a fixed walk, no search for the next one
+#pragma unroll
+            for (int i = 0; i < MAXCH; ++i) {
+              if ((hitmask >> i) & 1u) {
+                const uint4 v = sh[tid + i * NTHR];
+                count_pair_pos(v.x, vlo16, A);
+                count_pair_pos(v.y, vlo16, A);
+                count_pair_pos(v.z, vlo16, A);
+                count_pair_pos(v.w, vlo16, A);
+              }
+            }
+            hitmask = 0;
           }
         } else {
           while (hitmask) {
