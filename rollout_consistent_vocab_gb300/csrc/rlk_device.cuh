@@ -44,7 +44,7 @@ constexpr int WIN = 1024;            // candidate window, in bf16 order keys (8 
 constexpr int TMA_PIECES = 4;
 constexpr int BUSY_HITS = 16;        // candidate chunks per warp above which it counts locally
 constexpr int DENSE_HITS = 128;      // ... and above which it counts every element of a hit chunk
-constexpr int FULL_HITS = 416;       // ... and above which it walks all its chunks in a fixed order
+constexpr int FULL_HITS = 352;       // ... and above which it walks all its chunks in a fixed order
 constexpr float LOG2E = 1.4426950408889634f;   // log2(e)
 constexpr float FX_SCALE = 17592186044416.0f;  // 2^44: fixed-point scale of masses
 constexpr unsigned long long TIMEOUT_NS = 200000000ull;   // 0.2 s bound on every wait

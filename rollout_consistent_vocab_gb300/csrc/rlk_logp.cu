@@ -469,16 +469,24 @@ logp_kernel(const KParams P) {
               count_pair_pos(v.w, vlo16, A);
             }
           } else {
-            // nearly every chunk hit: a fixed walk, no search for the next one
+            // nearly every chunk hit: a fixed walk without branches.  A chunk
+            // that is not hit has no element at or above the window bottom, so
+            // its adds are all predicated off; only the last chunk, which a
+            // thread may not own, keeps its test
 #pragma unroll
-            for (int i = 0; i < MAXCH; ++i) {
-              if ((hitmask >> i) & 1u) {
-                const uint4 v = sh[tid + i * NTHR];
-                count_pair_pos(v.x, vlo16, A);
-                count_pair_pos(v.y, vlo16, A);
-                count_pair_pos(v.z, vlo16, A);
-                count_pair_pos(v.w, vlo16, A);
-              }
+            for (int i = 0; i < MAXCH - 1; ++i) {
+              const uint4 v = sh[tid + i * NTHR];
+              count_pair_pos(v.x, vlo16, A);
+              count_pair_pos(v.y, vlo16, A);
+              count_pair_pos(v.z, vlo16, A);
+              count_pair_pos(v.w, vlo16, A);
+            }
+            if ((hitmask >> (MAXCH - 1)) & 1u) {
+              const uint4 v = sh[tid + (MAXCH - 1) * NTHR];
+              count_pair_pos(v.x, vlo16, A);
+              count_pair_pos(v.y, vlo16, A);
+              count_pair_pos(v.z, vlo16, A);
+              count_pair_pos(v.w, vlo16, A);
             }
             hitmask = 0;
           }
