@@ -392,3 +392,29 @@ def test_top_p_only_high_temperature_rows_all_checked():
     check_rows_parallel(st, bits, tau, p, k, tg, f, r, s)
     assert st.rows == T
     record("top-p only tau1.0/1.3 p0.9-0.99 hot1-512", st)
+
+
+def test_negative_logit_rows_dense_windows():
+    """Hot-set logits shifted by -40, so every logit of a row is negative (the
+    row maximum about -16): at temperature 1.3 and top-p 0.99 the candidate
+    window holds tens of thousands of negative values and is counted by the
+    dense form's general branch (order keys of negative values), at p 0.9 and
+    with top-k 128 by the sparser paths.  Every row against the oracle."""
+    T = 256
+    rng = np.random.default_rng(23)
+    x, hot, n = W.hot_logits(T, 1, 512, seed=23, device=DEV)
+    x = (x.float() - 40.0).to(torch.bfloat16)
+    tau = rng.choice([1.0, 1.3], T).astype(np.float32)
+    p = rng.choice([0.9, 0.99], T).astype(np.float32)
+    k = rng.choice([-1, -1, 128], T).astype(np.int32)
+    bits = bits_of(x)
+    assert ((bits[:, :VR] & 0x8000) != 0).all()      # every real logit negative
+    forced = np.zeros(T, bool)
+    forced[rng.choice(T, T // 10, replace=False)] = True
+    tg = oracle_targets_parallel(bits, tau, p, k, forced, seed=23)
+    f, r, s = run_pair(x, _t(tg, torch.int32), _t(tau, torch.float32), _t(p, torch.float32),
+                       _t(k, torch.int32))
+    st = Stats()
+    check_rows_parallel(st, bits, tau, p, k, tg, f, r, s)
+    assert st.rows == T
+    record("negative logits tau1.0/1.3 p0.9/0.99 k off/128", st)
