@@ -793,7 +793,7 @@ def run_ours(args, rank, world, local):
         g10 = (1e-2 * torch.randn(10_000_000, generator=gen, device=dev)).to(torch.bfloat16)
         cold, warm = norm_ms(g10, True), norm_ms(g10, False)
         del g10
-        gnorm = {"kernel": "sqnorm_kernel (128-bit fixed-point per thread, exact exponent bins) + finalize",
+        gnorm = {"kernel": "sqnorm16_kernel (BF16/FP16: per-magnitude counts in shared memory) or sqnorm_kernel (FP32: 128-bit fixed-point per thread), exact exponent bins, + finalize",
                  "calls": "one grad_norm call = clear bins + accumulate + finalize, median of "
                           f"{args.norm_steps}",
                  "bf16_10m": {"ms_l2_flushed": cold, "ms_l2_warm": warm,

@@ -275,6 +275,24 @@ __global__ void __launch_bounds__(NORM_THREADS, NORM_MIN_BLOCKS) sqnorm_kernel(c
 // and infinite squares to their counters): the same exact sum, with no
 // per-element arithmetic beyond the add.
 
+// Both 15-bit magnitudes of a 32-bit word add one to their counters at byte
+// address base + 4 m, each add a predicated instruction (zero magnitudes add
+// nothing and issue nothing): no branch per element.
+__device__ __forceinline__ void count_mag_pair(uint32_t w, uint32_t base) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b32 m0, m1, a0, a1;\n\t"
+      "and.b32 m0, %0, 32767;\n\t"
+      "shr.b32 m1, %0, 16;\n\t"
+      "and.b32 m1, m1, 32767;\n\t"
+      "setp.ne.u32 p0, m0, 0;\n\t"
+      "setp.ne.u32 p1, m1, 0;\n\t"
+      "mad.lo.u32 a0, m0, 4, %1;\n\t"
+      "mad.lo.u32 a1, m1, 4, %1;\n\t"
+      "@p0 red.shared.add.u32 [a0], 1;\n\t"
+      "@p1 red.shared.add.u32 [a1], 1;\n\t}"
+      :: "r"(w), "r"(base) : "memory");
+}
+
 constexpr int H16_THREADS = 1024;
 constexpr int NPAT = 32768;
 constexpr uint32_t H16_SMEM = NPAT * 4u;
@@ -289,11 +307,8 @@ __global__ void __launch_bounds__(H16_THREADS, 1) sqnorm16_kernel(const char* x,
   for (int i = tid; i < NPAT / 4; i += H16_THREADS) reinterpret_cast<uint4*>(cnt)[i] = make_uint4(0u, 0u, 0u, 0u);
   for (int i = tid; i < NB; i += H16_THREADS) sb[i] = 0ull;
   __syncthreads();
-  auto add2 = [&](uint32_t w) {                      // the two elements of a 32-bit word
-    const uint32_t lo = w & 0x7FFFu, hi = (w >> 16) & 0x7FFFu;
-    if (lo) atomicAdd(&cnt[lo], 1u);
-    if (hi) atomicAdd(&cnt[hi], 1u);
-  };
+  const uint32_t cbase = static_cast<uint32_t>(__cvta_generic_to_shared(cnt));
+  auto add2 = [&](uint32_t w) { count_mag_pair(w, cbase); };   // the two elements of a word
   const uint4* vx = reinterpret_cast<const uint4*>(x + head * 2);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * H16_THREADS;
   int64_t i = static_cast<int64_t>(blockIdx.x) * H16_THREADS + tid;
