@@ -393,9 +393,20 @@ __global__ void sqnorm_finalize_kernel(const unsigned long long* bins, double* o
   __shared__ unsigned long long dig[ND];
   const int lane = threadIdx.x;
   if (lane < ND) dig[lane] = 0ull;
+  // every load first (independent), then the adds
+  constexpr int PER_LANE = (INF_BIN - 1 + 31) / 32;
+  unsigned long long vb[PER_LANE];
+#pragma unroll
+  for (int q = 0; q < PER_LANE; ++q) {
+    const int e = 1 + lane + 32 * q;
+    vb[q] = e < INF_BIN ? bins[e] : 0ull;
+  }
+  const unsigned long long nan_b = bins[NAN_BIN], inf_b = bins[INF_BIN];
   __syncwarp();
-  for (int e = 1 + lane; e < INF_BIN; e += 32) {
-    const unsigned long long v = bins[e];
+#pragma unroll
+  for (int q = 0; q < PER_LANE; ++q) {
+    const int e = 1 + lane + 32 * q;
+    const unsigned long long v = vb[q];
     if (!v) continue;
     const int s = e - 1, L = s >> 5, sh = s & 31;
     const unsigned long long lo = v << sh;
@@ -406,11 +417,11 @@ __global__ void sqnorm_finalize_kernel(const unsigned long long* bins, double* o
   }
   __syncwarp();
   if (lane != 0) return;
-  if (bins[NAN_BIN]) {
+  if (nan_b) {
     out[0] = out[1] = __longlong_as_double(0x7ff8000000000000ll);
     return;
   }
-  if (bins[INF_BIN]) {
+  if (inf_b) {
     out[0] = out[1] = __longlong_as_double(0x7ff0000000000000ll);
     return;
   }
