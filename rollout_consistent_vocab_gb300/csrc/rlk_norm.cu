@@ -294,6 +294,7 @@ __device__ __forceinline__ void count_mag_pair(uint32_t w, uint32_t base) {
 }
 
 constexpr int H16_THREADS = 1024;
+constexpr int H16_MIN_VEC = 8;    // 16-byte vectors per thread below which fewer blocks run
 constexpr int NPAT = 32768;
 constexpr uint32_t H16_SMEM = NPAT * 4u;
 
@@ -516,7 +517,7 @@ extern "C" rlk_status rlk_sqnorm_accumulate(const void* x, int64_t n, int32_t dt
     }
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t want = (nvec + H16_THREADS * 16 - 1) / (H16_THREADS * 16);
+    const int64_t want = (nvec + H16_THREADS * H16_MIN_VEC - 1) / (H16_THREADS * H16_MIN_VEC);
     const unsigned g16 = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(want, std::max(1, sms))));
     if (dtype == RLK_DT_BF16) sqnorm16_kernel<RLK_DT_BF16><<<g16, H16_THREADS, H16_SMEM, st>>>(xc, head, nvec, n, b);
     else sqnorm16_kernel<RLK_DT_F16><<<g16, H16_THREADS, H16_SMEM, st>>>(xc, head, nvec, n, b);
