@@ -54,6 +54,10 @@ struct __align__(128) ShardSmem {
   alignas(128) uint4 shard[SHARD_CHUNKS];
 };
 constexpr size_t SHARD_SMEM_NO_COPY = offsetof(ShardSmem, shard);
+// the counts kernel given chunk maxima copies the row's maxima (2 bytes per
+// chunk) into the start of the shard area
+constexpr uint32_t CMAX_ROW_BYTES = SHARD_CHUNKS * 2u;
+static_assert(CMAX_ROW_BYTES % 16u == 0u, "bulk copies move 16-byte multiples");
 static_assert(sizeof(ShardSmem) + 1024 <= 233472 / CTAS_PER_SM, "shared memory budget of 5 CTAs per SM");
 
 struct ShardParams {
@@ -243,6 +247,15 @@ __global__ void __launch_bounds__(NTHR, CMAX ? 16 : CTAS_PER_SM) shard_counts_ke
   const int64_t row = blockIdx.x;
   const int r = P.shard;
   const int nchunks = (r == NSHARD - 1) ? LAST_CHUNKS : SHARD_CHUNKS;
+  const uint32_t bar = smem_addr(&S.bar_load);
+  if (CMAX && tid == 0) {
+    // the row's chunk maxima go out first, while the window is formed from
+    // the gathered summaries (every row waits for the copy before it ends)
+    mbar_init(bar, 1);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive_expect_tx(bar, CMAX_ROW_BYTES);
+    bulk_load(smem_addr(S.shard), P.in_cmax + row * SHARD_CHUNKS, CMAX_ROW_BYTES, bar, evict_first_policy());
+  }
   const RowParams rp = row_params(P.tau_arr, P.tau_s, P.p_arr, P.p_s, P.k_arr, P.k_s, P.target, row);
   const bool sel = rp.valid && !rp.greedy && (rp.k_on || rp.p_on);
   for (int i = tid; i < WIN; i += NTHR) S.hist[i] = 0u;
@@ -255,18 +268,18 @@ __global__ void __launch_bounds__(NTHR, CMAX ? 16 : CTAS_PER_SM) shard_counts_ke
     const float xm = P.g_max[static_cast<int64_t>(r) * P.T + row];
     const bool count = (xm > -INFINITY) && (xm < INFINITY) && lo <= hi && okey_of(xm) >= lo;
     if (CMAX && count) {
-      // phase 1's chunk maxima pick the chunks to read, straight from global memory
-      __syncthreads();          // histogram zeroed
+      // phase 1's chunk maxima (copied to shared memory) pick the chunks to
+      // read, straight from global memory
+      __syncthreads();          // histogram zeroed, copy barrier initialised
+      if (!mbar_wait_bounded(bar)) mbar_wait_bounded(bar);
       const float vlo_f = key_value(lo);
-      const uint16_t* cmax = P.in_cmax + row * SHARD_CHUNKS;
+      const uint16_t* cmax = reinterpret_cast<const uint16_t*>(S.shard);
       const uint4* rowv = reinterpret_cast<const uint4*>(P.logits + row * P.stride);
-      // all of this thread's chunk maxima first (independent loads), then the
-      // few chunks that reach the window
       uint32_t hit = 0;
 #pragma unroll
       for (int i = 0; i < MAXCH; ++i) {
         const int ch = tid + i * NTHR;
-        if (ch < nchunks && __uint_as_float(static_cast<uint32_t>(__ldg(cmax + ch)) << 16) >= vlo_f)
+        if (ch < nchunks && __uint_as_float(static_cast<uint32_t>(cmax[ch]) << 16) >= vlo_f)
           hit |= 1u << i;
       }
       while (hit) {
@@ -315,6 +328,8 @@ __global__ void __launch_bounds__(NTHR, CMAX ? 16 : CTAS_PER_SM) shard_counts_ke
   uint4* dst = reinterpret_cast<uint4*>(P.out_counts + row * WIN);
   const uint4* src = reinterpret_cast<const uint4*>(S.hist);
   for (int i = tid; i < WIN / 4; i += NTHR) dst[i] = src[i];
+  // the chunk-maxima copy writes this CTA's shared memory: it lands before the CTA ends
+  if (CMAX && tid == 0 && !mbar_wait_bounded(bar)) mbar_wait_bounded(bar);
 }
 
 // ------------------------------------------------------------ lower windows
@@ -660,7 +675,7 @@ rlk_status launch_shard(void (*kernel)(ShardParams), const ShardParams& P, cudaS
     configured[dev] = true;
   }
   // the counts kernel with chunk maxima never touches the shard copy
-  const size_t smem = (WHICH == 1 && P.in_cmax) ? SHARD_SMEM_NO_COPY : sizeof(ShardSmem);
+  const size_t smem = (WHICH == 1 && P.in_cmax) ? SHARD_SMEM_NO_COPY + CMAX_ROW_BYTES : sizeof(ShardSmem);
   kernel<<<static_cast<unsigned>(P.T), NTHR, smem, stream>>>(P);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(RLK_ECUDA, "kernel launch: %s", cudaGetErrorString(e));
