@@ -161,6 +161,18 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "=r"(ok) : "r"(bar), "r"(parity), "r"(static_cast<uint32_t>(RLK_WAIT_HINT_NS)) : "memory");
   return ok != 0;
 }
+// The same test with acquire semantics at cluster scope: a message that
+// completes the barrier releases at cluster scope what its sender had
+// observed, and this makes it visible to the waiting thread.
+__device__ __forceinline__ bool mbar_try_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok) : "r"(bar), "r"(parity), "r"(static_cast<uint32_t>(RLK_WAIT_HINT_NS)) : "memory");
+  return ok != 0;
+}
 // Bounded wait on phase 0 of a barrier: gives up after TIMEOUT_NS of wall time.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar) {
   if (mbar_try(bar, 0)) return true;
@@ -191,6 +203,20 @@ constexpr unsigned long long DRAIN_SUM = 6 * TIMEOUT_NS;
 constexpr unsigned long long DRAIN_LEAD = 8 * TIMEOUT_NS;
 __device__ __forceinline__ bool mbar_wait_until(uint32_t bar, unsigned long long deadline) {
   while (!mbar_try(bar, 0)) {
+    if (global_timer() > deadline) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ bool mbar_wait_bounded_cl(uint32_t bar) {
+  if (mbar_try_cl(bar, 0)) return true;
+  const unsigned long long t0 = global_timer();
+  while (!mbar_try_cl(bar, 0)) {
+    if (global_timer() - t0 > TIMEOUT_NS) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ bool mbar_wait_until_cl(uint32_t bar, unsigned long long deadline) {
+  while (!mbar_try_cl(bar, 0)) {
     if (global_timer() > deadline) return false;
   }
   return true;

@@ -294,16 +294,15 @@ logp_kernel(const KParams P) {
   if (sel)
     for (int i = tid; i < WIN; i += NTHR) S.merged[i] = 0u;
   __syncthreads();
-  // S0: barriers initialised and the leader's histogram zeroed.  One thread
-  // publishes all of it to the cluster (the block barrier above orders the
-  // other threads' stores before its fence); everyone arrives relaxed.
-  if (tid == 0) {
-    if (sel && r == 0) asm volatile("fence.acq_rel.cluster;" ::: "memory");
-    else asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
+  // S0: barriers initialised; one thread publishes the initialisations to the
+  // cluster and everyone arrives relaxed.  The leader's zeroed histogram
+  // needs no fence here: a peer adds to it only after its window wait has
+  // acquired, at cluster scope, every exchange message including the
+  // leader's, and the leader sends that message after the block barrier
+  // above, so the message's release covers the zero stores.
+  if (tid == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   cluster_arrive_relaxed();
-  // the leader needs the target's logit at the end: start the load now, after
-  // the cluster fence above (a fence would wait for it)
+  // the leader needs the target's logit at the end: start the load now
   const float xt = (r == 0 && !SAMPLE) ? __uint_as_float(static_cast<uint32_t>(__ldg(rowp + t)) << 16) : 0.0f;
   uint32_t flags = 0;
   if (!mbar_wait_bounded(bar_load)) {
@@ -381,15 +380,17 @@ logp_kernel(const KParams P) {
   if (sel) {
     if (tid == 0) {
       // the window of candidate keys, the same in every CTA of the cluster
-      // (top-p-only rows: both exchanges in)
-      if (late_mid && !mbar_wait_bounded(bar_mid)) {
+      // (top-p-only rows: both exchanges in).  The waits acquire at cluster
+      // scope: after them this CTA's adds into the leader's histogram are
+      // ordered after the leader's zeroing of it.
+      if (late_mid && !mbar_wait_bounded_cl(bar_mid)) {
         flags |= FLAG_TIMEOUT;
-        mbar_wait_until(bar_mid, t_start + DRAIN_MID);   // resident for late messages
+        mbar_wait_until_cl(bar_mid, t_start + DRAIN_MID);   // resident for late messages
       }
       const uint32_t bar_w = late_mid ? bar_mid2 : bar_mid;
-      if (!mbar_wait_bounded(bar_w)) {
+      if (!mbar_wait_bounded_cl(bar_w)) {
         flags |= FLAG_TIMEOUT;
-        mbar_wait_until(bar_w, t_start + (late_mid ? DRAIN_MID2 : DRAIN_MID));   // resident for late messages
+        mbar_wait_until_cl(bar_w, t_start + (late_mid ? DRAIN_MID2 : DRAIN_MID));   // resident for late messages
       }
       int L = 0x7fffffff;
       float M = -INFINITY;
