@@ -344,7 +344,7 @@ logp_kernel(const KParams P) {
     }
   }
 
-  cluster_wait();              // S0 complete: peers' barriers and histogram are ready
+  cluster_wait();              // S0 complete: every CTA's barriers are initialised
   // Restricted rows send their maximum and bound now and overlap the
   // exchange with the sum-exp pass; top-p-only rows then exchange their
   // sum-exp (which sets the candidate window) in a second round.
