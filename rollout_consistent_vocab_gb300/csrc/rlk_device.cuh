@@ -314,25 +314,6 @@ __device__ __forceinline__ float block_sum_fixed(float v, SM& S) {
   return r;
 }
 
-// block_sum_fixed (same tree, same bits) that also returns the block's sum of
-// an integer n in `total`.
-template <class SM>
-__device__ __forceinline__ float block_sum_fixed_count(float v, int n, int& total, SM& S) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = v + __shfl_xor_sync(0xffffffffu, v, o);
-  n = __reduce_add_sync(0xffffffffu, n);
-  if (lane == 0) { S.red_f[warp] = v; S.red_i[warp] = n; }
-  __syncthreads();
-  float r = S.red_f[0];
-  int t = S.red_i[0];
-#pragma unroll
-  for (int w = 1; w < NWARP; ++w) { r = r + S.red_f[w]; t += S.red_i[w]; }
-  __syncthreads();
-  total = t;
-  return r;
-}
-
 template <class SM>
 __device__ __forceinline__ int block_min_int(int v, SM& S) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1062,12 +1043,6 @@ __device__ __forceinline__ unsigned long long chunk_support_mass(uint4 v, __nv_b
     m += qfx(__uint_as_float(b << 16), M, c);
   }
   return m;
-}
-
-__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
 }
 
 }  // namespace rlk
