@@ -715,10 +715,13 @@ __device__ __noinline__ SelResult select_support(SM& S, uint32_t* cnt0, uint32_t
 
 // Selection by one warp when the first window holds every threshold (the
 // common case).  Keys hi, hi-1, ..., lo are taken in blocks of 32 x
-// RLK_SEL_KPL (consecutive keys per lane; 4 measured fastest, 8 slower): first
-// a scan of the counts alone finds the
-// top-k boundary, then one scan of the fixed-point masses over S_k finds the
-// nucleus boundary.  Returns false if a threshold may lie below the window.
+// RLK_SEL_KPL (consecutive keys per lane; 4 measured fastest, 8 slower).  A
+// top-k row whose k-th key lies in the first block is resolved in one pass
+// over it (counts and fixed-point masses scanned together: the k-th key, the
+// mass of S_k, then the nucleus boundary from the same registers); otherwise
+// a scan of the counts alone finds the top-k boundary, then one scan of the
+// masses over S_k finds the nucleus boundary.  Returns false if a threshold
+// may lie below the window.
 __device__ __forceinline__ uint32_t warp_incl_scan_u32(uint32_t v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
@@ -747,11 +750,84 @@ __device__ __forceinline__ bool select_warp(const uint32_t* cnt, int hi, int lo,
   const int n = hi - lo + 1;
   int imax = n - 1;
   uint32_t sup_k = 0;
+  // ---- top-k rows whose k-th key lies in the first block: counts, masses,
+  // the k-th key and the nucleus in one pass over that block
+  uint32_t carry0 = 0;          // counts of the blocks already scanned for the k-th key
+  int b_start = 0;
+  if (k_on) {
+    uint32_t cj[KPL], lc = 0;
+    unsigned long long mj[KPL], lm = 0;
+#pragma unroll
+    for (int j = 0; j < KPL; ++j) {
+      const int i = KPL * lane + j;
+      cj[j] = (i < n) ? cnt[i] : 0u;
+      mj[j] = cj[j] ? cj[j] * qfx(key_value(hi - i), M, c) : 0ull;
+      lc += cj[j];
+      lm += mj[j];
+    }
+    const uint32_t ic = warp_incl_scan_u32(lc);
+    const unsigned long long im = warp_incl_scan_u64(lm);
+    // the k-th key: the first whose inclusive count reaches k
+    uint32_t rc = ic - lc;
+    unsigned long long rm = im - lm;
+    int f = -1;
+    uint32_t fc = 0;
+    unsigned long long fm = 0;
+#pragma unroll
+    for (int j = 0; j < KPL; ++j) {
+      if (f < 0 && rc < static_cast<uint32_t>(k) && rc + cj[j] >= static_cast<uint32_t>(k)) {
+        f = KPL * lane + j;
+        fc = rc + cj[j];
+        fm = rm + mj[j];
+      }
+      rc += cj[j];
+      rm += mj[j];
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, f >= 0);
+    if (bal) {
+      const int src = __ffs(bal) - 1;
+      const int fi = __shfl_sync(0xffffffffu, f, src);
+      const uint32_t skc = __shfl_sync(0xffffffffu, fc, src);
+      const unsigned long long zk = __shfl_sync(0xffffffffu, fm, src);   // the mass of S_k
+      if (!p_on) {
+        out = SelResult{skc, zk, hi - fi};
+        return true;
+      }
+      const unsigned long long T = nucleus_bound(p, zk);
+      rc = ic - lc;
+      rm = im - lm;
+      int g = -1;
+      uint32_t gc = 0;
+      unsigned long long gm = 0;
+#pragma unroll
+      for (int j = 0; j < KPL; ++j) {
+        const int i = KPL * lane + j;
+        if (g < 0 && i <= fi && rm < T && (rm + mj[j] >= T || i == fi)) {
+          g = i;
+          gc = rc + cj[j];
+          gm = rm + mj[j];
+        }
+        rc += cj[j];
+        rm += mj[j];
+      }
+      const unsigned bg = __ballot_sync(0xffffffffu, g >= 0);
+      if (bg) {                          // (always: the maximum's own mass makes T >= 1)
+        const int sg = __ffs(bg) - 1;
+        out = SelResult{__shfl_sync(0xffffffffu, gc, sg), __shfl_sync(0xffffffffu, gm, sg),
+                        hi - __shfl_sync(0xffffffffu, g, sg)};
+        return true;
+      }
+    } else {
+      // the k-th key lies further down: the count scan goes on from the next block
+      carry0 = __shfl_sync(0xffffffffu, ic, 31);
+      b_start = BLK;
+    }
+  }
   // ---- top-k boundary from the counts
   if (k_on) {
-    uint32_t carry = 0;
+    uint32_t carry = carry0;
     int fi = -1;
-    for (int b0 = 0; b0 < n && fi < 0; b0 += BLK) {
+    for (int b0 = b_start; b0 < n && fi < 0; b0 += BLK) {
       uint32_t cj[KPL], lc = 0;
 #pragma unroll
       for (int j = 0; j < KPL; ++j) {
