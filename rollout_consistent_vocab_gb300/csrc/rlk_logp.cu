@@ -67,7 +67,7 @@ struct __align__(16) Mid2Slot {
 struct __align__(16) Summary {
   float xm;        // shard maximum
   float l;         // sum over the shard of exp(s_j - m_r) (NaN if the shard holds a NaN)
-  uint32_t aux;    // greedy: first column holding the maximum; otherwise histogram-add bytes / 4 sent
+  uint32_t aux;    // greedy: first column holding the maximum; otherwise 0
   uint32_t flags;
 };
 
@@ -86,7 +86,7 @@ struct __align__(128) Smem {
   int32_t found_i;
   uint32_t found_c;
   unsigned long long found_m;
-  uint32_t npush;
+  uint32_t npush;                  // leader: the peers' histogram adds, in 4-byte units
   int32_t win[4];
   float bc_f[4];
   int32_t sel_done;
@@ -284,7 +284,10 @@ logp_kernel(const KParams P) {
     // messages from the 7 peers: 16 bytes each
     if (sel) mbar_arrive_expect_tx(bar_mid, (NSHARD - 1) * 16);
     if (sel && !k_on) mbar_arrive_expect_tx(bar_mid2, (NSHARD - 1) * 16);
-    if (r == 0) mbar_arrive_expect_tx(bar_sum, (NSHARD - 1) * 16);
+    // the peers' summaries (16 bytes each) and, on restricted rows, each peer
+    // warp's 4-byte add of the number of histogram adds it sent
+    if (r == 0)
+      mbar_arrive_expect_tx(bar_sum, (NSHARD - 1) * 16 + (sel ? (NSHARD - 1) * NWARP * 4 : 0));
     if (BWD && r != 0) {
       mbar_init(bar_lead, 1);
       mbar_arrive_expect_tx(bar_lead, 16);
@@ -562,15 +565,18 @@ logp_kernel(const KParams P) {
         for (int i = tid; i < SAMP_BITWORDS; i += NTHR) wb[i] = 0u;
       }
     }
-    // the leader learns how many add bytes (in 4-byte units) each peer sent from its summary
+    // the leader learns how many add bytes (in 4-byte units) the peers sent:
+    // each peer warp adds its number into the leader's counter, completing
+    // on the summaries' barrier (each warp on its own: no block barrier
+    // before the peer ends)
     sent = __reduce_add_sync(0xffffffffu, sent);
-    if ((tid & 31) == 0 && sent) atomicAdd(&S.npush, sent);
-    __syncthreads();
+    if (r != 0 && (tid & 31) == 0)
+      red_async_add(map_rank(smem_addr(&S.npush), 0), sent, map_rank(bar_sum, 0));
   }
 
   // ---- 5. summary to the leader
   if (tid == 0) {
-    const uint4 msg = make_uint4(__float_as_uint(xm), __float_as_uint(l), sel ? S.npush : first, flags);
+    const uint4 msg = make_uint4(__float_as_uint(xm), __float_as_uint(l), sel ? 0u : first, flags);
     if (r == 0) *reinterpret_cast<uint4*>(&S.slot[0]) = msg;
     else st_async_v4(map_rank(smem_addr(&S.slot[r]), 0), msg, map_rank(bar_sum, 0));
   }
@@ -601,12 +607,10 @@ logp_kernel(const KParams P) {
     bool timed_out = !mbar_wait_bounded(bar_sum);
     // after a timeout, stay resident until every peer is past its own
     // bounded waits (its summary and adds are then in); the adds can only be
-    // awaited once every summary has announced their number
+    // awaited once every peer warp has announced their number
     const bool sums_in = !timed_out || mbar_wait_until(bar_sum, t_start + DRAIN_SUM);
     if (sel && sums_in) {
-      uint32_t pushed = 0;
-#pragma unroll
-      for (int q = 1; q < NSHARD; ++q) pushed += S.slot[q].aux;
+      const uint32_t pushed = S.npush;     // complete with the summaries
       mbar_arrive_expect_tx(bar_hist, 4u * pushed);
       if (!mbar_wait_bounded(bar_hist)) {
         timed_out = true;
