@@ -104,3 +104,22 @@ def test_targets_do_not_depend_on_chunking():
             assert o.restr == -math.inf
         elif not forced[i]:
             assert o.restr > -math.inf
+
+
+def test_scaled_tolerance_term():
+    """scale_tol widens the bound by scale_tol * max(|M|, |x_t|) / tau: on a
+    row whose maximum is 24 at temperature 1e-3 (scaled logits of 24000) a
+    deviation of 4e-3 passes with 2.4e-7 (bound 5.8e-3) and fails without;
+    at temperature 1 the same term adds only 5.8e-6."""
+    row = make_row(0.0, {3: 24.0, 9: 23.0})
+    assert abs(oc.scaled_magnitude(row, 1e-3, 9) - 24.0 / float(np.float32(1e-3))) < 1e-6
+    assert oc.scaled_magnitude(row, 0.0, 9) == 0.0
+    r = oracle.logp_row(row, 1e-3, 1.0, -1, 9)
+    st = oc.Stats()
+    oc.check_row(st, row, 1e-3, 1.0, -1, 9, r.full + 4e-3, r.restr + 4e-3, r.support, scale_tol=2.4e-7)
+    with pytest.raises(AssertionError):
+        oc.check_row(oc.Stats(), row, 1e-3, 1.0, -1, 9, r.full + 4e-3, r.restr + 4e-3, r.support)
+    r1 = oracle.logp_row(row, 1.0, 1.0, -1, 9)
+    with pytest.raises(AssertionError):
+        oc.check_row(oc.Stats(), row, 1.0, 1.0, -1, 9, r1.full + 4e-5, r1.restr, r1.support,
+                     scale_tol=2.4e-7)

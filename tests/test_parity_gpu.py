@@ -418,3 +418,30 @@ def test_negative_logit_rows_dense_windows():
     check_rows_parallel(st, bits, tau, p, k, tg, f, r, s)
     assert st.rows == T
     record("negative logits tau1.0/1.3 p0.9/0.99 k off/128", st)
+
+
+def test_extreme_temperatures_all_rows():
+    """Temperatures far from 1 (1e-3, 0.05, 5, 50) with top-p 0.5 .. 1 and
+    top-k off, 1, 7, 1000: near-greedy rows whose masses underflow to the
+    maximum's ties, and near-flat rows whose nucleus reaches below the first
+    window (the global-memory windows).  Every row against the oracle; the
+    tolerance adds 2.4e-7 max(|M|, |x_t|) / tau to 2e-5: at temperature 1e-3
+    the scaled logits reach about 2.4e4, and float32 holds each to a relative
+    2^-24 (the oracle rounds every x / tau, the kernel (x_t - M) / tau), four
+    such roundings at most."""
+    T = 128
+    rng = np.random.default_rng(29)
+    x, hot, n = W.hot_logits(T, 1, 64, seed=29, device=DEV)
+    tau = rng.choice([1e-3, 0.05, 5.0, 50.0], T).astype(np.float32)
+    p = rng.choice([0.5, 0.9, 0.999, 1.0], T).astype(np.float32)
+    k = rng.choice([-1, 1, 7, 1000], T).astype(np.int32)
+    bits = bits_of(x)
+    forced = np.zeros(T, bool)
+    forced[rng.choice(T, T // 10, replace=False)] = True
+    tg = oracle_targets_parallel(bits, tau, p, k, forced, seed=29)
+    f, r, s = run_pair(x, _t(tg, torch.int32), _t(tau, torch.float32), _t(p, torch.float32),
+                       _t(k, torch.int32))
+    st = Stats()
+    check_rows_parallel(st, bits, tau, p, k, tg, f, r, s, scale_tol=2.4e-7)
+    assert st.rows == T
+    record("extreme temperatures 1e-3..50, p 0.5..1, k off/1/7/1000", st)
