@@ -445,3 +445,29 @@ def test_extreme_temperatures_all_rows():
     check_rows_parallel(st, bits, tau, p, k, tg, f, r, s, scale_tol=2.4e-7)
     assert st.rows == T
     record("extreme temperatures 1e-3..50, p 0.5..1, k off/1/7/1000", st)
+
+
+def test_coarse_ties_all_rows():
+    """Logits quantised to 17 values (multiples of 0.5 in [-4, 4]): every
+    threshold falls inside a tie class of thousands of tokens, so the
+    top-k support (ties kept) is far larger than k and the nucleus takes or
+    drops whole classes.  Every row against the oracle."""
+    T = 96
+    rng = np.random.default_rng(31)
+    g = torch.Generator(device=DEV).manual_seed(31)
+    x = torch.full((T, VP), float("-inf"), device=DEV)
+    x[:, :VR] = torch.clamp(torch.round(2.0 * torch.randn((T, VR), generator=g, device=DEV)) / 2.0, -4.0, 4.0)
+    x = x.to(torch.bfloat16)
+    tau = rng.choice([0.7, 1.0, 1.3], T).astype(np.float32)
+    p = rng.choice([0.5, 0.9, 0.99, 1.0], T).astype(np.float32)
+    k = rng.choice([-1, 1, 10, 1000, 50000], T).astype(np.int32)
+    bits = bits_of(x)
+    forced = np.zeros(T, bool)
+    forced[rng.choice(T, T // 10, replace=False)] = True
+    tg = oracle_targets_parallel(bits, tau, p, k, forced, seed=31)
+    f, r, s = run_pair(x, _t(tg, torch.int32), _t(tau, torch.float32), _t(p, torch.float32),
+                       _t(k, torch.int32))
+    st = Stats()
+    check_rows_parallel(st, bits, tau, p, k, tg, f, r, s)
+    assert st.rows == T
+    record("coarse ties: 17 values, tau 0.7-1.3, p 0.5-1, k off/1/10/1000/50000", st)
