@@ -235,3 +235,27 @@ def test_bitmap_draw_equals_cluster_draw(case):
     torch.cuda.synchronize()
     for g, w in zip(got, want):
         assert torch.equal(g.view(torch.int32), w.view(torch.int32))
+
+
+def test_sampler_coarse_ties():
+    """Logits quantised to 17 values: tie classes of thousands of tokens at
+    every threshold, so the draw picks among equal-mass tokens (inverse CDF
+    in column order) and supports take or drop whole classes.  Every row's
+    token against the oracle's draw with the same random word."""
+    T = 48
+    rng = np.random.default_rng(47)
+    g = torch.Generator(device=DEV).manual_seed(47)
+    x = torch.full((T, VP), float("-inf"), device=DEV)
+    x[:, :VR] = torch.clamp(torch.round(2.0 * torch.randn((T, VR), generator=g, device=DEV)) / 2.0, -4.0, 4.0)
+    x = x.to(torch.bfloat16)
+    tau = rng.choice([0.7, 1.0, 1.3], T).astype(np.float32)
+    p = rng.choice([0.5, 0.9, 1.0], T).astype(np.float32)
+    k = rng.choice([-1, 10, 1000], T).astype(np.int32)
+    u = rng.integers(0, 2 ** 32, T, dtype=np.uint64).astype(np.uint32)
+    bits = bits_of(x)
+    tok, restr, full, sup = pkg.sample(x, _t(tau, torch.float32), _t(p, torch.float32),
+                                       _t(k, torch.int32), uniform=_u32_tensor(u))
+    torch.cuda.synchronize()
+    near = check_draws(bits, tau, p, k, u, tok.cpu().numpy(), restr.cpu().numpy(),
+                       full.cpu().numpy(), sup.cpu().numpy())
+    assert near <= 1
