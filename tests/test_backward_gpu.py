@@ -267,3 +267,34 @@ def test_backward_full_size_sampled_rows():
                     g_full.cpu().numpy(), g_restr.cpu().numpy(), g[ridx].cpu().numpy(), rows=rows)
     del g, wl
     torch.cuda.empty_cache()
+
+
+def test_backward_coarse_ties():
+    """Logits quantised to 17 values: the support takes or drops tie classes
+    of thousands of tokens, so each class's gradient is either all inside
+    (a_in) or all outside (a_out).  Both backward forms against the oracle,
+    element by element."""
+    T = 10
+    rng = np.random.default_rng(37)
+    g = torch.Generator(device=DEV).manual_seed(37)
+    x = torch.full((T, VP), float("-inf"), device=DEV)
+    x[:, :VR] = torch.clamp(torch.round(2.0 * torch.randn((T, VR), generator=g, device=DEV)) / 2.0, -4.0, 4.0)
+    x = x.to(torch.bfloat16)
+    tau = rng.choice([0.7, 1.3], T).astype(np.float32)
+    p = rng.choice([0.5, 0.9, 1.0], T).astype(np.float32)
+    k = rng.choice([-1, 10, 1000], T).astype(np.int32)
+    bits = bits_of(x)
+    t = oracle_targets(bits, tau, p, k, rng, set(rng.choice(T, 2, replace=False).tolist()))
+    gf = rng.standard_normal(T).astype(np.float32)
+    gr = rng.standard_normal(T).astype(np.float32)
+    args = (_t(tau, torch.float32), _t(p, torch.float32), _t(k, torch.int32))
+    single = pkg.logp_backward(x, _t(t, torch.int32), *args, grad_full=_t(gf, torch.float32),
+                               grad_restr=_t(gr, torch.float32), dtype=torch.float32)
+    _, _, _, stats = pkg.logp_pair_save(x, _t(t, torch.int32), *args)
+    saved = torch.empty((T, VP), dtype=torch.float32, device=DEV)
+    pkg.logp_backward_saved(x, _t(t, torch.int32), stats, _t(tau, torch.float32),
+                            grad_full=_t(gf, torch.float32), grad_restr=_t(gr, torch.float32),
+                            out=saved)
+    torch.cuda.synchronize()
+    for got in (single, saved):
+        check_grad_rows(bits, tau, p, k, t, gf, gr, got.cpu().numpy())
