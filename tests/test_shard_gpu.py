@@ -227,3 +227,20 @@ def test_sharded_resolves_every_row_of_deep_top_p_workloads():
     k = _t([-1, -1, -1, 100000, 70000, 3000, 120000, 20000], torch.int32)
     s0, s3 = compare(xw, tw, tau, p, k)
     assert (s3 == -2).sum() >= 5
+
+
+def test_sharded_coarse_ties_bitwise():
+    """Logits quantised to 17 values (tie classes of thousands of tokens at
+    every threshold, supports reaching below the first window): the sharded
+    form bit for bit against the fused pass on every row."""
+    T = 64
+    rng = np.random.default_rng(43)
+    g = torch.Generator(device=DEV).manual_seed(43)
+    x = torch.full((T, VP), float("-inf"), device=DEV)
+    x[:, :VR] = torch.clamp(torch.round(2.0 * torch.randn((T, VR), generator=g, device=DEV)) / 2.0, -4.0, 4.0)
+    x = x.to(torch.bfloat16)
+    tau = torch.as_tensor(rng.choice([0.7, 1.0, 1.3], T).astype(np.float32), device=DEV)
+    p = torch.as_tensor(rng.choice([0.5, 0.9, 0.99, 1.0], T).astype(np.float32), device=DEV)
+    k = torch.as_tensor(rng.choice([-1, 1, 10, 1000, 50000], T).astype(np.int32), device=DEV)
+    t = torch.as_tensor(rng.integers(0, VR, T).astype(np.int32), device=DEV)
+    compare(x, t, tau, p, k)
