@@ -528,24 +528,52 @@ def run_ours(args, rank, world, local):
         outs_h = [torch.empty(T_ROWS, dtype=torch.float32, pin_memory=True) for _ in range(3)]
         sup_h = torch.empty(T_ROWS, dtype=torch.int32, pin_memory=True)
 
+        # the rows in chunks: the host-to-device copy of chunk c + 1 runs on a
+        # copy stream beside the pass over chunk c (the host link, not the
+        # kernels, bounds this leg); a chunk is refilled only after the
+        # previous step's pass over it
+        copy_stream = torch.cuda.Stream(device=dev)
+        nch = 8
+        bounds = [(c * T_ROWS // nch, (c + 1) * T_ROWS // nch) for c in range(nch)]
+        ev_in = [torch.cuda.Event() for _ in range(nch)]
+        ev_done = [torch.cuda.Event() for _ in range(nch)]
+        for ev in ev_done:
+            ev.record(stream)
+
         def e2e_step():
-            x.copy_(hx, non_blocking=True)
-            ref.copy_(hr, non_blocking=True)
-            tg.copy_(ht, non_blocking=True)
-            pkg.logp_kl(x, ref, tg, TAU, TOP_P, TOP_K, out_full=full, out_restr=restr,
-                        out_support=sup, out_full_ref=full_ref, out_kl=kl, stream=stream)
-            outs_h[0].copy_(full, non_blocking=True)
-            outs_h[1].copy_(restr, non_blocking=True)
-            outs_h[2].copy_(kl, non_blocking=True)
-            sup_h.copy_(sup, non_blocking=True)
+            for c, (a, b) in enumerate(bounds):
+                with torch.cuda.stream(copy_stream):
+                    copy_stream.wait_event(ev_done[c])
+                    x[a:b].copy_(hx[a:b], non_blocking=True)
+                    ref[a:b].copy_(hr[a:b], non_blocking=True)
+                    tg[a:b].copy_(ht[a:b], non_blocking=True)
+                    ev_in[c].record(copy_stream)
+                stream.wait_event(ev_in[c])
+                pkg.logp_kl(x[a:b], ref[a:b], tg[a:b], TAU, TOP_P, TOP_K, out_full=full[a:b],
+                            out_restr=restr[a:b], out_support=sup[a:b], out_full_ref=full_ref[a:b],
+                            out_kl=kl[a:b], stream=stream)
+                ev_done[c].record(stream)
+                outs_h[0][a:b].copy_(full[a:b], non_blocking=True)
+                outs_h[1][a:b].copy_(restr[a:b], non_blocking=True)
+                outs_h[2][a:b].copy_(kl[a:b], non_blocking=True)
+                sup_h[a:b].copy_(sup[a:b], non_blocking=True)
 
         e2e_step()
         torch.cuda.synchronize()
+        # the host link alone: one pinned copy of the policy logits
+        l0 = torch.cuda.Event(enable_timing=True)
+        l1 = torch.cuda.Event(enable_timing=True)
+        l0.record(stream)
+        x.copy_(hx, non_blocking=True)
+        l1.record(stream)
+        torch.cuda.synchronize()
+        link_gbs = hx.numel() * 2 / (l0.elapsed_time(l1) / 1e3) / 1e9
         if world > 1:
             dist.barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        copy_stream.wait_event(e0)
         for _ in range(args.e2e_steps):
             e2e_step()
         e1.record(stream)
@@ -554,7 +582,12 @@ def run_ours(args, rank, world, local):
         h2d = hx.numel() * 2 + hr.numel() * 2 + ht.numel() * 4
         d2h = 3 * 4 * T_ROWS + 4 * T_ROWS
         e2e = {"value": throughput(world, T_ROWS, args.e2e_steps, et), "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": et / args.e2e_steps,
+               "link_h2d_gbs": link_gbs,
+               "frac_of_link": h2d / (et / args.e2e_steps / 1e3) / 1e9 / link_gbs,
+               "pipeline": f"{nch} row chunks: the pinned host-to-device copy of chunk c + 1 on a "
+                           "copy stream beside the pass over chunk c"}
 
     # ---- the vocabulary-sharded form of the policy pair pass (8 shard buffers):
     #      8 summary launches (which also keep each 16-byte chunk's maximum), 8
