@@ -391,6 +391,15 @@ def run_ours(args, rank, world, local):
     ref = W.perturbed_copy(x, 0.05, seed=rank_seed(102, rank))
     tg = W.structural_targets(T_ROWS, hot, n, seed=rank_seed(2, rank), device=dev)
     del hot, n
+    if args.e2e_steps > 0:
+        # pinned host copies of the inputs for the end-to-end leg, allocated
+        # while the process's host memory is fresh
+        hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+        hr = torch.empty(ref.shape, dtype=ref.dtype, pin_memory=True)
+        ht = torch.empty(tg.shape, dtype=tg.dtype, pin_memory=True)
+        hx.copy_(x)
+        hr.copy_(ref)
+        ht.copy_(tg)
     f32 = dict(dtype=torch.float32, device=dev)
     full, restr, kl, full_ref = (torch.empty(T_ROWS, **f32) for _ in range(4))
     sup = torch.empty(T_ROWS, dtype=torch.int32, device=dev)
@@ -519,12 +528,6 @@ def run_ours(args, rank, world, local):
     # ---- end to end through the public API from pinned host buffers
     e2e = None
     if args.e2e_steps > 0:
-        hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
-        hr = torch.empty(ref.shape, dtype=ref.dtype, pin_memory=True)
-        ht = torch.empty(tg.shape, dtype=tg.dtype, pin_memory=True)
-        hx.copy_(x)
-        hr.copy_(ref)
-        ht.copy_(tg)
         outs_h = [torch.empty(T_ROWS, dtype=torch.float32, pin_memory=True) for _ in range(3)]
         sup_h = torch.empty(T_ROWS, dtype=torch.int32, pin_memory=True)
 
@@ -560,14 +563,17 @@ def run_ours(args, rank, world, local):
 
         e2e_step()
         torch.cuda.synchronize()
-        # the host link alone: one pinned copy of the policy logits
-        l0 = torch.cuda.Event(enable_timing=True)
-        l1 = torch.cuda.Event(enable_timing=True)
-        l0.record(stream)
-        x.copy_(hx, non_blocking=True)
-        l1.record(stream)
-        torch.cuda.synchronize()
-        link_gbs = hx.numel() * 2 / (l0.elapsed_time(l1) / 1e3) / 1e9
+        # the host link alone: one pinned copy of each logits buffer
+        link_ms = []
+        for hbuf, dbuf in ((hx, x), (hr, ref)):
+            l0 = torch.cuda.Event(enable_timing=True)
+            l1 = torch.cuda.Event(enable_timing=True)
+            l0.record(stream)
+            dbuf.copy_(hbuf, non_blocking=True)
+            l1.record(stream)
+            torch.cuda.synchronize()
+            link_ms.append(l0.elapsed_time(l1))
+        link_gbs = (hx.numel() + hr.numel()) * 2 / (sum(link_ms) / 1e3) / 1e9
         if world > 1:
             dist.barrier()
         e0 = torch.cuda.Event(enable_timing=True)
@@ -585,6 +591,7 @@ def run_ours(args, rank, world, local):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": et / args.e2e_steps,
                "link_h2d_gbs": link_gbs,
+               "link_h2d_gbs_per_buffer": [hx.numel() * 2 / (ms / 1e3) / 1e9 for ms in link_ms],
                "frac_of_link": h2d / (et / args.e2e_steps / 1e3) / 1e9 / link_gbs,
                "pipeline": f"{nch} row chunks: the pinned host-to-device copy of chunk c + 1 on a "
                            "copy stream beside the pass over chunk c"}
