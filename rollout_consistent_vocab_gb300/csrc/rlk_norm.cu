@@ -9,7 +9,7 @@
 // A square q = M 2^(E-150) (M < 2^24) is an integer multiple of 2^(E-150).
 // Instead of one shared-memory add per element, each thread keeps a 128-bit
 // fixed-point accumulator whose unit is 2^(eb-150).  A square with
-// eb <= E <= eb + 32 adds M << (E - eb) (< 2^56) to a 64-bit batch sum,
+// eb <= E <= eb + 31 adds M << (E - eb) (< 2^55) to a 64-bit batch sum,
 // folded into the 128-bit value after every batch of at most 32 squares.  A
 // square above that window moves the window up, to 8 binades above it: the
 // accumulator's low bits that would fall out are first written to the bins
@@ -42,7 +42,7 @@ namespace {
 constexpr int NB = RLK_NORM_BINS;
 constexpr int NAN_BIN = 0;
 constexpr int INF_BIN = NB - 1;
-constexpr int WIN_BINADES = 32;    // window of a thread accumulator: M << 32 < 2^56
+constexpr int WIN_BINADES = 31;    // window of a thread accumulator: M << 31 < 2^55
 constexpr int HEADROOM = 8;        // binades left above a new largest square when the window moves
 constexpr int PIECE = 24;          // bits per piece written to a bin (each increment < 2^24)
 constexpr int NORM_THREADS = 256;
@@ -51,7 +51,7 @@ constexpr int NORM_THREADS = 256;
 #endif
 // 16-byte loads per batch (two batches in flight): measured best at 4 for
 // FP32 and 2 for the 16-bit types, whose 8 squares per vector make the loop
-// longer.  A batch sum takes at most 32 terms of < 2^56 (plus a remainder of
+// longer.  A batch sum takes at most 32 terms of < 2^55 (plus a remainder of
 // fewer) before it is folded.
 template <int DT>
 __host__ __device__ constexpr int norm_unroll() { return DT == RLK_DT_F32 ? 4 : 2; }
@@ -60,7 +60,7 @@ static_assert(4 * 4 <= 128 && 2 * 8 <= 128, "batch sum capacity");
 struct Acc {
   int eb;                          // the accumulator's unit is 2^(eb - 150)
   unsigned long long lo, hi;       // its 128-bit value
-  unsigned long long s;            // batch sum in the same unit (at most 255 terms < 2^56)
+  unsigned long long s;            // batch sum in the same unit (at most 255 terms < 2^55)
   uint32_t nan, inf;               // NaN and infinite squares seen
 };
 
@@ -139,7 +139,7 @@ __device__ __forceinline__ void acc_add(Acc& a, uint32_t u, unsigned long long* 
       return;
     }
     // a new largest square: move the window up, leaving HEADROOM binades above
-    // it, but never past eb = 254 - 32, so that an exponent field of 255 (NaN,
+    // it, but never past eb = 254 - 31, so that an exponent field of 255 (NaN,
     // infinity) stays outside the window
     acc_fold(a);
     acc_spill(a, min(e - (WIN_BINADES - HEADROOM), 254 - WIN_BINADES) - a.eb, sb);
@@ -151,15 +151,18 @@ __device__ __forceinline__ void acc_add(Acc& a, uint32_t u, unsigned long long* 
 // The common case, without branches: a square inside the window joins the
 // batch sum.  Returns true for a square it leaves to acc_add: nonzero and
 // outside the window (including NaN and infinite squares, whose exponent
-// field is above eb + 32 because eb <= 254 - 32).
+// field is above eb + 31 because eb <= 254 - 31).
 __device__ __forceinline__ bool acc_fast(Acc& a, uint32_t u) {
   const uint32_t d = (u >> 23) - static_cast<uint32_t>(a.eb);   // a NaN's sign bit makes d large
-  const bool in = d <= static_cast<uint32_t>(WIN_BINADES);
-  const unsigned long long v = static_cast<unsigned long long>((u & 0x7FFFFFu) | 0x800000u)
-                               << (d & 63u);
-  a.s += in ? v : 0ull;
-  return !in && u != 0u;
+  // 2^d, or 0 outside the window: the shift amount is clamped at 32, and
+  // the window is d <= 31 (WIN_BINADES)
+  uint32_t p2;
+  asm("shl.b32 %0, 1, %1;" : "=r"(p2) : "r"(d));
+  // M 2^d joins the batch sum as one widening multiply-add
+  asm("mad.wide.u32 %0, %1, %2, %0;" : "+l"(a.s) : "r"((u & 0x7FFFFFu) | 0x800000u), "r"(p2));
+  return p2 == 0u && u != 0u;
 }
+static_assert(WIN_BINADES == 31, "acc_fast's window is the range of a 32-bit shift");
 
 // The FP32 square of one element, rounded to nearest even.
 template <int DT>
@@ -169,6 +172,16 @@ __device__ __forceinline__ uint32_t square_bits(uint32_t raw) {
   else if (DT == RLK_DT_BF16) g = __uint_as_float(raw << 16);
   else g = __half2float(__ushort_as_half(static_cast<unsigned short>(raw)));
   return __float_as_uint(__fmul_rn(g, g));
+}
+
+// The FP32 squares of two FP32 elements (raw bits), one packed product
+// rounded to nearest even in each lane.
+__device__ __forceinline__ void square2(uint32_t x0, uint32_t x1, uint32_t& q0, uint32_t& q1) {
+  unsigned long long p;
+  asm("{\n\t.reg .b64 t;\n\tmov.b64 t, {%1, %2};\n\tmul.rn.f32x2 %0, t, t;\n\t}"
+      : "=l"(p) : "r"(x0), "r"(x1));
+  q0 = static_cast<uint32_t>(p);
+  q1 = static_cast<uint32_t>(p >> 32);
 }
 
 // Element j of a 16-byte vector (raw bits; j may be a runtime value).
@@ -185,8 +198,17 @@ __device__ __forceinline__ void acc_vec(Acc& a, const uint4& v, unsigned long lo
   constexpr int NQ = DT == RLK_DT_F32 ? 4 : 8;
   const int eb0 = a.eb;
   bool rest = false;
+  if (DT == RLK_DT_F32) {
+    // the four squares as two packed products (each lane rounded as a scalar product)
+    uint32_t q[4];
+    square2(v.x, v.y, q[0], q[1]);
+    square2(v.z, v.w, q[2], q[3]);
 #pragma unroll
-  for (int j = 0; j < NQ; ++j) rest |= acc_fast(a, square_bits<DT>(vec_elem<DT>(v, j)));
+    for (int j = 0; j < 4; ++j) rest |= acc_fast(a, q[j]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) rest |= acc_fast(a, square_bits<DT>(vec_elem<DT>(v, j)));
+  }
   if (rest) {                      // rare: the squares acc_fast left, by its own test at eb0
 #pragma unroll 1
     for (int j = 0; j < NQ; ++j) {
