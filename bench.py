@@ -525,47 +525,29 @@ def run_ours(args, rank, world, local):
         del xk, hk, nk, tk
         torch.cuda.empty_cache()
 
-    # ---- end to end through the public API from pinned host buffers
+    # ---- end to end through the public API from pinned host buffers: one
+    #      rlk_logp_kl_host call per step (the copies of row range c + 1 on a
+    #      copy stream beside the passes over range c, the results copied back)
     e2e = None
     if args.e2e_steps > 0:
-        outs_h = [torch.empty(T_ROWS, dtype=torch.float32, pin_memory=True) for _ in range(3)]
-        sup_h = torch.empty(T_ROWS, dtype=torch.int32, pin_memory=True)
-
-        # the rows in chunks: the host-to-device copy of chunk c + 1 runs on a
-        # copy stream beside the pass over chunk c (the host link, not the
-        # kernels, bounds this leg); a chunk is refilled only after the
-        # previous step's pass over it
-        copy_stream = torch.cuda.Stream(device=dev)
         nch = 8
-        bounds = [(c * T_ROWS // nch, (c + 1) * T_ROWS // nch) for c in range(nch)]
-        ev_in = [torch.cuda.Event() for _ in range(nch)]
-        ev_done = [torch.cuda.Event() for _ in range(nch)]
-        for ev in ev_done:
-            ev.record(stream)
+        copy_stream = torch.cuda.Stream(device=dev)
+        ws = torch.empty(pkg.logp_kl_host_workspace_bytes(T_ROWS), dtype=torch.uint8, device=dev)
+        outs_h = [torch.empty(T_ROWS, dtype=dt, pin_memory=True)
+                  for dt in (torch.float32, torch.float32, torch.int32, torch.float32, torch.float32)]
 
         def e2e_step():
-            for c, (a, b) in enumerate(bounds):
-                with torch.cuda.stream(copy_stream):
-                    copy_stream.wait_event(ev_done[c])
-                    x[a:b].copy_(hx[a:b], non_blocking=True)
-                    ref[a:b].copy_(hr[a:b], non_blocking=True)
-                    tg[a:b].copy_(ht[a:b], non_blocking=True)
-                    ev_in[c].record(copy_stream)
-                stream.wait_event(ev_in[c])
-                pkg.logp_kl(x[a:b], ref[a:b], tg[a:b], TAU, TOP_P, TOP_K, out_full=full[a:b],
-                            out_restr=restr[a:b], out_support=sup[a:b], out_full_ref=full_ref[a:b],
-                            out_kl=kl[a:b], stream=stream)
-                ev_done[c].record(stream)
-                outs_h[0][a:b].copy_(full[a:b], non_blocking=True)
-                outs_h[1][a:b].copy_(restr[a:b], non_blocking=True)
-                outs_h[2][a:b].copy_(kl[a:b], non_blocking=True)
-                sup_h[a:b].copy_(sup[a:b], non_blocking=True)
+            pkg.logp_kl_host(hx, hr, ht, TAU, TOP_P, TOP_K, out_full=outs_h[0], out_restr=outs_h[1],
+                             out_support=outs_h[2], out_full_ref=outs_h[3], out_kl=outs_h[4],
+                             workspace=ws, chunks=nch, copy_stream=copy_stream, stream=stream)
 
         e2e_step()
         torch.cuda.synchronize()
-        # the host link alone: the step's copies (the same chunks on the copy
-        # stream) with no pass, best of three
-        h2d = hx.numel() * 2 + hr.numel() * 2 + ht.numel() * 4
+        e2e_same = all(torch.equal(h.view(torch.int32), d.cpu().view(torch.int32))
+                       for h, d in zip(outs_h, step_out))
+        # the host link alone: the same rows in the same chunks, whole rows,
+        # on the copy stream with no pass, best of three
+        bounds = [(c * T_ROWS // nch, (c + 1) * T_ROWS // nch) for c in range(nch)]
         link_ms = []
         for _ in range(3):
             l0 = torch.cuda.Event(enable_timing=True)
@@ -575,31 +557,32 @@ def run_ours(args, rank, world, local):
                 for a, b in bounds:
                     x[a:b].copy_(hx[a:b], non_blocking=True)
                     ref[a:b].copy_(hr[a:b], non_blocking=True)
-                    tg[a:b].copy_(ht[a:b], non_blocking=True)
             l1.record(copy_stream)
             torch.cuda.synchronize()
             link_ms.append(l0.elapsed_time(l1))
-        link_gbs = h2d / (min(link_ms) / 1e3) / 1e9
+        link_gbs = (hx.numel() + hr.numel()) * 2 / (min(link_ms) / 1e3) / 1e9
         if world > 1:
             dist.barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        copy_stream.wait_event(e0)
         for _ in range(args.e2e_steps):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
         et = max_over_ranks(e0.elapsed_time(e1), dev)
-        d2h = 3 * 4 * T_ROWS + 4 * T_ROWS
+        h2d = 2 * T_ROWS * VREAL * 2 + T_ROWS * 4       # the real columns of both tensors, the targets
+        d2h = 5 * 4 * T_ROWS
         e2e = {"value": throughput(world, T_ROWS, args.e2e_steps, et), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": et / args.e2e_steps,
                "link_h2d_gbs": link_gbs,
-               "link_note": "the same chunked pinned copies with no pass, best of three",
+               "link_note": "whole-row pinned copies in the same chunks on the copy stream, no pass, best of three",
                "frac_of_link": h2d / (et / args.e2e_steps / 1e3) / 1e9 / link_gbs,
-               "pipeline": f"{nch} row chunks: the pinned host-to-device copy of chunk c + 1 on a "
-                           "copy stream beside the pass over chunk c"}
+               "call": f"rlk_logp_kl_host, {nch} row ranges: the copies of range c + 1 (the 151936 real "
+                       "columns of each row) on a copy stream beside the passes over range c",
+               "outputs_equal_device_path": e2e_same}
+        del ws
 
     # ---- the vocabulary-sharded form of the policy pair pass (8 shard buffers):
     #      8 summary launches (which also keep each 16-byte chunk's maximum), 8

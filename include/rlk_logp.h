@@ -75,7 +75,7 @@ extern "C" {
 #define RLK_VOCAB_REAL 151936
 #define RLK_NUM_SHARDS 8
 #define RLK_SHARD_WIDTH 19072
-#define RLK_ABI_VERSION 4
+#define RLK_ABI_VERSION 5
 
 typedef enum {
   RLK_OK = 0,
@@ -151,6 +151,38 @@ rlk_status rlk_logp_kl(const rlk_logp_args* policy, const void* ref_logits,
                        int64_t ref_row_stride, float* out_full, float* out_restr,
                        int32_t* out_support, float* out_full_ref, float* out_kl,
                        void* stream);
+
+/* rlk_logp_kl on inputs that live in host memory, the copies in: the
+ * rows go in `chunks` row ranges; the host-to-device copy of range c + 1
+ * runs on copy_stream while the passes over range c run on `stream`, and
+ * each range's results are copied back on `stream`.  The host link, not
+ * the passes, then bounds the call.  Each row's results are bit-identical to
+ * rlk_logp_kl on the same logits (the passes only see the rows of a range,
+ * and a row's results do not depend on its batch).
+ *   policy: as for rlk_logp_kl, except that policy->logits and
+ *     policy->target are HOST pointers (pinned memory, or the copies cannot
+ *     run beside the passes).  The per-row parameter arrays
+ *     (temperature/top_p/top_k) and err_count stay device pointers or NULL.
+ *   ref_logits, ref_row_stride: the reference logits in host memory.
+ *   out_full, out_restr, out_support, out_full_ref, out_kl: HOST pointers,
+ *     required as for rlk_logp_kl; valid once `stream` has completed.
+ *   workspace: device scratch of RLK_LOGP_KL_HOST_WORKSPACE_BYTES(T) bytes,
+ *     256-byte aligned: both logits tensors (real columns only, 151936 of
+ *     each row are copied), the targets and the five outputs.  A call's
+ *     first copy waits for the work already queued on `stream`, so
+ *     consecutive calls may share one workspace on the same streams.
+ *   chunks: number of row ranges, >= 1 (capped at T).
+ *   copy_stream: the stream for the host-to-device copies; NULL (or equal
+ *     to `stream`) runs everything on `stream`, with no overlap.
+ * Asynchronous: no host synchronisation; the library allocates no memory
+ * (it creates and releases a few CUDA events).  RLK_EINVAL for missing
+ * pointers or chunks < 1, RLK_EALIGN for a misaligned workspace, RLK_ECUDA
+ * for a failed copy, event or launch. */
+#define RLK_LOGP_KL_HOST_WORKSPACE_BYTES(T) ((size_t)(T) * 610304u + 6u * ((((size_t)(T) * 4u) + 255u) & ~(size_t)255u))
+rlk_status rlk_logp_kl_host(const rlk_logp_args* policy, const void* ref_logits,
+                            int64_t ref_row_stride, float* out_full, float* out_restr,
+                            int32_t* out_support, float* out_full_ref, float* out_kl,
+                            void* workspace, int32_t chunks, void* stream, void* copy_stream);
 
 /* The reference half of rlk_logp_kl on its own: the full-vocabulary logprob
  * of each row's target under ref->logits, and out_kl[i] = full_policy[i] -

@@ -63,6 +63,7 @@ class ShardArgs(ctypes.Structure):
 
 
 COMPUTE = ("rlk_logp_full", "rlk_logp_restricted", "rlk_logp_pair", "rlk_logp_kl", "rlk_logp_kl_ref",
+           "rlk_logp_kl_host",
            "rlk_logp_backward", "rlk_logp_pair_save", "rlk_logp_backward_saved", "rlk_sample",
            "rlk_sample_noalloc", "rlk_linear_logp", "rlk_linear_logp_pair",
            "rlk_logp_shard_summary", "rlk_logp_shard_counts", "rlk_logp_merge",
@@ -90,6 +91,7 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     lib.rlk_logp_pair.argtypes = [A, VP, VP, VP, VP]
     lib.rlk_logp_kl.argtypes = [A, VP, ctypes.c_int64, VP, VP, VP, VP, VP, VP]
     lib.rlk_logp_kl_ref.argtypes = [A, VP, VP, VP, VP]
+    lib.rlk_logp_kl_host.argtypes = [A, VP, ctypes.c_int64, VP, VP, VP, VP, VP, VP, ctypes.c_int32, VP, VP]
     lib.rlk_logp_backward.argtypes = [A, VP, VP, VP, ctypes.c_int64, ctypes.c_int32, VP, VP, VP, VP]
     lib.rlk_logp_pair_save.argtypes = [A, VP, VP, VP, VP, VP]
     lib.rlk_sample.argtypes = [A, ctypes.c_uint64, VP, VP, VP, VP, VP, VP, VP, VP]
@@ -119,7 +121,7 @@ def load_library(path: str = LIB) -> ctypes.CDLL:
     lib.rlk_last_error.restype = ctypes.c_char_p
     lib.rlk_abi_version.argtypes = []
     lib.rlk_abi_version.restype = ctypes.c_int
-    if lib.rlk_abi_version() != 4:
+    if lib.rlk_abi_version() != 5:
         raise ImportError("librlk_logp.so ABI version mismatch")
     _lib = lib
     return lib
@@ -241,6 +243,44 @@ def logp_kl(logits, ref_logits, target, temperature=1.0, top_p=1.0, top_k=-1, *,
     check(lib.rlk_logp_kl(ctypes.byref(a), ref_logits.data_ptr() if a.T else None,
                           ref_logits.stride(0) if a.T else VOCAB_PADDED,
                           *[_ptr(o) for o in outs], _stream(stream)))
+    return tuple(outs)
+
+
+def logp_kl_host_workspace_bytes(T: int) -> int:
+    """RLK_LOGP_KL_HOST_WORKSPACE_BYTES(T): both logits tensors, the targets and five outputs."""
+    return T * 2 * VOCAB_PADDED * 2 + 6 * ((T * 4 + 255) // 256 * 256)
+
+
+def logp_kl_host(logits, ref_logits, target, temperature=1.0, top_p=1.0, top_k=-1, *, out_full=None,
+                 out_restr=None, out_support=None, out_full_ref=None, out_kl=None, workspace=None,
+                 chunks=8, copy_stream=None, err_count=None, stream=None, device=None):
+    """logp_kl on host-resident inputs (pinned CPU tensors: logits and ref_logits
+    bf16 [T, >=152576], target int32 [T]): the copies in run on ``copy_stream``
+    beside the passes, range by range.  Per-row parameters, if tensors, are on
+    the GPU.  Returns pinned CPU tensors (full, restricted, support, full_ref,
+    kl), valid once ``stream`` has completed."""
+    lib = load_library()
+    torch = _torch()
+    for t, name in ((logits, "logits"), (ref_logits, "ref_logits"), (target, "target")):
+        if t.is_cuda:
+            raise ValueError(f"{name} must be a host (CPU) tensor")
+    a = make_args(logits, target, temperature, top_p, top_k, err_count)
+    if ref_logits.dtype != torch.bfloat16 or ref_logits.shape[0] != a.T or ref_logits.stride(1) != 1 \
+            or ref_logits.shape[1] < VOCAB_PADDED:
+        raise ValueError("ref_logits must be a bf16 [T, >=152576] tensor like logits")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    outs = [o if o is not None else torch.empty((a.T,), dtype=dt, pin_memory=True) for o, dt in
+            ((out_full, torch.float32), (out_restr, torch.float32), (out_support, torch.int32),
+             (out_full_ref, torch.float32), (out_kl, torch.float32))]
+    if workspace is None:
+        workspace = torch.empty(logp_kl_host_workspace_bytes(a.T), dtype=torch.uint8, device=dev)
+    if workspace.numel() * workspace.element_size() < logp_kl_host_workspace_bytes(a.T) or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor of at least logp_kl_host_workspace_bytes(T) bytes")
+    check(lib.rlk_logp_kl_host(ctypes.byref(a), ref_logits.data_ptr() if a.T else None,
+                               ref_logits.stride(0) if a.T else VOCAB_PADDED,
+                               *[_ptr(o) for o in outs], workspace.data_ptr() if a.T else None,
+                               int(chunks), _stream(stream),
+                               copy_stream.cuda_stream if copy_stream is not None else None))
     return tuple(outs)
 
 

@@ -10,7 +10,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, f) for f in ("rlk_logp.cu", "rlk_shard.cu", "rlk_grad.cu", "rlk_noalloc.cu",
-                                          "rlk_linear.cu", "rlk_norm.cu")]
+                                          "rlk_linear.cu", "rlk_norm.cu", "rlk_host_io.cu")]
 HEADERS = [os.path.join(CSRC, "rlk_device.cuh"), os.path.join(CSRC, "rlk_host.h")]
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "lib")

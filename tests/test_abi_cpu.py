@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.rlk_abi_version() == 4
+    assert lib.rlk_abi_version() == 5
     assert lib.rlk_status_string(0) == b"ok"
     assert lib.rlk_status_string(2) == b"misaligned pointer or stride"
 
@@ -118,6 +118,37 @@ def test_empty_batch_is_a_noop(lib):
     a = _args(T=0, logits=None, target=None)
     assert lib.rlk_logp_pair(ctypes.byref(a), None, None, None, None) == b.RLK_OK
     assert lib.rlk_logp_full(ctypes.byref(a), None, None) == b.RLK_OK
+
+
+def test_kl_host_validation(lib):
+    """The host-input step checks everything before its first CUDA call."""
+    a = _args()
+    WS = 0x60000                      # 256-byte aligned
+    def call(args=a, ref=0x50000, stride=b.VOCAB_PADDED, outs=(OUT, None, None, OUT, OUT), ws=WS,
+             chunks=4):
+        return lib.rlk_logp_kl_host(ctypes.byref(args) if args is not None else None, ref, stride,
+                                    *outs, ws, chunks, None, None)
+    assert call(args=None) == b.RLK_EINVAL
+    assert call(args=_args(T=-1)) == b.RLK_EINVAL
+    assert call(args=_args(T=1 << 27)) == b.RLK_EINVAL
+    assert call(args=_args(logits=None)) == b.RLK_EINVAL
+    assert call(args=_args(target=None)) == b.RLK_EINVAL
+    assert call(args=_args(row_stride=152575)) == b.RLK_EINVAL
+    assert call(ref=None) == b.RLK_EINVAL
+    assert call(stride=152575) == b.RLK_EINVAL
+    assert call(args=_args(top_p_scalar=0.0)) == b.RLK_EINVAL
+    assert call(args=_args(top_k_scalar=0)) == b.RLK_EINVAL
+    assert call(args=_args(temperature=0x40001)) == b.RLK_EALIGN
+    assert call(outs=(None, None, None, OUT, OUT)) == b.RLK_EINVAL
+    assert call(outs=(OUT, None, None, None, OUT)) == b.RLK_EINVAL
+    assert call(outs=(OUT, None, None, OUT, None)) == b.RLK_EINVAL
+    assert call(outs=(OUT, OUT + 2, None, OUT, OUT)) == b.RLK_EALIGN
+    assert call(ws=None) == b.RLK_EINVAL
+    assert call(ws=WS + 16) == b.RLK_EALIGN
+    assert call(chunks=0) == b.RLK_EINVAL
+    # host logits need no 16-byte alignment (they are copied), and T = 0 is a no-op
+    assert call(args=_args(T=0, logits=None, target=None), ref=None, ws=None) == b.RLK_OK
+    assert lib.rlk_last_error()
 
 
 def test_kl_ref_validation(lib):
@@ -393,6 +424,8 @@ def test_binding_sizes_match_the_header_macros():
         assert b.linear_workspace_bytes(T) == lw
         lp = eval(re.sub(r"\(size_t\)|u\b", "", macro(text, "RLK_LINEAR_PAIR_WORKSPACE_BYTES")).replace("(T)", f"({T})"))
         assert b.linear_pair_workspace_bytes(T) == lp
+        kh = eval(re.sub(r"\(size_t\)|u\b", "", macro(text, "RLK_LOGP_KL_HOST_WORKSPACE_BYTES")).replace("(T)", f"({T})"))
+        assert b.logp_kl_host_workspace_bytes(T) == kh
     assert int(macro(text, "RLK_SHARD_CHUNKS")) == b.SHARD_CHUNKS
     assert int(macro(norm, "RLK_NORM_BINS")) == b.NORM_BINS
     assert int(macro(text, "RLK_VOCAB_PADDED")) == b.VOCAB_PADDED
