@@ -171,13 +171,15 @@ rlk_status rlk_logp_kl(const rlk_logp_args* policy, const void* ref_logits,
  *     each row are copied), the targets and the five outputs.  A call's
  *     first copy waits for the work already queued on `stream`, so
  *     consecutive calls may share one workspace on the same streams.
- *   chunks: number of row ranges, >= 1 (capped at T).
+ *   chunks: number of row ranges, >= 1 (capped at T and at
+ *     RLK_KL_HOST_MAX_CHUNKS).
  *   copy_stream: the stream for the host-to-device copies; NULL (or equal
  *     to `stream`) runs everything on `stream`, with no overlap.
  * Asynchronous: no host synchronisation; the library allocates no memory
  * (it creates and releases a few CUDA events).  RLK_EINVAL for missing
  * pointers or chunks < 1, RLK_EALIGN for a misaligned workspace, RLK_ECUDA
  * for a failed copy, event or launch. */
+#define RLK_KL_HOST_MAX_CHUNKS 4096
 #define RLK_LOGP_KL_HOST_WORKSPACE_BYTES(T) ((size_t)(T) * 610304u + 6u * ((((size_t)(T) * 4u) + 255u) & ~(size_t)255u))
 rlk_status rlk_logp_kl_host(const rlk_logp_args* policy, const void* ref_logits,
                             int64_t ref_row_stride, float* out_full, float* out_restr,

@@ -125,7 +125,9 @@ extern "C" rlk_status rlk_logp_kl_host(const rlk_logp_args* policy, const void* 
   if (!aligned(workspace, 256)) return fail(RLK_EALIGN, "workspace is not 256-byte aligned");
   if (chunks < 1) return fail(RLK_EINVAL, "chunks = %d < 1", chunks);
 
-  const int64_t nch = chunks < T ? chunks : T;
+  // at most T ranges, and at most RLK_KL_HOST_MAX_CHUNKS (each range costs an event)
+  int64_t nch = chunks < T ? chunks : T;
+  if (nch > RLK_KL_HOST_MAX_CHUNKS) nch = RLK_KL_HOST_MAX_CHUNKS;
   const Workspace w = carve(workspace, T);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaStream_t cs = copy_stream ? static_cast<cudaStream_t>(copy_stream) : st;
